@@ -1,0 +1,362 @@
+"""Benchmark of the routed-expert MoE layer on GB300.
+
+One step = one pass of the whole layer (permute + gather, fused gate/up/SiLU
+grouped GEMM, down grouped GEMM, combine; plus the activation quantisers in
+the A8/A4 modes) over one batch of seeded synthetic inputs already resident in
+HBM.  The default workload is the W4A16 decode block batch (8 concurrent
+32-token blocks, H=2048, 256 experts, I=512, top-8).
+
+Prints one JSON line (rank 0).  --impl reference times the CPU oracle on the
+host cores instead (a bounded sample of the same workload).
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+import torch  # noqa: E402
+
+import synth as S  # noqa: E402
+
+METRIC = "MoE-layer tokens/s and achieved HBM GB/s or tensor-pipe % vs GB300 peak, 1 GPU"
+L2_BYTES = 129 * 1024 * 1024
+
+
+def _peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            p = json.load(f)
+        return float(p["hbm_gbs"]), float(p["bf16_tflops"]), "measured"
+    except Exception:
+        return 6800.0, 1900.0, "fallback"
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons sampled during the timed region."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "100"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        self.lines = []
+        if self.proc is not None:
+            time.sleep(0.25)
+            self.proc.terminate()
+            try:
+                out, _ = self.proc.communicate(timeout=5)
+            except Exception:
+                self.proc.kill()
+                out = ""
+            self.lines = [ln for ln in out.splitlines() if ln.strip()]
+
+    def summary(self):
+        sm, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in getattr(self, "lines", []):
+            f = [x.strip() for x in ln.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                mx = float(f[2])
+            except ValueError:
+                continue
+            for n, v in zip(names, f[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": mx, "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+def _dist():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def gate_up_bytes(wl: S.Workload, touched: int) -> int:
+    """Algorithmic bytes of one gate/up launch: each touched expert's gate and up
+    matrices (codes + scales) once, the gathered activations read once, h written once."""
+    L = S.layout(wl.wfmt, wl.E, wl.H, wl.I)
+    per_expert = 0
+    for m in (S.GATE, S.UP):
+        N, K = L.dims(m)
+        per_expert += S.code_bytes(wl.wfmt, N, K) + S.scale_bytes(wl.wfmt, N, K)
+    act = {S.ACT_BF16: wl.H * 2, S.ACT_INT8_G128: wl.H + wl.H // 128 * 4,
+           S.ACT_NVFP4_G16: wl.H // 2 + wl.H // 16 + 4}[wl.act]
+    return touched * per_expert + wl.P * act + wl.P * wl.I * 2
+
+
+def run_ours(args, wl):
+    import quantized_moe_expert_routed_gb300 as M
+
+    world, rank, local = _dist()
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    x, ids, w, blob, hdr, L = S.make_inputs(wl, device=dev)
+    layer = M.Layer(blob, hdr)
+    E, T, k, P = wl.E, wl.T, wl.k, wl.P
+    stream = torch.cuda.current_stream(dev)
+    ws = M.workspace(layer, wl.act, T, k, device=dev)
+    out = torch.empty((T, wl.H), dtype=torch.bfloat16, device=dev)
+    flush = torch.empty(2 * L2_BYTES, dtype=torch.uint8, device=dev)
+
+    # Preallocated per-step buffers for the stepwise path (same kernels as mnw_moe_forward,
+    # called one by one so the gate/up launch can be timed on its own stream).
+    offsets = torch.empty(E + 1, dtype=torch.int32, device=dev)
+    sorted_assign = torch.empty(P, dtype=torch.int32, device=dev)
+    assign_pos = torch.empty(P, dtype=torch.int32, device=dev)
+    err = torch.zeros(1, dtype=torch.int32, device=dev)
+    lib = M.load()
+    import ctypes
+    sp = ctypes.c_void_p(stream.cuda_stream)
+    ptr = lambda t: ctypes.c_void_p(t.data_ptr())  # noqa: E731
+    gemm_name = {(S.FMT_BF16, S.ACT_BF16): "bf16", (S.FMT_INT8_G128, S.ACT_BF16): "w8a16",
+                 (S.FMT_INT4_G128, S.ACT_BF16): "w4a16", (S.FMT_INT8_G128, S.ACT_INT8_G128): "w8a8",
+                 (S.FMT_INT4_G128, S.ACT_INT8_G128): "w4a8",
+                 (S.FMT_NVFP4_G16, S.ACT_NVFP4_G16): "nvfp4"}[(wl.wfmt, wl.act)]
+    gemm = getattr(lib, f"mnw_moe_grouped_gemm_{gemm_name}")
+    h = torch.empty((P, wl.I), dtype=torch.bfloat16, device=dev)
+    y = torch.empty((P, wl.H), dtype=torch.bfloat16, device=dev)
+    if wl.act == S.ACT_BF16:
+        xa = torch.empty((P, wl.H), dtype=torch.bfloat16, device=dev)
+    elif wl.act == S.ACT_INT8_G128:
+        xq = torch.empty((P, wl.H), dtype=torch.int8, device=dev)
+        xs = torch.empty((P, wl.H // 128), dtype=torch.float32, device=dev)
+        hq = torch.empty((P, wl.I), dtype=torch.int8, device=dev)
+        hs = torch.empty((P, wl.I // 128), dtype=torch.float32, device=dev)
+    else:
+        xq = torch.empty((P, wl.H // 2), dtype=torch.uint8, device=dev)
+        xs = torch.empty((P, wl.H // 16), dtype=torch.uint8, device=dev)
+        xo = torch.empty((P,), dtype=torch.float32, device=dev)
+        hq = torch.empty((P, wl.I // 2), dtype=torch.uint8, device=dev)
+        hs = torch.empty((P, wl.I // 16), dtype=torch.uint8, device=dev)
+        ho = torch.empty((P,), dtype=torch.float32, device=dev)
+
+    def chk(rc, what):
+        if rc != 0:
+            raise RuntimeError(f"{what} failed: {lib.mnw_status_string(rc).decode()}")
+
+    def step(ev_g0=None, ev_g1=None):
+        launches = 0
+        if wl.act == S.ACT_BF16:
+            chk(lib.mnw_moe_permute(ptr(ids), T, k, E, ptr(offsets), ptr(sorted_assign), ptr(assign_pos), ptr(x),
+                                    wl.H, ptr(xa), ptr(err), sp), "permute")
+            launches += 2
+            if ev_g0 is not None:
+                ev_g0.record(stream)
+            chk(gemm(layer.handle, 0, ptr(xa), ptr(offsets), P, ptr(h), ptr(err), sp), "gate_up")
+            if ev_g1 is not None:
+                ev_g1.record(stream)
+            chk(gemm(layer.handle, 1, ptr(h), ptr(offsets), P, ptr(y), ptr(err), sp), "down")
+            launches += 2
+        else:
+            chk(lib.mnw_moe_permute(ptr(ids), T, k, E, ptr(offsets), ptr(sorted_assign), ptr(assign_pos), None, 0,
+                                    None, ptr(err), sp), "permute")
+            o1 = ptr(xo) if wl.act == S.ACT_NVFP4_G16 else None
+            o2 = ptr(ho) if wl.act == S.ACT_NVFP4_G16 else None
+            chk(lib.mnw_moe_quantize_act(wl.act, ptr(x), P, wl.H, ptr(sorted_assign), k, ptr(xq), ptr(xs), o1, sp),
+                "quantize x")
+            if ev_g0 is not None:
+                ev_g0.record(stream)
+            if wl.act == S.ACT_INT8_G128:
+                chk(gemm(layer.handle, 0, ptr(xq), ptr(xs), ptr(offsets), P, ptr(h), None, ptr(err), sp), "gate_up")
+            else:
+                chk(gemm(layer.handle, 0, ptr(xq), ptr(xs), o1, ptr(offsets), P, ptr(h), ptr(err), sp), "gate_up")
+            if ev_g1 is not None:
+                ev_g1.record(stream)
+            chk(lib.mnw_moe_quantize_act(wl.act, ptr(h), P, wl.I, None, 1, ptr(hq), ptr(hs), o2, sp), "quantize h")
+            if wl.act == S.ACT_INT8_G128:
+                chk(gemm(layer.handle, 1, ptr(hq), ptr(hs), ptr(offsets), P, ptr(y), None, ptr(err), sp), "down")
+            else:
+                chk(gemm(layer.handle, 1, ptr(hq), ptr(hs), o2, ptr(offsets), P, ptr(y), ptr(err), sp), "down")
+            launches += 5
+        chk(lib.mnw_moe_combine(ptr(y), ptr(assign_pos), ptr(w), T, k, wl.H, ptr(out), sp), "combine")
+        return launches + 1
+
+    for _ in range(args.warmup):
+        step()
+        flush.zero_()
+    torch.cuda.synchronize()
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True),
+           torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    launches = 0
+    with ClockSampler(local) as clk:
+        for i in range(args.steps):
+            flush.zero_()  # L2 flush between timed iterations (outside the events)
+            e0, e1, g0, g1 = ev[i]
+            e0.record(stream)
+            launches += step(g0, g1)
+            e1.record(stream)
+        torch.cuda.synchronize()
+    step_ms = [a.elapsed_time(b) for a, b, _, _ in ev]
+    gu_ms = [a.elapsed_time(b) for _, _, a, b in ev]
+    total_ms = sum(step_ms)
+    if world > 1:
+        t = torch.tensor([total_ms], device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        total_ms = float(t.item())
+    e = int(err.item())
+    if e:
+        raise RuntimeError(f"device error word {e:#x}")
+
+    # end-to-end through the host-buffer entry point (copies inside the timed region)
+    wsh = M.workspace(layer, wl.act, T, k, host=True, device=dev)
+    xh, idh, wh = x.cpu().pin_memory(), ids.cpu().pin_memory(), w.cpu().pin_memory()
+    outh = torch.empty((T, wl.H), dtype=torch.bfloat16).pin_memory()
+    for _ in range(max(1, args.warmup)):
+        M.mnw_moe_forward_host(layer, wl.act, xh, idh, wh, wsh, outh)
+    e2e_ms = []
+    for _ in range(args.steps):
+        flush.zero_()
+        torch.cuda.synchronize()
+        t0 = time.perf_counter()
+        M.mnw_moe_forward_host(layer, wl.act, xh, idh, wh, wsh, outh)
+        e2e_ms.append((time.perf_counter() - t0) * 1e3)
+
+    touched = int(torch.unique(ids[(ids >= 0) & (ids < E)]).numel())
+    return dict(total_ms=total_ms, step_ms=step_ms, gu_ms=gu_ms, launches=launches, world=world, rank=rank,
+                clocks=clk.summary(), e2e_ms=e2e_ms, touched=touched, ids=ids)
+
+
+def cpu_sample_tokens(wl: S.Workload, budget_s: float):
+    """How many tokens of the workload the oracle runs in about budget_s seconds."""
+    macs_per_token = 3 * wl.H * wl.I * wl.k
+    rate = 6.0e7 if wl.wfmt != S.FMT_BF16 else 1.0e8  # oracle MAC/s (single thread, with decode)
+    return max(1, min(wl.T, int(budget_s * rate / macs_per_token)))
+
+
+def run_oracle_sample(wl: S.Workload, ntok: int, inputs=None):
+    import oracle
+    if inputs is None:
+        x, ids, w, blob, hdr, L = S.make_inputs(wl, device="cuda" if torch.cuda.is_available() else "cpu")
+    else:
+        x, ids, w, blob = inputs
+    rows = np.linspace(0, wl.T - 1, ntok).astype(np.int32)
+    b = blob.cpu().numpy()
+    xb, idn, wn = S.bf16_bits_np(x), ids.cpu().numpy(), w.cpu().numpy()
+    t0 = time.perf_counter()
+    oracle.moe_forward(b, wl.act, xb, idn, wn, rows=rows)
+    dt = time.perf_counter() - t0
+    return ntok / dt, dt
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--workload", default="decode_w4a16", choices=sorted(S.WORKLOADS))
+    ap.add_argument("--cpu-budget", type=float, default=15.0, help="seconds of oracle time for cpu_baseline")
+    args = ap.parse_args()
+    wl = S.WORKLOADS[args.workload]
+    world, rank, local = _dist()
+    if world > 1 and not torch.distributed.is_initialized():
+        torch.distributed.init_process_group("nccl" if torch.cuda.is_available() else "gloo")
+    config = {"workload": wl.name, "T": wl.T, "H": wl.H, "E": wl.E, "I": wl.I, "k": wl.k,
+              "weights": ["bf16", "int8_g128", "int4_g128", "nvfp4_g16"][wl.wfmt],
+              "activations": ["bf16", "int8_g128", "nvfp4_g16"][wl.act], "routing": wl.routing,
+              "l2": "flushed between timed steps (2x L2 buffer written outside the events)"}
+
+    if args.impl == "reference":
+        if rank != 0:
+            return
+        per_step = max(2.0, min(20.0, 120.0 / max(1, args.steps + args.warmup)))
+        ntok = cpu_sample_tokens(wl, per_step)
+        x, ids, w, blob, hdr, L = S.make_inputs(wl, device="cuda" if torch.cuda.is_available() else "cpu")
+        inputs = (x, ids, w, blob)
+        for _ in range(min(args.warmup, 1)):
+            run_oracle_sample(wl, max(1, ntok // 4), inputs)
+        rates, times = [], []
+        for _ in range(args.steps):
+            r, dt = run_oracle_sample(wl, ntok, inputs)
+            rates.append(r)
+            times.append(dt)
+        value = statistics.median(rates)
+        sample = f"{ntok} of {wl.T} tokens per step (token-by-token oracle, evenly spaced rows)"
+        print(json.dumps({
+            "impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": args.gpus,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": statistics.median(times) * 1e3,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic", "config": config,
+            "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": 1, "kind": "oracle", "sample": sample},
+            "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}))
+        return
+
+    r = run_ours(args, wl)
+    if rank != 0:
+        return
+    hbm, bf16_peak, peak_kind = _peaks()
+    ms = r["total_ms"] / args.steps
+    value = r["world"] * wl.T / (r["total_ms"] / args.steps / 1e3)
+    gu_ms = statistics.mean(r["gu_ms"])
+    gu_bytes = gate_up_bytes(wl, r["touched"])
+    achieved = gu_bytes / (gu_ms / 1e3) / 1e9
+    layer_bytes = S.algorithmic_bytes(wl, r["ids"].cpu())
+    e2e_ms = statistics.median(r["e2e_ms"])
+    h2d = wl.T * wl.H * 2 + wl.P * 4 * 2
+    d2h = wl.T * wl.H * 2
+
+    # CPU baseline: the oracle on a bounded token sample, rank 0 only
+    ntok = cpu_sample_tokens(wl, args.cpu_budget)
+    cpu_rate, cpu_dt = run_oracle_sample(wl, ntok)
+
+    profile_traffic = None
+    try:
+        with open(os.path.join(ROOT, "profiles", "traffic.json")) as f:
+            profile_traffic = json.load(f).get(f"{wl.name}:gate_up")
+    except Exception:
+        pass
+    dtype = {S.ACT_BF16: "bf16", S.ACT_INT8_G128: "int8xint8->f32 (f16 MMA)",
+             S.ACT_NVFP4_G16: "e2m1xe2m1->f32 (f16 MMA)"}[wl.act]
+    line = {
+        "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": r["world"], "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": dtype, "data": "synthetic (seeded, shapes of the workload)",
+        "config": config,
+        "layer_effective_gbs": layer_bytes / (ms / 1e3) / 1e9,
+        "roofline": {"kernel": "grouped gate/up/SiLU GEMM", "bound": "hbm", "achieved": achieved, "peak": hbm,
+                     "unit": "GB/s", "frac": achieved / hbm, "peak_kind": peak_kind,
+                     "bytes_per_launch": gu_bytes, "launch_ms": gu_ms, "traffic": profile_traffic},
+        "cpu_baseline": {"value": cpu_rate, "unit": "tokens/s", "cores": 1, "kind": "oracle",
+                         "sample": f"{ntok} of {wl.T} tokens, {cpu_dt:.1f} s single-threaded"},
+        "e2e": {"value": wl.T / (e2e_ms / 1e3), "unit": "tokens/s", "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h},
+        "gpu_launches": r["launches"],
+        "clocks": r["clocks"],
+    }
+    print(json.dumps(line))
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,212 @@
+/*
+ * mnw_moe.h -- C ABI of the GB300 (sm_103a) routed-expert MoE layer.
+ *
+ * The layer: every token t has k routed experts ids[t, 0..k) with routing
+ * weights w[t, 0..k).  Each expert e is a SwiGLU feed-forward block,
+ *   h = SiLU(x . Wg[e]^T) * (x . Wu[e]^T)      Wg, Wu: [I, H]
+ *   y = h . Wd[e]^T                             Wd: [H, I]
+ * and out[t] = sum_j w[t, j] * y(t, j).  The expert matrices are stored in one
+ * of the quantised formats of the "LLaDA2.2-flash-minnow" model card,
+ * section "Checkpoints and precision" (precision table): BF16; signed INT8 or
+ * signed INT4 with one FP16 scale per 128 weights; NVFP4 (E2M1 values, E4M3
+ * scale per 16, FP32 outer scale per expert matrix).  The "coder543/minnow"
+ * README, section "Quantization", gives the execution modes: INT4/INT8
+ * weights dequantised to BF16 (W4A16/W8A16); the optional INT8 activation
+ * mode (W4A8/W8A8: activations quantised per group of 128 with an FP32 scale,
+ * INT32 group dot products, scales applied in FP32); NVFP4 W4A4 with
+ * activations quantised to E2M1 / E4M3-per-16 / FP32-per-row; fused
+ * gate/up/SiLU kernels and GPU routing for 32-token decode blocks.
+ *
+ * Conventions for every call below
+ *  - Pointers marked "device" are CUDA device pointers owned by the caller;
+ *    the library never allocates, frees or keeps them.  Device buffers must be
+ *    16-byte aligned; the expert blob must be 256-byte aligned.
+ *  - Work is enqueued on `stream` and the call returns without synchronising,
+ *    except mnw_moe_read_error() and mnw_moe_forward_host(), which say so.
+ *  - BF16 tensors are row-major arrays of 16-bit bfloat16 values.
+ *  - A return value other than MNW_OK means nothing was enqueued.  Errors that
+ *    only the device can see (an expert id outside [0, E), a wait that ran out)
+ *    are OR-ed into a caller-provided 32-bit device error word (MNW_DEVERR_*)
+ *    that the caller zeroes beforehand and reads with mnw_moe_read_error().
+ *  - Results are deterministic: no floating-point atomics.
+ *
+ * Expert blob layout (defined by this library; little-endian):
+ *   bytes [0, 256): header.  char[4] "MNWB"; u32 version = 1; u32 wfmt
+ *   (mnw_wfmt); u32 E; u32 H; u32 I; u32 group (0 BF16, 128 INT8/INT4, 16
+ *   NVFP4); u32 header_bytes = 256; u64 data_offset; u64 expert_stride;
+ *   u64 codes_off[3]; u64 scales_off[3]; u64 outer_off[3] (gate, up, down,
+ *   relative to the expert's start); u64 total_bytes; zero padding; u32
+ *   CRC-32 (IEEE 802.3) of bytes [0, 252) stored at byte 252.
+ *   Expert e starts at data_offset + e * expert_stride (a multiple of 256).
+ *   Each matrix [N][K] (gate/up: N = I, K = H; down: N = H, K = I) is stored
+ *   row-major, K fastest, every section 256-byte aligned:
+ *     BF16:  u16 codes [N][K]
+ *     INT8:  i8 codes [N][K];   f16 scales [N][K/128]
+ *     INT4:  u8 codes [N][K/2] (element 2c in the low nibble of byte c);
+ *            f16 scales [N][K/128]
+ *     NVFP4: u8 codes [N][K/2] (same nibble order); E4M3 scales [N][K/16];
+ *            f32 outer scale (one per matrix)
+ *   H and I must be multiples of 128 (INT4 and NVFP4: multiples of 256).
+ */
+#ifndef MNW_MOE_H
+#define MNW_MOE_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* A CUDA stream (cudaStream_t); 0 is the legacy default stream. */
+typedef void* mnw_stream;
+
+enum mnw_status {
+  MNW_OK = 0,
+  MNW_E_INVALID_ARG = 1,        /* null/misaligned pointer, negative size, bad enum */
+  MNW_E_UNSUPPORTED = 2,        /* shape outside what the kernels support */
+  MNW_E_BAD_BLOB = 3,           /* header magic/version/CRC/sizes do not check out */
+  MNW_E_WORKSPACE_TOO_SMALL = 4,
+  MNW_E_CUDA = 5,               /* a CUDA runtime call failed */
+  MNW_E_MODE = 6                /* activation mode not allowed for the weight format */
+};
+
+/* Bits of the device error word. */
+#define MNW_DEVERR_BAD_EXPERT_ID 0x1u  /* an id outside [0, E); that assignment was dropped */
+#define MNW_DEVERR_TIMEOUT 0x2u        /* a kernel-internal wait ran out; its output is invalid */
+
+enum mnw_wfmt { MNW_FMT_BF16 = 0, MNW_FMT_INT8_G128 = 1, MNW_FMT_INT4_G128 = 2, MNW_FMT_NVFP4_G16 = 3 };
+enum mnw_afmt { MNW_ACT_BF16 = 0, MNW_ACT_INT8_G128 = 1, MNW_ACT_NVFP4_G16 = 2 };
+enum mnw_kind { MNW_KIND_GATE_UP = 0, MNW_KIND_DOWN = 1 };
+
+typedef struct mnw_moe_layer mnw_moe_layer;
+
+/* Human-readable name of a status code (static storage). */
+const char* mnw_status_string(int status);
+
+/* Describe an expert blob.  `header_host` is a host copy of the blob's first
+ * 256 bytes; `blob_dev` the whole blob in device memory (borrowed, not
+ * copied; it must outlive the layer).  Validates magic, version, CRC and the
+ * section sizes against `blob_bytes`.  On success *out is a host object
+ * released by mnw_moe_layer_destroy(). */
+int mnw_moe_layer_init(const void* header_host, const void* blob_dev, size_t blob_bytes,
+                       mnw_moe_layer** out);
+void mnw_moe_layer_destroy(mnw_moe_layer* layer);
+/* Shape of a layer: any output pointer may be NULL. */
+int mnw_moe_layer_info(const mnw_moe_layer* layer, int* wfmt, int* E, int* H, int* I);
+
+/* a1 -- token permutation ("GPU routing", minnow README, "Quantization").
+ * ids: device int32 [T*k], assignment a = t*k + j goes to expert ids[a].
+ * Writes (device): expert_offsets int32 [E+1] (exclusive prefix of the
+ * per-expert counts; expert_offsets[E] = number of valid assignments),
+ * sorted_assign int32 [T*k] (sorted_assign[p] = a; slots past the valid count
+ * hold -1), assign_pos int32 [T*k] (inverse map; -1 for a dropped id).
+ * Positions are stable: within an expert, assignments keep increasing a.
+ * If x (device bf16 [T, H]) and x_perm (device bf16 [T*k, H]) are both
+ * non-NULL, also gathers x_perm[p] = x[sorted_assign[p] / k] (zeros where
+ * sorted_assign[p] is -1).  An id outside [0, E) sets MNW_DEVERR_BAD_EXPERT_ID
+ * in *err (device, may be NULL) and is dropped.  Limits: 1 <= k <= 32,
+ * 1 <= E <= 1024, T*k <= 2^24.  T = 0 is a no-op. */
+int mnw_moe_permute(const int32_t* ids, int T, int k, int E, int32_t* expert_offsets,
+                    int32_t* sorted_assign, int32_t* assign_pos, const void* x, int H,
+                    void* x_perm, uint32_t* err, mnw_stream stream);
+
+/* a2 -- dynamic activation quantisation of R rows of K BF16 values.
+ * Row r reads x[src] with src = r, or, when row_index (device int32 [R]) is
+ * non-NULL, src = row_index[r] / index_div (a negative row_index gives a
+ * zero row).  act = MNW_ACT_INT8_G128 ("LLaDA2.2-flash-minnow" model card,
+ * W8A8 paragraph): per 128 values, scale = amax / 127 (FP32),
+ * code = clamp(rne(x / scale), -127, 127); codes int8 [R, K], scales f32
+ * [R, K/128]; row_outer unused.  act = MNW_ACT_NVFP4_G16 (model card, NVFP4
+ * row): outer = amax_row / 2688; per 16 values sb = e4m3_rn_satfinite(
+ * (amax_block / outer) / 6), code = e2m1_rn_satfinite(x / (sb * outer));
+ * codes u8 [R, K/2] (even element in the low nibble), scales E4M3 u8
+ * [R, K/16], row_outer f32 [R].  Every step is one IEEE binary32 operation
+ * with round-to-nearest-even; the results are bit-exact.  K must be a
+ * multiple of 128 (INT8) or 16 (NVFP4). */
+int mnw_moe_quantize_act(int act, const void* x, int R, int K, const int32_t* row_index,
+                         int index_div, void* codes, void* scales, float* row_outer,
+                         mnw_stream stream);
+
+/* a3/a4/a6 -- grouped expert GEMMs.  Rows [expert_offsets[e],
+ * expert_offsets[e+1]) of the activation operand belong to expert e
+ * (expert_offsets: device int32 [E+1], as written by mnw_moe_permute).
+ * kind = MNW_KIND_GATE_UP: K = H, out (device bf16 [P, I]) =
+ *   bf16(SiLU(a . Wg^T) * (a . Wu^T)), the gate/up/SiLU fusion of the minnow
+ *   README, "Quantization".
+ * kind = MNW_KIND_DOWN: K = I, out (device bf16 [P, H]) = bf16(a . Wd^T).
+ * Accumulation is FP32 on the tensor cores.
+ *
+ * bf16 / w8a16 / w4a16: a is device bf16 [P, K]; the weights (BF16, INT8 or
+ * INT4 with FP16 group scales) are dequantised on chip on their way into the
+ * BF16 tensor cores, with no expanded copy in memory ("LLaDA2.2-flash-minnow"
+ * model card, paragraph after the precision table).  INT codes enter as exact
+ * BF16 integers; each 128-wide group's dot product is scaled by its FP16
+ * scale and summed in FP32. */
+int mnw_moe_grouped_gemm_bf16(const mnw_moe_layer* layer, int kind, const void* a,
+                              const int32_t* expert_offsets, int P, void* out, uint32_t* err,
+                              mnw_stream stream);
+int mnw_moe_grouped_gemm_w8a16(const mnw_moe_layer* layer, int kind, const void* a,
+                               const int32_t* expert_offsets, int P, void* out, uint32_t* err,
+                               mnw_stream stream);
+int mnw_moe_grouped_gemm_w4a16(const mnw_moe_layer* layer, int kind, const void* a,
+                               const int32_t* expert_offsets, int P, void* out, uint32_t* err,
+                               mnw_stream stream);
+/* w8a8 / w4a8 (model card, W8A8/W4A8 paragraph): a_codes device int8 [P, K]
+ * and a_scales device f32 [P, K/128] from mnw_moe_quantize_act(INT8_G128).
+ * For every 128-wide group g the exact integer dot product D_g of the codes is
+ * formed, then out accumulates (s_w * s_a) * D_g in FP32.  group_dots (device
+ * int32, may be NULL) receives every D_g, layout [P][C][K/128] with
+ * C = 2*I (gate columns, then up columns) or H: a test hook. */
+int mnw_moe_grouped_gemm_w8a8(const mnw_moe_layer* layer, int kind, const int8_t* a_codes,
+                              const float* a_scales, const int32_t* expert_offsets, int P,
+                              void* out, int32_t* group_dots, uint32_t* err, mnw_stream stream);
+int mnw_moe_grouped_gemm_w4a8(const mnw_moe_layer* layer, int kind, const int8_t* a_codes,
+                              const float* a_scales, const int32_t* expert_offsets, int P,
+                              void* out, int32_t* group_dots, uint32_t* err, mnw_stream stream);
+/* nvfp4 (model card, NVFP4 row): a_codes device u8 [P, K/2], a_sf device
+ * E4M3 u8 [P, K/16], a_outer device f32 [P] from
+ * mnw_moe_quantize_act(NVFP4_G16).  out = sum of block-scaled products times
+ * outer_w[e] * a_outer[p]. */
+int mnw_moe_grouped_gemm_nvfp4(const mnw_moe_layer* layer, int kind, const uint8_t* a_codes,
+                               const uint8_t* a_sf, const float* a_outer,
+                               const int32_t* expert_offsets, int P, void* out, uint32_t* err,
+                               mnw_stream stream);
+
+/* a5 -- combine: out[t] = bf16(sum_j w[t, j] * y[assign_pos[t*k + j]]) with
+ * FP32 accumulation in ascending j; assignments with assign_pos < 0 are
+ * skipped.  y: device bf16 [P, H]; assign_pos: device int32 [T*k];
+ * w: device f32 [T, k]; out: device bf16 [T, H].  H % 8 == 0. */
+int mnw_moe_combine(const void* y, const int32_t* assign_pos, const float* w, int T, int k,
+                    int H, void* out, mnw_stream stream);
+
+/* The whole layer: permute -> (quantise x) -> gate/up/SiLU -> (quantise h)
+ * -> down -> combine, all on `stream`, with every intermediate in `ws`
+ * (device, at least mnw_moe_workspace_size() bytes, 256-byte aligned).  act
+ * must suit the weight format: BF16 for BF16/INT8/INT4 weights, INT8_G128
+ * for INT8/INT4 weights, NVFP4_G16 for NVFP4 weights.  x: device bf16
+ * [T, H]; ids: device int32 [T, k]; w: device f32 [T, k]; out: device bf16
+ * [T, H].  The device error word is the first 4 bytes of ws
+ * (mnw_moe_workspace_error_word); it is cleared by this call. */
+size_t mnw_moe_workspace_size(const mnw_moe_layer* layer, int act, int T, int k);
+int mnw_moe_forward(const mnw_moe_layer* layer, int act, const void* x, const int32_t* ids,
+                    const float* w, int T, int k, void* out, void* ws, size_t ws_bytes,
+                    mnw_stream stream);
+uint32_t* mnw_moe_workspace_error_word(void* ws);
+
+/* The whole layer from and to HOST buffers (pinned memory gives overlap):
+ * copies x, ids, w into ws, runs mnw_moe_forward, copies out back and
+ * synchronises `stream`.  ws must hold mnw_moe_workspace_size_host() bytes.
+ * Returns MNW_E_CUDA if the device error word is non-zero afterwards. */
+size_t mnw_moe_workspace_size_host(const mnw_moe_layer* layer, int act, int T, int k);
+int mnw_moe_forward_host(const mnw_moe_layer* layer, int act, const void* x_host,
+                         const int32_t* ids_host, const float* w_host, int T, int k,
+                         void* out_host, void* ws, size_t ws_bytes, mnw_stream stream);
+
+/* Synchronise `stream`, then copy the device error word to *out_host. */
+int mnw_moe_read_error(const uint32_t* err, uint32_t* out_host, mnw_stream stream);
+
+#ifdef __cplusplus
+}
+#endif
+#endif

@@ -1,0 +1,415 @@
+// mnw_api.cu -- the C ABI of include/mnw_moe.h: argument checks, the expert
+// blob header, workspace layout and the whole-layer orchestration.  No call
+// here synchronises except mnw_moe_read_error() and mnw_moe_forward_host().
+#include <cudaTypedefs.h>
+
+#include <cstring>
+#include <mutex>
+
+#include "mnw_internal.h"
+
+namespace mnw {
+
+// ---- tensor maps ------------------------------------------------------------
+
+static PFN_cuTensorMapEncodeTiled_v12000 get_encode() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  });
+  return fn;
+}
+
+bool encode_map(CUtensorMap* map, CUtensorMapDataType dtype, int rank, const void* base, const uint64_t* dims,
+                const uint64_t* strides_bytes, const uint32_t* box, CUtensorMapSwizzle swizzle) {
+  auto fn = get_encode();
+  if (!fn) return false;
+  cuuint64_t d[5], s[4];
+  cuuint32_t b[5], es[5];
+  for (int i = 0; i < rank; ++i) {
+    d[i] = dims[i];
+    b[i] = box[i];
+    es[i] = 1;
+    if (i < rank - 1) s[i] = strides_bytes[i];
+  }
+  CUresult r = fn(map, dtype, rank, const_cast<void*>(base), d, s, b, es, CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle,
+                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+// ---- blob header ------------------------------------------------------------
+
+static uint32_t rd32(const uint8_t* p) {
+  return static_cast<uint32_t>(p[0]) | (static_cast<uint32_t>(p[1]) << 8) | (static_cast<uint32_t>(p[2]) << 16) |
+         (static_cast<uint32_t>(p[3]) << 24);
+}
+static uint64_t rd64(const uint8_t* p) { return rd32(p) | (static_cast<uint64_t>(rd32(p + 4)) << 32); }
+
+// CRC-32, reflected polynomial 0xEDB88320, table driven.
+static uint32_t crc32(const uint8_t* p, size_t n) {
+  static uint32_t table[256];
+  static std::once_flag once;
+  std::call_once(once, [] {
+    for (uint32_t i = 0; i < 256; ++i) {
+      uint32_t c = i;
+      for (int k = 0; k < 8; ++k) c = (c & 1) ? 0xEDB88320u ^ (c >> 1) : c >> 1;
+      table[i] = c;
+    }
+  });
+  uint32_t c = 0xFFFFFFFFu;
+  for (size_t i = 0; i < n; ++i) c = table[(c ^ p[i]) & 0xFF] ^ (c >> 8);
+  return c ^ 0xFFFFFFFFu;
+}
+
+static uint64_t code_bytes(int wfmt, uint64_t N, uint64_t K) {
+  switch (wfmt) {
+    case MNW_FMT_BF16: return N * K * 2;
+    case MNW_FMT_INT8_G128: return N * K;
+    default: return N * K / 2;
+  }
+}
+static uint64_t scale_bytes(int wfmt, uint64_t N, uint64_t K) {
+  switch (wfmt) {
+    case MNW_FMT_INT8_G128:
+    case MNW_FMT_INT4_G128: return N * (K / 128) * 2;
+    case MNW_FMT_NVFP4_G16: return N * (K / 16);
+    default: return 0;
+  }
+}
+
+static bool act_allowed(int wfmt, int act) {
+  if (act == MNW_ACT_BF16) return wfmt != MNW_FMT_NVFP4_G16;
+  if (act == MNW_ACT_INT8_G128) return wfmt == MNW_FMT_INT8_G128 || wfmt == MNW_FMT_INT4_G128;
+  if (act == MNW_ACT_NVFP4_G16) return wfmt == MNW_FMT_NVFP4_G16;
+  return false;
+}
+
+// ---- workspace layout ----------------------------------------------------------
+
+struct WsLayout {
+  size_t err, offsets, sorted, pos;
+  size_t xa, xb, xc;   // x operand: bf16 rows | codes, scales, outer
+  size_t h, ha, hb, hc;
+  size_t y;
+  size_t hx, hids, hw, hout;  // staging for the host-buffer entry point
+  size_t total, total_host;
+};
+
+static size_t al(size_t x) { return (x + 255) / 256 * 256; }
+
+static WsLayout ws_layout(const mnw_moe_layer* L, int act, int T, int k) {
+  WsLayout w{};
+  const size_t P = static_cast<size_t>(T) * k, H = L->H, I = L->I, E = L->E;
+  size_t o = 0;
+  w.err = o; o += 256;
+  w.offsets = o; o = al(o + (E + 1) * 4);
+  w.sorted = o; o = al(o + P * 4);
+  w.pos = o; o = al(o + P * 4);
+  if (act == MNW_ACT_BF16) {
+    w.xa = o; o = al(o + P * H * 2);
+  } else if (act == MNW_ACT_INT8_G128) {
+    w.xa = o; o = al(o + P * H);
+    w.xb = o; o = al(o + P * (H / 128) * 4);
+  } else {
+    w.xa = o; o = al(o + P * H / 2);
+    w.xb = o; o = al(o + P * H / 16);
+    w.xc = o; o = al(o + P * 4);
+  }
+  w.h = o; o = al(o + P * I * 2);
+  if (act == MNW_ACT_INT8_G128) {
+    w.ha = o; o = al(o + P * I);
+    w.hb = o; o = al(o + P * (I / 128) * 4);
+  } else if (act == MNW_ACT_NVFP4_G16) {
+    w.ha = o; o = al(o + P * I / 2);
+    w.hb = o; o = al(o + P * I / 16);
+    w.hc = o; o = al(o + P * 4);
+  }
+  w.y = o; o = al(o + P * H * 2);
+  w.total = o;
+  w.hx = o; o = al(o + static_cast<size_t>(T) * H * 2);
+  w.hids = o; o = al(o + P * 4);
+  w.hw = o; o = al(o + P * 4);
+  w.hout = o; o = al(o + static_cast<size_t>(T) * H * 2);
+  w.total_host = o;
+  return w;
+}
+
+static int gemm_for(const mnw_moe_layer* L, int act, int kind, const void* a0, const void* a1, const void* a2,
+                    const int32_t* offsets, int P, void* out, uint32_t* err, cudaStream_t st) {
+  return run_gemm(L, L->wfmt, act, kind, a0, a1, a2, offsets, P, out, nullptr, err, st);
+}
+
+}  // namespace mnw
+
+using namespace mnw;
+
+extern "C" {
+
+const char* mnw_status_string(int status) {
+  switch (status) {
+    case MNW_OK: return "ok";
+    case MNW_E_INVALID_ARG: return "invalid argument";
+    case MNW_E_UNSUPPORTED: return "unsupported shape";
+    case MNW_E_BAD_BLOB: return "bad expert blob";
+    case MNW_E_WORKSPACE_TOO_SMALL: return "workspace too small";
+    case MNW_E_CUDA: return "CUDA error";
+    case MNW_E_MODE: return "activation mode not allowed for this weight format";
+    default: return "unknown status";
+  }
+}
+
+int mnw_moe_layer_init(const void* header_host, const void* blob_dev, size_t blob_bytes, mnw_moe_layer** out) {
+  if (!header_host || !blob_dev || !out) return MNW_E_INVALID_ARG;
+  *out = nullptr;
+  if (!aligned(blob_dev, 256)) return MNW_E_INVALID_ARG;
+  const uint8_t* h = static_cast<const uint8_t*>(header_host);
+  if (std::memcmp(h, "MNWB", 4) != 0 || rd32(h + 4) != 1 || rd32(h + 28) != 256) return MNW_E_BAD_BLOB;
+  if (crc32(h, 252) != rd32(h + 252)) return MNW_E_BAD_BLOB;
+  mnw_moe_layer L{};
+  L.wfmt = static_cast<int>(rd32(h + 8));
+  L.E = static_cast<int>(rd32(h + 12));
+  L.H = static_cast<int>(rd32(h + 16));
+  L.I = static_cast<int>(rd32(h + 20));
+  L.group = static_cast<int>(rd32(h + 24));
+  L.data_offset = rd64(h + 32);
+  L.expert_stride = rd64(h + 40);
+  for (int m = 0; m < 3; ++m) {
+    L.codes_off[m] = rd64(h + 48 + 8 * m);
+    L.scales_off[m] = rd64(h + 72 + 8 * m);
+    L.outer_off[m] = rd64(h + 96 + 8 * m);
+  }
+  const uint64_t total = rd64(h + 120);
+  if (L.wfmt < 0 || L.wfmt > 3 || L.E < 1 || L.E > 1024 || L.H <= 0 || L.I <= 0) return MNW_E_BAD_BLOB;
+  const int want_group[4] = {0, 128, 128, 16};
+  if (L.group != want_group[L.wfmt]) return MNW_E_BAD_BLOB;
+  if (L.H % 128 || L.I % 128) return MNW_E_UNSUPPORTED;
+  // INT4 and NVFP4 stream 256 K values (128 bytes) per row and stage.
+  if ((L.wfmt == MNW_FMT_NVFP4_G16 || L.wfmt == MNW_FMT_INT4_G128) && (L.H % 256 || L.I % 256))
+    return MNW_E_UNSUPPORTED;
+  if (total > blob_bytes || L.data_offset % 256 || L.expert_stride % 256 ||
+      L.data_offset + static_cast<uint64_t>(L.E) * L.expert_stride > total)
+    return MNW_E_BAD_BLOB;
+  L.blob = static_cast<const uint8_t*>(blob_dev);
+  L.blob_bytes = blob_bytes;
+  for (int m = 0; m < 3; ++m) {
+    const uint64_t N = m == 2 ? L.H : L.I, K = m == 2 ? L.I : L.H;
+    if (L.codes_off[m] % 256 || L.codes_off[m] + code_bytes(L.wfmt, N, K) > L.expert_stride) return MNW_E_BAD_BLOB;
+    if (scale_bytes(L.wfmt, N, K) &&
+        (L.scales_off[m] % 256 || L.scales_off[m] + scale_bytes(L.wfmt, N, K) > L.expert_stride))
+      return MNW_E_BAD_BLOB;
+    if (L.wfmt == MNW_FMT_NVFP4_G16 && (L.outer_off[m] % 4 || L.outer_off[m] + 4 > L.expert_stride))
+      return MNW_E_BAD_BLOB;
+  }
+  if (cudaGetDevice(&L.device) != cudaSuccess) return MNW_E_CUDA;
+  if (cudaDeviceGetAttribute(&L.num_sms, cudaDevAttrMultiProcessorCount, L.device) != cudaSuccess)
+    return MNW_E_CUDA;
+  // Weight tensor maps: every expert's matrix m seen as one 3-D tensor [E][N][row].
+  const uint8_t* experts = L.blob + L.data_offset;
+  for (int m = 0; m < 3; ++m) {
+    const uint64_t N = m == 2 ? L.H : L.I, K = m == 2 ? L.I : L.H;
+    bool ok;
+    if (L.wfmt == MNW_FMT_BF16) {
+      const uint64_t dims[3] = {K, N, static_cast<uint64_t>(L.E)};
+      const uint64_t strides[2] = {K * 2, L.expert_stride};
+      const uint32_t box[3] = {64, 128, 1};
+      ok = encode_map(&L.tm_codes[m], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, experts + L.codes_off[m], dims, strides,
+                      box, CU_TENSOR_MAP_SWIZZLE_128B);
+    } else {
+      const uint64_t row = code_bytes(L.wfmt, 1, K);
+      const uint64_t dims[3] = {row, N, static_cast<uint64_t>(L.E)};
+      const uint64_t strides[2] = {row, L.expert_stride};
+      const uint32_t box[3] = {128, 128, 1};
+      ok = encode_map(&L.tm_codes[m], CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, experts + L.codes_off[m], dims, strides, box,
+                      CU_TENSOR_MAP_SWIZZLE_128B);
+    }
+    if (ok && L.wfmt == MNW_FMT_NVFP4_G16) {
+      const uint64_t dims[3] = {K / 16, N, static_cast<uint64_t>(L.E)};
+      const uint64_t strides[2] = {K / 16, L.expert_stride};
+      const uint32_t box[3] = {16, 128, 1};
+      ok = encode_map(&L.tm_sf[m], CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, experts + L.scales_off[m], dims, strides, box,
+                      CU_TENSOR_MAP_SWIZZLE_NONE);
+    }
+    if (!ok) return MNW_E_CUDA;
+  }
+  mnw_moe_layer* p = new (std::nothrow) mnw_moe_layer(L);
+  if (!p) return MNW_E_INVALID_ARG;
+  *out = p;
+  return MNW_OK;
+}
+
+void mnw_moe_layer_destroy(mnw_moe_layer* layer) { delete layer; }
+
+int mnw_moe_layer_info(const mnw_moe_layer* L, int* wfmt, int* E, int* H, int* I) {
+  if (!L) return MNW_E_INVALID_ARG;
+  if (wfmt) *wfmt = L->wfmt;
+  if (E) *E = L->E;
+  if (H) *H = L->H;
+  if (I) *I = L->I;
+  return MNW_OK;
+}
+
+int mnw_moe_permute(const int32_t* ids, int T, int k, int E, int32_t* expert_offsets, int32_t* sorted_assign,
+                    int32_t* assign_pos, const void* x, int H, void* x_perm, uint32_t* err, mnw_stream stream) {
+  if (T < 0 || k < 1 || k > 32 || E < 1 || E > 1024) return MNW_E_INVALID_ARG;
+  if (static_cast<long long>(T) * k > (1LL << 24)) return MNW_E_UNSUPPORTED;
+  if (T == 0) return MNW_OK;
+  if (!ids || !expert_offsets || !sorted_assign || !assign_pos) return MNW_E_INVALID_ARG;
+  if ((x == nullptr) != (x_perm == nullptr)) return MNW_E_INVALID_ARG;
+  if (x && (H <= 0 || H % 8 || !aligned(x, 16) || !aligned(x_perm, 16))) return MNW_E_INVALID_ARG;
+  cudaError_t e = launch_permute(ids, T, k, E, expert_offsets, sorted_assign, assign_pos, x, H, x_perm, err,
+                                 static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? MNW_OK : MNW_E_CUDA;
+}
+
+int mnw_moe_quantize_act(int act, const void* x, int R, int K, const int32_t* row_index, int index_div, void* codes,
+                         void* scales, float* row_outer, mnw_stream stream) {
+  if (R < 0 || K <= 0) return MNW_E_INVALID_ARG;
+  if (act == MNW_ACT_INT8_G128) {
+    if (K % 128) return MNW_E_UNSUPPORTED;
+  } else if (act == MNW_ACT_NVFP4_G16) {
+    if (K % 16) return MNW_E_UNSUPPORTED;
+    if (!row_outer || !aligned(row_outer, 4)) return MNW_E_INVALID_ARG;
+  } else {
+    return MNW_E_INVALID_ARG;
+  }
+  if (row_index && index_div < 1) return MNW_E_INVALID_ARG;
+  if (R == 0) return MNW_OK;
+  if (!x || !codes || !scales || !aligned(x, 16) || !aligned(codes, 16) || !aligned(scales, 4))
+    return MNW_E_INVALID_ARG;
+  cudaError_t e = launch_quantize(act, x, R, K, row_index, index_div, codes, scales, row_outer,
+                                  static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? MNW_OK : MNW_E_CUDA;
+}
+
+int mnw_moe_grouped_gemm_bf16(const mnw_moe_layer* L, int kind, const void* a, const int32_t* offs, int P, void* out,
+                              uint32_t* err, mnw_stream stream) {
+  return run_gemm(L, MNW_FMT_BF16, MNW_ACT_BF16, kind, a, nullptr, nullptr, offs, P, out, nullptr, err,
+                  static_cast<cudaStream_t>(stream));
+}
+int mnw_moe_grouped_gemm_w8a16(const mnw_moe_layer* L, int kind, const void* a, const int32_t* offs, int P, void* out,
+                               uint32_t* err, mnw_stream stream) {
+  return run_gemm(L, MNW_FMT_INT8_G128, MNW_ACT_BF16, kind, a, nullptr, nullptr, offs, P, out, nullptr, err,
+                  static_cast<cudaStream_t>(stream));
+}
+int mnw_moe_grouped_gemm_w4a16(const mnw_moe_layer* L, int kind, const void* a, const int32_t* offs, int P, void* out,
+                               uint32_t* err, mnw_stream stream) {
+  return run_gemm(L, MNW_FMT_INT4_G128, MNW_ACT_BF16, kind, a, nullptr, nullptr, offs, P, out, nullptr, err,
+                  static_cast<cudaStream_t>(stream));
+}
+int mnw_moe_grouped_gemm_w8a8(const mnw_moe_layer* L, int kind, const int8_t* q, const float* s, const int32_t* offs,
+                              int P, void* out, int32_t* dots, uint32_t* err, mnw_stream stream) {
+  return run_gemm(L, MNW_FMT_INT8_G128, MNW_ACT_INT8_G128, kind, q, s, nullptr, offs, P, out, dots, err,
+                  static_cast<cudaStream_t>(stream));
+}
+int mnw_moe_grouped_gemm_w4a8(const mnw_moe_layer* L, int kind, const int8_t* q, const float* s, const int32_t* offs,
+                              int P, void* out, int32_t* dots, uint32_t* err, mnw_stream stream) {
+  return run_gemm(L, MNW_FMT_INT4_G128, MNW_ACT_INT8_G128, kind, q, s, nullptr, offs, P, out, dots, err,
+                  static_cast<cudaStream_t>(stream));
+}
+int mnw_moe_grouped_gemm_nvfp4(const mnw_moe_layer* L, int kind, const uint8_t* c, const uint8_t* sf, const float* o,
+                               const int32_t* offs, int P, void* out, uint32_t* err, mnw_stream stream) {
+  return run_gemm(L, MNW_FMT_NVFP4_G16, MNW_ACT_NVFP4_G16, kind, c, sf, o, offs, P, out, nullptr, err,
+                  static_cast<cudaStream_t>(stream));
+}
+
+int mnw_moe_combine(const void* y, const int32_t* assign_pos, const float* w, int T, int k, int H, void* out,
+                    mnw_stream stream) {
+  if (T < 0 || k < 1 || k > 32 || H <= 0 || H % 8) return MNW_E_INVALID_ARG;
+  if (T == 0) return MNW_OK;
+  if (!y || !assign_pos || !w || !out || !aligned(y, 16) || !aligned(out, 16)) return MNW_E_INVALID_ARG;
+  cudaError_t e = launch_combine(y, assign_pos, w, T, k, H, out, static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? MNW_OK : MNW_E_CUDA;
+}
+
+size_t mnw_moe_workspace_size(const mnw_moe_layer* L, int act, int T, int k) {
+  if (!L || T < 0 || k < 1) return 0;
+  return ws_layout(L, act, T, k).total;
+}
+size_t mnw_moe_workspace_size_host(const mnw_moe_layer* L, int act, int T, int k) {
+  if (!L || T < 0 || k < 1) return 0;
+  return ws_layout(L, act, T, k).total_host;
+}
+uint32_t* mnw_moe_workspace_error_word(void* ws) { return static_cast<uint32_t*>(ws); }
+
+int mnw_moe_forward(const mnw_moe_layer* L, int act, const void* x, const int32_t* ids, const float* w, int T, int k,
+                    void* out, void* ws, size_t ws_bytes, mnw_stream stream) {
+  if (!L || T < 0 || k < 1 || k > 32 || k > L->E) return MNW_E_INVALID_ARG;
+  if (!act_allowed(L->wfmt, act)) return MNW_E_MODE;
+  if (T == 0) return MNW_OK;
+  if (!x || !ids || !w || !out || !ws || !aligned(x, 16) || !aligned(out, 16) || !aligned(ws, 256))
+    return MNW_E_INVALID_ARG;
+  const WsLayout W = ws_layout(L, act, T, k);
+  if (ws_bytes < W.total) return MNW_E_WORKSPACE_TOO_SMALL;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  uint8_t* b = static_cast<uint8_t*>(ws);
+  uint32_t* err = reinterpret_cast<uint32_t*>(b + W.err);
+  int32_t* offs = reinterpret_cast<int32_t*>(b + W.offsets);
+  int32_t* sorted = reinterpret_cast<int32_t*>(b + W.sorted);
+  int32_t* pos = reinterpret_cast<int32_t*>(b + W.pos);
+  const int P = T * k, H = L->H, I = L->I;
+  if (cudaMemsetAsync(err, 0, 4, st) != cudaSuccess) return MNW_E_CUDA;
+  int rc;
+  if (act == MNW_ACT_BF16) {
+    rc = mnw_moe_permute(ids, T, k, L->E, offs, sorted, pos, x, H, b + W.xa, err, stream);
+    if (rc) return rc;
+    rc = gemm_for(L, act, MNW_KIND_GATE_UP, b + W.xa, nullptr, nullptr, offs, P, b + W.h, err, st);
+    if (rc) return rc;
+    rc = gemm_for(L, act, MNW_KIND_DOWN, b + W.h, nullptr, nullptr, offs, P, b + W.y, err, st);
+    if (rc) return rc;
+  } else {
+    rc = mnw_moe_permute(ids, T, k, L->E, offs, sorted, pos, nullptr, 0, nullptr, err, stream);
+    if (rc) return rc;
+    float* xo = act == MNW_ACT_NVFP4_G16 ? reinterpret_cast<float*>(b + W.xc) : nullptr;
+    float* ho = act == MNW_ACT_NVFP4_G16 ? reinterpret_cast<float*>(b + W.hc) : nullptr;
+    rc = mnw_moe_quantize_act(act, x, P, H, sorted, k, b + W.xa, b + W.xb, xo, stream);
+    if (rc) return rc;
+    rc = gemm_for(L, act, MNW_KIND_GATE_UP, b + W.xa, b + W.xb, xo, offs, P, b + W.h, err, st);
+    if (rc) return rc;
+    rc = mnw_moe_quantize_act(act, b + W.h, P, I, nullptr, 1, b + W.ha, b + W.hb, ho, stream);
+    if (rc) return rc;
+    rc = gemm_for(L, act, MNW_KIND_DOWN, b + W.ha, b + W.hb, ho, offs, P, b + W.y, err, st);
+    if (rc) return rc;
+  }
+  return mnw_moe_combine(b + W.y, pos, w, T, k, H, out, stream);
+}
+
+int mnw_moe_forward_host(const mnw_moe_layer* L, int act, const void* x_host, const int32_t* ids_host,
+                         const float* w_host, int T, int k, void* out_host, void* ws, size_t ws_bytes,
+                         mnw_stream stream) {
+  if (!L || T < 0 || k < 1) return MNW_E_INVALID_ARG;
+  if (T == 0) return MNW_OK;
+  if (!x_host || !ids_host || !w_host || !out_host || !ws) return MNW_E_INVALID_ARG;
+  const WsLayout W = ws_layout(L, act, T, k);
+  if (ws_bytes < W.total_host) return MNW_E_WORKSPACE_TOO_SMALL;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  uint8_t* b = static_cast<uint8_t*>(ws);
+  const size_t xb = static_cast<size_t>(T) * L->H * 2, ib = static_cast<size_t>(T) * k * 4;
+  if (cudaMemcpyAsync(b + W.hx, x_host, xb, cudaMemcpyHostToDevice, st) != cudaSuccess ||
+      cudaMemcpyAsync(b + W.hids, ids_host, ib, cudaMemcpyHostToDevice, st) != cudaSuccess ||
+      cudaMemcpyAsync(b + W.hw, w_host, ib, cudaMemcpyHostToDevice, st) != cudaSuccess)
+    return MNW_E_CUDA;
+  int rc = mnw_moe_forward(L, act, b + W.hx, reinterpret_cast<const int32_t*>(b + W.hids),
+                           reinterpret_cast<const float*>(b + W.hw), T, k, b + W.hout, ws, W.total, stream);
+  if (rc) return rc;
+  if (cudaMemcpyAsync(out_host, b + W.hout, xb, cudaMemcpyDeviceToHost, st) != cudaSuccess) return MNW_E_CUDA;
+  uint32_t e = 0;
+  rc = mnw_moe_read_error(reinterpret_cast<const uint32_t*>(b + W.err), &e, stream);
+  if (rc) return rc;
+  return e ? MNW_E_CUDA : MNW_OK;
+}
+
+int mnw_moe_read_error(const uint32_t* err, uint32_t* out_host, mnw_stream stream) {
+  if (!err || !out_host) return MNW_E_INVALID_ARG;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  if (cudaStreamSynchronize(st) != cudaSuccess) return MNW_E_CUDA;
+  if (cudaMemcpy(out_host, err, 4, cudaMemcpyDeviceToHost) != cudaSuccess) return MNW_E_CUDA;
+  return MNW_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,922 @@
+// mnw_gemm.cu -- grouped expert GEMMs on the 5th-generation tensor cores.
+//
+// One persistent kernel template covers every format and mode of the
+// "LLaDA2.2-flash-minnow" model card's precision table (and the activation
+// modes of the coder543/minnow README, "Quantization"):
+//
+//   weights BF16  + activations BF16   (A from smem via TMA,            BF16 MMA)
+//   weights INT8/INT4 + BF16            (codes as exact BF16 integers in TMEM,
+//                                        one accumulator per 128-group, FP16 group
+//                                        scale applied in FP32)
+//   weights INT8/INT4 + INT8 per 128    (codes as exact FP16 integers in TMEM/smem,
+//                                        INT32-exact group dots, FP32 rescale by s_w*s_a)
+//   weights NVFP4 + NVFP4               (block-scaled E2M1 values as exact FP16,
+//                                        outer scales applied in the epilogue)
+//
+// Dequantisation happens in registers on the way into the tensor cores; no
+// expanded weight copy exists in memory.  INT codes are exact in BF16/FP16, so
+// the only rounding in the INT paths is the FP32 accumulation: each 128-wide
+// group's dot product is exact (|D| < 2^24) and is scaled and summed in FP32.
+//
+// Layout of the problem ("swap AB"): the weight matrix supplies the M = 128
+// rows of the MMA (128 output features per tile) and the tokens routed to one
+// expert supply N (16..128 columns).  Decode batches route only a few tokens
+// to each expert, so this keeps the MMA full while the weights stream
+// through once.  A work unit is (expert, token tile of BN rows, 128-feature
+// tile); every CTA walks units blockIdx.x, blockIdx.x + gridDim.x, ... over
+// the device-side tile table built from expert_offsets (no host sync).
+//
+// Warp roles (448 threads):
+//   warp 0      TMA producer: weight tiles (raw codes) + group scales + token tiles
+//   warp 1      MMA issuer (one thread); owns the TMEM allocation
+//   warps 2-9   converters: raw weight codes -> BF16/FP16 operand in TMEM
+//               (tcgen05.st); INT8/FP4 token codes -> FP16 operand in shared memory
+//   warps 10-13 epilogue: TMEM accumulators -> (group rescale) -> SiLU(g)*u or y
+//               -> BF16 global
+//
+// TMEM (512 columns): operand-A ring (slots of 64 K per matrix), then the
+// accumulators; in the grouped modes two per-group accumulators (one drains
+// while the next fills) and the FP32 running sum.  With BF16 weights A never
+// enters TMEM and the accumulators may use all 512 columns.
+//
+// Every wait is bounded (mnw_ptx.cuh); on a timeout all roles leave their
+// loops, outstanding copies and MMAs are drained with a time limit, TMEM is
+// freed and MNW_DEVERR_TIMEOUT is reported through the error word.
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+
+#include <cstdio>
+
+#include "mnw_internal.h"
+#include "mnw_ptx.cuh"
+
+namespace mnw {
+
+enum { WF_BF16 = 0, WF_INT8 = 1, WF_INT4 = 2, WF_NVFP4 = 3 };
+enum { AM_BF16 = 0, AM_INT8 = 1, AM_FP4 = 2 };
+
+constexpr int kBM = 128;
+constexpr int kConvWarps = 8;
+constexpr int kEpiWarps = 4;
+constexpr int kWarpTma = 0, kWarpMma = 1, kWarpConv0 = 2, kWarpEpi0 = kWarpConv0 + kConvWarps;
+constexpr int kThreads = (kWarpEpi0 + kEpiWarps) * 32;
+constexpr int kMaxStages = 8;
+constexpr int kASlots = 4;
+constexpr int kTmemCols = 512;
+
+
+struct GemmArgs {
+  const int32_t* offsets;
+  int E, P, K, N, BN, n_tiles, stages, nmat, acc_slots, acc_base, aslots, sum_base;
+  uint32_t stage_bytes, off_a[2], off_asf[2], off_b, off_braw, off_bsf;
+  uint32_t off_scales, scale_mat_bytes, off_tab, off_sa, off_bars;
+  const uint8_t* experts;
+  uint64_t expert_stride;
+  uint64_t scales_off[2], outer_off[2];
+  const float* a_scales;
+  const float* a_outer;
+  __nv_bfloat16* out;
+  int32_t* dots;
+  uint32_t* err;
+};
+
+struct Bars {
+  uint64_t full[kMaxStages], empty[kMaxStages], bconv[kMaxStages];
+  uint64_t afull[kASlots], aempty[kASlots];
+  uint64_t accfull[2], accempty[2];
+  uint64_t sfull[2], sempty[2];
+  uint64_t final_mma;
+  uint32_t tmem_base;
+  int abort;
+};
+
+template <int WF>
+struct WT {
+  static constexpr int kStage = WF == WF_BF16 ? 64 : (WF == WF_INT8 ? 128 : 256);  // K per stage
+  static constexpr int kSub = kStage / 64;                                          // 64-K sub-chunks
+  static constexpr bool kTs = WF != WF_BF16;                                         // A from TMEM
+  static constexpr bool kScales = WF == WF_INT8 || WF == WF_INT4;                    // FP16 group scales
+};
+
+// ---------------------------------------------------------------------------
+// conversions (register level)
+// ---------------------------------------------------------------------------
+
+__device__ __forceinline__ uint32_t bf16x2_sub(uint32_t a, uint32_t b) {
+  uint32_t d;
+  asm("sub.rn.bf16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+  return d;
+}
+__device__ __forceinline__ uint32_t f16x2_sub(uint32_t a, uint32_t b) {
+  uint32_t d;
+  asm("sub.rn.f16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+  return d;
+}
+__device__ __forceinline__ uint32_t f16x2_mul(uint32_t a, uint32_t b) {
+  uint32_t d;
+  asm("mul.rn.f16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+  return d;
+}
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
+  uint32_t d;
+  asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(d) : "f"(hi), "f"(lo));
+  return d;
+}
+
+// 32 signed INT4 codes (one 16-byte chunk, element 2c in the low nibble of
+// byte c) -> 16 words of (even, odd) pairs holding the integers q exactly, as
+// BF16 (kBf16) or FP16.  The group scale is applied later, in FP32.
+template <bool kBf16>
+__device__ __forceinline__ void cvt_int4x32(const uint4 v, uint32_t (&o)[16]) {
+  const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const uint32_t hi = w[i] >> 4;
+#pragma unroll
+    for (int b = 0; b < 4; ++b) {
+      const uint32_t x = prmt(w[i], hi, 0x0400u + 0x0101u * b);  // byte b: low nibble -> half 0, high -> half 1
+      if (kBf16) {
+        // 0x4308 ^ n is BF16 128 + (n_signed + 8); subtracting 136 is exact.
+        o[i * 4 + b] = bf16x2_sub(and_xor(x, 0x000F000Fu, 0x43084308u), 0x43084308u);
+      } else {
+        // FP16 1024 + (n_signed + 8) minus 1032.
+        o[i * 4 + b] = f16x2_sub(and_xor(x, 0x000F000Fu, 0x64086408u), 0x64086408u);
+      }
+    }
+  }
+}
+
+// 32 signed INT8 codes (two 16-byte chunks) -> 16 words holding the integers
+// q exactly, as BF16 (kBf16) or FP16.
+template <bool kBf16>
+__device__ __forceinline__ void cvt_int8x32(const uint4 v0, const uint4 v1, uint32_t (&o)[16]) {
+  const uint32_t w[8] = {v0.x, v0.y, v0.z, v0.w, v1.x, v1.y, v1.z, v1.w};
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    const uint32_t u = w[i] ^ 0x80808080u;  // q + 128 per byte
+    if (kBf16) {
+      float f[4];
+#pragma unroll
+      for (int b = 0; b < 4; ++b) {
+        // 0x4B0000uu is FP32 2^23 + u; minus (2^23 + 128) gives q exactly.
+        f[b] = __fsub_rn(__uint_as_float(prmt(u, 0x4B000000u, 0x7540u + b)), 8388736.0f);
+      }
+      o[2 * i] = pack_bf16x2(f[0], f[1]);
+      o[2 * i + 1] = pack_bf16x2(f[2], f[3]);
+    } else {
+      // 0x64uu is FP16 1024 + u; minus 1152 gives q exactly.
+      o[2 * i] = f16x2_sub(prmt(u, 0x64646464u, 0x4140u), 0x64806480u);
+      o[2 * i + 1] = f16x2_sub(prmt(u, 0x64646464u, 0x4342u), 0x64806480u);
+    }
+  }
+}
+
+// 32 E2M1 codes (one 16-byte chunk) with the E4M3 scales of its two 16-blocks
+// -> 16 words of exact FP16 products.
+__device__ __forceinline__ void cvt_fp4x32(const uint4 v, uint32_t sf0, uint32_t sf1, uint32_t (&o)[16]) {
+  uint32_t s0, s1;
+  asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(s0) : "h"(static_cast<uint16_t>(sf0 | (sf0 << 8))));
+  asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(s1) : "h"(static_cast<uint16_t>(sf1 | (sf1 << 8))));
+  const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    uint32_t h0, h1, h2, h3;
+    asm("{\n\t.reg .b8 b0, b1, b2, b3;\n\tmov.b32 {b0, b1, b2, b3}, %4;\n\t"
+        "cvt.rn.f16x2.e2m1x2 %0, b0;\n\tcvt.rn.f16x2.e2m1x2 %1, b1;\n\t"
+        "cvt.rn.f16x2.e2m1x2 %2, b2;\n\tcvt.rn.f16x2.e2m1x2 %3, b3;\n\t}"
+        : "=r"(h0), "=r"(h1), "=r"(h2), "=r"(h3)
+        : "r"(w[i]));
+    const uint32_t s = i < 2 ? s0 : s1;
+    o[4 * i + 0] = f16x2_mul(h0, s);
+    o[4 * i + 1] = f16x2_mul(h1, s);
+    o[4 * i + 2] = f16x2_mul(h2, s);
+    o[4 * i + 3] = f16x2_mul(h3, s);
+  }
+}
+
+// Address of 16-byte chunk c of row r in a 128-byte-swizzled tile.
+__device__ __forceinline__ uint32_t sw128(uint32_t base, int r, int c) {
+  return base + r * 128 + ((c ^ (r & 7)) << 4);
+}
+__device__ __forceinline__ uint4 lds128(uint32_t addr) {
+  uint4 v;
+  asm volatile("ld.shared.v4.u32 {%0,%1,%2,%3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "r"(addr));
+  return v;
+}
+__device__ __forceinline__ void sts128(uint32_t addr, uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
+  asm volatile("st.shared.v4.u32 [%0], {%1,%2,%3,%4};" ::"r"(addr), "r"(a), "r"(b), "r"(c), "r"(d) : "memory");
+}
+
+// ---------------------------------------------------------------------------
+// work decomposition
+// ---------------------------------------------------------------------------
+
+struct Unit {
+  int e, tt, nt, row0, nrows;
+};
+
+__device__ __forceinline__ Unit decode_unit(const int* tab_prefix, const int* tab_off, int E, int n_tiles, int BN,
+                                            int u) {
+  Unit x;
+  const int t = u / n_tiles;
+  x.nt = u - t * n_tiles;
+  int lo = 0, hi = E - 1;
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if (tab_prefix[mid] <= t) lo = mid;
+    else hi = mid - 1;
+  }
+  x.e = lo;
+  x.tt = t - tab_prefix[lo];
+  x.row0 = tab_off[lo] + x.tt * BN;
+  x.nrows = min(BN, tab_off[lo + 1] - x.row0);
+  return x;
+}
+
+// Drain wait used on the way out: ignores the abort flag, bounded in time.
+__device__ __forceinline__ void drain_wait(uint64_t* bar, uint32_t parity) {
+  const uint64_t t0 = globaltimer();
+  while (!mbar_try_wait(bar, parity)) {
+    if (globaltimer() - t0 > kWaitLimitNs) return;
+  }
+}
+
+// ---------------------------------------------------------------------------
+// the kernel
+// ---------------------------------------------------------------------------
+
+template <int WF, int AM, bool kGateUp>
+__global__ void __launch_bounds__(kThreads, 1)
+    moe_gemm_kernel(const __grid_constant__ CUtensorMap tmA0, const __grid_constant__ CUtensorMap tmA1,
+                    const __grid_constant__ CUtensorMap tmS0, const __grid_constant__ CUtensorMap tmS1,
+                    const __grid_constant__ CUtensorMap tmB, const __grid_constant__ CUtensorMap tmBs,
+                    const GemmArgs args) {
+  using T = WT<WF>;
+  constexpr int kNmat = kGateUp ? 2 : 1;
+  constexpr bool kBconv = AM != AM_BF16;
+  // Grouped: one accumulator per 128-wide K group, rescaled in FP32 (INT weights).
+  constexpr bool kGrouped = AM == AM_INT8 || (AM == AM_BF16 && T::kScales);
+  constexpr bool kBf16Mma = AM == AM_BF16;
+
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  Bars* bars = reinterpret_cast<Bars*>(smem + args.off_bars);
+  int* tab_prefix = reinterpret_cast<int*>(smem + args.off_tab);
+  int* tab_off = tab_prefix + (args.E + 1);
+  volatile int* abort = &bars->abort;
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int E = args.E, BN = args.BN, S = args.stages;
+  const int nks = args.K / T::kStage;
+  const int G = args.K / 128;
+
+  // ---- set-up ----
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kMaxStages; ++s) {
+      mbar_init(&bars->full[s], 1);
+      mbar_init(&bars->empty[s], ((T::kTs || kBconv) ? kConvWarps : 0) + 1);
+      mbar_init(&bars->bconv[s], kConvWarps);
+    }
+    for (int i = 0; i < kASlots; ++i) {
+      mbar_init(&bars->afull[i], kConvWarps);
+      mbar_init(&bars->aempty[i], 1);
+    }
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&bars->accfull[i], 1);
+      mbar_init(&bars->accempty[i], kEpiWarps);
+      mbar_init(&bars->sfull[i], 1);
+      mbar_init(&bars->sempty[i], kEpiWarps);
+    }
+    mbar_init(&bars->final_mma, 1);
+    bars->abort = 0;
+    fence_barrier_init();
+  }
+  if (warp == kWarpMma) {
+    tmem_alloc(&bars->tmem_base, kTmemCols);
+    tmem_relinquish();
+  }
+  if (warp == kWarpTma && lane == 0) {
+    tma_prefetch_desc(&tmA0);
+    if (kGateUp) tma_prefetch_desc(&tmA1);
+    tma_prefetch_desc(&tmB);
+  }
+  // Tile table: tab_prefix[e] = first tile of expert e, tab_off = expert_offsets.
+  if (warp == 2) {
+    const int per = (E + 31) / 32;
+    int local = 0;
+    for (int i = 0; i < per; ++i) {
+      const int e = lane * per + i;
+      if (e < E) {
+        const int o0 = __ldg(args.offsets + e), o1 = __ldg(args.offsets + e + 1);
+        tab_off[e] = o0;
+        local += max(0, (o1 - o0 + BN - 1) / BN);
+      }
+    }
+    int incl = local;
+#pragma unroll
+    for (int d = 1; d < 32; d <<= 1) {
+      const int o = __shfl_up_sync(0xffffffffu, incl, d);
+      if (lane >= d) incl += o;
+    }
+    int run = incl - local;
+    for (int i = 0; i < per; ++i) {
+      const int e = lane * per + i;
+      if (e < E) {
+        tab_prefix[e] = run;
+        const int o0 = tab_off[e], o1 = __ldg(args.offsets + e + 1);
+        run += max(0, (o1 - o0 + BN - 1) / BN);
+      }
+    }
+    if (lane == 31) {
+      tab_prefix[E] = incl;
+      tab_off[E] = __ldg(args.offsets + E);
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = bars->tmem_base;
+  const int units = tab_prefix[E] * args.n_tiles;
+
+  if (warp == kWarpTma) {
+    // ======================= producer =======================
+    if (lane == 0) {
+      uint32_t it = 0, uit = 0, sit = 0;  // stages issued, units visited, scale loads issued
+      bool ok = true;
+      const uint32_t a_bytes = kNmat * 16384u + (WF == WF_NVFP4 ? kNmat * 2048u : 0u);
+      uint32_t b_bytes;
+      if (AM == AM_BF16) b_bytes = T::kSub * BN * 128u;
+      else if (AM == AM_INT8) b_bytes = (T::kStage / 128) * BN * 128u;
+      else b_bytes = BN * 128u + BN * 16u;
+      const uint32_t tx = a_bytes + b_bytes;
+      for (int u = blockIdx.x; ok && u < units; u += gridDim.x, ++uit) {
+        const Unit x = decode_unit(tab_prefix, tab_off, E, args.n_tiles, BN, u);
+        const int n0 = x.nt * kBM;
+        if (T::kScales) {
+          const uint32_t sb = uit & 1;
+          if (!bounded_wait(&bars->sempty[sb], ((uit >> 1) & 1) ^ 1, abort, args.err)) { ok = false; break; }
+          mbar_arrive_expect_tx(&bars->sfull[sb], kNmat * args.scale_mat_bytes);
+          for (int m = 0; m < kNmat; ++m) {
+            const uint8_t* src = args.experts + static_cast<uint64_t>(x.e) * args.expert_stride +
+                                 args.scales_off[m] + static_cast<uint64_t>(n0) * G * 2;
+            bulk_load(smem + args.off_scales + (sb * kNmat + m) * args.scale_mat_bytes, src, args.scale_mat_bytes,
+                      &bars->sfull[sb]);
+          }
+          ++sit;
+        }
+        for (int ks = 0; ks < nks; ++ks, ++it) {
+          const int s = it % S;
+          const uint32_t ph = (it / S) & 1;
+          if (!bounded_wait(&bars->empty[s], ph ^ 1, abort, args.err)) { ok = false; break; }
+          uint8_t* st = smem + s * args.stage_bytes;
+          mbar_arrive_expect_tx(&bars->full[s], tx);
+          const int kx = WF == WF_BF16 ? ks * 64 : ks * 128;  // elements (BF16) or bytes (codes)
+          tma_load_3d(st + args.off_a[0], &tmA0, &bars->full[s], kx, n0, x.e);
+          if (kGateUp) tma_load_3d(st + args.off_a[1], &tmA1, &bars->full[s], kx, n0, x.e);
+          if (WF == WF_NVFP4) {
+            tma_load_3d(st + args.off_asf[0], &tmS0, &bars->full[s], ks * 16, n0, x.e);
+            if (kGateUp) tma_load_3d(st + args.off_asf[1], &tmS1, &bars->full[s], ks * 16, n0, x.e);
+          }
+          if (AM == AM_BF16) {
+            for (int b = 0; b < T::kSub; ++b)
+              tma_load_2d(st + args.off_b + b * BN * 128, &tmB, &bars->full[s], ks * T::kStage + b * 64, x.row0);
+          } else if (AM == AM_INT8) {
+            for (int b = 0; b < T::kStage / 128; ++b)
+              tma_load_2d(st + args.off_braw + b * BN * 128, &tmB, &bars->full[s], ks * T::kStage + b * 128,
+                          x.row0);
+          } else {
+            tma_load_2d(st + args.off_braw, &tmB, &bars->full[s], ks * 128, x.row0);
+            tma_load_2d(st + args.off_bsf, &tmBs, &bars->full[s], ks * 16, x.row0);
+          }
+        }
+      }
+      if (!ok || *abort) {
+        // Let every copy already issued land before the CTA exits.
+        const uint32_t first = it > static_cast<uint32_t>(S) ? it - S : 0;
+        for (uint32_t j = first; j < it; ++j) drain_wait(&bars->full[j % S], (j / S) & 1);
+        if (T::kScales)
+          for (uint32_t j = sit > 2 ? sit - 2 : 0; j < sit; ++j) drain_wait(&bars->sfull[j & 1], (j >> 1) & 1);
+      }
+    }
+  } else if (warp == kWarpMma) {
+    // ======================= MMA issuer =======================
+    if (lane == 0) {
+      const uint32_t idesc = idesc_f16(kBM, BN, kBf16Mma);
+      uint32_t it = 0, ait = 0, acc_it = 0;
+      bool ok = true, issued = false;
+      uint32_t d_base = 0;
+      for (int u = blockIdx.x; ok && u < units; u += gridDim.x) {
+        if (!kGrouped) {
+          const uint32_t slot = acc_it % args.acc_slots;
+          if (!bounded_wait(&bars->accempty[slot], ((acc_it / args.acc_slots) & 1) ^ 1, abort, args.err)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          d_base = tmem + args.acc_base + slot * kNmat * BN;
+        }
+        for (int ks = 0; ok && ks < nks; ++ks, ++it) {
+          const int s = it % S;
+          const uint32_t ph = (it / S) & 1;
+          if (!bounded_wait(kBconv ? &bars->bconv[s] : &bars->full[s], ph, abort, args.err)) { ok = false; break; }
+          tc_fence_after();
+          const uint32_t st = smem_u32(smem + s * args.stage_bytes);
+          for (int sc = 0; sc < T::kSub; ++sc) {
+            const int kg = ks * T::kStage + sc * 64;
+            uint32_t gslot = 0;
+            if (kGrouped) {
+              gslot = acc_it & 1;
+              if ((kg & 127) == 0) {
+                if (!bounded_wait(&bars->accempty[gslot], ((acc_it >> 1) & 1) ^ 1, abort, args.err)) {
+                  ok = false;
+                  break;
+                }
+                tc_fence_after();
+              }
+              d_base = tmem + args.acc_base + gslot * kNmat * BN;
+            }
+            const uint32_t aslot = ait % args.aslots;
+            if (T::kTs) {
+              if (!bounded_wait(&bars->afull[aslot], (ait / args.aslots) & 1, abort, args.err)) { ok = false; break; }
+              tc_fence_after();
+            }
+            const uint32_t b_tile = st + args.off_b + sc * BN * 128;
+#pragma unroll
+            for (int kk = 0; kk < 4; ++kk) {
+              const uint64_t bdesc = sdesc_sw128(b_tile + kk * 32);
+              const uint32_t acc = kGrouped ? ((kg & 127) != 0 || kk != 0) : (ks != 0 || sc != 0 || kk != 0);
+#pragma unroll
+              for (int m = 0; m < kNmat; ++m) {
+                if (T::kTs) {
+                  mma_ts(d_base + m * BN, tmem + aslot * (kNmat * 32) + m * 32 + kk * 8, bdesc, idesc, acc);
+                } else {
+                  mma_ss(d_base + m * BN, sdesc_sw128(st + args.off_a[m] + kk * 32), bdesc, idesc, acc);
+                }
+              }
+            }
+            issued = true;
+            if (T::kTs) {
+              mma_commit(&bars->aempty[aslot]);
+              ++ait;
+            }
+            if (kGrouped && ((kg + 64) & 127) == 0) {
+              mma_commit(&bars->accfull[gslot]);
+              ++acc_it;
+            }
+          }
+          if (!ok) break;
+          mma_commit(&bars->empty[s]);
+        }
+        if (ok && !kGrouped) {
+          mma_commit(&bars->accfull[acc_it % args.acc_slots]);
+          ++acc_it;
+        }
+      }
+      if (issued) {
+        mma_commit(&bars->final_mma);
+        drain_wait(&bars->final_mma, 0);
+      }
+    }
+  } else if (warp < kWarpEpi0) {
+    // ======================= converters =======================
+    const int cw = warp - kWarpConv0;   // 0..7
+    const int q = warp & 3;             // TMEM lane quarter this warp may access
+    const int h = cw >> 2;              // which 32-K half of each 64-K sub-chunk
+    const int r = q * 32 + lane;        // weight row within the tile
+    const int ctid = cw * 32 + lane;    // 0..255
+    uint32_t it = 0, ait = 0, uit = 0;
+    bool ok = true;
+    if (T::kTs || kBconv) {
+      for (int u = blockIdx.x; ok && u < units; u += gridDim.x, ++uit) {
+        for (int ks = 0; ks < nks; ++ks, ++it) {
+          const int s = it % S;
+          if (!bounded_wait(&bars->full[s], (it / S) & 1, abort, args.err)) { ok = false; break; }
+          const uint32_t st = smem_u32(smem + s * args.stage_bytes);
+          if (kBconv) {
+            // token codes -> FP16 operand tile (128-byte swizzle, BN rows per 64-K box)
+            const uint32_t braw = st + args.off_braw, bdst = st + args.off_b;
+            if (AM == AM_INT8) {
+              const int chunks = (T::kStage / 128) * BN * 8;
+              for (int i = ctid; i < chunks; i += kConvWarps * 32) {
+                const int rb = i / (BN * 8), rem = i - rb * BN * 8, row = rem >> 3, c = rem & 7;
+                const uint4 v = lds128(sw128(braw + rb * BN * 128, row, c));
+                uint32_t o[16];
+                const uint4 zero = make_uint4(0, 0, 0, 0);
+                cvt_int8x32<false>(v, zero, o);  // first 8 words hold the 16 converted values
+                const int kk = rb * 128 + c * 16, cb = kk >> 6, cc = (kk & 63) >> 3;
+                const uint32_t tile = bdst + cb * BN * 128;
+                sts128(sw128(tile, row, cc), o[0], o[1], o[2], o[3]);
+                sts128(sw128(tile, row, cc + 1), o[4], o[5], o[6], o[7]);
+              }
+            } else {
+              const uint32_t bsf = st + args.off_bsf;
+              const int chunks = BN * 8;
+              for (int i = ctid; i < chunks; i += kConvWarps * 32) {
+                const int row = i >> 3, c = i & 7;
+                const uint4 v = lds128(sw128(braw, row, c));
+                uint32_t sfp;
+                asm volatile("ld.shared.u16 %0, [%1];" : "=r"(sfp) : "r"(bsf + row * 16 + c * 2));
+                uint32_t o[16];
+                cvt_fp4x32(v, sfp & 0xFF, (sfp >> 8) & 0xFF, o);
+                const int cb = c >> 1, cc = (c & 1) * 4;
+                const uint32_t tile = bdst + cb * BN * 128;
+#pragma unroll
+                for (int j = 0; j < 4; ++j) sts128(sw128(tile, row, cc + j), o[4 * j], o[4 * j + 1], o[4 * j + 2], o[4 * j + 3]);
+              }
+            }
+            fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&bars->bconv[s]);
+          }
+          if (T::kTs) {
+            for (int sc = 0; sc < T::kSub; ++sc, ++ait) {
+              const uint32_t aslot = ait % args.aslots;
+              if (!bounded_wait(&bars->aempty[aslot], ((ait / args.aslots) & 1) ^ 1, abort, args.err)) {
+                ok = false;
+                break;
+              }
+              tc_fence_after();
+              const int kin = sc * 64 + h * 32;            // K offset inside the stage
+#pragma unroll
+              for (int m = 0; m < kNmat; ++m) {
+                const uint32_t abase = st + args.off_a[m];
+                uint32_t o[16];
+                if (WF == WF_INT4) {
+                  const uint4 v = lds128(sw128(abase, r, kin >> 5));  // 32 codes = one 16-byte chunk
+                  cvt_int4x32<AM == AM_BF16>(v, o);
+                } else if (WF == WF_INT8) {
+                  const uint4 v0 = lds128(sw128(abase, r, kin >> 4));  // 32 codes = two chunks
+                  const uint4 v1 = lds128(sw128(abase, r, (kin >> 4) + 1));
+                  cvt_int8x32<AM == AM_BF16>(v0, v1, o);
+                } else {  // NVFP4
+                  const uint4 v = lds128(sw128(abase, r, kin >> 5));
+                  uint32_t sfp;
+                  asm volatile("ld.shared.u16 %0, [%1];" : "=r"(sfp) : "r"(st + args.off_asf[m] + r * 16 + (kin >> 4)));
+                  cvt_fp4x32(v, sfp & 0xFF, (sfp >> 8) & 0xFF, o);
+                }
+                tmem_st16(tmem + (static_cast<uint32_t>(q * 32) << 16) + aslot * (kNmat * 32) + m * 32 + h * 16, o);
+              }
+              tmem_wait_st();
+              tc_fence_before();
+              __syncwarp();
+              if (lane == 0) mbar_arrive(&bars->afull[aslot]);
+            }
+            if (!ok) break;
+          }
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&bars->empty[s]);
+        }
+      }
+    }
+  } else {
+    // ======================= epilogue =======================
+    const int q = warp & 3;
+    const int r = q * 32 + lane;
+    const uint32_t lane_bits = static_cast<uint32_t>(q * 32) << 16;
+    uint32_t acc_it = 0, uit = 0;
+    bool ok = true;
+    // each epilogue warp keeps its own copy of the tile's activation scales
+    float* sa = reinterpret_cast<float*>(smem + args.off_sa) + (warp - kWarpEpi0) * BN * G;
+    for (int u = blockIdx.x; ok && u < units; u += gridDim.x, ++uit) {
+      const Unit x = decode_unit(tab_prefix, tab_off, E, args.n_tiles, BN, u);
+      const int n0 = x.nt * kBM;
+      const int col = n0 + r;
+      if (!kGrouped) {
+        const uint32_t slot = acc_it % args.acc_slots;
+        if (!bounded_wait(&bars->accfull[slot], (acc_it / args.acc_slots) & 1, abort, args.err)) { ok = false; break; }
+        tc_fence_after();
+        const uint32_t d = tmem + lane_bits + args.acc_base + slot * kNmat * BN;
+        float ow[2] = {1.f, 1.f};
+        if (AM == AM_FP4) {
+          for (int m = 0; m < kNmat; ++m)
+            ow[m] = __ldg(reinterpret_cast<const float*>(args.experts + static_cast<uint64_t>(x.e) * args.expert_stride +
+                                                         args.outer_off[m]));
+        }
+        for (int j0 = 0; j0 < BN && j0 < x.nrows; j0 += 16) {
+          uint32_t g[16], up[16];
+          tmem_ld16(d + j0, g);
+          if (kGateUp) tmem_ld16(d + BN + j0, up);
+          tmem_wait_ld();
+#pragma unroll
+          for (int i = 0; i < 16; ++i) {
+            const int j = j0 + i;
+            if (j < x.nrows && x.row0 + j < args.P) {
+              float gv = __uint_as_float(g[i]);
+              float val;
+              float oa = 1.f;
+              if (AM == AM_FP4) {
+                oa = __ldg(args.a_outer + x.row0 + j);
+                gv = gv * (ow[0] * oa);
+              }
+              if (kGateUp) {
+                float uv = __uint_as_float(up[i]);
+                if (AM == AM_FP4) uv = uv * (ow[1] * oa);
+                val = __fdividef(gv, 1.f + __expf(-gv)) * uv;
+              } else {
+                val = gv;
+              }
+              args.out[static_cast<size_t>(x.row0 + j) * args.N + col] = __float2bfloat16_rn(val);
+            }
+          }
+        }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&bars->accempty[slot]);
+        ++acc_it;
+      } else {
+        // Grouped: one accumulator per 128-wide K group.  Each group's exact
+        // dot products D_g are scaled in FP32 (by s_w, times s_a in the A8
+        // mode) and added to a running sum held in TMEM.
+        const uint32_t sb = uit & 1;
+        if (!bounded_wait(&bars->sfull[sb], (uit >> 1) & 1, abort, args.err)) { ok = false; break; }
+        if (AM == AM_INT8) {
+          for (int i = lane; i < BN * G; i += 32) {
+            const int j = i / G, gg = i - j * G;
+            sa[i] = (j < x.nrows && x.row0 + j < args.P)
+                        ? __ldg(args.a_scales + static_cast<size_t>(x.row0 + j) * G + gg)
+                        : 0.f;
+          }
+          __syncwarp();
+        }
+        const __half* sw0 =
+            reinterpret_cast<const __half*>(smem + args.off_scales + (sb * kNmat + 0) * args.scale_mat_bytes) + r * G;
+        const __half* sw1 =
+            reinterpret_cast<const __half*>(smem + args.off_scales + (sb * kNmat + (kNmat - 1)) * args.scale_mat_bytes) +
+            r * G;
+        const uint32_t dsum = tmem + lane_bits + args.sum_base;
+        for (int g = 0; g < G; ++g) {
+          const uint32_t slot = acc_it & 1;
+          if (!bounded_wait(&bars->accfull[slot], (acc_it >> 1) & 1, abort, args.err)) { ok = false; break; }
+          tc_fence_after();
+          const uint32_t d = tmem + lane_bits + args.acc_base + slot * kNmat * BN;
+          const float w0 = __half2float(sw0[g]), w1 = __half2float(sw1[g]);
+          const bool last = g == G - 1;
+          for (int j0 = 0; j0 < BN && j0 < x.nrows; j0 += 16) {
+            uint32_t d0[16], d1[16], s0[16], s1[16];
+            tmem_ld16(d + j0, d0);
+            if (kGateUp) tmem_ld16(d + BN + j0, d1);
+            if (g > 0) {
+              tmem_ld16(dsum + j0, s0);
+              if (kGateUp) tmem_ld16(dsum + BN + j0, s1);
+            }
+            tmem_wait_ld();
+#pragma unroll
+            for (int i = 0; i < 16; ++i) {
+              const int j = j0 + i;
+              float f0 = w0, f1 = w1;
+              if (AM == AM_INT8) {
+                const float s_a = sa[j * G + g];
+                f0 = __fmul_rn(w0, s_a);
+                f1 = __fmul_rn(w1, s_a);
+              }
+              const float a0 = __fmaf_rn(f0, __uint_as_float(d0[i]), g > 0 ? __uint_as_float(s0[i]) : 0.f);
+              float a1 = 0.f;
+              if (kGateUp) a1 = __fmaf_rn(f1, __uint_as_float(d1[i]), g > 0 ? __uint_as_float(s1[i]) : 0.f);
+              if (args.dots && j < x.nrows) {
+                const size_t C = static_cast<size_t>(kNmat) * args.N;
+                const size_t base = (static_cast<size_t>(x.row0 + j) * C) * G;
+                args.dots[base + static_cast<size_t>(col) * G + g] = __float2int_rn(__uint_as_float(d0[i]));
+                if (kGateUp)
+                  args.dots[base + static_cast<size_t>(args.N + col) * G + g] = __float2int_rn(__uint_as_float(d1[i]));
+              }
+              if (last) {
+                if (j < x.nrows && x.row0 + j < args.P) {
+                  const float val = kGateUp ? __fdividef(a0, 1.f + __expf(-a0)) * a1 : a0;
+                  args.out[static_cast<size_t>(x.row0 + j) * args.N + col] = __float2bfloat16_rn(val);
+                }
+              } else {
+                s0[i] = __float_as_uint(a0);
+                s1[i] = __float_as_uint(a1);
+              }
+            }
+            if (!last) {
+              tmem_st16(dsum + j0, s0);
+              if (kGateUp) tmem_st16(dsum + BN + j0, s1);
+            }
+          }
+          if (!last) tmem_wait_st();
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&bars->accempty[slot]);
+          ++acc_it;
+        }
+        if (!ok) break;
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&bars->sempty[sb]);
+      }
+    }
+  }
+
+  // ---- teardown ----
+  tc_fence_before();
+  __syncthreads();
+  if (warp == kWarpMma) {
+    tc_fence_after();
+    tmem_dealloc(tmem, kTmemCols);
+  }
+}
+
+// ---------------------------------------------------------------------------
+// host side
+// ---------------------------------------------------------------------------
+
+namespace {
+
+constexpr size_t kSmemLimit = 232448;  // max dynamic shared memory per block on sm_103
+
+inline uint32_t align_up(uint32_t x, uint32_t a) { return (x + a - 1) / a * a; }
+
+struct Plan {
+  GemmArgs args;
+  size_t smem;
+};
+
+// Lay out one stage and the fixed areas for a given BN; returns false if
+// fewer than two stages fit.
+bool plan_smem(int wf, int am, bool gate_up, int K, int E, int BN, Plan* p) {
+  const int nmat = gate_up ? 2 : 1;
+  const int kstage = wf == WF_BF16 ? 64 : (wf == WF_INT8 ? 128 : 256);
+  GemmArgs& a = p->args;
+  uint32_t off = 0;
+  for (int m = 0; m < 2; ++m) {
+    a.off_a[m] = off;
+    if (m < nmat) off += 16384;
+  }
+  for (int m = 0; m < 2; ++m) {
+    a.off_asf[m] = off;
+    if (wf == WF_NVFP4 && m < nmat) off += 2048;
+  }
+  off = align_up(off, 1024);
+  a.off_b = off;
+  off += (kstage / 64) * BN * 128;
+  off = align_up(off, 1024);
+  a.off_braw = off;
+  if (am == AM_INT8) off += (kstage / 128) * BN * 128;
+  if (am == AM_FP4) off += BN * 128;
+  off = align_up(off, 1024);
+  a.off_bsf = off;
+  if (am == AM_FP4) off += BN * 16;
+  off = align_up(off, 1024);
+  a.stage_bytes = off;
+
+  const int G = K / 128;
+  uint32_t fixed = 0;
+  a.scale_mat_bytes = (wf == WF_INT8 || wf == WF_INT4) ? 128u * G * 2u : 0u;
+  const uint32_t scales = 2 * nmat * a.scale_mat_bytes;
+  const uint32_t tab = align_up(2u * (E + 1) * 4u, 16);
+  const uint32_t sa = am == AM_INT8 ? align_up(kEpiWarps * BN * G * 4u, 16) : 0u;
+  const uint32_t bars = align_up(sizeof(Bars), 16);
+  fixed = scales + tab + sa + bars;
+  const size_t budget = kSmemLimit - 1024;  // alignment slack
+  if (fixed + 2 * a.stage_bytes > budget) return false;
+  int stages = static_cast<int>((budget - fixed) / a.stage_bytes);
+  if (stages > kMaxStages) stages = kMaxStages;
+  a.stages = stages;
+  uint32_t o = stages * a.stage_bytes;
+  a.off_scales = o;
+  o += scales;
+  a.off_tab = o;
+  o += tab;
+  a.off_sa = o;
+  o += sa;
+  a.off_bars = align_up(o, 16);
+  o = a.off_bars + bars;
+  p->smem = o + 1024;
+  return true;
+}
+
+template <int WF, int AM, bool GU>
+cudaError_t launch_one(const CUtensorMap* maps, const GemmArgs& a, size_t smem, int grid, cudaStream_t st) {
+  auto kern = moe_gemm_kernel<WF, AM, GU>;
+  static bool attr = false;
+  if (!attr) {
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(kSmemLimit));
+    if (e != cudaSuccess) return e;
+    attr = true;
+  }
+  kern<<<grid, kThreads, smem, st>>>(maps[0], maps[1], maps[2], maps[3], maps[4], maps[5], a);
+  return cudaGetLastError();
+}
+
+template <int WF, int AM>
+cudaError_t launch_kind(bool gate_up, const CUtensorMap* maps, const GemmArgs& a, size_t smem, int grid,
+                        cudaStream_t st) {
+  return gate_up ? launch_one<WF, AM, true>(maps, a, smem, grid, st) : launch_one<WF, AM, false>(maps, a, smem, grid, st);
+}
+
+}  // namespace
+
+int run_gemm(const mnw_moe_layer* L, int wfmt, int act, int kind, const void* a0, const void* a1, const void* a2,
+             const int32_t* offsets, int P, void* out, int32_t* dots, uint32_t* err, cudaStream_t st) {
+  if (!L || (kind != MNW_KIND_GATE_UP && kind != MNW_KIND_DOWN) || P < 0) return MNW_E_INVALID_ARG;
+  if (L->wfmt != wfmt) return MNW_E_MODE;
+  if (P == 0) return MNW_OK;
+  if (!a0 || !offsets || !out || !aligned(a0, 16) || !aligned(out, 16)) return MNW_E_INVALID_ARG;
+  if (act == MNW_ACT_INT8_G128 && (!a1 || !aligned(a1, 16))) return MNW_E_INVALID_ARG;
+  if (act == MNW_ACT_NVFP4_G16 && (!a1 || !a2 || !aligned(a1, 16) || !aligned(a2, 16))) return MNW_E_INVALID_ARG;
+  const bool gate_up = kind == MNW_KIND_GATE_UP;
+  const int K = gate_up ? L->H : L->I;
+  const int N = gate_up ? L->I : L->H;
+  const int nmat = gate_up ? 2 : 1;
+  const int am = act;  // MNW_ACT_* match AM_*
+  const int wf = wfmt;
+
+  // Token tile: the power of two (16..max) nearest above the mean rows per expert.
+  const bool grouped = am == AM_INT8 || (am == AM_BF16 && (wf == WF_INT8 || wf == WF_INT4));
+  // TMEM budget (512 columns): operand-A ring + accumulators (+ running sums when grouped).
+  const int max_bn = grouped ? (gate_up ? 64 : 128) : (am == AM_FP4 ? 64 : 128);
+  const int mean = (P + L->E - 1) / L->E;
+  int BN = 16;
+  while (BN < mean && BN < max_bn) BN *= 2;
+  Plan plan{};
+  while (!plan_smem(wf, am, gate_up, K, L->E, BN, &plan)) {
+    if (BN == 16) return MNW_E_UNSUPPORTED;
+    BN /= 2;
+  }
+  GemmArgs& a = plan.args;
+  const bool ts = wf != WF_BF16;
+  a.offsets = offsets;
+  a.E = L->E;
+  a.P = P;
+  a.K = K;
+  a.N = N;
+  a.BN = BN;
+  a.n_tiles = N / kBM;
+  a.nmat = nmat;
+  if (grouped) {
+    // [A ring | 2 group accumulators | running sum]
+    a.aslots = gate_up ? 2 : 4;
+    a.acc_base = a.aslots * nmat * 32;
+    a.acc_slots = 2;
+    a.sum_base = a.acc_base + 2 * nmat * BN;
+    if (a.sum_base + nmat * BN > kTmemCols) return MNW_E_UNSUPPORTED;
+  } else {
+    a.aslots = kASlots;
+    a.acc_base = ts ? kASlots * nmat * 32 : 0;
+    const int acc_cols = kTmemCols - a.acc_base;
+    a.acc_slots = (2 * nmat * BN <= acc_cols) ? 2 : 1;
+    a.sum_base = 0;
+    if (nmat * BN > acc_cols) return MNW_E_UNSUPPORTED;
+  }
+  a.experts = L->blob + L->data_offset;
+  a.expert_stride = L->expert_stride;
+  const int m0 = gate_up ? 0 : 2;
+  for (int m = 0; m < nmat; ++m) {
+    a.scales_off[m] = L->scales_off[m0 + m];
+    a.outer_off[m] = L->outer_off[m0 + m];
+  }
+  a.a_scales = am == AM_INT8 ? static_cast<const float*>(a1) : nullptr;
+  a.a_outer = am == AM_FP4 ? static_cast<const float*>(a2) : nullptr;
+  a.out = static_cast<__nv_bfloat16*>(out);
+  a.dots = am == AM_INT8 ? dots : nullptr;
+  a.err = err;
+
+  // Tensor maps: 0/1 weight codes, 2/3 NVFP4 weight scales, 4 tokens, 5 token scales.
+  CUtensorMap maps[6];
+  memset(maps, 0, sizeof(maps));
+  maps[0] = L->tm_codes[m0];
+  if (gate_up) maps[1] = L->tm_codes[1];
+  if (wf == WF_NVFP4) {
+    maps[2] = L->tm_sf[m0];
+    if (gate_up) maps[3] = L->tm_sf[1];
+  }
+  const uint64_t Pu = static_cast<uint64_t>(P);
+  bool ok;
+  if (am == AM_BF16) {
+    const uint64_t dims[2] = {static_cast<uint64_t>(K), Pu};
+    const uint64_t strides[1] = {static_cast<uint64_t>(K) * 2};
+    const uint32_t box[2] = {64, static_cast<uint32_t>(BN)};
+    ok = encode_map(&maps[4], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, a0, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_128B);
+  } else if (am == AM_INT8) {
+    const uint64_t dims[2] = {static_cast<uint64_t>(K), Pu};
+    const uint64_t strides[1] = {static_cast<uint64_t>(K)};
+    const uint32_t box[2] = {128, static_cast<uint32_t>(BN)};
+    ok = encode_map(&maps[4], CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, a0, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_128B);
+  } else {
+    const uint64_t dims[2] = {static_cast<uint64_t>(K / 2), Pu};
+    const uint64_t strides[1] = {static_cast<uint64_t>(K / 2)};
+    const uint32_t box[2] = {128, static_cast<uint32_t>(BN)};
+    ok = encode_map(&maps[4], CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, a0, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_128B);
+    const uint64_t dims2[2] = {static_cast<uint64_t>(K / 16), Pu};
+    const uint64_t strides2[1] = {static_cast<uint64_t>(K / 16)};
+    const uint32_t box2[2] = {16, static_cast<uint32_t>(BN)};
+    ok = ok && encode_map(&maps[5], CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, a1, dims2, strides2, box2,
+                          CU_TENSOR_MAP_SWIZZLE_NONE);
+  }
+  if (!ok) return MNW_E_INVALID_ARG;
+
+  const int grid = L->num_sms;
+  cudaError_t e = cudaErrorInvalidValue;
+  switch (wf * 3 + am) {
+    case WF_BF16 * 3 + AM_BF16: e = launch_kind<WF_BF16, AM_BF16>(gate_up, maps, a, plan.smem, grid, st); break;
+    case WF_INT8 * 3 + AM_BF16: e = launch_kind<WF_INT8, AM_BF16>(gate_up, maps, a, plan.smem, grid, st); break;
+    case WF_INT4 * 3 + AM_BF16: e = launch_kind<WF_INT4, AM_BF16>(gate_up, maps, a, plan.smem, grid, st); break;
+    case WF_INT8 * 3 + AM_INT8: e = launch_kind<WF_INT8, AM_INT8>(gate_up, maps, a, plan.smem, grid, st); break;
+    case WF_INT4 * 3 + AM_INT8: e = launch_kind<WF_INT4, AM_INT8>(gate_up, maps, a, plan.smem, grid, st); break;
+    case WF_NVFP4 * 3 + AM_FP4: e = launch_kind<WF_NVFP4, AM_FP4>(gate_up, maps, a, plan.smem, grid, st); break;
+    default: return MNW_E_MODE;
+  }
+  return e == cudaSuccess ? MNW_OK : MNW_E_CUDA;
+}
+
+}  // namespace mnw

@@ -1,0 +1,43 @@
+// mnw_internal.h -- host-side state shared by the library's translation units.
+#pragma once
+#include <cstddef>
+#include <cstdint>
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include "../../include/mnw_moe.h"
+
+struct mnw_moe_layer {
+  int wfmt, E, H, I, group;
+  const uint8_t* blob;        // device, borrowed
+  size_t blob_bytes;
+  uint64_t data_offset, expert_stride;
+  uint64_t codes_off[3], scales_off[3], outer_off[3];
+  int device, num_sms;
+  // Weight tensor maps (built once): codes per matrix, NVFP4 block scales per matrix.
+  CUtensorMap tm_codes[3];
+  CUtensorMap tm_sf[3];
+};
+
+namespace mnw {
+
+inline bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
+
+// Encode a tiled tensor map; returns false on failure.
+bool encode_map(CUtensorMap* map, CUtensorMapDataType dtype, int rank, const void* base, const uint64_t* dims,
+                const uint64_t* strides_bytes, const uint32_t* box, CUtensorMapSwizzle swizzle);
+
+// Launchers (arguments already validated by the ABI functions).
+cudaError_t launch_permute(const int32_t* ids, int T, int k, int E, int32_t* offsets, int32_t* sorted_assign,
+                           int32_t* assign_pos, const void* x, int H, void* x_perm, uint32_t* err,
+                           cudaStream_t st);
+cudaError_t launch_combine(const void* y, const int32_t* assign_pos, const float* w, int T, int k, int H,
+                           void* out, cudaStream_t st);
+cudaError_t launch_quantize(int act, const void* x, int R, int K, const int32_t* row_index, int index_div,
+                            void* codes, void* scales, float* row_outer, cudaStream_t st);
+// Grouped GEMM for weight format wfmt and activation mode act.
+int run_gemm(const mnw_moe_layer* L, int wfmt, int act, int kind, const void* a0, const void* a1,
+             const void* a2, const int32_t* offsets, int P, void* out, int32_t* dots, uint32_t* err,
+             cudaStream_t st);
+
+}  // namespace mnw

@@ -1,0 +1,169 @@
+// mnw_quant.cu -- dynamic activation quantisers (bit-exact by construction:
+// every step is one IEEE binary32 operation with round-to-nearest-even, and
+// the FP8/FP4 roundings use the hardware's rn.satfinite conversions).
+//
+//  INT8 per 128 ("LLaDA2.2-flash-minnow" model card, W8A8/W4A8 paragraph):
+//    scale = amax / 127, code = clamp(rne(x / scale), -127, 127); amax 0 gives
+//    scale 0 and codes 0.  One warp per (row, 128-group), 4 values per lane.
+//  NVFP4 (model card, NVFP4 row, activation column): outer = amax_row / 2688,
+//    sb = e4m3(amax_16 / outer / 6), code = e2m1(x / (sb * outer)).  One warp
+//    per row; lane l handles 16-blocks l, l+32, ...
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+
+#include "mnw_internal.h"
+#include "mnw_ptx.cuh"
+
+namespace mnw {
+
+__device__ __forceinline__ int source_row(int r, const int32_t* row_index, int index_div) {
+  if (!row_index) return r;
+  const int a = __ldg(row_index + r);
+  return a < 0 ? -1 : a / index_div;
+}
+
+__global__ void __launch_bounds__(256) quant_int8_g128_kernel(const __nv_bfloat16* __restrict__ x, int R, int K,
+                                                              const int32_t* __restrict__ row_index,
+                                                              int index_div, int8_t* __restrict__ codes,
+                                                              float* __restrict__ scales) {
+  const int G = K / 128;
+  const long long total = static_cast<long long>(R) * G;
+  const int lane = threadIdx.x & 31;
+  for (long long wg = static_cast<long long>(blockIdx.x) * 8 + (threadIdx.x >> 5); wg < total;
+       wg += static_cast<long long>(gridDim.x) * 8) {
+    const int r = static_cast<int>(wg / G), g = static_cast<int>(wg % G);
+    const int src = source_row(r, row_index, index_div);
+    float v[4] = {0.f, 0.f, 0.f, 0.f};
+    if (src >= 0) {
+      const uint2 raw = __ldg(reinterpret_cast<const uint2*>(x + static_cast<size_t>(src) * K + g * 128) + lane);
+      const float2 a = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&raw.x));
+      const float2 b = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&raw.y));
+      v[0] = a.x; v[1] = a.y; v[2] = b.x; v[3] = b.y;
+    }
+    float amax = fmaxf(fmaxf(fabsf(v[0]), fabsf(v[1])), fmaxf(fabsf(v[2]), fabsf(v[3])));
+#pragma unroll
+    for (int d = 16; d > 0; d >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, d));
+    uint32_t packed = 0;
+    float scale = 0.f;
+    if (amax > 0.f) {
+      scale = __fdiv_rn(amax, 127.0f);
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        int q = __float2int_rn(__fdiv_rn(v[i], scale));
+        q = max(-127, min(127, q));
+        packed |= (static_cast<uint32_t>(q) & 0xFFu) << (8 * i);
+      }
+    }
+    reinterpret_cast<uint32_t*>(codes + static_cast<size_t>(r) * K + g * 128)[lane] = packed;
+    if (lane == 0) scales[static_cast<size_t>(r) * G + g] = scale;
+  }
+}
+
+__device__ __forceinline__ uint8_t e4m3_rn_satfinite(float s) {
+  uint16_t pair;
+  asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(pair) : "f"(0.0f), "f"(s));
+  return static_cast<uint8_t>(pair & 0xFF);
+}
+__device__ __forceinline__ float e4m3_to_float(uint8_t b) {
+  uint32_t h2;
+  const uint16_t in = static_cast<uint16_t>(b);
+  asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h2) : "h"(in));
+  return __half2float(__ushort_as_half(static_cast<uint16_t>(h2 & 0xFFFF)));
+}
+// Two values to one byte of E2M1 codes: lo in the low nibble, hi in the high one.
+__device__ __forceinline__ uint32_t e2m1x2_rn_satfinite(float lo, float hi) {
+  uint32_t out;
+  asm("{\n\t.reg .b8 t;\n\tcvt.rn.satfinite.e2m1x2.f32 t, %1, %2;\n\tcvt.u32.u8 %0, t;\n\t}"
+      : "=r"(out)
+      : "f"(hi), "f"(lo));
+  return out;
+}
+
+__global__ void __launch_bounds__(256) quant_nvfp4_g16_kernel(const __nv_bfloat16* __restrict__ x, int R, int K,
+                                                              const int32_t* __restrict__ row_index,
+                                                              int index_div, uint8_t* __restrict__ codes,
+                                                              uint8_t* __restrict__ sf, float* __restrict__ outer) {
+  const int lane = threadIdx.x & 31;
+  const int nb = K / 16;
+  for (int r = blockIdx.x * 8 + (threadIdx.x >> 5); r < R; r += gridDim.x * 8) {
+    const int src = source_row(r, row_index, index_div);
+    uint8_t* crow = codes + static_cast<size_t>(r) * (K / 2);
+    uint8_t* srow = sf + static_cast<size_t>(r) * nb;
+    const __nv_bfloat16* xr = src >= 0 ? x + static_cast<size_t>(src) * K : nullptr;
+    // row amax
+    float amax = 0.f;
+    if (xr) {
+      for (int b = lane; b < nb; b += 32) {
+        const uint4* p = reinterpret_cast<const uint4*>(xr + b * 16);
+        const uint4 q0 = __ldg(p), q1 = __ldg(p + 1);
+        const uint32_t w[8] = {q0.x, q0.y, q0.z, q0.w, q1.x, q1.y, q1.z, q1.w};
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          const float2 f = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&w[i]));
+          amax = fmaxf(amax, fmaxf(fabsf(f.x), fabsf(f.y)));
+        }
+      }
+    }
+#pragma unroll
+    for (int d = 16; d > 0; d >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, d));
+    const float o = __fdiv_rn(amax, 2688.0f);
+    if (lane == 0) outer[r] = o;
+    for (int b = lane; b < nb; b += 32) {
+      uint2 packed = make_uint2(0, 0);
+      uint8_t sbyte = 0;
+      if (xr && o != 0.f) {
+        const uint4* p = reinterpret_cast<const uint4*>(xr + b * 16);
+        const uint4 q0 = __ldg(p), q1 = __ldg(p + 1);
+        const uint32_t w[8] = {q0.x, q0.y, q0.z, q0.w, q1.x, q1.y, q1.z, q1.w};
+        float v[16];
+        float ab = 0.f;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          const float2 f = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&w[i]));
+          v[2 * i] = f.x;
+          v[2 * i + 1] = f.y;
+          ab = fmaxf(ab, fmaxf(fabsf(f.x), fabsf(f.y)));
+        }
+        sbyte = e4m3_rn_satfinite(__fdiv_rn(__fdiv_rn(ab, o), 6.0f));
+        const float d = __fmul_rn(e4m3_to_float(sbyte), o);
+        if (d != 0.f) {
+          uint32_t lo = 0, hi = 0;
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            lo |= e2m1x2_rn_satfinite(__fdiv_rn(v[2 * i], d), __fdiv_rn(v[2 * i + 1], d)) << (8 * i);
+            hi |= e2m1x2_rn_satfinite(__fdiv_rn(v[8 + 2 * i], d), __fdiv_rn(v[8 + 2 * i + 1], d)) << (8 * i);
+          }
+          packed = make_uint2(lo, hi);
+        }
+      }
+      reinterpret_cast<uint2*>(crow)[b] = packed;
+      srow[b] = sbyte;
+    }
+  }
+}
+
+cudaError_t launch_quantize(int act, const void* x, int R, int K, const int32_t* row_index, int index_div,
+                            void* codes, void* scales, float* row_outer, cudaStream_t st) {
+  int dev = 0, sms = 148;
+  cudaGetDevice(&dev);
+  cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  if (act == MNW_ACT_INT8_G128) {
+    const long long warps = static_cast<long long>(R) * (K / 128);
+    long long blocks = (warps + 7) / 8;
+    if (blocks > static_cast<long long>(sms) * 16) blocks = static_cast<long long>(sms) * 16;
+    if (blocks < 1) blocks = 1;
+    quant_int8_g128_kernel<<<static_cast<int>(blocks), 256, 0, st>>>(
+        static_cast<const __nv_bfloat16*>(x), R, K, row_index, index_div, static_cast<int8_t*>(codes),
+        static_cast<float*>(scales));
+  } else {
+    long long blocks = (static_cast<long long>(R) + 7) / 8;
+    if (blocks > static_cast<long long>(sms) * 16) blocks = static_cast<long long>(sms) * 16;
+    if (blocks < 1) blocks = 1;
+    quant_nvfp4_g16_kernel<<<static_cast<int>(blocks), 256, 0, st>>>(
+        static_cast<const __nv_bfloat16*>(x), R, K, row_index, index_div, static_cast<uint8_t*>(codes),
+        static_cast<uint8_t*>(scales), row_outer);
+  }
+  return cudaGetLastError();
+}
+
+}  // namespace mnw

@@ -1,0 +1,242 @@
+// mnw_route.cu -- token permutation into expert-sorted order, the row gather,
+// and the top-k weighted combine.
+//
+// Permutation ("GPU routing for 32-token decode blocks", coder543/minnow
+// README, "Quantization"): a single CTA ranks every assignment a = t*k + j
+// stably within its expert, with no atomics whose order could leak into the
+// result.  Each of the 32 warps owns a contiguous segment of assignments; a
+// first pass counts per (warp, expert) with warp match-any groups, a scan over
+// (expert, warp) turns counts into starting positions, and a second pass
+// re-walks the segment in order, ranking lanes that share an expert by lane
+// index.
+#include <cuda_bf16.h>
+
+#include "mnw_internal.h"
+#include "mnw_ptx.cuh"
+
+namespace mnw {
+
+constexpr int kPermThreads = 1024;
+constexpr int kPermWarps = kPermThreads / 32;
+constexpr int kPermBatchesInFlight = 8;  // id loads issued ahead per lane
+
+__global__ void __launch_bounds__(kPermThreads, 1)
+    permute_kernel(const int32_t* __restrict__ ids, int P, int E, int32_t* __restrict__ offsets,
+                   int32_t* __restrict__ sorted_assign, int32_t* __restrict__ assign_pos,
+                   uint32_t* __restrict__ err) {
+  extern __shared__ int32_t sm[];
+  int32_t* cnt = sm;                       // [kPermWarps][E]: counts, then next position
+  int32_t* tot = sm + kPermWarps * E;      // [E]
+  __shared__ int32_t warp_tot[kPermWarps];
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+
+  for (int i = tid; i < kPermWarps * E; i += kPermThreads) cnt[i] = 0;
+  for (int a = tid; a < P; a += kPermThreads) sorted_assign[a] = -1;
+  __syncthreads();
+
+  const int seg = (P + kPermWarps - 1) / kPermWarps;
+  const int a0 = min(P, warp * seg), a1 = min(P, a0 + seg);
+  int32_t* my = cnt + warp * E;
+
+  // Pass 1: per-warp counts.
+  for (int base = a0; base < a1; base += 32 * kPermBatchesInFlight) {
+    int idv[kPermBatchesInFlight];
+#pragma unroll
+    for (int b = 0; b < kPermBatchesInFlight; ++b) {
+      const int a = base + b * 32 + lane;
+      idv[b] = a < a1 ? __ldg(ids + a) : INT32_MIN;
+    }
+#pragma unroll
+    for (int b = 0; b < kPermBatchesInFlight; ++b) {
+      const int a = base + b * 32 + lane;
+      const bool active = a < a1;
+      const int id = idv[b];
+      const bool valid = active && id >= 0 && id < E;
+      if (active && !valid && err) atomicOr(err, MNW_DEVERR_BAD_EXPERT_ID);
+      const uint32_t vmask = __ballot_sync(0xffffffffu, valid);
+      if (valid) {
+        const uint32_t peers = __match_any_sync(vmask, id);
+        if (lane == __ffs(peers) - 1) my[id] += __popc(peers);
+      }
+      __syncwarp();
+    }
+  }
+  __syncthreads();
+
+  // Exclusive prefix over warps for every expert; totals per expert.
+  for (int e = tid; e < E; e += kPermThreads) {
+    int run = 0;
+    for (int w = 0; w < kPermWarps; ++w) {
+      const int c = cnt[w * E + e];
+      cnt[w * E + e] = run;
+      run += c;
+    }
+    tot[e] = run;
+  }
+  __syncthreads();
+
+  // Exclusive scan of the totals over experts (E <= kPermThreads).
+  const int v = tid < E ? tot[tid] : 0;
+  int incl = v;
+#pragma unroll
+  for (int d = 1; d < 32; d <<= 1) {
+    const int o = __shfl_up_sync(0xffffffffu, incl, d);
+    if (lane >= d) incl += o;
+  }
+  if (lane == 31) warp_tot[warp] = incl;
+  __syncthreads();
+  if (warp == 0) {
+    int t = warp_tot[lane];
+    int ti = t;
+#pragma unroll
+    for (int d = 1; d < 32; d <<= 1) {
+      const int o = __shfl_up_sync(0xffffffffu, ti, d);
+      if (lane >= d) ti += o;
+    }
+    warp_tot[lane] = ti - t;  // exclusive prefix of warp totals
+  }
+  __syncthreads();
+  const int excl = incl - v + warp_tot[warp];
+  if (tid < E) {
+    offsets[tid] = excl;
+    tot[tid] = excl;
+    if (tid == E - 1) offsets[E] = excl + v;
+  }
+  __syncthreads();
+  for (int i = tid; i < kPermWarps * E; i += kPermThreads) cnt[i] += tot[i % E];
+  __syncthreads();
+
+  // Pass 2: stable positions.
+  const uint32_t lt_mask = (1u << lane) - 1u;
+  for (int base = a0; base < a1; base += 32 * kPermBatchesInFlight) {
+    int idv[kPermBatchesInFlight];
+#pragma unroll
+    for (int b = 0; b < kPermBatchesInFlight; ++b) {
+      const int a = base + b * 32 + lane;
+      idv[b] = a < a1 ? __ldg(ids + a) : INT32_MIN;
+    }
+#pragma unroll
+    for (int b = 0; b < kPermBatchesInFlight; ++b) {
+      const int a = base + b * 32 + lane;
+      const bool active = a < a1;
+      const int id = idv[b];
+      const bool valid = active && id >= 0 && id < E;
+      const uint32_t vmask = __ballot_sync(0xffffffffu, valid);
+      uint32_t peers = 0;
+      if (valid) {
+        peers = __match_any_sync(vmask, id);
+        const int pos = my[id] + __popc(peers & lt_mask);
+        assign_pos[a] = pos;
+        sorted_assign[pos] = a;
+      } else if (active) {
+        assign_pos[a] = -1;
+      }
+      __syncwarp();
+      if (valid && lane == __ffs(peers) - 1) my[id] += __popc(peers);
+      __syncwarp();
+    }
+  }
+}
+
+// x_perm[p] = x[sorted_assign[p] / k], zeros where sorted_assign[p] < 0.  One
+// warp per row, 16-byte vectors.
+__global__ void __launch_bounds__(256) gather_rows_kernel(const uint4* __restrict__ x, int H8,
+                                                          const int32_t* __restrict__ sorted_assign, int P,
+                                                          int k, uint4* __restrict__ x_perm) {
+  const int warps = gridDim.x * 8;
+  for (int p = blockIdx.x * 8 + (threadIdx.x >> 5); p < P; p += warps) {
+    const int a = __ldg(sorted_assign + p);
+    uint4* dst = x_perm + static_cast<size_t>(p) * H8;
+    if (a < 0) {
+      for (int c = threadIdx.x & 31; c < H8; c += 32) dst[c] = make_uint4(0, 0, 0, 0);
+      continue;
+    }
+    const uint4* src = x + static_cast<size_t>(a / k) * H8;
+    for (int c = threadIdx.x & 31; c < H8; c += 32) dst[c] = __ldg(src + c);
+  }
+}
+
+// out[t] = bf16(sum_j w[t, j] * y[assign_pos[t*k + j]]), FP32, j ascending.
+__global__ void __launch_bounds__(256) combine_kernel(const uint4* __restrict__ y,
+                                                      const int32_t* __restrict__ assign_pos,
+                                                      const float* __restrict__ w, int T, int k, int H8,
+                                                      uint4* __restrict__ out) {
+  __shared__ int32_t s_pos[8][32];
+  __shared__ float s_w[8][32];
+  const int warps = gridDim.x * 8;
+  const int lane = threadIdx.x & 31, wib = threadIdx.x >> 5;
+  for (int t = blockIdx.x * 8 + wib; t < T; t += warps) {
+    // slot j's position and weight, staged once per token
+    s_pos[wib][lane] = lane < k ? __ldg(assign_pos + static_cast<size_t>(t) * k + lane) : -1;
+    s_w[wib][lane] = lane < k ? __ldg(w + static_cast<size_t>(t) * k + lane) : 0.f;
+    __syncwarp();
+    for (int c = lane; c < H8; c += 32) {
+      float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+      for (int j = 0; j < k; ++j) {
+        const int p = s_pos[wib][j];
+        const float wj = s_w[wib][j];
+        if (p < 0) continue;
+        const uint4 v = __ldg(y + static_cast<size_t>(p) * H8 + c);
+        const uint32_t vv[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          const float2 f = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&vv[i]));
+          acc[2 * i] = __fmaf_rn(wj, f.x, acc[2 * i]);
+          acc[2 * i + 1] = __fmaf_rn(wj, f.y, acc[2 * i + 1]);
+        }
+      }
+      uint32_t o[4];
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        __nv_bfloat162 b = __floats2bfloat162_rn(acc[2 * i], acc[2 * i + 1]);
+        o[i] = *reinterpret_cast<uint32_t*>(&b);
+      }
+      out[static_cast<size_t>(t) * H8 + c] = make_uint4(o[0], o[1], o[2], o[3]);
+    }
+    __syncwarp();
+  }
+}
+
+static int grid_for(int rows_per_block, int n, int cap) {
+  int g = (n + rows_per_block - 1) / rows_per_block;
+  return g < 1 ? 1 : (g > cap ? cap : g);
+}
+
+cudaError_t launch_permute(const int32_t* ids, int T, int k, int E, int32_t* offsets, int32_t* sorted_assign,
+                           int32_t* assign_pos, const void* x, int H, void* x_perm, uint32_t* err,
+                           cudaStream_t st) {
+  const int P = T * k;
+  const size_t smem = static_cast<size_t>(kPermWarps + 1) * E * sizeof(int32_t);
+  static bool attr_set = false;
+  if (!attr_set) {
+    cudaError_t e = cudaFuncSetAttribute(permute_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         static_cast<int>((kPermWarps + 1) * 1024 * sizeof(int32_t)));
+    if (e != cudaSuccess) return e;
+    attr_set = true;
+  }
+  permute_kernel<<<1, kPermThreads, smem, st>>>(ids, P, E, offsets, sorted_assign, assign_pos, err);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  if (x && x_perm && P > 0) {
+    int dev = 0, sms = 148;
+    cudaGetDevice(&dev);
+    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    gather_rows_kernel<<<grid_for(8, P, sms * 8), 256, 0, st>>>(static_cast<const uint4*>(x), H / 8,
+                                                                 sorted_assign, P, k,
+                                                                 static_cast<uint4*>(x_perm));
+    e = cudaGetLastError();
+  }
+  return e;
+}
+
+cudaError_t launch_combine(const void* y, const int32_t* assign_pos, const float* w, int T, int k, int H,
+                           void* out, cudaStream_t st) {
+  int dev = 0, sms = 148;
+  cudaGetDevice(&dev);
+  cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  combine_kernel<<<grid_for(8, T, sms * 8), 256, 0, st>>>(static_cast<const uint4*>(y), assign_pos, w, T, k,
+                                                          H / 8, static_cast<uint4*>(out));
+  return cudaGetLastError();
+}
+
+}  // namespace mnw

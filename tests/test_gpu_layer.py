@@ -1,0 +1,84 @@
+"""Whole-layer parity: mnw_moe_forward against the oracle's token-by-token
+layer, on every workload (small ones in full, large ones on sampled tokens,
+each token's output depending only on its own row)."""
+import numpy as np
+import pytest
+import torch
+
+import oracle as O
+import synth as S
+from gpu_util import REL_L2, REL_L2_NVFP4, assert_close, to_np_bits
+
+pytestmark = pytest.mark.gpu
+DEV = "cuda"
+
+
+@pytest.fixture(scope="module")
+def M():
+    import quantized_moe_expert_routed_gb300 as M
+    M.load()
+    return M
+
+
+def _run(M, wl, rows=None, scale_down=None):
+    if scale_down:
+        wl = S.Workload(**{**wl.__dict__, **scale_down})
+    x, ids, w, blob, hdr, L = S.make_inputs(wl, device=DEV)
+    layer = M.Layer(blob, hdr)
+    ws = M.workspace(layer, wl.act, wl.T, wl.k)
+    out = M.mnw_moe_forward(layer, wl.act, x, ids, w, ws=ws)
+    err = M.mnw_moe_read_error(M.workspace_error_word(ws))
+    assert err == 0
+    if rows is None:
+        rows = np.arange(wl.T, dtype=np.int32)
+    want = O.moe_forward(blob.cpu().numpy(), wl.act, S.bf16_bits_np(x), ids.cpu().numpy(), w.cpu().numpy(),
+                         rows=rows)
+    got = out[torch.from_numpy(rows).long().to(DEV)]
+    tol = REL_L2_NVFP4 if wl.act == S.ACT_NVFP4_G16 else REL_L2
+    return assert_close(got, want, rel_l2=tol, what=wl.name)
+
+
+def test_tiny_w8a16_full(M):
+    _run(M, S.WORKLOADS["tiny_w8a16"])
+
+
+@pytest.mark.parametrize("name", ["decode_w4a16", "w8a8_2048", "prefill_nvfp4", "large_w4a16", "large_bf16"])
+def test_small_versions_full(M, name):
+    """Each workload's formats, modes and routing at a size the oracle runs in full."""
+    wl = S.WORKLOADS[name]
+    small = dict(T=48, E=64, H=512, I=256 if wl.wfmt != S.FMT_NVFP4_G16 else 512)
+    _run(M, wl, scale_down=small)
+
+
+@pytest.mark.parametrize("name,nrows", [("decode_w4a16", 16), ("w8a8_2048", 8), ("prefill_nvfp4", 8),
+                                        ("large_w4a16", 3), ("large_bf16", 3)])
+def test_full_size_sampled(M, name, nrows):
+    wl = S.WORKLOADS[name]
+    rows = np.linspace(0, wl.T - 1, nrows).astype(np.int32)
+    _run(M, wl, rows=rows)
+
+
+def test_forward_host_buffers(M):
+    wl = S.WORKLOADS["tiny_w8a16"]
+    x, ids, w, blob, hdr, L = S.make_inputs(wl, device=DEV)
+    layer = M.Layer(blob, hdr)
+    ws = M.workspace(layer, wl.act, wl.T, wl.k, host=True)
+    out_h = torch.empty((wl.T, wl.H), dtype=torch.bfloat16).pin_memory()
+    M.mnw_moe_forward_host(layer, wl.act, x.cpu().pin_memory(), ids.cpu().pin_memory(), w.cpu().pin_memory(), ws,
+                           out_h)
+    ref = M.mnw_moe_forward(layer, wl.act, x, ids, w)
+    assert torch.equal(out_h.view(torch.int16), ref.cpu().view(torch.int16))
+
+
+def test_deterministic_and_bad_ids(M):
+    wl = S.Workload(**{**S.WORKLOADS["decode_w4a16"].__dict__, "E": 32, "H": 512, "I": 256})
+    x, ids, w, blob, hdr, L = S.make_inputs(wl, device=DEV)
+    layer = M.Layer(blob, hdr)
+    a = M.mnw_moe_forward(layer, wl.act, x, ids, w)
+    b = M.mnw_moe_forward(layer, wl.act, x, ids, w)
+    assert torch.equal(a.view(torch.int16), b.view(torch.int16))
+    ids2 = ids.clone()
+    ids2[0, 0] = 1000
+    ws = M.workspace(layer, wl.act, wl.T, wl.k)
+    M.mnw_moe_forward(layer, wl.act, x, ids2, w, ws=ws)
+    assert M.mnw_moe_read_error(M.workspace_error_word(ws)) & M.DEVERR_BAD_EXPERT_ID
