@@ -22,6 +22,7 @@ FMT_BF16, FMT_INT8_G128, FMT_INT4_G128, FMT_NVFP4_G16 = 0, 1, 2, 3
 ACT_BF16, ACT_INT8_G128, ACT_NVFP4_G16 = 0, 1, 2
 KIND_GATE_UP, KIND_DOWN = 0, 1
 DEVERR_BAD_EXPERT_ID, DEVERR_TIMEOUT = 0x1, 0x2
+PATH_AUTO, PATH_TCGEN05, PATH_WARP_MMA = 0, 1, 2
 
 # Symbols of include/mnw_moe.h, with their ctypes signatures.
 _P, _I, _SZ, _U32P = ctypes.c_void_p, ctypes.c_int, ctypes.c_size_t, ctypes.c_void_p
@@ -45,6 +46,7 @@ SIGNATURES = {
     "mnw_moe_workspace_size_host": (_SZ, [_P, _I, _I, _I]),
     "mnw_moe_forward_host": (_I, [_P, _I, _P, _P, _P, _I, _I, _P, _P, _SZ, _P]),
     "mnw_moe_read_error": (_I, [_P, _P, _P]),
+    "mnw_moe_set_gemm_path": (_I, [_I]),
 }
 
 _lib = None
@@ -260,3 +262,8 @@ def mnw_moe_read_error(err, stream=None) -> int:
     out = ctypes.c_uint32()
     _check(load().mnw_moe_read_error(_ptr(err), ctypes.byref(out), _stream(stream)), "mnw_moe_read_error")
     return out.value
+
+
+def mnw_moe_set_gemm_path(path: int) -> None:
+    """Process-wide grouped-GEMM kernel choice (PATH_AUTO, PATH_TCGEN05, PATH_WARP_MMA)."""
+    _check(load().mnw_moe_set_gemm_path(path), "mnw_moe_set_gemm_path")

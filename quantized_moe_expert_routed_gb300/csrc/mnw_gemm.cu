@@ -15,8 +15,9 @@
 //
 // Dequantisation happens in registers on the way into the tensor cores; no
 // expanded weight copy exists in memory.  INT codes are exact in BF16/FP16, so
-// the only rounding in the INT paths is the FP32 accumulation: each 128-wide
-// group's dot product is exact (|D| < 2^24) and is scaled and summed in FP32.
+// the weights themselves are never rounded: each 128-wide group's dot product
+// is accumulated in FP32 on the tensor cores (exact for INT8 activations,
+// since |D| < 2^24) and is scaled and summed in FP32.
 //
 // Layout of the problem ("swap AB"): the weight matrix supplies the M = 128
 // rows of the MMA (128 output features per tile) and the tokens routed to one
@@ -47,6 +48,7 @@
 
 #include <cstdio>
 
+#include "mnw_convert.cuh"
 #include "mnw_internal.h"
 #include "mnw_ptx.cuh"
 
@@ -61,7 +63,8 @@ constexpr int kEpiWarps = 4;
 constexpr int kWarpTma = 0, kWarpMma = 1, kWarpConv0 = 2, kWarpEpi0 = kWarpConv0 + kConvWarps;
 constexpr int kThreads = (kWarpEpi0 + kEpiWarps) * 32;
 constexpr int kMaxStages = 8;
-constexpr int kASlots = 4;
+constexpr int kMaxASlots = 8;   // operand-A ring slots in TMEM (runtime count <= this)
+constexpr int kMaxAcc = 8;      // accumulator slots (runtime count <= this)
 constexpr int kTmemCols = 512;
 
 
@@ -82,8 +85,8 @@ struct GemmArgs {
 
 struct Bars {
   uint64_t full[kMaxStages], empty[kMaxStages], bconv[kMaxStages];
-  uint64_t afull[kASlots], aempty[kASlots];
-  uint64_t accfull[2], accempty[2];
+  uint64_t afull[kMaxASlots], aempty[kMaxASlots];
+  uint64_t accfull[kMaxAcc], accempty[kMaxAcc];
   uint64_t sfull[2], sempty[2];
   uint64_t final_mma;
   uint32_t tmem_base;
@@ -97,115 +100,6 @@ struct WT {
   static constexpr bool kTs = WF != WF_BF16;                                         // A from TMEM
   static constexpr bool kScales = WF == WF_INT8 || WF == WF_INT4;                    // FP16 group scales
 };
-
-// ---------------------------------------------------------------------------
-// conversions (register level)
-// ---------------------------------------------------------------------------
-
-__device__ __forceinline__ uint32_t bf16x2_sub(uint32_t a, uint32_t b) {
-  uint32_t d;
-  asm("sub.rn.bf16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
-  return d;
-}
-__device__ __forceinline__ uint32_t f16x2_sub(uint32_t a, uint32_t b) {
-  uint32_t d;
-  asm("sub.rn.f16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
-  return d;
-}
-__device__ __forceinline__ uint32_t f16x2_mul(uint32_t a, uint32_t b) {
-  uint32_t d;
-  asm("mul.rn.f16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
-  return d;
-}
-__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
-  uint32_t d;
-  asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(d) : "f"(hi), "f"(lo));
-  return d;
-}
-
-// 32 signed INT4 codes (one 16-byte chunk, element 2c in the low nibble of
-// byte c) -> 16 words of (even, odd) pairs holding the integers q exactly, as
-// BF16 (kBf16) or FP16.  The group scale is applied later, in FP32.
-template <bool kBf16>
-__device__ __forceinline__ void cvt_int4x32(const uint4 v, uint32_t (&o)[16]) {
-  const uint32_t w[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    const uint32_t hi = w[i] >> 4;
-#pragma unroll
-    for (int b = 0; b < 4; ++b) {
-      const uint32_t x = prmt(w[i], hi, 0x0400u + 0x0101u * b);  // byte b: low nibble -> half 0, high -> half 1
-      if (kBf16) {
-        // 0x4308 ^ n is BF16 128 + (n_signed + 8); subtracting 136 is exact.
-        o[i * 4 + b] = bf16x2_sub(and_xor(x, 0x000F000Fu, 0x43084308u), 0x43084308u);
-      } else {
-        // FP16 1024 + (n_signed + 8) minus 1032.
-        o[i * 4 + b] = f16x2_sub(and_xor(x, 0x000F000Fu, 0x64086408u), 0x64086408u);
-      }
-    }
-  }
-}
-
-// 32 signed INT8 codes (two 16-byte chunks) -> 16 words holding the integers
-// q exactly, as BF16 (kBf16) or FP16.
-template <bool kBf16>
-__device__ __forceinline__ void cvt_int8x32(const uint4 v0, const uint4 v1, uint32_t (&o)[16]) {
-  const uint32_t w[8] = {v0.x, v0.y, v0.z, v0.w, v1.x, v1.y, v1.z, v1.w};
-#pragma unroll
-  for (int i = 0; i < 8; ++i) {
-    const uint32_t u = w[i] ^ 0x80808080u;  // q + 128 per byte
-    if (kBf16) {
-      float f[4];
-#pragma unroll
-      for (int b = 0; b < 4; ++b) {
-        // 0x4B0000uu is FP32 2^23 + u; minus (2^23 + 128) gives q exactly.
-        f[b] = __fsub_rn(__uint_as_float(prmt(u, 0x4B000000u, 0x7540u + b)), 8388736.0f);
-      }
-      o[2 * i] = pack_bf16x2(f[0], f[1]);
-      o[2 * i + 1] = pack_bf16x2(f[2], f[3]);
-    } else {
-      // 0x64uu is FP16 1024 + u; minus 1152 gives q exactly.
-      o[2 * i] = f16x2_sub(prmt(u, 0x64646464u, 0x4140u), 0x64806480u);
-      o[2 * i + 1] = f16x2_sub(prmt(u, 0x64646464u, 0x4342u), 0x64806480u);
-    }
-  }
-}
-
-// 32 E2M1 codes (one 16-byte chunk) with the E4M3 scales of its two 16-blocks
-// -> 16 words of exact FP16 products.
-__device__ __forceinline__ void cvt_fp4x32(const uint4 v, uint32_t sf0, uint32_t sf1, uint32_t (&o)[16]) {
-  uint32_t s0, s1;
-  asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(s0) : "h"(static_cast<uint16_t>(sf0 | (sf0 << 8))));
-  asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(s1) : "h"(static_cast<uint16_t>(sf1 | (sf1 << 8))));
-  const uint32_t w[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    uint32_t h0, h1, h2, h3;
-    asm("{\n\t.reg .b8 b0, b1, b2, b3;\n\tmov.b32 {b0, b1, b2, b3}, %4;\n\t"
-        "cvt.rn.f16x2.e2m1x2 %0, b0;\n\tcvt.rn.f16x2.e2m1x2 %1, b1;\n\t"
-        "cvt.rn.f16x2.e2m1x2 %2, b2;\n\tcvt.rn.f16x2.e2m1x2 %3, b3;\n\t}"
-        : "=r"(h0), "=r"(h1), "=r"(h2), "=r"(h3)
-        : "r"(w[i]));
-    const uint32_t s = i < 2 ? s0 : s1;
-    o[4 * i + 0] = f16x2_mul(h0, s);
-    o[4 * i + 1] = f16x2_mul(h1, s);
-    o[4 * i + 2] = f16x2_mul(h2, s);
-    o[4 * i + 3] = f16x2_mul(h3, s);
-  }
-}
-
-// Address of 16-byte chunk c of row r in a 128-byte-swizzled tile.
-__device__ __forceinline__ uint32_t sw128(uint32_t base, int r, int c) {
-  return base + r * 128 + ((c ^ (r & 7)) << 4);
-}
-__device__ __forceinline__ uint4 lds128(uint32_t addr) {
-  uint4 v;
-  asm volatile("ld.shared.v4.u32 {%0,%1,%2,%3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "r"(addr));
-  return v;
-}
-__device__ __forceinline__ void sts128(uint32_t addr, uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
-  asm volatile("st.shared.v4.u32 [%0], {%1,%2,%3,%4};" ::"r"(addr), "r"(a), "r"(b), "r"(c), "r"(d) : "memory");
-}
 
 // ---------------------------------------------------------------------------
 // work decomposition
@@ -277,13 +171,15 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&bars->empty[s], ((T::kTs || kBconv) ? kConvWarps : 0) + 1);
       mbar_init(&bars->bconv[s], kConvWarps);
     }
-    for (int i = 0; i < kASlots; ++i) {
+    for (int i = 0; i < kMaxASlots; ++i) {
       mbar_init(&bars->afull[i], kConvWarps);
       mbar_init(&bars->aempty[i], 1);
     }
-    for (int i = 0; i < 2; ++i) {
+    for (int i = 0; i < kMaxAcc; ++i) {
       mbar_init(&bars->accfull[i], 1);
       mbar_init(&bars->accempty[i], kEpiWarps);
+    }
+    for (int i = 0; i < 2; ++i) {
       mbar_init(&bars->sfull[i], 1);
       mbar_init(&bars->sempty[i], kEpiWarps);
     }
@@ -425,9 +321,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int kg = ks * T::kStage + sc * 64;
             uint32_t gslot = 0;
             if (kGrouped) {
-              gslot = acc_it & 1;
+              gslot = acc_it % args.acc_slots;
               if ((kg & 127) == 0) {
-                if (!bounded_wait(&bars->accempty[gslot], ((acc_it >> 1) & 1) ^ 1, abort, args.err)) {
+                if (!bounded_wait(&bars->accempty[gslot], ((acc_it / args.acc_slots) & 1) ^ 1, abort, args.err)) {
                   ok = false;
                   break;
                 }
@@ -645,8 +541,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             r * G;
         const uint32_t dsum = tmem + lane_bits + args.sum_base;
         for (int g = 0; g < G; ++g) {
-          const uint32_t slot = acc_it & 1;
-          if (!bounded_wait(&bars->accfull[slot], (acc_it >> 1) & 1, abort, args.err)) { ok = false; break; }
+          const uint32_t slot = acc_it % args.acc_slots;
+          if (!bounded_wait(&bars->accfull[slot], (acc_it / args.acc_slots) & 1, abort, args.err)) { ok = false; break; }
           tc_fence_after();
           const uint32_t d = tmem + lane_bits + args.acc_base + slot * kNmat * BN;
           const float w0 = __half2float(sw0[g]), w1 = __half2float(sw1[g]);
@@ -814,6 +710,15 @@ int run_gemm(const mnw_moe_layer* L, int wfmt, int act, int kind, const void* a0
   if (!a0 || !offsets || !out || !aligned(a0, 16) || !aligned(out, 16)) return MNW_E_INVALID_ARG;
   if (act == MNW_ACT_INT8_G128 && (!a1 || !aligned(a1, 16))) return MNW_E_INVALID_ARG;
   if (act == MNW_ACT_NVFP4_G16 && (!a1 || !a2 || !aligned(a1, 16) || !aligned(a2, 16))) return MNW_E_INVALID_ARG;
+  // Few tokens per expert: the warp-MMA kernel streams INT weights faster (see
+  // mnw_gemm_warp.cu); larger token tiles use tcgen05 below.
+  const int mean_rows = (P + L->E - 1) / L->E;
+  const int path = gemm_path();
+  if (warp_gemm_applicable(L, wfmt, act, kind) &&
+      (path == MNW_PATH_WARP_MMA || (path == MNW_PATH_AUTO && mean_rows <= 64))) {
+    const int nt = mean_rows <= 8 ? 1 : (mean_rows <= 16 ? 2 : 4);
+    return run_gemm_warp(L, wfmt, act, kind, a0, a1, offsets, P, nt, out, dots, err, st);
+  }
   const bool gate_up = kind == MNW_KIND_GATE_UP;
   const int K = gate_up ? L->H : L->I;
   const int N = gate_up ? L->I : L->H;
@@ -843,20 +748,26 @@ int run_gemm(const mnw_moe_layer* L, int wfmt, int act, int kind, const void* a0
   a.BN = BN;
   a.n_tiles = N / kBM;
   a.nmat = nmat;
-  if (grouped) {
-    // [A ring | 2 group accumulators | running sum]
-    a.aslots = gate_up ? 2 : 4;
-    a.acc_base = a.aslots * nmat * 32;
-    a.acc_slots = 2;
-    a.sum_base = a.acc_base + 2 * nmat * BN;
-    if (a.sum_base + nmat * BN > kTmemCols) return MNW_E_UNSUPPORTED;
-  } else {
-    a.aslots = kASlots;
-    a.acc_base = ts ? kASlots * nmat * 32 : 0;
-    const int acc_cols = kTmemCols - a.acc_base;
-    a.acc_slots = (2 * nmat * BN <= acc_cols) ? 2 : 1;
-    a.sum_base = 0;
-    if (nmat * BN > acc_cols) return MNW_E_UNSUPPORTED;
+  {
+    // TMEM columns: [A ring | accumulator slots | running sum (grouped)].
+    // Deep rings hide the converter -> MMA -> epilogue hand-off latency; small
+    // token tiles leave room for more slots.
+    const int a_cols = ts ? nmat * 32 : 0;
+    const int d_cols = nmat * BN;
+    const int sum_cols = grouped ? nmat * BN : 0;
+    int na = ts ? 2 : 0, nacc = grouped ? 2 : 1;
+    auto fits = [&](int x, int y) { return x * a_cols + y * d_cols + sum_cols <= kTmemCols; };
+    if (!fits(na, nacc)) return MNW_E_UNSUPPORTED;
+    // grow in turn: accumulators to 2, A ring to 4, accumulators to 4, A ring to 8, accumulators to 8
+    const int steps[5][2] = {{0, 2}, {4, 0}, {0, 4}, {8, 0}, {0, 8}};
+    for (const auto& st : steps) {
+      if (st[0]) while (ts && na < st[0] && fits(na + 1, nacc)) ++na;
+      if (st[1]) while (nacc < st[1] && fits(na, nacc + 1)) ++nacc;
+    }
+    a.aslots = ts ? na : 1;
+    a.acc_slots = nacc;
+    a.acc_base = na * a_cols;
+    a.sum_base = a.acc_base + nacc * d_cols;
   }
   a.experts = L->blob + L->data_offset;
   a.expert_stride = L->expert_stride;

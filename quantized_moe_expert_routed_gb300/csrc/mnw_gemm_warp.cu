@@ -1,0 +1,523 @@
+// mnw_gemm_warp.cu -- grouped expert GEMMs for INT8/INT4 weights when few
+// tokens are routed to each expert (decode batches, the INT8-activation mode
+// at moderate batch).
+//
+// Measured on GB300 (sm_103a): a tcgen05.mma of kind::f16 with M = 128 costs
+// ~96 SM cycles whatever N <= 64 is, so with 8-16 tokens per expert one MMA
+// moves only 2048 weights per ~96 cycles -- under half of what streaming INT4
+// weights at HBM rate requires.  The warp-level m16n8k16 MMA moves 256
+// weights per cycle per SM at N = 8 (16 warps), so for this regime the
+// weights are dequantised straight into MMA operand registers:
+//
+//   TMA (one producer warp)  raw weight codes of a 128-K group for 256 weight
+//                            rows, and the group's slice of the expert's
+//                            token tile, into a shared-memory ring
+//   8 MMA warps (x2 CTAs/SM) codes -> exact BF16/FP16 integers in registers,
+//                            m16n8k16 MMAs into a per-group accumulator, then
+//                            acc += s_w (* s_a) * group_dot in FP32; SiLU(g)*u
+//                            or y written as BF16 straight from registers
+//
+// Weight format and numerics follow the "LLaDA2.2-flash-minnow" model card,
+// "Checkpoints and precision" (signed INT8/INT4, one FP16 scale per 128
+// weights; the W8A8/W4A8 mode's INT32 group dot products combined in FP32).
+// The weights are never rounded (integer codes are exact in BF16/FP16); each
+// 128-wide group's dot product is accumulated in FP32 (exact for INT8
+// activations) and combined exactly as in the tcgen05 path (mnw_gemm.cu), so
+// the two kernels give identical bits in the INT8-activation mode.
+//
+// Operand mapping.  Within one 128-K group, lane (g = lane/4, t = lane%4)
+// owns K = 32t .. 32t+31 of its rows (16 contiguous code bytes for INT4, 32
+// for INT8, 64 bytes of BF16 activations).  For k-step s (0..7) its A/B
+// fragment slots {2t, 2t+1} hold K = 32t+4s+{0,1} and slots {2t+8, 2t+9}
+// hold K = 32t+4s+{2,3}.  A and B use the same assignment, so the dot
+// product is unchanged and no shuffle is needed.
+//
+// Work unit: (expert, token tile of 8*NT rows, block of 256 weight rows).
+// gate/up: rows are 128 gate features + the same 128 up features, so each
+// thread ends with gate and up of the same (token, feature) and applies
+// SiLU(g)*u in registers.  down: 256 consecutive rows of Wd.
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+
+#include "mnw_convert.cuh"
+#include "mnw_internal.h"
+#include "mnw_ptx.cuh"
+
+namespace mnw {
+namespace warpmma {
+
+enum { WF_INT8 = 1, WF_INT4 = 2 };
+enum { AM_BF16 = 0, AM_INT8 = 1 };
+
+constexpr int kMmaWarps = 8;
+constexpr int kThreads = (1 + kMmaWarps) * 32;  // warp 0 = producer
+constexpr int kMaxStages = 12;
+constexpr int kRowsPerBox = 128;
+// CTAs per SM: two (16 MMA warps) for 8-token tiles, whose registers fit; one otherwise.
+template <int NT>
+constexpr int ctas_per_sm() { return NT == 1 ? 2 : 1; }
+
+struct Args {
+  const int32_t* offsets;
+  int E, P, K, N, BN, n_blocks, stages;
+  uint32_t stage_bytes, off_b, box_bytes, off_scales, scale_box_bytes, off_tab, off_bars;
+  const uint8_t* experts;
+  uint64_t expert_stride;
+  uint64_t scales_off[2];  // box 0 / box 1 matrices (gate, up) or (down, down)
+  int box_row_off[2];      // row offset of box 1 within its matrix (0 for gate/up, 128 for down)
+  const float* a_scales;   // INT8 activations: [P][K/128]
+  __nv_bfloat16* out;
+  int32_t* dots;
+  uint32_t* err;
+};
+
+struct Bars {
+  uint64_t full[kMaxStages], empty[kMaxStages];
+  uint64_t sfull[2], sempty[2];
+  int abort;
+};
+
+__device__ __forceinline__ void hmma_bf16(float (&c)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+      "{%0,%1,%2,%3};"
+      : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+__device__ __forceinline__ void hmma_f16(float (&c)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+      "{%0,%1,%2,%3};"
+      : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+
+// Work unit -> (expert, token tile, row block).
+struct Unit {
+  int e, rb, row0, nrows;
+};
+__device__ __forceinline__ Unit decode(const int* tab_prefix, const int* tab_off, int E, int n_blocks, int BN,
+                                       int u) {
+  Unit x;
+  const int t = u / n_blocks;
+  x.rb = u - t * n_blocks;
+  int lo = 0, hi = E - 1;
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if (tab_prefix[mid] <= t) lo = mid;
+    else hi = mid - 1;
+  }
+  x.e = lo;
+  x.row0 = tab_off[lo] + (t - tab_prefix[lo]) * BN;
+  x.nrows = min(BN, tab_off[lo + 1] - x.row0);
+  return x;
+}
+
+__device__ __forceinline__ void drain(uint64_t* bar, uint32_t parity) {
+  const uint64_t t0 = globaltimer();
+  while (!mbar_try_wait(bar, parity)) {
+    if (globaltimer() - t0 > kWaitLimitNs) return;
+  }
+}
+
+// Two (even, odd) operand words from byte pair (2p, 2p+1) of 8 INT4 codes.
+template <bool kBf16>
+__device__ __forceinline__ void int4_pair(uint32_t w, int p, uint32_t& lo, uint32_t& hi) {
+  const uint32_t sh = w >> 4;
+  const int b0 = 2 * p, b1 = 2 * p + 1;
+  const uint32_t x0 = prmt(w, sh, 0x0400u + 0x0101u * b0), x1 = prmt(w, sh, 0x0400u + 0x0101u * b1);
+  if (kBf16) {
+    lo = bf16x2_sub(and_xor(x0, 0x000F000Fu, 0x43084308u), 0x43084308u);
+    hi = bf16x2_sub(and_xor(x1, 0x000F000Fu, 0x43084308u), 0x43084308u);
+  } else {
+    lo = f16x2_sub(and_xor(x0, 0x000F000Fu, 0x64086408u), 0x64086408u);
+    hi = f16x2_sub(and_xor(x1, 0x000F000Fu, 0x64086408u), 0x64086408u);
+  }
+}
+// Two operand words from the 4 INT8 codes of one 32-bit word.
+template <bool kBf16>
+__device__ __forceinline__ void int8_pair(uint32_t w, uint32_t& lo, uint32_t& hi) {
+  const uint32_t u = w ^ 0x80808080u;
+  if (kBf16) {
+    float f[4];
+#pragma unroll
+    for (int b = 0; b < 4; ++b) f[b] = __fsub_rn(__uint_as_float(prmt(u, 0x4B000000u, 0x7540u + b)), 8388736.0f);
+    lo = pack_bf16x2(f[0], f[1]);
+    hi = pack_bf16x2(f[2], f[3]);
+  } else {
+    lo = f16x2_sub(prmt(u, 0x64646464u, 0x4140u), 0x64806480u);
+    hi = f16x2_sub(prmt(u, 0x64646464u, 0x4342u), 0x64806480u);
+  }
+}
+__device__ __forceinline__ uint32_t word_of(const uint4& v, int i) {
+  return i == 0 ? v.x : i == 1 ? v.y : i == 2 ? v.z : v.w;
+}
+
+template <int WF, int AM, bool kGateUp, int NT>
+__global__ void __launch_bounds__(kThreads, ctas_per_sm<NT>())
+    moe_gemm_warp_kernel(const __grid_constant__ CUtensorMap tmA0, const __grid_constant__ CUtensorMap tmA1,
+                         const __grid_constant__ CUtensorMap tmB, const Args args) {
+  constexpr bool kBf16 = AM == AM_BF16;
+  constexpr int kRB = WF == WF_INT4 ? 64 : 128;  // code bytes of one row per 128-K group
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  Bars* bars = reinterpret_cast<Bars*>(smem + args.off_bars);
+  int* tab_prefix = reinterpret_cast<int*>(smem + args.off_tab);
+  int* tab_off = tab_prefix + (args.E + 1);
+  volatile int* abort = &bars->abort;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int E = args.E, BN = args.BN, S = args.stages, G = args.K / 128;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kMaxStages; ++s) {
+      mbar_init(&bars->full[s], 1);
+      mbar_init(&bars->empty[s], kMmaWarps);
+    }
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&bars->sfull[i], 1);
+      mbar_init(&bars->sempty[i], kMmaWarps);
+    }
+    bars->abort = 0;
+    fence_barrier_init();
+  }
+  if (warp == 1) {  // tile table: first tile of each expert
+    const int per = (E + 31) / 32;
+    int local = 0;
+    for (int i = 0; i < per; ++i) {
+      const int e = lane * per + i;
+      if (e < E) {
+        const int o0 = __ldg(args.offsets + e), o1 = __ldg(args.offsets + e + 1);
+        tab_off[e] = o0;
+        local += max(0, (o1 - o0 + BN - 1) / BN);
+      }
+    }
+    int incl = local;
+#pragma unroll
+    for (int d = 1; d < 32; d <<= 1) {
+      const int o = __shfl_up_sync(0xffffffffu, incl, d);
+      if (lane >= d) incl += o;
+    }
+    int run = incl - local;
+    for (int i = 0; i < per; ++i) {
+      const int e = lane * per + i;
+      if (e < E) {
+        tab_prefix[e] = run;
+        run += max(0, (__ldg(args.offsets + e + 1) - tab_off[e] + BN - 1) / BN);
+      }
+    }
+    if (lane == 31) {
+      tab_prefix[E] = incl;
+      tab_off[E] = __ldg(args.offsets + E);
+    }
+  }
+  __syncthreads();
+  const int units = tab_prefix[E] * args.n_blocks;
+  const int rows_per_block = kGateUp ? kRowsPerBox : 2 * kRowsPerBox;
+
+  if (warp == 0) {
+    // ======================= producer =======================
+    if (lane == 0) {
+      tma_prefetch_desc(&tmA0);
+      tma_prefetch_desc(&tmA1);
+      tma_prefetch_desc(&tmB);
+      const uint32_t b_bytes = kBf16 ? 2u * BN * 128u : BN * 128u;
+      const uint32_t tx = 2u * args.box_bytes + b_bytes;
+      uint32_t it = 0, uit = 0, sit = 0;
+      bool ok = true;
+      for (int u = blockIdx.x; ok && u < units; u += gridDim.x, ++uit) {
+        const Unit x = decode(tab_prefix, tab_off, E, args.n_blocks, BN, u);
+        const int nb = x.rb * rows_per_block;
+        const uint32_t sb = uit & 1;
+        if (!bounded_wait(&bars->sempty[sb], ((uit >> 1) & 1) ^ 1, abort, args.err)) { ok = false; break; }
+        mbar_arrive_expect_tx(&bars->sfull[sb], 2 * args.scale_box_bytes);
+        for (int i = 0; i < 2; ++i) {
+          const uint8_t* src = args.experts + static_cast<uint64_t>(x.e) * args.expert_stride + args.scales_off[i] +
+                               static_cast<uint64_t>(nb + args.box_row_off[i]) * G * 2;
+          bulk_load(smem + args.off_scales + (sb * 2 + i) * args.scale_box_bytes, src, args.scale_box_bytes,
+                    &bars->sfull[sb]);
+        }
+        ++sit;
+        for (int grp = 0; grp < G; ++grp, ++it) {
+          const int s = it % S;
+          if (!bounded_wait(&bars->empty[s], ((it / S) & 1) ^ 1, abort, args.err)) { ok = false; break; }
+          uint8_t* st = smem + s * args.stage_bytes;
+          mbar_arrive_expect_tx(&bars->full[s], tx);
+          tma_load_3d(st, &tmA0, &bars->full[s], grp * kRB, nb + args.box_row_off[0], x.e);
+          tma_load_3d(st + args.box_bytes, &tmA1, &bars->full[s], grp * kRB, nb + args.box_row_off[1], x.e);
+          if (kBf16) {
+            tma_load_2d(st + args.off_b, &tmB, &bars->full[s], grp * 128, x.row0);
+            tma_load_2d(st + args.off_b + BN * 128, &tmB, &bars->full[s], grp * 128 + 64, x.row0);
+          } else {
+            tma_load_2d(st + args.off_b, &tmB, &bars->full[s], grp * 128, x.row0);
+          }
+        }
+      }
+      if (!ok || *abort) {
+        const uint32_t first = it > static_cast<uint32_t>(S) ? it - S : 0;
+        for (uint32_t j = first; j < it; ++j) drain(&bars->full[j % S], (j / S) & 1);
+        for (uint32_t j = sit > 2 ? sit - 2 : 0; j < sit; ++j) drain(&bars->sfull[j & 1], (j >> 1) & 1);
+      }
+    }
+    return;
+  }
+
+  // ======================= MMA warps =======================
+  const int w = warp - 1;            // 0..7: rows 16w .. 16w+15 of both boxes
+  const int g = lane >> 2, t = lane & 3;
+  uint32_t it = 0, uit = 0;
+  for (int u = blockIdx.x; u < units; u += gridDim.x, ++uit) {
+    const Unit x = decode(tab_prefix, tab_off, E, args.n_blocks, BN, u);
+    const int nb = x.rb * rows_per_block;
+    const uint32_t sb = uit & 1;
+    if (!bounded_wait(&bars->sfull[sb], (uit >> 1) & 1, abort, args.err)) return;
+    const __half* scl[2] = {
+        reinterpret_cast<const __half*>(smem + args.off_scales + (sb * 2 + 0) * args.scale_box_bytes),
+        reinterpret_cast<const __half*>(smem + args.off_scales + (sb * 2 + 1) * args.scale_box_bytes)};
+    float tot[2][NT][4];
+#pragma unroll
+    for (int i = 0; i < 2; ++i)
+#pragma unroll
+      for (int j = 0; j < NT; ++j)
+#pragma unroll
+        for (int q = 0; q < 4; ++q) tot[i][j][q] = 0.f;
+
+    for (int grp = 0; grp < G; ++grp, ++it) {
+      const int s = it % S;
+      if (!bounded_wait(&bars->full[s], (it / S) & 1, abort, args.err)) return;
+      const uint32_t st = smem_u32(smem + s * args.stage_bytes);
+      // raw codes: [box i][row g / g+8]
+      uint4 ar[2][2][WF == WF_INT4 ? 1 : 2];
+#pragma unroll
+      for (int i = 0; i < 2; ++i)
+#pragma unroll
+        for (int hh = 0; hh < 2; ++hh) {
+          const int r = 16 * w + g + 8 * hh;
+          const uint32_t box = st + i * args.box_bytes;
+          if constexpr (WF == WF_INT4) {
+            ar[i][hh][0] = lds128(box + r * 64 + t * 16);
+          } else {
+            ar[i][hh][0] = lds128(sw128(box, r, 2 * t));
+            ar[i][hh][1] = lds128(sw128(box, r, 2 * t + 1));
+          }
+        }
+      // token operand words: [n-tile j][16]
+      uint32_t bw[NT][16];
+#pragma unroll
+      for (int j = 0; j < NT; ++j) {
+        const int row = j * 8 + g;
+        if (kBf16) {
+          const uint32_t box = st + args.off_b + (t >> 1) * BN * 128;
+#pragma unroll
+          for (int c = 0; c < 4; ++c) {
+            const uint4 v = lds128(sw128(box, row, 4 * (t & 1) + c));
+            bw[j][4 * c] = v.x; bw[j][4 * c + 1] = v.y; bw[j][4 * c + 2] = v.z; bw[j][4 * c + 3] = v.w;
+          }
+        } else {
+          const uint4 v0 = lds128(sw128(st + args.off_b, row, 2 * t));
+          const uint4 v1 = lds128(sw128(st + args.off_b, row, 2 * t + 1));
+          uint32_t o[16];
+          cvt_int8x32<false>(v0, v1, o);
+#pragma unroll
+          for (int q = 0; q < 16; ++q) bw[j][q] = o[q];
+        }
+      }
+      float cg[2][NT][4];
+#pragma unroll
+      for (int i = 0; i < 2; ++i)
+#pragma unroll
+        for (int j = 0; j < NT; ++j)
+#pragma unroll
+          for (int q = 0; q < 4; ++q) cg[i][j][q] = 0.f;
+#pragma unroll
+      for (int ks = 0; ks < 8; ++ks) {
+#pragma unroll
+        for (int i = 0; i < 2; ++i) {
+          uint32_t a[4];  // {row g, slots 2t..}, {row g+8, 2t..}, {row g, 2t+8..}, {row g+8, 2t+8..}
+#pragma unroll
+          for (int hh = 0; hh < 2; ++hh) {
+            uint32_t lo, hi;
+            if constexpr (WF == WF_INT4) int4_pair<kBf16>(word_of(ar[i][hh][0], ks >> 1), ks & 1, lo, hi);
+            else int8_pair<kBf16>(word_of(ar[i][hh][ks >> 2], ks & 3), lo, hi);
+            a[hh] = lo;
+            a[2 + hh] = hi;
+          }
+#pragma unroll
+          for (int j = 0; j < NT; ++j) {
+            if (kBf16) hmma_bf16(cg[i][j], a, bw[j][2 * ks], bw[j][2 * ks + 1]);
+            else hmma_f16(cg[i][j], a, bw[j][2 * ks], bw[j][2 * ks + 1]);
+          }
+        }
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&bars->empty[s]);  // codes and tokens of this stage are in registers
+      // FP32 group combine: tot += (s_w [* s_a]) * exact group dot
+#pragma unroll
+      for (int i = 0; i < 2; ++i) {
+        const float sw0 = __half2float(scl[i][(16 * w + g) * G + grp]);
+        const float sw1 = __half2float(scl[i][(16 * w + g + 8) * G + grp]);
+#pragma unroll
+        for (int j = 0; j < NT; ++j) {
+          const int tok0 = j * 8 + 2 * t;
+          float f00 = sw0, f01 = sw0, f10 = sw1, f11 = sw1;
+          if (!kBf16) {
+            const float sa0 = tok0 < x.nrows ? __ldg(args.a_scales + static_cast<size_t>(x.row0 + tok0) * G + grp) : 0.f;
+            const float sa1 =
+                tok0 + 1 < x.nrows ? __ldg(args.a_scales + static_cast<size_t>(x.row0 + tok0 + 1) * G + grp) : 0.f;
+            f00 = __fmul_rn(sw0, sa0); f01 = __fmul_rn(sw0, sa1);
+            f10 = __fmul_rn(sw1, sa0); f11 = __fmul_rn(sw1, sa1);
+          }
+          tot[i][j][0] = __fmaf_rn(f00, cg[i][j][0], tot[i][j][0]);
+          tot[i][j][1] = __fmaf_rn(f01, cg[i][j][1], tot[i][j][1]);
+          tot[i][j][2] = __fmaf_rn(f10, cg[i][j][2], tot[i][j][2]);
+          tot[i][j][3] = __fmaf_rn(f11, cg[i][j][3], tot[i][j][3]);
+          if (args.dots) {
+            // exact group dot products, layout [P][C][G]; C = 2N (gate, up) or N
+            const size_t C = kGateUp ? 2 * static_cast<size_t>(args.N) : static_cast<size_t>(args.N);
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+              const int tok = tok0 + (q & 1);
+              const int feat = nb + args.box_row_off[i] + 16 * w + g + 8 * (q >> 1);
+              const size_t col = kGateUp ? static_cast<size_t>(i) * args.N + feat : static_cast<size_t>(feat);
+              if (tok < x.nrows)
+                args.dots[(static_cast<size_t>(x.row0 + tok) * C + col) * G + grp] = __float2int_rn(cg[i][j][q]);
+            }
+          }
+        }
+      }
+    }
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&bars->sempty[sb]);
+    // epilogue straight from registers
+#pragma unroll
+    for (int j = 0; j < NT; ++j) {
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        const int tok = j * 8 + 2 * t + (q & 1);
+        if (tok >= x.nrows || x.row0 + tok >= args.P) continue;
+        const int r = 16 * w + g + 8 * (q >> 1);
+        __nv_bfloat16* orow = args.out + static_cast<size_t>(x.row0 + tok) * args.N;
+        if (kGateUp) {
+          const float gv = tot[0][j][q], uv = tot[1][j][q];
+          orow[nb + r] = __float2bfloat16_rn(__fdividef(gv, 1.f + __expf(-gv)) * uv);
+        } else {
+          orow[nb + r] = __float2bfloat16_rn(tot[0][j][q]);
+          orow[nb + kRowsPerBox + r] = __float2bfloat16_rn(tot[1][j][q]);
+        }
+      }
+    }
+  }
+}
+
+// ---------------------------------------------------------------------------
+// host side
+// ---------------------------------------------------------------------------
+
+namespace {
+constexpr size_t kSmemPerSm = 232448;
+inline size_t smem_limit(int nt) { return nt == 1 ? kSmemPerSm / 2 - 1024 : kSmemPerSm; }
+inline uint32_t align_up(uint32_t x, uint32_t a) { return (x + a - 1) / a * a; }
+
+template <int WF, int AM, bool GU, int NT>
+cudaError_t launch(const CUtensorMap* maps, const Args& a, size_t smem, int grid, cudaStream_t st) {
+  auto kern = moe_gemm_warp_kernel<WF, AM, GU, NT>;
+  static bool attr = false;
+  if (!attr) {
+    cudaError_t e =
+        cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem_limit(NT)));
+    if (e != cudaSuccess) return e;
+    attr = true;
+  }
+  kern<<<grid, kThreads, smem, st>>>(maps[0], maps[1], maps[2], a);
+  return cudaGetLastError();
+}
+
+template <int WF, int AM, bool GU>
+cudaError_t launch_nt(int nt, const CUtensorMap* maps, const Args& a, size_t smem, int grid, cudaStream_t st) {
+  switch (nt) {
+    case 1: return launch<WF, AM, GU, 1>(maps, a, smem, grid, st);
+    case 2: return launch<WF, AM, GU, 2>(maps, a, smem, grid, st);
+    default: return launch<WF, AM, GU, 4>(maps, a, smem, grid, st);
+  }
+}
+template <int WF, int AM>
+cudaError_t launch_kind(bool gu, int nt, const CUtensorMap* maps, const Args& a, size_t smem, int grid,
+                        cudaStream_t st) {
+  return gu ? launch_nt<WF, AM, true>(nt, maps, a, smem, grid, st) : launch_nt<WF, AM, false>(nt, maps, a, smem, grid, st);
+}
+}  // namespace
+
+}  // namespace warpmma
+
+bool warp_gemm_applicable(const mnw_moe_layer* L, int wfmt, int act, int kind) {
+  if (wfmt != MNW_FMT_INT8_G128 && wfmt != MNW_FMT_INT4_G128) return false;
+  if (act != MNW_ACT_BF16 && act != MNW_ACT_INT8_G128) return false;
+  if (kind == MNW_KIND_GATE_UP) return L->I % warpmma::kRowsPerBox == 0;
+  return L->H % (2 * warpmma::kRowsPerBox) == 0;
+}
+
+int run_gemm_warp(const mnw_moe_layer* L, int wfmt, int act, int kind, const void* a0, const void* a1,
+                  const int32_t* offsets, int P, int nt, void* out, int32_t* dots, uint32_t* err, cudaStream_t st) {
+  using namespace warpmma;
+  const bool gu = kind == MNW_KIND_GATE_UP;
+  const int K = gu ? L->H : L->I, N = gu ? L->I : L->H, G = K / 128;
+  const int BN = 8 * nt;
+  const int rb = wfmt == MNW_FMT_INT4_G128 ? 64 : 128;
+  Args a{};
+  a.offsets = offsets;
+  a.E = L->E;
+  a.P = P;
+  a.K = K;
+  a.N = N;
+  a.BN = BN;
+  a.n_blocks = gu ? N / kRowsPerBox : N / (2 * kRowsPerBox);
+  a.box_bytes = kRowsPerBox * rb;
+  a.off_b = 2 * a.box_bytes;
+  const uint32_t b_bytes = act == MNW_ACT_BF16 ? 2u * BN * 128u : BN * 128u;
+  a.stage_bytes = align_up(a.off_b + b_bytes, 1024);
+  a.scale_box_bytes = kRowsPerBox * G * 2;
+  const uint32_t fixed = 4 * a.scale_box_bytes + align_up(2u * (L->E + 1) * 4u, 16) + align_up(sizeof(Bars), 16);
+  const size_t budget = smem_limit(nt) - 1024;
+  if (fixed + 2 * a.stage_bytes > budget) return MNW_E_UNSUPPORTED;
+  int stages = static_cast<int>((budget - fixed) / a.stage_bytes);
+  a.stages = stages > kMaxStages ? kMaxStages : stages;
+  a.off_scales = a.stages * a.stage_bytes;
+  a.off_tab = a.off_scales + 4 * a.scale_box_bytes;
+  a.off_bars = align_up(a.off_tab + 2u * (L->E + 1) * 4u, 16);
+  const size_t smem = a.off_bars + sizeof(Bars) + 1024;
+  a.experts = L->blob + L->data_offset;
+  a.expert_stride = L->expert_stride;
+  const int m0 = gu ? 0 : 2, m1 = gu ? 1 : 2;
+  a.scales_off[0] = L->scales_off[m0];
+  a.scales_off[1] = L->scales_off[m1];
+  a.box_row_off[0] = 0;
+  a.box_row_off[1] = gu ? 0 : kRowsPerBox;
+  a.a_scales = act == MNW_ACT_INT8_G128 ? static_cast<const float*>(a1) : nullptr;
+  a.out = static_cast<__nv_bfloat16*>(out);
+  a.dots = act == MNW_ACT_INT8_G128 ? dots : nullptr;
+  a.err = err;
+
+  CUtensorMap maps[3];
+  maps[0] = L->tm_wcodes[m0];
+  maps[1] = L->tm_wcodes[m1];
+  const uint64_t dims[2] = {static_cast<uint64_t>(K), static_cast<uint64_t>(P)};
+  bool ok;
+  if (act == MNW_ACT_BF16) {
+    const uint64_t strides[1] = {static_cast<uint64_t>(K) * 2};
+    const uint32_t box[2] = {64, static_cast<uint32_t>(BN)};
+    ok = encode_map(&maps[2], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, a0, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_128B);
+  } else {
+    const uint64_t strides[1] = {static_cast<uint64_t>(K)};
+    const uint32_t box[2] = {128, static_cast<uint32_t>(BN)};
+    ok = encode_map(&maps[2], CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, a0, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_128B);
+  }
+  if (!ok) return MNW_E_INVALID_ARG;
+  const int grid = L->num_sms * (nt == 1 ? 2 : 1);
+  cudaError_t e;
+  if (wfmt == MNW_FMT_INT4_G128 && act == MNW_ACT_BF16) e = launch_kind<WF_INT4, AM_BF16>(gu, nt, maps, a, smem, grid, st);
+  else if (wfmt == MNW_FMT_INT8_G128 && act == MNW_ACT_BF16) e = launch_kind<WF_INT8, AM_BF16>(gu, nt, maps, a, smem, grid, st);
+  else if (wfmt == MNW_FMT_INT4_G128) e = launch_kind<WF_INT4, AM_INT8>(gu, nt, maps, a, smem, grid, st);
+  else e = launch_kind<WF_INT8, AM_INT8>(gu, nt, maps, a, smem, grid, st);
+  return e == cudaSuccess ? MNW_OK : MNW_E_CUDA;
+}
+
+}  // namespace mnw

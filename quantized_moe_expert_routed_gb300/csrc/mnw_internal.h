@@ -17,6 +17,8 @@ struct mnw_moe_layer {
   // Weight tensor maps (built once): codes per matrix, NVFP4 block scales per matrix.
   CUtensorMap tm_codes[3];
   CUtensorMap tm_sf[3];
+  // Per-128-group weight tiles for the warp-MMA kernel (INT8/INT4 only).
+  CUtensorMap tm_wcodes[3];
 };
 
 namespace mnw {
@@ -39,5 +41,11 @@ cudaError_t launch_quantize(int act, const void* x, int R, int K, const int32_t*
 int run_gemm(const mnw_moe_layer* L, int wfmt, int act, int kind, const void* a0, const void* a1,
              const void* a2, const int32_t* offsets, int P, void* out, int32_t* dots, uint32_t* err,
              cudaStream_t st);
+// Warp-MMA grouped GEMM (INT8/INT4 weights, few tokens per expert); nt = token tile / 8.
+bool warp_gemm_applicable(const mnw_moe_layer* L, int wfmt, int act, int kind);
+int run_gemm_warp(const mnw_moe_layer* L, int wfmt, int act, int kind, const void* a0, const void* a1,
+                  const int32_t* offsets, int P, int nt, void* out, int32_t* dots, uint32_t* err, cudaStream_t st);
+// Process-wide GEMM path selection (MNW_PATH_*).
+int gemm_path();
 
 }  // namespace mnw

@@ -11,6 +11,8 @@
 // index.
 #include <cuda_bf16.h>
 
+#include <algorithm>
+
 #include "mnw_internal.h"
 #include "mnw_ptx.cuh"
 
@@ -157,43 +159,49 @@ __global__ void __launch_bounds__(256) gather_rows_kernel(const uint4* __restric
 }
 
 // out[t] = bf16(sum_j w[t, j] * y[assign_pos[t*k + j]]), FP32, j ascending.
+// One thread per (token, 8 columns); the k row loads of a thread are issued
+// before any of them is consumed (up to 8 in flight), so the kernel runs at
+// memory rate even for a 256-token decode batch.
 __global__ void __launch_bounds__(256) combine_kernel(const uint4* __restrict__ y,
                                                       const int32_t* __restrict__ assign_pos,
                                                       const float* __restrict__ w, int T, int k, int H8,
                                                       uint4* __restrict__ out) {
-  __shared__ int32_t s_pos[8][32];
-  __shared__ float s_w[8][32];
-  const int warps = gridDim.x * 8;
-  const int lane = threadIdx.x & 31, wib = threadIdx.x >> 5;
-  for (int t = blockIdx.x * 8 + wib; t < T; t += warps) {
-    // slot j's position and weight, staged once per token
-    s_pos[wib][lane] = lane < k ? __ldg(assign_pos + static_cast<size_t>(t) * k + lane) : -1;
-    s_w[wib][lane] = lane < k ? __ldg(w + static_cast<size_t>(t) * k + lane) : 0.f;
-    __syncwarp();
-    for (int c = lane; c < H8; c += 32) {
-      float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-      for (int j = 0; j < k; ++j) {
-        const int p = s_pos[wib][j];
-        const float wj = s_w[wib][j];
-        if (p < 0) continue;
-        const uint4 v = __ldg(y + static_cast<size_t>(p) * H8 + c);
-        const uint32_t vv[4] = {v.x, v.y, v.z, v.w};
+  const long long total = static_cast<long long>(T) * H8;
+  for (long long i = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x; i < total;
+       i += static_cast<long long>(gridDim.x) * blockDim.x) {
+    const int t = static_cast<int>(i / H8), c = static_cast<int>(i - static_cast<long long>(t) * H8);
+    float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+    for (int j0 = 0; j0 < k; j0 += 8) {
+      uint4 v[8];
+      float wj[8];
+      bool use[8];
 #pragma unroll
-        for (int i = 0; i < 4; ++i) {
-          const float2 f = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&vv[i]));
-          acc[2 * i] = __fmaf_rn(wj, f.x, acc[2 * i]);
-          acc[2 * i + 1] = __fmaf_rn(wj, f.y, acc[2 * i + 1]);
+      for (int jj = 0; jj < 8; ++jj) {
+        const int j = j0 + jj;
+        const int p = j < k ? __ldg(assign_pos + static_cast<size_t>(t) * k + j) : -1;
+        use[jj] = p >= 0;
+        wj[jj] = use[jj] ? __ldg(w + static_cast<size_t>(t) * k + j) : 0.f;
+        v[jj] = use[jj] ? __ldg(y + static_cast<size_t>(p) * H8 + c) : make_uint4(0, 0, 0, 0);
+      }
+#pragma unroll
+      for (int jj = 0; jj < 8; ++jj) {
+        if (!use[jj]) continue;
+        const uint32_t vv[4] = {v[jj].x, v[jj].y, v[jj].z, v[jj].w};
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          const float2 f = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&vv[q]));
+          acc[2 * q] = __fmaf_rn(wj[jj], f.x, acc[2 * q]);
+          acc[2 * q + 1] = __fmaf_rn(wj[jj], f.y, acc[2 * q + 1]);
         }
       }
-      uint32_t o[4];
-#pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        __nv_bfloat162 b = __floats2bfloat162_rn(acc[2 * i], acc[2 * i + 1]);
-        o[i] = *reinterpret_cast<uint32_t*>(&b);
-      }
-      out[static_cast<size_t>(t) * H8 + c] = make_uint4(o[0], o[1], o[2], o[3]);
     }
-    __syncwarp();
+    uint32_t o[4];
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      __nv_bfloat162 bb = __floats2bfloat162_rn(acc[2 * q], acc[2 * q + 1]);
+      o[q] = *reinterpret_cast<uint32_t*>(&bb);
+    }
+    out[i] = make_uint4(o[0], o[1], o[2], o[3]);
   }
 }
 
@@ -234,8 +242,10 @@ cudaError_t launch_combine(const void* y, const int32_t* assign_pos, const float
   int dev = 0, sms = 148;
   cudaGetDevice(&dev);
   cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-  combine_kernel<<<grid_for(8, T, sms * 8), 256, 0, st>>>(static_cast<const uint4*>(y), assign_pos, w, T, k,
-                                                          H / 8, static_cast<uint4*>(out));
+  const long long threads = static_cast<long long>(T) * (H / 8);
+  const int blocks = static_cast<int>(std::min<long long>((threads + 255) / 256, static_cast<long long>(sms) * 16));
+  combine_kernel<<<blocks < 1 ? 1 : blocks, 256, 0, st>>>(static_cast<const uint4*>(y), assign_pos, w, T, k, H / 8,
+                                                          static_cast<uint4*>(out));
   return cudaGetLastError();
 }
 

@@ -14,8 +14,10 @@ the layer's arithmetic.  It draws:
 
 Every random number comes from a counter-based 32-bit hash of
 (seed, stream, index) computed with integer tensor ops only; normals come from
-a fixed table of N(0, 1) quantiles indexed by 16 hash bits.  The same call
-gives the same bits on CPU and on GPU.
+a fixed table of N(0, 1) quantiles indexed by 16 hash bits, so activations,
+uniform routing and weight codes are the same bits on CPU and GPU.  The few
+floating steps (softmax weights, Zipf keys) may differ in the last ulp between
+devices: a comparison draws its inputs once, on one device, and copies them.
 
 The blob layout written here is documented in ``include/mnw_moe.h``.
 """
@@ -297,20 +299,24 @@ def expert_blob(wfmt: int, E: int, H: int, I: int, seed: int, sigma: float = 0.0
             o0 = L.outer_off[m]
             body[:, o0:o0 + 4] = outer.reshape(E, 1).view(torch.uint8).reshape(E, 4)
             continue
-        # per expert to bound the working set
-        for e in range(E):
-            w = normal_f64(seed, st, N * K, device, start=e * N * K).reshape(N, K) * sigma
+        # blocks of experts at a time to bound the working set
+        per = N * K
+        step = max(1, min(E, (1 << 25) // per))
+        for e0 in range(0, E, step):
+            ne = min(step, E - e0)
+            w = normal_f64(seed, st, ne * per, device, start=e0 * per).reshape(ne, N, K) * sigma
+            rows = body[e0:e0 + ne]
             if wfmt == FMT_BF16:
-                body[e, c0:c0 + N * K * 2] = w.to(torch.float32).to(torch.bfloat16).view(torch.uint8).reshape(-1)
+                rows[:, c0:c0 + per * 2] = w.to(torch.float32).to(torch.bfloat16).view(torch.uint8).reshape(ne, -1)
                 continue
             if wfmt == FMT_INT8_G128:
                 q, s16 = _quantise_absmax(w, 127, -127)
-                body[e, c0:c0 + N * K] = q.to(torch.int8).view(torch.uint8).reshape(-1)
+                rows[:, c0:c0 + per] = q.to(torch.int8).view(torch.uint8).reshape(ne, -1)
             else:
                 q, s16 = _quantise_absmax(w, 7, -8)
-                body[e, c0:c0 + N * K // 2] = _pack_nibbles(q).reshape(-1)
+                rows[:, c0:c0 + per // 2] = _pack_nibbles(q).reshape(ne, -1)
             s0 = L.scales_off[m]
-            body[e, s0:s0 + N * (K // 128) * 2] = s16.contiguous().view(torch.uint8).reshape(-1)
+            rows[:, s0:s0 + N * (K // 128) * 2] = s16.contiguous().view(torch.uint8).reshape(ne, -1)
     hdr = header_bytes(L)
     blob = torch.empty((L.total_bytes,), dtype=torch.uint8, device=device)
     blob[:256] = torch.frombuffer(bytearray(hdr), dtype=torch.uint8).to(device)

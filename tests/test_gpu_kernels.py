@@ -189,3 +189,55 @@ def test_gemm_empty_experts_and_zero_rows(M):
     h = M.mnw_moe_grouped_gemm_w4a16(layer, M.KIND_GATE_UP, xp, off)
     oh = O.gemm_a16(blob.numpy(), O.KIND_GATE_UP, to_np_bits(xp), off.cpu().numpy())
     assert_close(h, oh, what="empty experts")
+
+
+@pytest.mark.parametrize("wfmt,act", [(S.FMT_INT4_G128, S.ACT_BF16), (S.FMT_INT8_G128, S.ACT_BF16),
+                                      (S.FMT_INT4_G128, S.ACT_INT8_G128), (S.FMT_INT8_G128, S.ACT_INT8_G128)])
+@pytest.mark.parametrize("T,k,E", [(40, 2, 8), (64, 8, 16), (130, 4, 8)])
+def test_warp_and_tcgen05_paths_agree_bitwise(M, wfmt, act, T, k, E):
+    """Both grouped-GEMM kernels sum each 128-wide group on the tensor cores in
+    FP32 and combine the groups with the same FP32 operations.  With INT8
+    activations every group dot is an exact integer, so the outputs are
+    identical bits; with BF16 activations the in-group FP32 sums may round in
+    a different order, so the outputs agree to that rounding."""
+    H, I = 512, 256
+    blob, hdr, ids, x = _setup(wfmt, E, H, I, T, k, seed=17 * T + wfmt)
+    layer = M.Layer(blob.to(DEV), hdr)
+    off, sa, pos, xp = M.mnw_moe_permute(ids.to(DEV), E, x=x.to(DEV))
+    outs = []
+    try:
+        for path in (M.PATH_TCGEN05, M.PATH_WARP_MMA):
+            M.mnw_moe_set_gemm_path(path)
+            if act == S.ACT_BF16:
+                fn = M.mnw_moe_grouped_gemm_w4a16 if wfmt == S.FMT_INT4_G128 else M.mnw_moe_grouped_gemm_w8a16
+                h = fn(layer, M.KIND_GATE_UP, xp, off)
+                y = fn(layer, M.KIND_DOWN, h, off)
+                outs.append((h, y, None))
+            else:
+                fn = M.mnw_moe_grouped_gemm_w4a8 if wfmt == S.FMT_INT4_G128 else M.mnw_moe_grouped_gemm_w8a8
+                q, s = M.mnw_moe_quantize_act(M.ACT_INT8_G128, x.to(DEV), row_index=sa, index_div=k)
+                h, dots = fn(layer, M.KIND_GATE_UP, q, s, off, want_dots=True)
+                hq, hs = M.mnw_moe_quantize_act(M.ACT_INT8_G128, h)
+                y = fn(layer, M.KIND_DOWN, hq, hs, off)
+                outs.append((h, y, dots))
+    finally:
+        M.mnw_moe_set_gemm_path(M.PATH_AUTO)
+    (h0, y0, d0), (h1, y1, d1) = outs
+    if act == S.ACT_INT8_G128:
+        assert torch.equal(h0.view(torch.int16), h1.view(torch.int16))
+        assert torch.equal(y0.view(torch.int16), y1.view(torch.int16))
+    else:
+        for p0, p1 in ((h0, h1), (y0, y1)):
+            a, b = p0.double(), p1.double()
+            assert (a - b).norm() <= 2e-3 * b.norm()
+            assert ((a - b).abs() > b.abs() * 2.0 ** -7 + 1e-6).float().mean() <= 1e-3
+    if d0 is not None:
+        valid = int(off[-1])
+        assert torch.equal(d0[:valid], d1[:valid])
+    # and the warp path matches the oracle
+    o_off = off.cpu().numpy()
+    if act == S.ACT_BF16:
+        oh = O.gemm_a16(blob.numpy(), O.KIND_GATE_UP, to_np_bits(xp), o_off)
+    else:
+        oh = O.gemm_a8(blob.numpy(), O.KIND_GATE_UP, q.cpu().numpy(), s.cpu().numpy(), o_off)
+    assert_close(h1, oh, what="warp path gate_up")
