@@ -213,6 +213,28 @@ int mnw_moe_forward_host(const mnw_moe_layer* layer, int act, const void* x_host
 enum mnw_path { MNW_PATH_AUTO = 0, MNW_PATH_TCGEN05 = 1, MNW_PATH_WARP_MMA = 2 };
 int mnw_moe_set_gemm_path(int path);
 
+/* The whole layer with no device allocation and no caller workspace (the
+ * pages have no counterpart; this is an integration convenience).  For
+ * callers that cannot allocate device memory -- e.g. a plugin in a process
+ * whose GPU memory is owned up front by another allocator with no hook for
+ * plugins, or a latency-critical path that must not pay cudaMalloc's implicit
+ * synchronisation.  Same kernels and results as mnw_moe_forward(), with the
+ * intermediates in one fixed array of MNW_STATIC_WS_BYTES compiled into the
+ * library; every GPU that loads the library holds that array until exit.
+ *  - Requests whose mnw_moe_workspace_size() exceeds MNW_STATIC_WS_BYTES
+ *    return MNW_E_WORKSPACE_TOO_SMALL before anything is enqueued.
+ *  - The first call on each device looks up the array's device address (a
+ *    CUDA runtime query, no allocation); make that first call before any
+ *    stream capture on that device.
+ *  - All calls share the array: calls that overlap on the GPU race and corrupt
+ *    each other's results.  Serialise them (one stream).
+ *  - err (device, may be NULL) receives this call's device error word
+ *    (MNW_DEVERR_*); the word is cleared by every call.
+ * x, ids, w, out are as for mnw_moe_forward(). */
+#define MNW_STATIC_WS_BYTES (32u * 1024u * 1024u)
+int mnw_moe_forward_static(const mnw_moe_layer* layer, int act, const void* x, const int32_t* ids,
+                           const float* w, int T, int k, void* out, uint32_t* err, mnw_stream stream);
+
 /* Synchronise `stream`, then copy the device error word to *out_host. */
 int mnw_moe_read_error(const uint32_t* err, uint32_t* out_host, mnw_stream stream);
 

@@ -47,6 +47,7 @@ SIGNATURES = {
     "mnw_moe_forward_host": (_I, [_P, _I, _P, _P, _P, _I, _I, _P, _P, _SZ, _P]),
     "mnw_moe_read_error": (_I, [_P, _P, _P]),
     "mnw_moe_set_gemm_path": (_I, [_I]),
+    "mnw_moe_forward_static": (_I, [_P, _I, _P, _P, _P, _I, _I, _P, _U32P, _P]),
 }
 
 _lib = None
@@ -267,3 +268,17 @@ def mnw_moe_read_error(err, stream=None) -> int:
 def mnw_moe_set_gemm_path(path: int) -> None:
     """Process-wide grouped-GEMM kernel choice (PATH_AUTO, PATH_TCGEN05, PATH_WARP_MMA)."""
     _check(load().mnw_moe_set_gemm_path(path), "mnw_moe_set_gemm_path")
+
+
+STATIC_WS_BYTES = 32 * 1024 * 1024
+
+
+def mnw_moe_forward_static(layer, act, x, ids, w, out=None, err=None, stream=None):
+    """The whole layer with the library's built-in scratch array: no workspace
+    and no device allocation by the library (see include/mnw_moe.h)."""
+    T, k = ids.shape
+    if out is None:
+        out = torch.empty((T, layer.H), dtype=torch.bfloat16, device=x.device)
+    _check(load().mnw_moe_forward_static(layer.handle, act, _ptr(x), _ptr(ids), _ptr(w), T, k, _ptr(out), _ptr(err),
+                                         _stream(stream)), "mnw_moe_forward_static")
+    return out
