@@ -716,7 +716,7 @@ int run_gemm(const mnw_moe_layer* L, int wfmt, int act, int kind, const void* a0
   const int path = gemm_path();
   if (warp_gemm_applicable(L, wfmt, act, kind) &&
       (path == MNW_PATH_WARP_MMA || (path == MNW_PATH_AUTO && mean_rows <= 64))) {
-    const int nt = mean_rows <= 8 ? 1 : (mean_rows <= 16 ? 2 : 4);
+    const int nt = mean_rows <= 4 ? 1 : (mean_rows <= 16 ? 2 : 4);
     return run_gemm_warp(L, wfmt, act, kind, a0, a1, offsets, P, nt, out, dots, err, st);
   }
   const bool gate_up = kind == MNW_KIND_GATE_UP;

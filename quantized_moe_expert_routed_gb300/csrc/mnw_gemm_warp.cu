@@ -53,9 +53,9 @@ constexpr int kMmaWarps = 8;
 constexpr int kThreads = (1 + kMmaWarps) * 32;  // warp 0 = producer
 constexpr int kMaxStages = 12;
 constexpr int kRowsPerBox = 128;
-// CTAs per SM: two (16 MMA warps) for 8-token tiles, whose registers fit; one otherwise.
-template <int NT>
-constexpr int ctas_per_sm() { return NT == 1 ? 2 : 1; }
+// CTAs per SM: two (16 MMA warps) where the registers of one thread fit in 96
+// (8-token tiles, and 16-token tiles of INT4), one otherwise.
+constexpr int ctas_per_sm(int wf, int nt) { return (nt == 1 || (nt == 2 && wf == 2)) ? 2 : 1; }
 
 struct Args {
   const int32_t* offsets;
@@ -154,7 +154,7 @@ __device__ __forceinline__ uint32_t word_of(const uint4& v, int i) {
 }
 
 template <int WF, int AM, bool kGateUp, int NT>
-__global__ void __launch_bounds__(kThreads, ctas_per_sm<NT>())
+__global__ void __launch_bounds__(kThreads, ctas_per_sm(WF, NT))
     moe_gemm_warp_kernel(const __grid_constant__ CUtensorMap tmA0, const __grid_constant__ CUtensorMap tmA1,
                          const __grid_constant__ CUtensorMap tmB, const Args args) {
   constexpr bool kBf16 = AM == AM_BF16;
@@ -223,6 +223,8 @@ __global__ void __launch_bounds__(kThreads, ctas_per_sm<NT>())
       const uint32_t b_bytes = kBf16 ? 2u * BN * 128u : BN * 128u;
       const uint32_t tx = 2u * args.box_bytes + b_bytes;
       uint32_t it = 0, uit = 0, sit = 0;
+      int s = 0;
+      uint32_t ph = 0;  // stage index and phase of `it`, kept without divisions
       bool ok = true;
       for (int u = blockIdx.x; ok && u < units; u += gridDim.x, ++uit) {
         const Unit x = decode(tab_prefix, tab_off, E, args.n_blocks, BN, u);
@@ -238,8 +240,7 @@ __global__ void __launch_bounds__(kThreads, ctas_per_sm<NT>())
         }
         ++sit;
         for (int grp = 0; grp < G; ++grp, ++it) {
-          const int s = it % S;
-          if (!bounded_wait(&bars->empty[s], ((it / S) & 1) ^ 1, abort, args.err)) { ok = false; break; }
+          if (!bounded_wait(&bars->empty[s], ph ^ 1, abort, args.err)) { ok = false; break; }
           uint8_t* st = smem + s * args.stage_bytes;
           mbar_arrive_expect_tx(&bars->full[s], tx);
           tma_load_3d(st, &tmA0, &bars->full[s], grp * kRB, nb + args.box_row_off[0], x.e);
@@ -250,6 +251,7 @@ __global__ void __launch_bounds__(kThreads, ctas_per_sm<NT>())
           } else {
             tma_load_2d(st + args.off_b, &tmB, &bars->full[s], grp * 128, x.row0);
           }
+          if (++s == S) { s = 0; ph ^= 1; }
         }
       }
       if (!ok || *abort) {
@@ -265,6 +267,29 @@ __global__ void __launch_bounds__(kThreads, ctas_per_sm<NT>())
   const int w = warp - 1;            // 0..7: rows 16w .. 16w+15 of both boxes
   const int g = lane >> 2, t = lane & 3;
   uint32_t it = 0, uit = 0;
+  int s = 0;
+  uint32_t ph = 0;
+  // lane-constant shared-memory offsets (swizzled chunk positions)
+  uint32_t b_off[NT][4];
+#pragma unroll
+  for (int j = 0; j < NT; ++j) {
+    const int row = j * 8 + g;
+#pragma unroll
+    for (int c = 0; c < 4; ++c)
+      b_off[j][c] = kBf16 ? args.off_b + (t >> 1) * BN * 128 + row * 128 + (((4 * (t & 1) + c) ^ (row & 7)) << 4)
+                          : args.off_b + row * 128 + (((2 * t + (c & 1)) ^ (row & 7)) << 4);
+  }
+  uint32_t a_off[2][2][2];
+#pragma unroll
+  for (int i = 0; i < 2; ++i)
+#pragma unroll
+    for (int hh = 0; hh < 2; ++hh) {
+      const int r = 16 * w + g + 8 * hh;
+#pragma unroll
+      for (int c = 0; c < 2; ++c)
+        a_off[i][hh][c] = i * args.box_bytes +
+                          (WF == WF_INT4 ? r * 64 + t * 16 : r * 128 + (((2 * t + c) ^ (r & 7)) << 4));
+    }
   for (int u = blockIdx.x; u < units; u += gridDim.x, ++uit) {
     const Unit x = decode(tab_prefix, tab_off, E, args.n_blocks, BN, u);
     const int nb = x.rb * rows_per_block;
@@ -282,39 +307,32 @@ __global__ void __launch_bounds__(kThreads, ctas_per_sm<NT>())
         for (int q = 0; q < 4; ++q) tot[i][j][q] = 0.f;
 
     for (int grp = 0; grp < G; ++grp, ++it) {
-      const int s = it % S;
-      if (!bounded_wait(&bars->full[s], (it / S) & 1, abort, args.err)) return;
+      if (!bounded_wait(&bars->full[s], ph, abort, args.err)) return;
       const uint32_t st = smem_u32(smem + s * args.stage_bytes);
+      const int s_now = s;
+      if (++s == S) { s = 0; ph ^= 1; }
       // raw codes: [box i][row g / g+8]
       uint4 ar[2][2][WF == WF_INT4 ? 1 : 2];
 #pragma unroll
       for (int i = 0; i < 2; ++i)
 #pragma unroll
         for (int hh = 0; hh < 2; ++hh) {
-          const int r = 16 * w + g + 8 * hh;
-          const uint32_t box = st + i * args.box_bytes;
-          if constexpr (WF == WF_INT4) {
-            ar[i][hh][0] = lds128(box + r * 64 + t * 16);
-          } else {
-            ar[i][hh][0] = lds128(sw128(box, r, 2 * t));
-            ar[i][hh][1] = lds128(sw128(box, r, 2 * t + 1));
-          }
+          ar[i][hh][0] = lds128(st + a_off[i][hh][0]);
+          if constexpr (WF != WF_INT4) ar[i][hh][1] = lds128(st + a_off[i][hh][1]);
         }
       // token operand words: [n-tile j][16]
       uint32_t bw[NT][16];
 #pragma unroll
       for (int j = 0; j < NT; ++j) {
-        const int row = j * 8 + g;
         if (kBf16) {
-          const uint32_t box = st + args.off_b + (t >> 1) * BN * 128;
 #pragma unroll
           for (int c = 0; c < 4; ++c) {
-            const uint4 v = lds128(sw128(box, row, 4 * (t & 1) + c));
+            const uint4 v = lds128(st + b_off[j][c]);
             bw[j][4 * c] = v.x; bw[j][4 * c + 1] = v.y; bw[j][4 * c + 2] = v.z; bw[j][4 * c + 3] = v.w;
           }
         } else {
-          const uint4 v0 = lds128(sw128(st + args.off_b, row, 2 * t));
-          const uint4 v1 = lds128(sw128(st + args.off_b, row, 2 * t + 1));
+          const uint4 v0 = lds128(st + b_off[j][0]);
+          const uint4 v1 = lds128(st + b_off[j][1]);
           uint32_t o[16];
           cvt_int8x32<false>(v0, v1, o);
 #pragma unroll
@@ -349,7 +367,7 @@ __global__ void __launch_bounds__(kThreads, ctas_per_sm<NT>())
         }
       }
       __syncwarp();
-      if (lane == 0) mbar_arrive(&bars->empty[s]);  // codes and tokens of this stage are in registers
+      if (lane == 0) mbar_arrive(&bars->empty[s_now]);  // codes and tokens of this stage are in registers
       // FP32 group combine: tot += (s_w [* s_a]) * exact group dot
 #pragma unroll
       for (int i = 0; i < 2; ++i) {
@@ -414,7 +432,7 @@ __global__ void __launch_bounds__(kThreads, ctas_per_sm<NT>())
 
 namespace {
 constexpr size_t kSmemPerSm = 232448;
-inline size_t smem_limit(int nt) { return nt == 1 ? kSmemPerSm / 2 - 1024 : kSmemPerSm; }
+inline size_t smem_limit(int wf, int nt) { return ctas_per_sm(wf, nt) == 2 ? kSmemPerSm / 2 - 1024 : kSmemPerSm; }
 inline uint32_t align_up(uint32_t x, uint32_t a) { return (x + a - 1) / a * a; }
 
 template <int WF, int AM, bool GU, int NT>
@@ -423,7 +441,7 @@ cudaError_t launch(const CUtensorMap* maps, const Args& a, size_t smem, int grid
   static bool attr = false;
   if (!attr) {
     cudaError_t e =
-        cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem_limit(NT)));
+        cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem_limit(WF, NT)));
     if (e != cudaSuccess) return e;
     attr = true;
   }
@@ -476,7 +494,7 @@ int run_gemm_warp(const mnw_moe_layer* L, int wfmt, int act, int kind, const voi
   a.stage_bytes = align_up(a.off_b + b_bytes, 1024);
   a.scale_box_bytes = kRowsPerBox * G * 2;
   const uint32_t fixed = 4 * a.scale_box_bytes + align_up(2u * (L->E + 1) * 4u, 16) + align_up(sizeof(Bars), 16);
-  const size_t budget = smem_limit(nt) - 1024;
+  const size_t budget = smem_limit(wfmt, nt) - 1024;
   if (fixed + 2 * a.stage_bytes > budget) return MNW_E_UNSUPPORTED;
   int stages = static_cast<int>((budget - fixed) / a.stage_bytes);
   a.stages = stages > kMaxStages ? kMaxStages : stages;
@@ -511,7 +529,7 @@ int run_gemm_warp(const mnw_moe_layer* L, int wfmt, int act, int kind, const voi
     ok = encode_map(&maps[2], CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, a0, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_128B);
   }
   if (!ok) return MNW_E_INVALID_ARG;
-  const int grid = L->num_sms * (nt == 1 ? 2 : 1);
+  const int grid = L->num_sms * ctas_per_sm(wfmt, nt);
   cudaError_t e;
   if (wfmt == MNW_FMT_INT4_G128 && act == MNW_ACT_BF16) e = launch_kind<WF_INT4, AM_BF16>(gu, nt, maps, a, smem, grid, st);
   else if (wfmt == MNW_FMT_INT8_G128 && act == MNW_ACT_BF16) e = launch_kind<WF_INT8, AM_BF16>(gu, nt, maps, a, smem, grid, st);
