@@ -710,12 +710,11 @@ int run_gemm(const mnw_moe_layer* L, int wfmt, int act, int kind, const void* a0
   if (!a0 || !offsets || !out || !aligned(a0, 16) || !aligned(out, 16)) return MNW_E_INVALID_ARG;
   if (act == MNW_ACT_INT8_G128 && (!a1 || !aligned(a1, 16))) return MNW_E_INVALID_ARG;
   if (act == MNW_ACT_NVFP4_G16 && (!a1 || !a2 || !aligned(a1, 16) || !aligned(a2, 16))) return MNW_E_INVALID_ARG;
-  // Few tokens per expert: the warp-MMA kernel streams INT weights faster (see
-  // mnw_gemm_warp.cu); larger token tiles use tcgen05 below.
+  // INT8/INT4 weights: the warp-MMA kernel (see mnw_gemm_warp.cu for why);
+  // BF16 and NVFP4 weights use tcgen05 below.
   const int mean_rows = (P + L->E - 1) / L->E;
   const int path = gemm_path();
-  if (warp_gemm_applicable(L, wfmt, act, kind) &&
-      (path == MNW_PATH_WARP_MMA || (path == MNW_PATH_AUTO && mean_rows <= 64))) {
+  if (warp_gemm_applicable(L, wfmt, act, kind) && path != MNW_PATH_TCGEN05) {
     const int nt = mean_rows <= 4 ? 1 : (mean_rows <= 16 ? 2 : 4);
     return run_gemm_warp(L, wfmt, act, kind, a0, a1, offsets, P, nt, out, dots, err, st);
   }

@@ -53,9 +53,9 @@ constexpr int kMmaWarps = 8;
 constexpr int kThreads = (1 + kMmaWarps) * 32;  // warp 0 = producer
 constexpr int kMaxStages = 12;
 constexpr int kRowsPerBox = 128;
-// CTAs per SM: two (16 MMA warps) where the registers of one thread fit in 96
-// (8-token tiles, and 16-token tiles of INT4), one otherwise.
-constexpr int ctas_per_sm(int wf, int nt) { return (nt == 1 || (nt == 2 && wf == 2)) ? 2 : 1; }
+// CTAs per SM: two (16 MMA warps) where a thread's registers fit in 96 (8- and
+// 16-token tiles); one for 32-token tiles, whose accumulators need more.
+constexpr int ctas_per_sm(int wf, int nt) { return nt <= 2 ? 2 : 1; }
 
 struct Args {
   const int32_t* offsets;
@@ -148,6 +148,16 @@ __device__ __forceinline__ void int8_pair(uint32_t w, uint32_t& lo, uint32_t& hi
     lo = f16x2_sub(prmt(u, 0x64646464u, 0x4140u), 0x64806480u);
     hi = f16x2_sub(prmt(u, 0x64646464u, 0x4342u), 0x64806480u);
   }
+}
+__device__ __forceinline__ uint2 lds64(uint32_t addr) {
+  uint2 v;
+  asm volatile("ld.shared.v2.u32 {%0,%1}, [%2];" : "=r"(v.x), "=r"(v.y) : "r"(addr));
+  return v;
+}
+__device__ __forceinline__ uint32_t lds32(uint32_t addr) {
+  uint32_t v;
+  asm volatile("ld.shared.u32 %0, [%1];" : "=r"(v) : "r"(addr));
+  return v;
 }
 __device__ __forceinline__ uint32_t word_of(const uint4& v, int i) {
   return i == 0 ? v.x : i == 1 ? v.y : i == 2 ? v.z : v.w;
@@ -320,25 +330,6 @@ __global__ void __launch_bounds__(kThreads, ctas_per_sm(WF, NT))
           ar[i][hh][0] = lds128(st + a_off[i][hh][0]);
           if constexpr (WF != WF_INT4) ar[i][hh][1] = lds128(st + a_off[i][hh][1]);
         }
-      // token operand words: [n-tile j][16]
-      uint32_t bw[NT][16];
-#pragma unroll
-      for (int j = 0; j < NT; ++j) {
-        if (kBf16) {
-#pragma unroll
-          for (int c = 0; c < 4; ++c) {
-            const uint4 v = lds128(st + b_off[j][c]);
-            bw[j][4 * c] = v.x; bw[j][4 * c + 1] = v.y; bw[j][4 * c + 2] = v.z; bw[j][4 * c + 3] = v.w;
-          }
-        } else {
-          const uint4 v0 = lds128(st + b_off[j][0]);
-          const uint4 v1 = lds128(st + b_off[j][1]);
-          uint32_t o[16];
-          cvt_int8x32<false>(v0, v1, o);
-#pragma unroll
-          for (int q = 0; q < 16; ++q) bw[j][q] = o[q];
-        }
-      }
       float cg[2][NT][4];
 #pragma unroll
       for (int i = 0; i < 2; ++i)
@@ -348,6 +339,18 @@ __global__ void __launch_bounds__(kThreads, ctas_per_sm(WF, NT))
           for (int q = 0; q < 4; ++q) cg[i][j][q] = 0.f;
 #pragma unroll
       for (int ks = 0; ks < 8; ++ks) {
+        // token operand of this k-step: K = 32t + 4ks .. +3 of each n-tile's row
+        uint32_t b0[NT], b1[NT];
+#pragma unroll
+        for (int j = 0; j < NT; ++j) {
+          if constexpr (kBf16) {
+            const uint2 v = lds64(st + b_off[j][ks >> 1] + 8 * (ks & 1));
+            b0[j] = v.x;
+            b1[j] = v.y;
+          } else {
+            int8_pair<false>(lds32(st + b_off[j][ks >> 2] + 4 * (ks & 3)), b0[j], b1[j]);
+          }
+        }
 #pragma unroll
         for (int i = 0; i < 2; ++i) {
           uint32_t a[4];  // {row g, slots 2t..}, {row g+8, 2t..}, {row g, 2t+8..}, {row g+8, 2t+8..}
@@ -361,8 +364,8 @@ __global__ void __launch_bounds__(kThreads, ctas_per_sm(WF, NT))
           }
 #pragma unroll
           for (int j = 0; j < NT; ++j) {
-            if (kBf16) hmma_bf16(cg[i][j], a, bw[j][2 * ks], bw[j][2 * ks + 1]);
-            else hmma_f16(cg[i][j], a, bw[j][2 * ks], bw[j][2 * ks + 1]);
+            if constexpr (kBf16) hmma_bf16(cg[i][j], a, b0[j], b1[j]);
+            else hmma_f16(cg[i][j], a, b0[j], b1[j]);
           }
         }
       }
