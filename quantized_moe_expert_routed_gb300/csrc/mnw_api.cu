@@ -141,8 +141,8 @@ static WsLayout ws_layout(const mnw_moe_layer* L, int act, int T, int k) {
 }
 
 static int gemm_for(const mnw_moe_layer* L, int act, int kind, const void* a0, const void* a1, const void* a2,
-                    const int32_t* offsets, int P, void* out, uint32_t* err, cudaStream_t st) {
-  return run_gemm(L, L->wfmt, act, kind, a0, a1, a2, offsets, P, out, nullptr, err, st);
+                    const int32_t* offsets, int P, void* out, uint32_t* err, uint32_t* sched, cudaStream_t st) {
+  return run_gemm(L, L->wfmt, act, kind, a0, a1, a2, offsets, P, out, nullptr, err, st, sched);
 }
 
 }  // namespace mnw
@@ -372,14 +372,17 @@ int mnw_moe_forward(const mnw_moe_layer* L, int act, const void* x, const int32_
   int32_t* sorted = reinterpret_cast<int32_t*>(b + W.sorted);
   int32_t* pos = reinterpret_cast<int32_t*>(b + W.pos);
   const int P = T * k, H = L->H, I = L->I;
-  if (cudaMemsetAsync(err, 0, 4, st) != cudaSuccess) return MNW_E_CUDA;
+  // The first 256 bytes of ws: error word, then a [claim, done] work counter per GEMM launch.
+  uint32_t* sched_gu = err + 16;
+  uint32_t* sched_dn = err + 18;
+  if (cudaMemsetAsync(err, 0, 256, st) != cudaSuccess) return MNW_E_CUDA;
   int rc;
   if (act == MNW_ACT_BF16) {
     rc = mnw_moe_permute(ids, T, k, L->E, offs, sorted, pos, x, H, b + W.xa, err, stream);
     if (rc) return rc;
-    rc = gemm_for(L, act, MNW_KIND_GATE_UP, b + W.xa, nullptr, nullptr, offs, P, b + W.h, err, st);
+    rc = gemm_for(L, act, MNW_KIND_GATE_UP, b + W.xa, nullptr, nullptr, offs, P, b + W.h, err, sched_gu, st);
     if (rc) return rc;
-    rc = gemm_for(L, act, MNW_KIND_DOWN, b + W.h, nullptr, nullptr, offs, P, b + W.y, err, st);
+    rc = gemm_for(L, act, MNW_KIND_DOWN, b + W.h, nullptr, nullptr, offs, P, b + W.y, err, sched_dn, st);
     if (rc) return rc;
   } else {
     rc = mnw_moe_permute(ids, T, k, L->E, offs, sorted, pos, nullptr, 0, nullptr, err, stream);
@@ -388,11 +391,11 @@ int mnw_moe_forward(const mnw_moe_layer* L, int act, const void* x, const int32_
     float* ho = act == MNW_ACT_NVFP4_G16 ? reinterpret_cast<float*>(b + W.hc) : nullptr;
     rc = mnw_moe_quantize_act(act, x, P, H, sorted, k, b + W.xa, b + W.xb, xo, stream);
     if (rc) return rc;
-    rc = gemm_for(L, act, MNW_KIND_GATE_UP, b + W.xa, b + W.xb, xo, offs, P, b + W.h, err, st);
+    rc = gemm_for(L, act, MNW_KIND_GATE_UP, b + W.xa, b + W.xb, xo, offs, P, b + W.h, err, sched_gu, st);
     if (rc) return rc;
     rc = mnw_moe_quantize_act(act, b + W.h, P, I, nullptr, 1, b + W.ha, b + W.hb, ho, stream);
     if (rc) return rc;
-    rc = gemm_for(L, act, MNW_KIND_DOWN, b + W.ha, b + W.hb, ho, offs, P, b + W.y, err, st);
+    rc = gemm_for(L, act, MNW_KIND_DOWN, b + W.ha, b + W.hb, ho, offs, P, b + W.y, err, sched_dn, st);
     if (rc) return rc;
   }
   return mnw_moe_combine(b + W.y, pos, w, T, k, H, out, stream);

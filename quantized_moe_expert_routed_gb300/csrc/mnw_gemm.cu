@@ -703,7 +703,8 @@ cudaError_t launch_kind(bool gate_up, const CUtensorMap* maps, const GemmArgs& a
 }  // namespace
 
 int run_gemm(const mnw_moe_layer* L, int wfmt, int act, int kind, const void* a0, const void* a1, const void* a2,
-             const int32_t* offsets, int P, void* out, int32_t* dots, uint32_t* err, cudaStream_t st) {
+             const int32_t* offsets, int P, void* out, int32_t* dots, uint32_t* err, cudaStream_t st,
+             uint32_t* sched) {
   if (!L || (kind != MNW_KIND_GATE_UP && kind != MNW_KIND_DOWN) || P < 0) return MNW_E_INVALID_ARG;
   if (L->wfmt != wfmt) return MNW_E_MODE;
   if (P == 0) return MNW_OK;
@@ -716,7 +717,7 @@ int run_gemm(const mnw_moe_layer* L, int wfmt, int act, int kind, const void* a0
   const int path = gemm_path();
   if (warp_gemm_applicable(L, wfmt, act, kind) && path != MNW_PATH_TCGEN05) {
     const int nt = mean_rows <= 4 ? 1 : (mean_rows <= 16 ? 2 : 4);
-    return run_gemm_warp(L, wfmt, act, kind, a0, a1, offsets, P, nt, out, dots, err, st);
+    return run_gemm_warp(L, wfmt, act, kind, a0, a1, offsets, P, nt, out, dots, err, sched, st);
   }
   const bool gate_up = kind == MNW_KIND_GATE_UP;
   const int K = gate_up ? L->H : L->I;

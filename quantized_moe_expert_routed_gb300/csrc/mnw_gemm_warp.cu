@@ -39,6 +39,9 @@
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
+#include <atomic>
+#include <mutex>
+
 #include "mnw_convert.cuh"
 #include "mnw_internal.h"
 #include "mnw_ptx.cuh"
@@ -69,11 +72,13 @@ struct Args {
   __nv_bfloat16* out;
   int32_t* dots;
   uint32_t* err;
+  uint32_t* sched;  // [claim, done]: zero at launch; the last CTA to finish zeroes it again
 };
 
 struct Bars {
   uint64_t full[kMaxStages], empty[kMaxStages];
   uint64_t sfull[2], sempty[2];
+  int unit[2];  // unit handed from the producer to the MMA warps, per scale buffer
   int abort;
 };
 
@@ -236,11 +241,20 @@ __global__ void __launch_bounds__(kThreads, ctas_per_sm(WF, NT))
       int s = 0;
       uint32_t ph = 0;  // stage index and phase of `it`, kept without divisions
       bool ok = true;
-      for (int u = blockIdx.x; ok && u < units; u += gridDim.x, ++uit) {
-        const Unit x = decode(tab_prefix, tab_off, E, args.n_blocks, BN, u);
-        const int nb = x.rb * rows_per_block;
+      // Units are claimed from a counter shared by the CTAs (the last wave
+      // stays balanced) and passed to the MMA warps through shared memory
+      // under the scale-buffer barrier.
+      for (;; ++uit) {
+        const int u = static_cast<int>(atomicAdd(args.sched, 1u));
         const uint32_t sb = uit & 1;
         if (!bounded_wait(&bars->sempty[sb], ((uit >> 1) & 1) ^ 1, abort, args.err)) { ok = false; break; }
+        bars->unit[sb] = u;
+        if (u >= units) {  // no more work: release the MMA warps
+          mbar_arrive(&bars->sfull[sb]);
+          break;
+        }
+        const Unit x = decode(tab_prefix, tab_off, E, args.n_blocks, BN, u);
+        const int nb = x.rb * rows_per_block;
         mbar_arrive_expect_tx(&bars->sfull[sb], 2 * args.scale_box_bytes);
         for (int i = 0; i < 2; ++i) {
           const uint8_t* src = args.experts + static_cast<uint64_t>(x.e) * args.expert_stride + args.scales_off[i] +
@@ -263,6 +277,11 @@ __global__ void __launch_bounds__(kThreads, ctas_per_sm(WF, NT))
           }
           if (++s == S) { s = 0; ph ^= 1; }
         }
+      }
+      // The last CTA to stop claiming resets the counter for its next user.
+      if (atomicAdd(args.sched + 1, 1u) == gridDim.x - 1) {
+        atomicExch(args.sched, 0u);
+        atomicExch(args.sched + 1, 0u);
       }
       if (!ok || *abort) {
         const uint32_t first = it > static_cast<uint32_t>(S) ? it - S : 0;
@@ -300,11 +319,13 @@ __global__ void __launch_bounds__(kThreads, ctas_per_sm(WF, NT))
         a_off[i][hh][c] = i * args.box_bytes +
                           (WF == WF_INT4 ? r * 64 + t * 16 : r * 128 + (((2 * t + c) ^ (r & 7)) << 4));
     }
-  for (int u = blockIdx.x; u < units; u += gridDim.x, ++uit) {
-    const Unit x = decode(tab_prefix, tab_off, E, args.n_blocks, BN, u);
-    const int nb = x.rb * rows_per_block;
+  for (;; ++uit) {
     const uint32_t sb = uit & 1;
     if (!bounded_wait(&bars->sfull[sb], (uit >> 1) & 1, abort, args.err)) return;
+    const int u = *reinterpret_cast<volatile int*>(&bars->unit[sb]);
+    if (u >= units) break;
+    const Unit x = decode(tab_prefix, tab_off, E, args.n_blocks, BN, u);
+    const int nb = x.rb * rows_per_block;
     const __half* scl[2] = {
         reinterpret_cast<const __half*>(smem + args.off_scales + (sb * 2 + 0) * args.scale_box_bytes),
         reinterpret_cast<const __half*>(smem + args.off_scales + (sb * 2 + 1) * args.scale_box_bytes)};
@@ -343,6 +364,8 @@ __global__ void __launch_bounds__(kThreads, ctas_per_sm(WF, NT))
         uint32_t b0[NT], b1[NT];
 #pragma unroll
         for (int j = 0; j < NT; ++j) {
+          b0[j] = b1[j] = 0;
+          if (j > 0 && 8 * j >= x.nrows) continue;  // n-tile past this unit's rows (uniform per warp)
           if constexpr (kBf16) {
             const uint2 v = lds64(st + b_off[j][ks >> 1] + 8 * (ks & 1));
             b0[j] = v.x;
@@ -364,6 +387,7 @@ __global__ void __launch_bounds__(kThreads, ctas_per_sm(WF, NT))
           }
 #pragma unroll
           for (int j = 0; j < NT; ++j) {
+            if (j > 0 && 8 * j >= x.nrows) continue;
             if constexpr (kBf16) hmma_bf16(cg[i][j], a, b0[j], b1[j]);
             else hmma_f16(cg[i][j], a, b0[j], b1[j]);
           }
@@ -434,6 +458,28 @@ __global__ void __launch_bounds__(kThreads, ctas_per_sm(WF, NT))
 // ---------------------------------------------------------------------------
 
 namespace {
+// Work counters for launches that bring none: a ring of [claim, done] pairs,
+// each reset to zero by the last CTA of the launch that used it.  A slot is
+// reused after kSchedSlots further launches.
+constexpr int kSchedSlots = 1024;
+static __device__ uint32_t g_sched_ring[2 * kSchedSlots];
+std::atomic<uint32_t> g_sched_next{0};
+std::mutex g_sched_mu;
+void* g_sched_addr[64] = {};
+
+uint32_t* next_sched_slot() {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
+  void* base = nullptr;
+  {
+    std::lock_guard<std::mutex> lock(g_sched_mu);
+    if (!g_sched_addr[dev] && cudaGetSymbolAddress(&g_sched_addr[dev], g_sched_ring) != cudaSuccess) return nullptr;
+    base = g_sched_addr[dev];
+  }
+  const uint32_t slot = g_sched_next.fetch_add(1) % kSchedSlots;
+  return static_cast<uint32_t*>(base) + 2 * slot;
+}
+
 constexpr size_t kSmemPerSm = 232448;
 inline size_t smem_limit(int wf, int nt) { return ctas_per_sm(wf, nt) == 2 ? kSmemPerSm / 2 - 1024 : kSmemPerSm; }
 inline uint32_t align_up(uint32_t x, uint32_t a) { return (x + a - 1) / a * a; }
@@ -477,7 +523,8 @@ bool warp_gemm_applicable(const mnw_moe_layer* L, int wfmt, int act, int kind) {
 }
 
 int run_gemm_warp(const mnw_moe_layer* L, int wfmt, int act, int kind, const void* a0, const void* a1,
-                  const int32_t* offsets, int P, int nt, void* out, int32_t* dots, uint32_t* err, cudaStream_t st) {
+                  const int32_t* offsets, int P, int nt, void* out, int32_t* dots, uint32_t* err, uint32_t* sched,
+                  cudaStream_t st) {
   using namespace warpmma;
   const bool gu = kind == MNW_KIND_GATE_UP;
   const int K = gu ? L->H : L->I, N = gu ? L->I : L->H, G = K / 128;
@@ -516,6 +563,8 @@ int run_gemm_warp(const mnw_moe_layer* L, int wfmt, int act, int kind, const voi
   a.out = static_cast<__nv_bfloat16*>(out);
   a.dots = act == MNW_ACT_INT8_G128 ? dots : nullptr;
   a.err = err;
+  a.sched = sched ? sched : next_sched_slot();
+  if (!a.sched) return MNW_E_CUDA;
 
   CUtensorMap maps[3];
   maps[0] = L->tm_wcodes[m0];

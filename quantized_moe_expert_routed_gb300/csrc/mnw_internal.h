@@ -38,13 +38,16 @@ cudaError_t launch_combine(const void* y, const int32_t* assign_pos, const float
 cudaError_t launch_quantize(int act, const void* x, int R, int K, const int32_t* row_index, int index_div,
                             void* codes, void* scales, float* row_outer, cudaStream_t st);
 // Grouped GEMM for weight format wfmt and activation mode act.
+// sched (nullable): a zeroed device counter that lets the kernel's CTAs claim
+// work units dynamically; NULL gives a static round-robin order.
 int run_gemm(const mnw_moe_layer* L, int wfmt, int act, int kind, const void* a0, const void* a1,
              const void* a2, const int32_t* offsets, int P, void* out, int32_t* dots, uint32_t* err,
-             cudaStream_t st);
+             cudaStream_t st, uint32_t* sched = nullptr);
 // Warp-MMA grouped GEMM (INT8/INT4 weights, few tokens per expert); nt = token tile / 8.
 bool warp_gemm_applicable(const mnw_moe_layer* L, int wfmt, int act, int kind);
 int run_gemm_warp(const mnw_moe_layer* L, int wfmt, int act, int kind, const void* a0, const void* a1,
-                  const int32_t* offsets, int P, int nt, void* out, int32_t* dots, uint32_t* err, cudaStream_t st);
+                  const int32_t* offsets, int P, int nt, void* out, int32_t* dots, uint32_t* err, uint32_t* sched,
+                  cudaStream_t st);
 // Process-wide GEMM path selection (MNW_PATH_*).
 int gemm_path();
 
