@@ -238,15 +238,6 @@ int mnw_moe_layer_init(const void* header_host, const void* blob_dev, size_t blo
       ok = encode_map(&L.tm_codes[m], CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, experts + L.codes_off[m], dims, strides, box,
                       CU_TENSOR_MAP_SWIZZLE_128B);
     }
-    if (ok && (L.wfmt == MNW_FMT_INT8_G128 || L.wfmt == MNW_FMT_INT4_G128)) {
-      // one 128-K group of 128 rows per box: 64 bytes (INT4, plain) or 128 bytes (INT8, 128-byte swizzle)
-      const uint64_t row = code_bytes(L.wfmt, 1, K);
-      const uint64_t dims[3] = {row, N, static_cast<uint64_t>(L.E)};
-      const uint64_t strides[2] = {row, L.expert_stride};
-      const uint32_t box[3] = {L.wfmt == MNW_FMT_INT4_G128 ? 64u : 128u, 128, 1};
-      ok = encode_map(&L.tm_wcodes[m], CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, experts + L.codes_off[m], dims, strides, box,
-                      L.wfmt == MNW_FMT_INT4_G128 ? CU_TENSOR_MAP_SWIZZLE_NONE : CU_TENSOR_MAP_SWIZZLE_128B);
-    }
     if (ok && L.wfmt == MNW_FMT_NVFP4_G16) {
       const uint64_t dims[3] = {K / 16, N, static_cast<uint64_t>(L.E)};
       const uint64_t strides[2] = {K / 16, L.expert_stride};

@@ -56,9 +56,12 @@ constexpr int kMmaWarps = 8;
 constexpr int kThreads = (1 + kMmaWarps) * 32;  // warp 0 = producer
 constexpr int kMaxStages = 12;
 constexpr int kRowsPerBox = 128;
-// CTAs per SM: two (16 MMA warps) where a thread's registers fit in 96 (8- and
-// 16-token tiles); one for 32-token tiles, whose accumulators need more.
-constexpr int ctas_per_sm(int wf, int nt) { return nt <= 2 ? 2 : 1; }
+constexpr int kGroups = 2;          // 128-K groups per pipeline stage
+constexpr int kBoxBytes = 128 * 128;  // one TMA box: 128 rows x 128 bytes
+// CTAs per SM: two (16 MMA warps) for INT4 with 8- and 16-token tiles, whose
+// registers fit in 96 and whose stages fit in half the shared memory; one
+// otherwise (INT8 stages are twice as large, 32-token accumulators need more).
+constexpr int ctas_per_sm(int wf, int nt) { return (nt <= 2 && wf == 2) ? 2 : 1; }
 
 struct Args {
   const int32_t* offsets;
@@ -173,7 +176,9 @@ __global__ void __launch_bounds__(kThreads, ctas_per_sm(WF, NT))
     moe_gemm_warp_kernel(const __grid_constant__ CUtensorMap tmA0, const __grid_constant__ CUtensorMap tmA1,
                          const __grid_constant__ CUtensorMap tmB, const Args args) {
   constexpr bool kBf16 = AM == AM_BF16;
-  constexpr int kRB = WF == WF_INT4 ? 64 : 128;  // code bytes of one row per 128-K group
+  // A stage holds kGroups 128-K groups: per weight row 128 contiguous code
+  // bytes (INT4) or two 128-byte pieces (INT8), 128-byte swizzled.
+  constexpr int kABoxes = WF == WF_INT4 ? 1 : 2;  // 16 KB boxes per 128-row block per stage
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   Bars* bars = reinterpret_cast<Bars*>(smem + args.off_bars);
@@ -235,8 +240,9 @@ __global__ void __launch_bounds__(kThreads, ctas_per_sm(WF, NT))
       tma_prefetch_desc(&tmA0);
       tma_prefetch_desc(&tmA1);
       tma_prefetch_desc(&tmB);
-      const uint32_t b_bytes = kBf16 ? 2u * BN * 128u : BN * 128u;
-      const uint32_t tx = 2u * args.box_bytes + b_bytes;
+      const uint32_t b_bytes = (kBf16 ? 4u : 2u) * BN * 128u;
+      const uint32_t tx = 2u * kABoxes * kBoxBytes + b_bytes;
+      const int nstages = (G + kGroups - 1) / kGroups;
       uint32_t it = 0, uit = 0, sit = 0;
       int s = 0;
       uint32_t ph = 0;  // stage index and phase of `it`, kept without divisions
@@ -263,18 +269,23 @@ __global__ void __launch_bounds__(kThreads, ctas_per_sm(WF, NT))
                     &bars->sfull[sb]);
         }
         ++sit;
-        for (int grp = 0; grp < G; ++grp, ++it) {
+        for (int ss = 0; ss < nstages; ++ss, ++it) {
           if (!bounded_wait(&bars->empty[s], ph ^ 1, abort, args.err)) { ok = false; break; }
           uint8_t* st = smem + s * args.stage_bytes;
           mbar_arrive_expect_tx(&bars->full[s], tx);
-          tma_load_3d(st, &tmA0, &bars->full[s], grp * kRB, nb + args.box_row_off[0], x.e);
-          tma_load_3d(st + args.box_bytes, &tmA1, &bars->full[s], grp * kRB, nb + args.box_row_off[1], x.e);
-          if (kBf16) {
-            tma_load_2d(st + args.off_b, &tmB, &bars->full[s], grp * 128, x.row0);
-            tma_load_2d(st + args.off_b + BN * 128, &tmB, &bars->full[s], grp * 128 + 64, x.row0);
-          } else {
-            tma_load_2d(st + args.off_b, &tmB, &bars->full[s], grp * 128, x.row0);
+          // weight codes: box (i, q) holds rows of block i, 128 bytes at byte (ss*kABoxes + q)*128
+#pragma unroll
+          for (int q = 0; q < kABoxes; ++q) {
+            tma_load_3d(st + (0 * kABoxes + q) * kBoxBytes, &tmA0, &bars->full[s], (ss * kABoxes + q) * 128,
+                        nb + args.box_row_off[0], x.e);
+            tma_load_3d(st + (1 * kABoxes + q) * kBoxBytes, &tmA1, &bars->full[s], (ss * kABoxes + q) * 128,
+                        nb + args.box_row_off[1], x.e);
           }
+          // tokens: 64-element BF16 boxes or 128-element INT8 boxes covering the stage's 256 K
+#pragma unroll
+          for (int b = 0; b < (kBf16 ? 4 : 2); ++b)
+            tma_load_2d(st + args.off_b + b * BN * 128, &tmB, &bars->full[s], ss * 256 + b * (kBf16 ? 64 : 128),
+                        x.row0);
           if (++s == S) { s = 0; ph ^= 1; }
         }
       }
@@ -308,17 +319,22 @@ __global__ void __launch_bounds__(kThreads, ctas_per_sm(WF, NT))
       b_off[j][c] = kBf16 ? args.off_b + (t >> 1) * BN * 128 + row * 128 + (((4 * (t & 1) + c) ^ (row & 7)) << 4)
                           : args.off_b + row * 128 + (((2 * t + (c & 1)) ^ (row & 7)) << 4);
   }
-  uint32_t a_off[2][2][2];
+  // a_off[gi][i][hh][c]: code chunk c of row 16w+g+8hh of block i for group gi of a stage
+  uint32_t a_off[kGroups][2][2][2];
 #pragma unroll
-  for (int i = 0; i < 2; ++i)
+  for (int gi = 0; gi < kGroups; ++gi)
 #pragma unroll
-    for (int hh = 0; hh < 2; ++hh) {
-      const int r = 16 * w + g + 8 * hh;
+    for (int i = 0; i < 2; ++i)
 #pragma unroll
-      for (int c = 0; c < 2; ++c)
-        a_off[i][hh][c] = i * args.box_bytes +
-                          (WF == WF_INT4 ? r * 64 + t * 16 : r * 128 + (((2 * t + c) ^ (r & 7)) << 4));
-    }
+      for (int hh = 0; hh < 2; ++hh) {
+        const int r = 16 * w + g + 8 * hh;
+#pragma unroll
+        for (int c = 0; c < 2; ++c)
+          a_off[gi][i][hh][c] =
+              WF == WF_INT4 ? i * kBoxBytes + r * 128 + (((4 * gi + t) ^ (r & 7)) << 4)
+                            : (2 * i + gi) * kBoxBytes + r * 128 + (((2 * t + c) ^ (r & 7)) << 4);
+      }
+  const uint32_t b_gstep = (kBf16 ? 2u : 1u) * BN * 128u;  // token boxes per group
   for (;; ++uit) {
     const uint32_t sb = uit & 1;
     if (!bounded_wait(&bars->sfull[sb], (uit >> 1) & 1, abort, args.err)) return;
@@ -337,19 +353,25 @@ __global__ void __launch_bounds__(kThreads, ctas_per_sm(WF, NT))
 #pragma unroll
         for (int q = 0; q < 4; ++q) tot[i][j][q] = 0.f;
 
-    for (int grp = 0; grp < G; ++grp, ++it) {
+    const int nstages = (G + kGroups - 1) / kGroups;
+    for (int ss = 0; ss < nstages; ++ss, ++it) {
       if (!bounded_wait(&bars->full[s], ph, abort, args.err)) return;
       const uint32_t st = smem_u32(smem + s * args.stage_bytes);
       const int s_now = s;
       if (++s == S) { s = 0; ph ^= 1; }
+#pragma unroll
+      for (int gi = 0; gi < kGroups; ++gi) {
+      const int grp = ss * kGroups + gi;
+      if (grp >= G) break;
+      const uint32_t stb = st + gi * b_gstep;
       // raw codes: [box i][row g / g+8]
       uint4 ar[2][2][WF == WF_INT4 ? 1 : 2];
 #pragma unroll
       for (int i = 0; i < 2; ++i)
 #pragma unroll
         for (int hh = 0; hh < 2; ++hh) {
-          ar[i][hh][0] = lds128(st + a_off[i][hh][0]);
-          if constexpr (WF != WF_INT4) ar[i][hh][1] = lds128(st + a_off[i][hh][1]);
+          ar[i][hh][0] = lds128(st + a_off[gi][i][hh][0]);
+          if constexpr (WF != WF_INT4) ar[i][hh][1] = lds128(st + a_off[gi][i][hh][1]);
         }
       float cg[2][NT][4];
 #pragma unroll
@@ -367,11 +389,11 @@ __global__ void __launch_bounds__(kThreads, ctas_per_sm(WF, NT))
           b0[j] = b1[j] = 0;
           if (j > 0 && 8 * j >= x.nrows) continue;  // n-tile past this unit's rows (uniform per warp)
           if constexpr (kBf16) {
-            const uint2 v = lds64(st + b_off[j][ks >> 1] + 8 * (ks & 1));
+            const uint2 v = lds64(stb + b_off[j][ks >> 1] + 8 * (ks & 1));
             b0[j] = v.x;
             b1[j] = v.y;
           } else {
-            int8_pair<false>(lds32(st + b_off[j][ks >> 2] + 4 * (ks & 3)), b0[j], b1[j]);
+            int8_pair<false>(lds32(stb + b_off[j][ks >> 2] + 4 * (ks & 3)), b0[j], b1[j]);
           }
         }
 #pragma unroll
@@ -393,8 +415,6 @@ __global__ void __launch_bounds__(kThreads, ctas_per_sm(WF, NT))
           }
         }
       }
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&bars->empty[s_now]);  // codes and tokens of this stage are in registers
       // FP32 group combine: tot += (s_w [* s_a]) * exact group dot
 #pragma unroll
       for (int i = 0; i < 2; ++i) {
@@ -429,6 +449,9 @@ __global__ void __launch_bounds__(kThreads, ctas_per_sm(WF, NT))
           }
         }
       }
+      }  // groups of the stage
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&bars->empty[s_now]);  // this stage's codes and tokens are consumed
     }
     __syncwarp();
     if (lane == 0) mbar_arrive(&bars->sempty[sb]);
@@ -529,7 +552,6 @@ int run_gemm_warp(const mnw_moe_layer* L, int wfmt, int act, int kind, const voi
   const bool gu = kind == MNW_KIND_GATE_UP;
   const int K = gu ? L->H : L->I, N = gu ? L->I : L->H, G = K / 128;
   const int BN = 8 * nt;
-  const int rb = wfmt == MNW_FMT_INT4_G128 ? 64 : 128;
   Args a{};
   a.offsets = offsets;
   a.E = L->E;
@@ -538,9 +560,10 @@ int run_gemm_warp(const mnw_moe_layer* L, int wfmt, int act, int kind, const voi
   a.N = N;
   a.BN = BN;
   a.n_blocks = gu ? N / kRowsPerBox : N / (2 * kRowsPerBox);
-  a.box_bytes = kRowsPerBox * rb;
-  a.off_b = 2 * a.box_bytes;
-  const uint32_t b_bytes = act == MNW_ACT_BF16 ? 2u * BN * 128u : BN * 128u;
+  const int a_boxes = wfmt == MNW_FMT_INT4_G128 ? 1 : 2;
+  a.box_bytes = kBoxBytes;
+  a.off_b = 2 * a_boxes * kBoxBytes;
+  const uint32_t b_bytes = (act == MNW_ACT_BF16 ? 4u : 2u) * BN * 128u;
   a.stage_bytes = align_up(a.off_b + b_bytes, 1024);
   a.scale_box_bytes = kRowsPerBox * G * 2;
   const uint32_t fixed = 4 * a.scale_box_bytes + align_up(2u * (L->E + 1) * 4u, 16) + align_up(sizeof(Bars), 16);
@@ -567,8 +590,8 @@ int run_gemm_warp(const mnw_moe_layer* L, int wfmt, int act, int kind, const voi
   if (!a.sched) return MNW_E_CUDA;
 
   CUtensorMap maps[3];
-  maps[0] = L->tm_wcodes[m0];
-  maps[1] = L->tm_wcodes[m1];
+  maps[0] = L->tm_codes[m0];
+  maps[1] = L->tm_codes[m1];
   const uint64_t dims[2] = {static_cast<uint64_t>(K), static_cast<uint64_t>(P)};
   bool ok;
   if (act == MNW_ACT_BF16) {

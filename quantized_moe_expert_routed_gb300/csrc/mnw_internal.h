@@ -17,8 +17,6 @@ struct mnw_moe_layer {
   // Weight tensor maps (built once): codes per matrix, NVFP4 block scales per matrix.
   CUtensorMap tm_codes[3];
   CUtensorMap tm_sf[3];
-  // Per-128-group weight tiles for the warp-MMA kernel (INT8/INT4 only).
-  CUtensorMap tm_wcodes[3];
 };
 
 namespace mnw {
