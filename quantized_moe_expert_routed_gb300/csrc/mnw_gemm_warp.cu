@@ -171,6 +171,100 @@ __device__ __forceinline__ uint32_t word_of(const uint4& v, int i) {
   return i == 0 ? v.x : i == 1 ? v.y : i == 2 ? v.z : v.w;
 }
 
+// One 128-K group of a stage for one warp: its 16 rows of both row blocks
+// against the first NTA token tiles (NTA is fixed per unit, so the body has
+// no branches and the compiler can interleave all of it), then the FP32
+// group combine tot += (s_w [* s_a]) * exact group dot.
+template <int WF, int AM, bool kGateUp, int NT, int NTA>
+__device__ __forceinline__ void group_step(const Args& args, uint32_t st, uint32_t stb,
+                                           const uint32_t (&a_off)[2][2][2], const uint32_t (&b_off)[NT][4],
+                                           const __half* scl0, const __half* scl1, int w, int g, int t, int grp,
+                                           int G, const Unit& x, int nb, float (&tot)[2][NT][4]) {
+  constexpr bool kBf16 = AM == AM_BF16;
+  // raw codes: [box i][row g / g+8]
+  uint4 ar[2][2][WF == WF_INT4 ? 1 : 2];
+#pragma unroll
+  for (int i = 0; i < 2; ++i)
+#pragma unroll
+    for (int hh = 0; hh < 2; ++hh) {
+      ar[i][hh][0] = lds128(st + a_off[i][hh][0]);
+      if constexpr (WF != WF_INT4) ar[i][hh][1] = lds128(st + a_off[i][hh][1]);
+    }
+  float cg[2][NTA][4];
+#pragma unroll
+  for (int i = 0; i < 2; ++i)
+#pragma unroll
+    for (int j = 0; j < NTA; ++j)
+#pragma unroll
+      for (int q = 0; q < 4; ++q) cg[i][j][q] = 0.f;
+#pragma unroll
+  for (int ks = 0; ks < 8; ++ks) {
+    // token operand of this k-step: K = 32t + 4ks .. +3 of each n-tile's row
+    uint32_t b0[NTA], b1[NTA];
+#pragma unroll
+    for (int j = 0; j < NTA; ++j) {
+      if constexpr (kBf16) {
+        const uint2 v = lds64(stb + b_off[j][ks >> 1] + 8 * (ks & 1));
+        b0[j] = v.x;
+        b1[j] = v.y;
+      } else {
+        int8_pair<false>(lds32(stb + b_off[j][ks >> 2] + 4 * (ks & 3)), b0[j], b1[j]);
+      }
+    }
+#pragma unroll
+    for (int i = 0; i < 2; ++i) {
+      uint32_t a[4];  // {row g, slots 2t..}, {row g+8, 2t..}, {row g, 2t+8..}, {row g+8, 2t+8..}
+#pragma unroll
+      for (int hh = 0; hh < 2; ++hh) {
+        uint32_t lo, hi;
+        if constexpr (WF == WF_INT4) int4_pair<kBf16>(word_of(ar[i][hh][0], ks >> 1), ks & 1, lo, hi);
+        else int8_pair<kBf16>(word_of(ar[i][hh][ks >> 2], ks & 3), lo, hi);
+        a[hh] = lo;
+        a[2 + hh] = hi;
+      }
+#pragma unroll
+      for (int j = 0; j < NTA; ++j) {
+        if constexpr (kBf16) hmma_bf16(cg[i][j], a, b0[j], b1[j]);
+        else hmma_f16(cg[i][j], a, b0[j], b1[j]);
+      }
+    }
+  }
+#pragma unroll
+  for (int i = 0; i < 2; ++i) {
+    const __half* scl = i == 0 ? scl0 : scl1;
+    const float sw0 = __half2float(scl[(16 * w + g) * G + grp]);
+    const float sw1 = __half2float(scl[(16 * w + g + 8) * G + grp]);
+#pragma unroll
+    for (int j = 0; j < NTA; ++j) {
+      const int tok0 = j * 8 + 2 * t;
+      float f00 = sw0, f01 = sw0, f10 = sw1, f11 = sw1;
+      if constexpr (!kBf16) {
+        const float sa0 = tok0 < x.nrows ? __ldg(args.a_scales + static_cast<size_t>(x.row0 + tok0) * G + grp) : 0.f;
+        const float sa1 =
+            tok0 + 1 < x.nrows ? __ldg(args.a_scales + static_cast<size_t>(x.row0 + tok0 + 1) * G + grp) : 0.f;
+        f00 = __fmul_rn(sw0, sa0); f01 = __fmul_rn(sw0, sa1);
+        f10 = __fmul_rn(sw1, sa0); f11 = __fmul_rn(sw1, sa1);
+      }
+      tot[i][j][0] = __fmaf_rn(f00, cg[i][j][0], tot[i][j][0]);
+      tot[i][j][1] = __fmaf_rn(f01, cg[i][j][1], tot[i][j][1]);
+      tot[i][j][2] = __fmaf_rn(f10, cg[i][j][2], tot[i][j][2]);
+      tot[i][j][3] = __fmaf_rn(f11, cg[i][j][3], tot[i][j][3]);
+      if (!kBf16 && args.dots) {
+        // exact group dot products, layout [P][C][G]; C = 2N (gate, up) or N
+        const size_t C = kGateUp ? 2 * static_cast<size_t>(args.N) : static_cast<size_t>(args.N);
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          const int tok = tok0 + (q & 1);
+          const int feat = nb + args.box_row_off[i] + 16 * w + g + 8 * (q >> 1);
+          const size_t col = kGateUp ? static_cast<size_t>(i) * args.N + feat : static_cast<size_t>(feat);
+          if (tok < x.nrows)
+            args.dots[(static_cast<size_t>(x.row0 + tok) * C + col) * G + grp] = __float2int_rn(cg[i][j][q]);
+        }
+      }
+    }
+  }
+}
+
 template <int WF, int AM, bool kGateUp, int NT>
 __global__ void __launch_bounds__(kThreads, ctas_per_sm(WF, NT))
     moe_gemm_warp_kernel(const __grid_constant__ CUtensorMap tmA0, const __grid_constant__ CUtensorMap tmA1,
@@ -249,9 +343,13 @@ __global__ void __launch_bounds__(kThreads, ctas_per_sm(WF, NT))
       bool ok = true;
       // Units are claimed from a counter shared by the CTAs (the last wave
       // stays balanced) and passed to the MMA warps through shared memory
-      // under the scale-buffer barrier.
+      // under the scale-buffer barrier.  The next unit is claimed while the
+      // current unit's last two stages are issued, so the atomic's latency
+      // hides behind them and the next unit's loads follow without a gap.
+      const int claim_at = nstages >= 2 ? nstages - 2 : 0;
+      int u_next = static_cast<int>(atomicAdd(args.sched, 1u));
       for (;; ++uit) {
-        const int u = static_cast<int>(atomicAdd(args.sched, 1u));
+        const int u = u_next;
         const uint32_t sb = uit & 1;
         if (!bounded_wait(&bars->sempty[sb], ((uit >> 1) & 1) ^ 1, abort, args.err)) { ok = false; break; }
         bars->unit[sb] = u;
@@ -270,6 +368,7 @@ __global__ void __launch_bounds__(kThreads, ctas_per_sm(WF, NT))
         }
         ++sit;
         for (int ss = 0; ss < nstages; ++ss, ++it) {
+          if (ss == claim_at) u_next = static_cast<int>(atomicAdd(args.sched, 1u));
           if (!bounded_wait(&bars->empty[s], ph ^ 1, abort, args.err)) { ok = false; break; }
           uint8_t* st = smem + s * args.stage_bytes;
           mbar_arrive_expect_tx(&bars->full[s], tx);
@@ -364,89 +463,20 @@ __global__ void __launch_bounds__(kThreads, ctas_per_sm(WF, NT))
       const int grp = ss * kGroups + gi;
       if (grp >= G) break;
       const uint32_t stb = st + gi * b_gstep;
-      // raw codes: [box i][row g / g+8]
-      uint4 ar[2][2][WF == WF_INT4 ? 1 : 2];
-#pragma unroll
-      for (int i = 0; i < 2; ++i)
-#pragma unroll
-        for (int hh = 0; hh < 2; ++hh) {
-          ar[i][hh][0] = lds128(st + a_off[gi][i][hh][0]);
-          if constexpr (WF != WF_INT4) ar[i][hh][1] = lds128(st + a_off[gi][i][hh][1]);
-        }
-      float cg[2][NT][4];
-#pragma unroll
-      for (int i = 0; i < 2; ++i)
-#pragma unroll
-        for (int j = 0; j < NT; ++j)
-#pragma unroll
-          for (int q = 0; q < 4; ++q) cg[i][j][q] = 0.f;
-#pragma unroll
-      for (int ks = 0; ks < 8; ++ks) {
-        // token operand of this k-step: K = 32t + 4ks .. +3 of each n-tile's row
-        uint32_t b0[NT], b1[NT];
-#pragma unroll
-        for (int j = 0; j < NT; ++j) {
-          b0[j] = b1[j] = 0;
-          if (j > 0 && 8 * j >= x.nrows) continue;  // n-tile past this unit's rows (uniform per warp)
-          if constexpr (kBf16) {
-            const uint2 v = lds64(stb + b_off[j][ks >> 1] + 8 * (ks & 1));
-            b0[j] = v.x;
-            b1[j] = v.y;
-          } else {
-            int8_pair<false>(lds32(stb + b_off[j][ks >> 2] + 4 * (ks & 3)), b0[j], b1[j]);
-          }
-        }
-#pragma unroll
-        for (int i = 0; i < 2; ++i) {
-          uint32_t a[4];  // {row g, slots 2t..}, {row g+8, 2t..}, {row g, 2t+8..}, {row g+8, 2t+8..}
-#pragma unroll
-          for (int hh = 0; hh < 2; ++hh) {
-            uint32_t lo, hi;
-            if constexpr (WF == WF_INT4) int4_pair<kBf16>(word_of(ar[i][hh][0], ks >> 1), ks & 1, lo, hi);
-            else int8_pair<kBf16>(word_of(ar[i][hh][ks >> 2], ks & 3), lo, hi);
-            a[hh] = lo;
-            a[2 + hh] = hi;
-          }
-#pragma unroll
-          for (int j = 0; j < NT; ++j) {
-            if (j > 0 && 8 * j >= x.nrows) continue;
-            if constexpr (kBf16) hmma_bf16(cg[i][j], a, b0[j], b1[j]);
-            else hmma_f16(cg[i][j], a, b0[j], b1[j]);
-          }
-        }
-      }
-      // FP32 group combine: tot += (s_w [* s_a]) * exact group dot
-#pragma unroll
-      for (int i = 0; i < 2; ++i) {
-        const float sw0 = __half2float(scl[i][(16 * w + g) * G + grp]);
-        const float sw1 = __half2float(scl[i][(16 * w + g + 8) * G + grp]);
-#pragma unroll
-        for (int j = 0; j < NT; ++j) {
-          const int tok0 = j * 8 + 2 * t;
-          float f00 = sw0, f01 = sw0, f10 = sw1, f11 = sw1;
-          if (!kBf16) {
-            const float sa0 = tok0 < x.nrows ? __ldg(args.a_scales + static_cast<size_t>(x.row0 + tok0) * G + grp) : 0.f;
-            const float sa1 =
-                tok0 + 1 < x.nrows ? __ldg(args.a_scales + static_cast<size_t>(x.row0 + tok0 + 1) * G + grp) : 0.f;
-            f00 = __fmul_rn(sw0, sa0); f01 = __fmul_rn(sw0, sa1);
-            f10 = __fmul_rn(sw1, sa0); f11 = __fmul_rn(sw1, sa1);
-          }
-          tot[i][j][0] = __fmaf_rn(f00, cg[i][j][0], tot[i][j][0]);
-          tot[i][j][1] = __fmaf_rn(f01, cg[i][j][1], tot[i][j][1]);
-          tot[i][j][2] = __fmaf_rn(f10, cg[i][j][2], tot[i][j][2]);
-          tot[i][j][3] = __fmaf_rn(f11, cg[i][j][3], tot[i][j][3]);
-          if (args.dots) {
-            // exact group dot products, layout [P][C][G]; C = 2N (gate, up) or N
-            const size_t C = kGateUp ? 2 * static_cast<size_t>(args.N) : static_cast<size_t>(args.N);
-#pragma unroll
-            for (int q = 0; q < 4; ++q) {
-              const int tok = tok0 + (q & 1);
-              const int feat = nb + args.box_row_off[i] + 16 * w + g + 8 * (q >> 1);
-              const size_t col = kGateUp ? static_cast<size_t>(i) * args.N + feat : static_cast<size_t>(feat);
-              if (tok < x.nrows)
-                args.dots[(static_cast<size_t>(x.row0 + tok) * C + col) * G + grp] = __float2int_rn(cg[i][j][q]);
-            }
-          }
+      // active token tiles of this unit (uniform across the CTA)
+      const int nta = NT == 1 ? 1 : min(NT, (x.nrows + 7) >> 3);
+      if (nta <= 1) {
+        group_step<WF, AM, kGateUp, NT, 1>(args, st, stb, a_off[gi], b_off, scl[0], scl[1], w, g, t, grp, G, x, nb, tot);
+      } else if constexpr (NT >= 2) {
+        if (nta == 2 || NT == 2) {
+          group_step<WF, AM, kGateUp, NT, (NT >= 2 ? 2 : 1)>(args, st, stb, a_off[gi], b_off, scl[0], scl[1], w, g, t,
+                                                            grp, G, x, nb, tot);
+        } else if (nta == 3) {
+          group_step<WF, AM, kGateUp, NT, (NT >= 3 ? 3 : 1)>(args, st, stb, a_off[gi], b_off, scl[0], scl[1], w, g, t,
+                                                            grp, G, x, nb, tot);
+        } else {
+          group_step<WF, AM, kGateUp, NT, NT>(args, st, stb, a_off[gi], b_off, scl[0], scl[1], w, g, t, grp, G, x, nb,
+                                              tot);
         }
       }
       }  // groups of the stage

@@ -52,16 +52,31 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
   return ok != 0;
 }
 
+// As mbar_try_wait, but the thread may stay suspended inside the instruction
+// until the phase completes or about `hint_ns` nanoseconds pass, instead of
+// returning at once: a waiting warp then takes no issue slots from the warps
+// that share its scheduler.
+__device__ __forceinline__ bool mbar_try_wait_sleep(uint64_t* bar, uint32_t parity, uint32_t hint_ns) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tmbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\tselp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity), "r"(hint_ns)
+      : "memory");
+  return ok != 0;
+}
+
 // Wait for the phase of `bar` with the given parity to complete.  Gives up
 // (returns false) when *abort is set by another warp, or after kWaitLimitNs,
-// in which case it sets *abort and ORs MNW_DEVERR_TIMEOUT into *err.
+// in which case it sets *abort and ORs MNW_DEVERR_TIMEOUT into *err.  Each
+// retry suspends for up to 10 us, so the abort flag is seen within ~80 us.
 __device__ __forceinline__ bool bounded_wait(uint64_t* bar, uint32_t parity, volatile int* abort,
                                              uint32_t* err) {
   if (mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = globaltimer();
   for (uint32_t it = 1;; ++it) {
-    if (mbar_try_wait(bar, parity)) return true;
-    if ((it & 63u) == 0) {
+    if (mbar_try_wait_sleep(bar, parity, 10000u)) return true;
+    if ((it & 7u) == 0) {
       if (*abort) return false;
       if (globaltimer() - t0 > kWaitLimitNs) {
         *abort = 1;
