@@ -205,9 +205,9 @@ int mnw_moe_forward_host(const mnw_moe_layer* layer, int act, const void* x_host
 
 /* Grouped-GEMM kernel selection, process-wide (a tuning and testing knob;
  * results agree to FP32 rounding order either way).  MNW_PATH_AUTO: INT8/INT4
- * weights with at most 64 tokens per expert on average use the warp-level MMA
- * kernel (operands dequantised straight into registers), everything else the
- * tcgen05 kernel.  MNW_PATH_TCGEN05 / MNW_PATH_WARP_MMA force one of them
+ * weights with fewer than 32 tokens per expert on average (P / E) use the
+ * warp-level MMA kernel (operands dequantised straight into registers),
+ * everything else the tcgen05 kernel.  MNW_PATH_TCGEN05 / MNW_PATH_WARP_MMA force one of them
  * (the warp kernel only covers INT8/INT4 weights with BF16 or INT8
  * activations).  Not synchronised with calls in flight on other threads. */
 enum mnw_path { MNW_PATH_AUTO = 0, MNW_PATH_TCGEN05 = 1, MNW_PATH_WARP_MMA = 2 };

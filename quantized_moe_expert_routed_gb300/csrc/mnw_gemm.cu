@@ -27,13 +27,14 @@
 // tile); every CTA walks units blockIdx.x, blockIdx.x + gridDim.x, ... over
 // the device-side tile table built from expert_offsets (no host sync).
 //
-// Warp roles (448 threads):
+// Warp roles (576 threads):
 //   warp 0      TMA producer: weight tiles (raw codes) + group scales + token tiles
 //   warp 1      MMA issuer (one thread); owns the TMEM allocation
 //   warps 2-9   converters: raw weight codes -> BF16/FP16 operand in TMEM
 //               (tcgen05.st); INT8/FP4 token codes -> FP16 operand in shared memory
-//   warps 10-13 epilogue: TMEM accumulators -> (group rescale) -> SiLU(g)*u or y
-//               -> BF16 global
+//   warps 10-17 epilogue: TMEM accumulators -> (group rescale) -> SiLU(g)*u or y
+//               -> BF16 global; two warps per TMEM lane quarter, each with half
+//               of the token columns
 //
 // TMEM (512 columns): operand-A ring (slots of 64 K per matrix), then the
 // accumulators; in the grouped modes two per-group accumulators (one drains
@@ -59,7 +60,7 @@ enum { AM_BF16 = 0, AM_INT8 = 1, AM_FP4 = 2 };
 
 constexpr int kBM = 128;
 constexpr int kConvWarps = 8;
-constexpr int kEpiWarps = 4;
+constexpr int kEpiWarps = 8;  // two per TMEM lane quarter, each taking half the token columns
 constexpr int kWarpTma = 0, kWarpMma = 1, kWarpConv0 = 2, kWarpEpi0 = kWarpConv0 + kConvWarps;
 constexpr int kThreads = (kWarpEpi0 + kEpiWarps) * 32;
 constexpr int kMaxStages = 8;
@@ -466,17 +467,27 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else {
     // ======================= epilogue =======================
+    // Warp e (0..7) reads TMEM lane quarter warp % 4 (row r of the tile) and
+    // the token columns [c0, c1): the first or second half of the tile, or,
+    // for tiles narrower than 32 columns, all of them (the second warp of the
+    // pair then only keeps the barrier phases in step).
     const int q = warp & 3;
     const int r = q * 32 + lane;
+    const int ew = warp - kWarpEpi0;
+    const int half = ew >> 2;
+    const int cpw = BN >= 32 ? BN / 2 : BN;
+    const int c0 = BN >= 32 ? half * cpw : (half ? BN : 0);
+    const int c1 = BN >= 32 ? c0 + cpw : (half ? BN : BN);
     const uint32_t lane_bits = static_cast<uint32_t>(q * 32) << 16;
     uint32_t acc_it = 0, uit = 0;
     bool ok = true;
-    // each epilogue warp keeps its own copy of the tile's activation scales
-    float* sa = reinterpret_cast<float*>(smem + args.off_sa) + (warp - kWarpEpi0) * BN * G;
+    // each epilogue warp keeps its own copy of its columns' activation scales
+    float* sa = reinterpret_cast<float*>(smem + args.off_sa) + ew * cpw * G;
     for (int u = blockIdx.x; ok && u < units; u += gridDim.x, ++uit) {
       const Unit x = decode_unit(tab_prefix, tab_off, E, args.n_tiles, BN, u);
       const int n0 = x.nt * kBM;
       const int col = n0 + r;
+      const int jend = min(c1, x.nrows);  // live columns of this warp: [c0, jend)
       if (!kGrouped) {
         const uint32_t slot = acc_it % args.acc_slots;
         if (!bounded_wait(&bars->accfull[slot], (acc_it / args.acc_slots) & 1, abort, args.err)) { ok = false; break; }
@@ -488,7 +499,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             ow[m] = __ldg(reinterpret_cast<const float*>(args.experts + static_cast<uint64_t>(x.e) * args.expert_stride +
                                                          args.outer_off[m]));
         }
-        for (int j0 = 0; j0 < BN && j0 < x.nrows; j0 += 16) {
+        for (int j0 = c0; j0 < jend; j0 += 16) {
           uint32_t g[16], up[16];
           tmem_ld16(d + j0, g);
           if (kGateUp) tmem_ld16(d + BN + j0, up);
@@ -496,7 +507,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
           for (int i = 0; i < 16; ++i) {
             const int j = j0 + i;
-            if (j < x.nrows && x.row0 + j < args.P) {
+            if (j < jend && x.row0 + j < args.P) {
               float gv = __uint_as_float(g[i]);
               float val;
               float oa = 1.f;
@@ -526,8 +537,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t sb = uit & 1;
         if (!bounded_wait(&bars->sfull[sb], (uit >> 1) & 1, abort, args.err)) { ok = false; break; }
         if (AM == AM_INT8) {
-          for (int i = lane; i < BN * G; i += 32) {
-            const int j = i / G, gg = i - j * G;
+          for (int i = lane; i < cpw * G; i += 32) {
+            const int j = c0 + i / G, gg = i - (i / G) * G;
             sa[i] = (j < x.nrows && x.row0 + j < args.P)
                         ? __ldg(args.a_scales + static_cast<size_t>(x.row0 + j) * G + gg)
                         : 0.f;
@@ -540,6 +551,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             reinterpret_cast<const __half*>(smem + args.off_scales + (sb * kNmat + (kNmat - 1)) * args.scale_mat_bytes) +
             r * G;
         const uint32_t dsum = tmem + lane_bits + args.sum_base;
+        const bool want_dots = AM == AM_INT8 && args.dots != nullptr;
         for (int g = 0; g < G; ++g) {
           const uint32_t slot = acc_it % args.acc_slots;
           if (!bounded_wait(&bars->accfull[slot], (acc_it / args.acc_slots) & 1, abort, args.err)) { ok = false; break; }
@@ -547,7 +559,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           const uint32_t d = tmem + lane_bits + args.acc_base + slot * kNmat * BN;
           const float w0 = __half2float(sw0[g]), w1 = __half2float(sw1[g]);
           const bool last = g == G - 1;
-          for (int j0 = 0; j0 < BN && j0 < x.nrows; j0 += 16) {
+          for (int j0 = c0; j0 < jend; j0 += 16) {
             uint32_t d0[16], d1[16], s0[16], s1[16];
             tmem_ld16(d + j0, d0);
             if (kGateUp) tmem_ld16(d + BN + j0, d1);
@@ -556,38 +568,42 @@ __global__ void __launch_bounds__(kThreads, 1)
               if (kGateUp) tmem_ld16(dsum + BN + j0, s1);
             }
             tmem_wait_ld();
+            if (want_dots) {
+              const size_t C = static_cast<size_t>(kNmat) * args.N;
+              for (int i = 0; i < 16; ++i) {
+                const int j = j0 + i;
+                if (j >= jend) break;
+                const size_t base = (static_cast<size_t>(x.row0 + j) * C) * G;
+                args.dots[base + static_cast<size_t>(col) * G + g] = __float2int_rn(__uint_as_float(d0[i]));
+                if (kGateUp)
+                  args.dots[base + static_cast<size_t>(args.N + col) * G + g] = __float2int_rn(__uint_as_float(d1[i]));
+              }
+            }
 #pragma unroll
             for (int i = 0; i < 16; ++i) {
-              const int j = j0 + i;
               float f0 = w0, f1 = w1;
               if (AM == AM_INT8) {
-                const float s_a = sa[j * G + g];
+                const float s_a = sa[(j0 - c0 + i) * G + g];
                 f0 = __fmul_rn(w0, s_a);
                 f1 = __fmul_rn(w1, s_a);
               }
               const float a0 = __fmaf_rn(f0, __uint_as_float(d0[i]), g > 0 ? __uint_as_float(s0[i]) : 0.f);
               float a1 = 0.f;
               if (kGateUp) a1 = __fmaf_rn(f1, __uint_as_float(d1[i]), g > 0 ? __uint_as_float(s1[i]) : 0.f);
-              if (args.dots && j < x.nrows) {
-                const size_t C = static_cast<size_t>(kNmat) * args.N;
-                const size_t base = (static_cast<size_t>(x.row0 + j) * C) * G;
-                args.dots[base + static_cast<size_t>(col) * G + g] = __float2int_rn(__uint_as_float(d0[i]));
-                if (kGateUp)
-                  args.dots[base + static_cast<size_t>(args.N + col) * G + g] = __float2int_rn(__uint_as_float(d1[i]));
-              }
-              if (last) {
-                if (j < x.nrows && x.row0 + j < args.P) {
-                  const float val = kGateUp ? __fdividef(a0, 1.f + __expf(-a0)) * a1 : a0;
-                  args.out[static_cast<size_t>(x.row0 + j) * args.N + col] = __float2bfloat16_rn(val);
-                }
-              } else {
-                s0[i] = __float_as_uint(a0);
-                s1[i] = __float_as_uint(a1);
-              }
+              s0[i] = __float_as_uint(a0);
+              s1[i] = __float_as_uint(a1);
             }
             if (!last) {
               tmem_st16(dsum + j0, s0);
               if (kGateUp) tmem_st16(dsum + BN + j0, s1);
+            } else {
+              for (int i = 0; i < 16; ++i) {
+                const int j = j0 + i;
+                if (j >= jend || x.row0 + j >= args.P) break;
+                const float a0 = __uint_as_float(s0[i]), a1 = __uint_as_float(s1[i]);
+                const float val = kGateUp ? __fdividef(a0, 1.f + __expf(-a0)) * a1 : a0;
+                args.out[static_cast<size_t>(x.row0 + j) * args.N + col] = __float2bfloat16_rn(val);
+              }
             }
           }
           if (!last) tmem_wait_st();
@@ -660,7 +676,8 @@ bool plan_smem(int wf, int am, bool gate_up, int K, int E, int BN, Plan* p) {
   a.scale_mat_bytes = (wf == WF_INT8 || wf == WF_INT4) ? 128u * G * 2u : 0u;
   const uint32_t scales = 2 * nmat * a.scale_mat_bytes;
   const uint32_t tab = align_up(2u * (E + 1) * 4u, 16);
-  const uint32_t sa = am == AM_INT8 ? align_up(kEpiWarps * BN * G * 4u, 16) : 0u;
+  const uint32_t cpw = BN >= 32 ? BN / 2 : BN;  // token columns per epilogue warp
+  const uint32_t sa = am == AM_INT8 ? align_up(kEpiWarps * cpw * G * 4u, 16) : 0u;
   const uint32_t bars = align_up(sizeof(Bars), 16);
   fixed = scales + tab + sa + bars;
   const size_t budget = kSmemLimit - 1024;  // alignment slack
@@ -711,11 +728,15 @@ int run_gemm(const mnw_moe_layer* L, int wfmt, int act, int kind, const void* a0
   if (!a0 || !offsets || !out || !aligned(a0, 16) || !aligned(out, 16)) return MNW_E_INVALID_ARG;
   if (act == MNW_ACT_INT8_G128 && (!a1 || !aligned(a1, 16))) return MNW_E_INVALID_ARG;
   if (act == MNW_ACT_NVFP4_G16 && (!a1 || !a2 || !aligned(a1, 16) || !aligned(a2, 16))) return MNW_E_INVALID_ARG;
-  // INT8/INT4 weights: the warp-MMA kernel (see mnw_gemm_warp.cu for why);
-  // BF16 and NVFP4 weights use tcgen05 below.
+  // INT8/INT4 weights with few tokens per expert: the warp-MMA kernel (see
+  // mnw_gemm_warp.cu for why).  From 32 tokens per expert on average the
+  // tcgen05 kernel below is as fast or faster (measured on GB300: 64 tokens
+  // per expert W8A8 369 vs 486 us for gate/up; 128 per expert W4A16 down
+  // 1036 vs 1463 us), and BF16/NVFP4 weights always use it.
   const int mean_rows = (P + L->E - 1) / L->E;
   const int path = gemm_path();
-  if (warp_gemm_applicable(L, wfmt, act, kind) && path != MNW_PATH_TCGEN05) {
+  const bool warp_ok = warp_gemm_applicable(L, wfmt, act, kind);
+  if (warp_ok && (path == MNW_PATH_WARP_MMA || (path == MNW_PATH_AUTO && mean_rows < 32))) {
     const int nt = mean_rows <= 4 ? 1 : (mean_rows <= 16 ? 2 : 4);
     return run_gemm_warp(L, wfmt, act, kind, a0, a1, offsets, P, nt, out, dots, err, sched, st);
   }
