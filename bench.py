@@ -339,11 +339,17 @@ def main():
     ntok = cpu_sample_tokens(wl, args.cpu_budget)
     cpu_rate, cpu_dt = run_oracle_sample(wl, ntok)
 
+    # DRAM traffic (read + write bytes) of one gate/up launch, from the ncu
+    # capture summarised in profiles/ (lines "<workload> <bytes> <summary file>");
+    # null for a workload without a capture of the current kernel.
     profile_traffic = None
     try:
-        with open(os.path.join(ROOT, "profiles", "traffic.json")) as f:
-            profile_traffic = json.load(f).get(f"{wl.name}:gate_up")
-    except Exception:
+        with open(os.path.join(ROOT, "profiles", "gate_up_dram_traffic.txt")) as f:
+            for ln in f:
+                parts = ln.split()
+                if len(parts) >= 2 and parts[0] == wl.name:
+                    profile_traffic = int(parts[1])
+    except OSError:
         pass
     dtype = {S.ACT_BF16: "bf16", S.ACT_INT8_G128: "int8xint8->f32 (f16 MMA)",
              S.ACT_NVFP4_G16: "e2m1xe2m1->f32 (f16 MMA)"}[wl.act]
