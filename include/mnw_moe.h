@@ -235,6 +235,19 @@ int mnw_moe_set_gemm_path(int path);
 int mnw_moe_forward_static(const mnw_moe_layer* layer, int act, const void* x, const int32_t* ids,
                            const float* w, int T, int k, void* out, uint32_t* err, mnw_stream stream);
 
+/* Self-test of the failure detection every kernel of this library relies on
+ * (the pages describe no such call; it exists so that the bounded waits can be
+ * tested on a GPU without a fault).  Launches one CTA of two warps on
+ * `stream`; each waits on a shared-memory barrier phase that nothing
+ * completes.  The first gives up after `limit_us` microseconds (1 .. 10^6),
+ * ORs MNW_DEVERR_TIMEOUT into the device word *err and raises the CTA's abort
+ * flag; the second waits with the library's own limit (2 s) and must leave
+ * through the abort flag instead, in which case 1 is OR-ed into the device
+ * word *left_early.  The kernel returns normally and the context stays
+ * usable.  Both words are caller-owned device memory, zeroed beforehand.
+ * Returns MNW_E_INVALID_ARG for null pointers or a limit out of range. */
+int mnw_moe_selftest_wait_timeout(uint32_t limit_us, uint32_t* err, uint32_t* left_early, mnw_stream stream);
+
 /* Synchronise `stream`, then copy the device error word to *out_host. */
 int mnw_moe_read_error(const uint32_t* err, uint32_t* out_host, mnw_stream stream);
 

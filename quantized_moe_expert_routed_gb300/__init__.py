@@ -48,6 +48,7 @@ SIGNATURES = {
     "mnw_moe_read_error": (_I, [_P, _P, _P]),
     "mnw_moe_set_gemm_path": (_I, [_I]),
     "mnw_moe_forward_static": (_I, [_P, _I, _P, _P, _P, _I, _I, _P, _U32P, _P]),
+    "mnw_moe_selftest_wait_timeout": (_I, [ctypes.c_uint32, _U32P, _U32P, _P]),
 }
 
 _lib = None
@@ -282,3 +283,10 @@ def mnw_moe_forward_static(layer, act, x, ids, w, out=None, err=None, stream=Non
     _check(load().mnw_moe_forward_static(layer.handle, act, _ptr(x), _ptr(ids), _ptr(w), T, k, _ptr(out), _ptr(err),
                                          _stream(stream)), "mnw_moe_forward_static")
     return out
+
+
+def mnw_moe_selftest_wait_timeout(limit_us, err, left_early, stream=None):
+    """Launch the bounded-wait self-test (see include/mnw_moe.h); err and
+    left_early are zeroed int32 device tensors of one element."""
+    _check(load().mnw_moe_selftest_wait_timeout(limit_us, _ptr(err), _ptr(left_early), _stream(stream)),
+           "mnw_moe_selftest_wait_timeout")

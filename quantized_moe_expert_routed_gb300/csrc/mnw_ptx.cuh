@@ -67,24 +67,28 @@ __device__ __forceinline__ bool mbar_try_wait_sleep(uint64_t* bar, uint32_t pari
 }
 
 // Wait for the phase of `bar` with the given parity to complete.  Gives up
-// (returns false) when *abort is set by another warp, or after kWaitLimitNs,
-// in which case it sets *abort and ORs MNW_DEVERR_TIMEOUT into *err.  Each
-// retry suspends for up to 10 us, so the abort flag is seen within ~80 us.
-__device__ __forceinline__ bool bounded_wait(uint64_t* bar, uint32_t parity, volatile int* abort,
-                                             uint32_t* err) {
+// (returns false) when *abort is set by another warp, or after limit_ns, in
+// which case it sets *abort and ORs MNW_DEVERR_TIMEOUT into *err.  Each retry
+// suspends for up to 10 us, so the abort flag is seen within ~80 us.
+__device__ __forceinline__ bool bounded_wait_for(uint64_t* bar, uint32_t parity, volatile int* abort, uint32_t* err,
+                                                 uint64_t limit_ns) {
   if (mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = globaltimer();
   for (uint32_t it = 1;; ++it) {
     if (mbar_try_wait_sleep(bar, parity, 10000u)) return true;
     if ((it & 7u) == 0) {
       if (*abort) return false;
-      if (globaltimer() - t0 > kWaitLimitNs) {
+      if (globaltimer() - t0 > limit_ns) {
         *abort = 1;
         if (err) atomicOr(err, MNW_DEVERR_TIMEOUT);
         return false;
       }
     }
   }
+}
+// The library's kernels wait at most kWaitLimitNs.
+__device__ __forceinline__ bool bounded_wait(uint64_t* bar, uint32_t parity, volatile int* abort, uint32_t* err) {
+  return bounded_wait_for(bar, parity, abort, err, kWaitLimitNs);
 }
 
 // ---- TMA (bulk tensor copies, global -> shared) ----------------------------

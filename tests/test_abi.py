@@ -53,6 +53,9 @@ def test_bad_arguments_rejected_before_any_launch(lib):
     assert lib.mnw_moe_combine(None, None, None, 2, 2, 12, None, None) == 1
     # GEMM without a layer
     assert lib.mnw_moe_grouped_gemm_w4a16(None, 0, None, None, 4, None, None, None) == 1
+    # bounded-wait self-test: null words, limit out of range
+    assert lib.mnw_moe_selftest_wait_timeout(1000, None, None, None) == 1
+    assert lib.mnw_moe_selftest_wait_timeout(0, ctypes.c_void_p(256), ctypes.c_void_p(512), None) == 1
 
 
 def test_blob_header_checks(lib):
