@@ -170,17 +170,14 @@ def run_ours(args, wl):
         if rc != 0:
             raise RuntimeError(f"{what} failed: {lib.mnw_status_string(rc).decode()}")
 
-    def step(ev_g0=None, ev_g1=None):
+    def step():
+        """The layer's kernels called one by one (prepares the gate/up inputs)."""
         launches = 0
         if wl.act == S.ACT_BF16:
             chk(lib.mnw_moe_permute(ptr(ids), T, k, E, ptr(offsets), ptr(sorted_assign), ptr(assign_pos), ptr(x),
                                     wl.H, ptr(xa), ptr(err), sp), "permute")
             launches += 2
-            if ev_g0 is not None:
-                ev_g0.record(stream)
             chk(gemm(layer.handle, 0, ptr(xa), ptr(offsets), P, ptr(h), ptr(err), sp), "gate_up")
-            if ev_g1 is not None:
-                ev_g1.record(stream)
             chk(gemm(layer.handle, 1, ptr(h), ptr(offsets), P, ptr(y), ptr(err), sp), "down")
             launches += 2
         else:
@@ -190,14 +187,10 @@ def run_ours(args, wl):
             o2 = ptr(ho) if wl.act == S.ACT_NVFP4_G16 else None
             chk(lib.mnw_moe_quantize_act(wl.act, ptr(x), P, wl.H, ptr(sorted_assign), k, ptr(xq), ptr(xs), o1, sp),
                 "quantize x")
-            if ev_g0 is not None:
-                ev_g0.record(stream)
             if wl.act == S.ACT_INT8_G128:
                 chk(gemm(layer.handle, 0, ptr(xq), ptr(xs), ptr(offsets), P, ptr(h), None, ptr(err), sp), "gate_up")
             else:
                 chk(gemm(layer.handle, 0, ptr(xq), ptr(xs), o1, ptr(offsets), P, ptr(h), ptr(err), sp), "gate_up")
-            if ev_g1 is not None:
-                ev_g1.record(stream)
             chk(lib.mnw_moe_quantize_act(wl.act, ptr(h), P, wl.I, None, 1, ptr(hq), ptr(hs), o2, sp), "quantize h")
             if wl.act == S.ACT_INT8_G128:
                 chk(gemm(layer.handle, 1, ptr(hq), ptr(hs), ptr(offsets), P, ptr(y), None, ptr(err), sp), "down")
@@ -207,35 +200,69 @@ def run_ours(args, wl):
         chk(lib.mnw_moe_combine(ptr(y), ptr(assign_pos), ptr(w), T, k, wl.H, ptr(out), sp), "combine")
         return launches + 1
 
+    # Headline: whole layer steps through the library's one-call entry point
+    # (its kernels launch back to back with programmatic dependent launch; no
+    # event sits between them).
+    ws_bytes = ws.numel()
+    fwd = lib.mnw_moe_forward
+
+    def layer_step():
+        chk(fwd(layer.handle, wl.act, ptr(x), ptr(ids), ptr(w), T, k, ptr(out), ptr(ws), ws_bytes, sp), "forward")
+        return 5 if wl.act == S.ACT_BF16 else 6  # permute, (gather | quantise x), gate/up, (quantise h), down, combine
+
+    def gate_up_only():
+        if wl.act == S.ACT_BF16:
+            chk(gemm(layer.handle, 0, ptr(xa), ptr(offsets), P, ptr(h), ptr(err), sp), "gate_up")
+        elif wl.act == S.ACT_INT8_G128:
+            chk(gemm(layer.handle, 0, ptr(xq), ptr(xs), ptr(offsets), P, ptr(h), None, ptr(err), sp), "gate_up")
+        else:
+            chk(gemm(layer.handle, 0, ptr(xq), ptr(xs), ptr(xo), ptr(offsets), P, ptr(h), ptr(err), sp), "gate_up")
+
     for _ in range(args.warmup):
-        step()
+        layer_step()
         l2_flush()
     torch.cuda.synchronize()
     if world > 1:
         torch.distributed.barrier()
     torch.cuda.synchronize()
 
-    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True),
-           torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
     launches = 0
     with ClockSampler(local) as clk:
         for i in range(args.steps):
             l2_flush()  # between timed iterations, outside the events
-            e0, e1, g0, g1 = ev[i]
+            e0, e1 = ev[i]
             e0.record(stream)
-            launches += step(g0, g1)
+            launches += layer_step()
             e1.record(stream)
         torch.cuda.synchronize()
-    step_ms = [a.elapsed_time(b) for a, b, _, _ in ev]
-    gu_ms = [a.elapsed_time(b) for _, _, a, b in ev]
+    step_ms = [a.elapsed_time(b) for a, b in ev]
     total_ms = sum(step_ms)
     if world > 1:
         t = torch.tensor([total_ms], device=dev)
         torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
         total_ms = float(t.item())
-    e = int(err.item())
+    e = M.mnw_moe_read_error(M.workspace_error_word(ws))
     if e:
         raise RuntimeError(f"device error word {e:#x}")
+
+    # Roofline: the fused gate/up GEMM launch alone, on inputs prepared by the
+    # same kernels as the layer (CUDA events on its stream, L2 flushed between).
+    step()
+    gev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    for i in range(args.steps + 1):
+        l2_flush()
+        if i == 0:
+            gate_up_only()  # warm
+            continue
+        g0, g1 = gev[i - 1]
+        g0.record(stream)
+        gate_up_only()
+        g1.record(stream)
+    torch.cuda.synchronize()
+    gu_ms = [a.elapsed_time(b) for a, b in gev]
+    if int(err.item()):
+        raise RuntimeError(f"device error word {int(err.item()):#x}")
 
     # end-to-end through the host-buffer entry point (copies inside the timed region)
     wsh = M.workspace(layer, wl.act, T, k, host=True, device=dev)

@@ -166,6 +166,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int G = args.K / 128;
 
   // ---- set-up ----
+  pdl_launch_dependents();
   if (threadIdx.x == 0) {
     for (int s = 0; s < kMaxStages; ++s) {
       mbar_init(&bars->full[s], 1);
@@ -197,6 +198,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (kGateUp) tma_prefetch_desc(&tmA1);
     tma_prefetch_desc(&tmB);
   }
+  // everything below reads or writes global memory the previous kernel may own
+  pdl_wait();
   // Tile table: tab_prefix[e] = first tile of expert e, tab_off = expert_offsets.
   if (warp == 2) {
     const int per = (E + 31) / 32;
@@ -707,8 +710,8 @@ cudaError_t launch_one(const CUtensorMap* maps, const GemmArgs& a, size_t smem, 
     if (e != cudaSuccess) return e;
     attr = true;
   }
-  kern<<<grid, kThreads, smem, st>>>(maps[0], maps[1], maps[2], maps[3], maps[4], maps[5], a);
-  return cudaGetLastError();
+  return launch_pdl(kern, dim3(grid), dim3(kThreads), smem, st, maps[0], maps[1], maps[2], maps[3], maps[4], maps[5],
+                    a);
 }
 
 template <int WF, int AM>

@@ -281,6 +281,7 @@ __global__ void __launch_bounds__(kThreads, ctas_per_sm(WF, NT))
   volatile int* abort = &bars->abort;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int E = args.E, BN = args.BN, S = args.stages, G = args.K / 128;
+  pdl_launch_dependents();
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < kMaxStages; ++s) {
@@ -294,6 +295,8 @@ __global__ void __launch_bounds__(kThreads, ctas_per_sm(WF, NT))
     bars->abort = 0;
     fence_barrier_init();
   }
+  // everything below reads or writes global memory the previous kernel may own
+  pdl_wait();
   if (warp == 1) {  // tile table: first tile of each expert
     const int per = (E + 31) / 32;
     int local = 0;
@@ -547,8 +550,7 @@ cudaError_t launch(const CUtensorMap* maps, const Args& a, size_t smem, int grid
     if (e != cudaSuccess) return e;
     attr = true;
   }
-  kern<<<grid, kThreads, smem, st>>>(maps[0], maps[1], maps[2], a);
-  return cudaGetLastError();
+  return launch_pdl(kern, dim3(grid), dim3(kThreads), smem, st, maps[0], maps[1], maps[2], a);
 }
 
 template <int WF, int AM, bool GU>

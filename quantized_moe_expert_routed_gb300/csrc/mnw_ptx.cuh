@@ -24,6 +24,16 @@ __device__ __forceinline__ uint64_t globaltimer() {
   return t;
 }
 
+// ---- programmatic dependent launch ------------------------------------------
+
+// Block until the kernel this one was launched behind has completed and its
+// writes are visible (returns at once for an ordinary launch).  Every kernel
+// of the library calls it before its first global-memory access.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+// Let the next kernel on the stream start its set-up now; it still waits for
+// this kernel's completion before it reads or writes global memory.
+__device__ __forceinline__ void pdl_launch_dependents() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
 // ---- mbarrier --------------------------------------------------------------
 
 __device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {

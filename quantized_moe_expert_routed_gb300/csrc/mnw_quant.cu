@@ -26,6 +26,8 @@ __global__ void __launch_bounds__(256) quant_int8_g128_kernel(const __nv_bfloat1
                                                               const int32_t* __restrict__ row_index,
                                                               int index_div, int8_t* __restrict__ codes,
                                                               float* __restrict__ scales) {
+  pdl_launch_dependents();
+  pdl_wait();
   const int G = K / 128;
   const long long total = static_cast<long long>(R) * G;
   const int lane = threadIdx.x & 31;
@@ -83,6 +85,8 @@ __global__ void __launch_bounds__(256) quant_nvfp4_g16_kernel(const __nv_bfloat1
                                                               const int32_t* __restrict__ row_index,
                                                               int index_div, uint8_t* __restrict__ codes,
                                                               uint8_t* __restrict__ sf, float* __restrict__ outer) {
+  pdl_launch_dependents();
+  pdl_wait();
   const int lane = threadIdx.x & 31;
   const int nb = K / 16;
   for (int r = blockIdx.x * 8 + (threadIdx.x >> 5); r < R; r += gridDim.x * 8) {
@@ -152,16 +156,16 @@ cudaError_t launch_quantize(int act, const void* x, int R, int K, const int32_t*
     long long blocks = (warps + 7) / 8;
     if (blocks > static_cast<long long>(sms) * 16) blocks = static_cast<long long>(sms) * 16;
     if (blocks < 1) blocks = 1;
-    quant_int8_g128_kernel<<<static_cast<int>(blocks), 256, 0, st>>>(
-        static_cast<const __nv_bfloat16*>(x), R, K, row_index, index_div, static_cast<int8_t*>(codes),
-        static_cast<float*>(scales));
+    return launch_pdl(quant_int8_g128_kernel, dim3(static_cast<int>(blocks)), dim3(256), 0, st,
+                      static_cast<const __nv_bfloat16*>(x), R, K, row_index, index_div, static_cast<int8_t*>(codes),
+                      static_cast<float*>(scales));
   } else {
     long long blocks = (static_cast<long long>(R) + 7) / 8;
     if (blocks > static_cast<long long>(sms) * 16) blocks = static_cast<long long>(sms) * 16;
     if (blocks < 1) blocks = 1;
-    quant_nvfp4_g16_kernel<<<static_cast<int>(blocks), 256, 0, st>>>(
-        static_cast<const __nv_bfloat16*>(x), R, K, row_index, index_div, static_cast<uint8_t*>(codes),
-        static_cast<uint8_t*>(scales), row_outer);
+    return launch_pdl(quant_nvfp4_g16_kernel, dim3(static_cast<int>(blocks)), dim3(256), 0, st,
+                      static_cast<const __nv_bfloat16*>(x), R, K, row_index, index_div, static_cast<uint8_t*>(codes),
+                      static_cast<uint8_t*>(scales), row_outer);
   }
   return cudaGetLastError();
 }

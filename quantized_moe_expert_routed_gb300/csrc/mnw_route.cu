@@ -31,8 +31,10 @@ __global__ void __launch_bounds__(kPermThreads, 1)
   int32_t* tot = sm + kPermWarps * E;      // [E]
   __shared__ int32_t warp_tot[kPermWarps];
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  pdl_launch_dependents();
 
   for (int i = tid; i < kPermWarps * E; i += kPermThreads) cnt[i] = 0;
+  pdl_wait();
   for (int a = tid; a < P; a += kPermThreads) sorted_assign[a] = -1;
   __syncthreads();
 
@@ -145,6 +147,8 @@ __global__ void __launch_bounds__(kPermThreads, 1)
 __global__ void __launch_bounds__(256) gather_rows_kernel(const uint4* __restrict__ x, int H8,
                                                           const int32_t* __restrict__ sorted_assign, int P,
                                                           int k, uint4* __restrict__ x_perm) {
+  pdl_launch_dependents();
+  pdl_wait();
   const int warps = gridDim.x * 8;
   for (int p = blockIdx.x * 8 + (threadIdx.x >> 5); p < P; p += warps) {
     const int a = __ldg(sorted_assign + p);
@@ -166,6 +170,8 @@ __global__ void __launch_bounds__(256) combine_kernel(const uint4* __restrict__ 
                                                       const int32_t* __restrict__ assign_pos,
                                                       const float* __restrict__ w, int T, int k, int H8,
                                                       uint4* __restrict__ out) {
+  pdl_launch_dependents();
+  pdl_wait();
   const long long total = static_cast<long long>(T) * H8;
   for (long long i = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x; i < total;
        i += static_cast<long long>(gridDim.x) * blockDim.x) {
@@ -222,17 +228,16 @@ cudaError_t launch_permute(const int32_t* ids, int T, int k, int E, int32_t* off
     if (e != cudaSuccess) return e;
     attr_set = true;
   }
-  permute_kernel<<<1, kPermThreads, smem, st>>>(ids, P, E, offsets, sorted_assign, assign_pos, err);
-  cudaError_t e = cudaGetLastError();
+  cudaError_t e = launch_pdl(permute_kernel, dim3(1), dim3(kPermThreads), smem, st, ids, P, E, offsets,
+                             sorted_assign, assign_pos, err);
   if (e != cudaSuccess) return e;
   if (x && x_perm && P > 0) {
     int dev = 0, sms = 148;
     cudaGetDevice(&dev);
     cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-    gather_rows_kernel<<<grid_for(8, P, sms * 8), 256, 0, st>>>(static_cast<const uint4*>(x), H / 8,
-                                                                 sorted_assign, P, k,
-                                                                 static_cast<uint4*>(x_perm));
-    e = cudaGetLastError();
+    e = launch_pdl(gather_rows_kernel, dim3(grid_for(8, P, sms * 8)), dim3(256), 0, st,
+                   static_cast<const uint4*>(x), H / 8, static_cast<const int32_t*>(sorted_assign), P, k,
+                   static_cast<uint4*>(x_perm));
   }
   return e;
 }
@@ -244,9 +249,8 @@ cudaError_t launch_combine(const void* y, const int32_t* assign_pos, const float
   cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
   const long long threads = static_cast<long long>(T) * (H / 8);
   const int blocks = static_cast<int>(std::min<long long>((threads + 255) / 256, static_cast<long long>(sms) * 16));
-  combine_kernel<<<blocks < 1 ? 1 : blocks, 256, 0, st>>>(static_cast<const uint4*>(y), assign_pos, w, T, k, H / 8,
-                                                          static_cast<uint4*>(out));
-  return cudaGetLastError();
+  return launch_pdl(combine_kernel, dim3(blocks < 1 ? 1 : blocks), dim3(256), 0, st, static_cast<const uint4*>(y),
+                    assign_pos, w, T, k, H / 8, static_cast<uint4*>(out));
 }
 
 }  // namespace mnw
