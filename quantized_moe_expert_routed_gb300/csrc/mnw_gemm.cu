@@ -128,6 +128,20 @@ __device__ __forceinline__ Unit decode_unit(const int* tab_prefix, const int* ta
   return x;
 }
 
+// Position in a ring of n slots: the slot and the parity of its current use,
+// advanced without a division.  The MMA-issuing thread runs alone and every
+// instruction between two MMAs delays the next one, so none of the rings of
+// this kernel is indexed with a runtime modulo.
+struct RingPos {
+  uint32_t slot = 0, phase = 0;
+  __device__ __forceinline__ void advance(uint32_t n) {
+    if (++slot == n) {
+      slot = 0;
+      phase ^= 1u;
+    }
+  }
+};
+
 // Drain wait used on the way out: ignores the abort flag, bounded in time.
 __device__ __forceinline__ void drain_wait(uint64_t* bar, uint32_t parity) {
   const uint64_t t0 = globaltimer();
@@ -242,6 +256,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ======================= producer =======================
     if (lane == 0) {
       uint32_t it = 0, uit = 0, sit = 0;  // stages issued, units visited, scale loads issued
+      RingPos sp;
       bool ok = true;
       const uint32_t a_bytes = kNmat * 16384u + (WF == WF_NVFP4 ? kNmat * 2048u : 0u);
       uint32_t b_bytes;
@@ -264,10 +279,9 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           ++sit;
         }
-        for (int ks = 0; ks < nks; ++ks, ++it) {
-          const int s = it % S;
-          const uint32_t ph = (it / S) & 1;
-          if (!bounded_wait(&bars->empty[s], ph ^ 1, abort, args.err)) { ok = false; break; }
+        for (int ks = 0; ks < nks; ++ks, ++it, sp.advance(S)) {
+          const int s = sp.slot;
+          if (!bounded_wait(&bars->empty[s], sp.phase ^ 1, abort, args.err)) { ok = false; break; }
           uint8_t* st = smem + s * args.stage_bytes;
           mbar_arrive_expect_tx(&bars->full[s], tx);
           const int kx = WF == WF_BF16 ? ks * 64 : ks * 128;  // elements (BF16) or bytes (codes)
@@ -302,45 +316,44 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ======================= MMA issuer =======================
     if (lane == 0) {
       const uint32_t idesc = idesc_f16(kBM, BN, kBf16Mma);
-      uint32_t it = 0, ait = 0, acc_it = 0;
+      const uint32_t S_ = static_cast<uint32_t>(S), na = static_cast<uint32_t>(args.aslots),
+                     nacc = static_cast<uint32_t>(args.acc_slots);
+      RingPos sp, ap, cp;  // stages, operand-A slots, accumulator slots
       bool ok = true, issued = false;
       uint32_t d_base = 0;
       for (int u = blockIdx.x; ok && u < units; u += gridDim.x) {
         if (!kGrouped) {
-          const uint32_t slot = acc_it % args.acc_slots;
-          if (!bounded_wait(&bars->accempty[slot], ((acc_it / args.acc_slots) & 1) ^ 1, abort, args.err)) {
+          if (!bounded_wait(&bars->accempty[cp.slot], cp.phase ^ 1, abort, args.err)) {
             ok = false;
             break;
           }
           tc_fence_after();
-          d_base = tmem + args.acc_base + slot * kNmat * BN;
+          d_base = tmem + args.acc_base + cp.slot * kNmat * BN;
         }
-        for (int ks = 0; ok && ks < nks; ++ks, ++it) {
-          const int s = it % S;
-          const uint32_t ph = (it / S) & 1;
-          if (!bounded_wait(kBconv ? &bars->bconv[s] : &bars->full[s], ph, abort, args.err)) { ok = false; break; }
+        for (int ks = 0; ok && ks < nks; ++ks, sp.advance(S_)) {
+          const int s = sp.slot;
+          if (!bounded_wait(kBconv ? &bars->bconv[s] : &bars->full[s], sp.phase, abort, args.err)) { ok = false; break; }
           tc_fence_after();
           const uint32_t st = smem_u32(smem + s * args.stage_bytes);
           for (int sc = 0; sc < T::kSub; ++sc) {
             const int kg = ks * T::kStage + sc * 64;
-            uint32_t gslot = 0;
             if (kGrouped) {
-              gslot = acc_it % args.acc_slots;
               if ((kg & 127) == 0) {
-                if (!bounded_wait(&bars->accempty[gslot], ((acc_it / args.acc_slots) & 1) ^ 1, abort, args.err)) {
+                if (!bounded_wait(&bars->accempty[cp.slot], cp.phase ^ 1, abort, args.err)) {
                   ok = false;
                   break;
                 }
                 tc_fence_after();
               }
-              d_base = tmem + args.acc_base + gslot * kNmat * BN;
+              d_base = tmem + args.acc_base + cp.slot * kNmat * BN;
             }
-            const uint32_t aslot = ait % args.aslots;
+            const uint32_t aslot = ap.slot;
             if (T::kTs) {
-              if (!bounded_wait(&bars->afull[aslot], (ait / args.aslots) & 1, abort, args.err)) { ok = false; break; }
+              if (!bounded_wait(&bars->afull[aslot], ap.phase, abort, args.err)) { ok = false; break; }
               tc_fence_after();
             }
             const uint32_t b_tile = st + args.off_b + sc * BN * 128;
+            const uint32_t a_tmem = tmem + aslot * (kNmat * 32);
 #pragma unroll
             for (int kk = 0; kk < 4; ++kk) {
               const uint64_t bdesc = sdesc_sw128(b_tile + kk * 32);
@@ -348,7 +361,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
               for (int m = 0; m < kNmat; ++m) {
                 if (T::kTs) {
-                  mma_ts(d_base + m * BN, tmem + aslot * (kNmat * 32) + m * 32 + kk * 8, bdesc, idesc, acc);
+                  mma_ts(d_base + m * BN, a_tmem + m * 32 + kk * 8, bdesc, idesc, acc);
                 } else {
                   mma_ss(d_base + m * BN, sdesc_sw128(st + args.off_a[m] + kk * 32), bdesc, idesc, acc);
                 }
@@ -357,19 +370,19 @@ __global__ void __launch_bounds__(kThreads, 1)
             issued = true;
             if (T::kTs) {
               mma_commit(&bars->aempty[aslot]);
-              ++ait;
+              ap.advance(na);
             }
             if (kGrouped && ((kg + 64) & 127) == 0) {
-              mma_commit(&bars->accfull[gslot]);
-              ++acc_it;
+              mma_commit(&bars->accfull[cp.slot]);
+              cp.advance(nacc);
             }
           }
           if (!ok) break;
           mma_commit(&bars->empty[s]);
         }
         if (ok && !kGrouped) {
-          mma_commit(&bars->accfull[acc_it % args.acc_slots]);
-          ++acc_it;
+          mma_commit(&bars->accfull[cp.slot]);
+          cp.advance(nacc);
         }
       }
       if (issued) {
@@ -384,13 +397,14 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int h = cw >> 2;              // which 32-K half of each 64-K sub-chunk
     const int r = q * 32 + lane;        // weight row within the tile
     const int ctid = cw * 32 + lane;    // 0..255
-    uint32_t it = 0, ait = 0, uit = 0;
+    const uint32_t S_ = static_cast<uint32_t>(S), na = static_cast<uint32_t>(args.aslots);
+    RingPos sp, ap;  // stages, operand-A slots
     bool ok = true;
     if (T::kTs || kBconv) {
-      for (int u = blockIdx.x; ok && u < units; u += gridDim.x, ++uit) {
-        for (int ks = 0; ks < nks; ++ks, ++it) {
-          const int s = it % S;
-          if (!bounded_wait(&bars->full[s], (it / S) & 1, abort, args.err)) { ok = false; break; }
+      for (int u = blockIdx.x; ok && u < units; u += gridDim.x) {
+        for (int ks = 0; ks < nks; ++ks, sp.advance(S_)) {
+          const int s = sp.slot;
+          if (!bounded_wait(&bars->full[s], sp.phase, abort, args.err)) { ok = false; break; }
           const uint32_t st = smem_u32(smem + s * args.stage_bytes);
           if (kBconv) {
             // token codes -> FP16 operand tile (128-byte swizzle, BN rows per 64-K box)
@@ -429,9 +443,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (lane == 0) mbar_arrive(&bars->bconv[s]);
           }
           if (T::kTs) {
-            for (int sc = 0; sc < T::kSub; ++sc, ++ait) {
-              const uint32_t aslot = ait % args.aslots;
-              if (!bounded_wait(&bars->aempty[aslot], ((ait / args.aslots) & 1) ^ 1, abort, args.err)) {
+            for (int sc = 0; sc < T::kSub; ++sc, ap.advance(na)) {
+              const uint32_t aslot = ap.slot;
+              if (!bounded_wait(&bars->aempty[aslot], ap.phase ^ 1, abort, args.err)) {
                 ok = false;
                 break;
               }
@@ -482,7 +496,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int c0 = BN >= 32 ? half * cpw : (half ? BN : 0);
     const int c1 = BN >= 32 ? c0 + cpw : (half ? BN : BN);
     const uint32_t lane_bits = static_cast<uint32_t>(q * 32) << 16;
-    uint32_t acc_it = 0, uit = 0;
+    const uint32_t nacc = static_cast<uint32_t>(args.acc_slots);
+    RingPos cp;  // accumulator slots
+    uint32_t uit = 0;
     bool ok = true;
     // each epilogue warp keeps its own copy of its columns' activation scales
     float* sa = reinterpret_cast<float*>(smem + args.off_sa) + ew * cpw * G;
@@ -492,8 +508,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int col = n0 + r;
       const int jend = min(c1, x.nrows);  // live columns of this warp: [c0, jend)
       if (!kGrouped) {
-        const uint32_t slot = acc_it % args.acc_slots;
-        if (!bounded_wait(&bars->accfull[slot], (acc_it / args.acc_slots) & 1, abort, args.err)) { ok = false; break; }
+        const uint32_t slot = cp.slot;
+        if (!bounded_wait(&bars->accfull[slot], cp.phase, abort, args.err)) { ok = false; break; }
         tc_fence_after();
         const uint32_t d = tmem + lane_bits + args.acc_base + slot * kNmat * BN;
         float ow[2] = {1.f, 1.f};
@@ -532,7 +548,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(&bars->accempty[slot]);
-        ++acc_it;
+        cp.advance(nacc);
       } else {
         // Grouped: one accumulator per 128-wide K group.  Each group's exact
         // dot products D_g are scaled in FP32 (by s_w, times s_a in the A8
@@ -556,8 +572,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t dsum = tmem + lane_bits + args.sum_base;
         const bool want_dots = AM == AM_INT8 && args.dots != nullptr;
         for (int g = 0; g < G; ++g) {
-          const uint32_t slot = acc_it % args.acc_slots;
-          if (!bounded_wait(&bars->accfull[slot], (acc_it / args.acc_slots) & 1, abort, args.err)) { ok = false; break; }
+          const uint32_t slot = cp.slot;
+          if (!bounded_wait(&bars->accfull[slot], cp.phase, abort, args.err)) { ok = false; break; }
           tc_fence_after();
           const uint32_t d = tmem + lane_bits + args.acc_base + slot * kNmat * BN;
           const float w0 = __half2float(sw0[g]), w1 = __half2float(sw1[g]);
@@ -613,7 +629,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           tc_fence_before();
           __syncwarp();
           if (lane == 0) mbar_arrive(&bars->accempty[slot]);
-          ++acc_it;
+          cp.advance(nacc);
         }
         if (!ok) break;
         __syncwarp();
