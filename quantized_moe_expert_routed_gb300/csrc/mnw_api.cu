@@ -3,6 +3,7 @@
 // here synchronises except mnw_moe_read_error() and mnw_moe_forward_host().
 #include <cudaTypedefs.h>
 
+#include <atomic>
 #include <cstring>
 #include <mutex>
 
@@ -411,9 +412,12 @@ int mnw_moe_forward_host(const mnw_moe_layer* L, int act, const void* x_host, co
                            reinterpret_cast<const float*>(b + W.hw), T, k, b + W.hout, ws, W.total, stream);
   if (rc) return rc;
   if (cudaMemcpyAsync(out_host, b + W.hout, xb, cudaMemcpyDeviceToHost, st) != cudaSuccess) return MNW_E_CUDA;
+  // The error word goes to host stack memory: a stream-ordered copy into
+  // pageable memory returns only once it, and so everything before it on the
+  // stream (the output copy included), has completed -- one wait, not two.
   uint32_t e = 0;
-  rc = mnw_moe_read_error(reinterpret_cast<const uint32_t*>(b + W.err), &e, stream);
-  if (rc) return rc;
+  if (cudaMemcpyAsync(&e, b + W.err, sizeof(e), cudaMemcpyDeviceToHost, st) != cudaSuccess) return MNW_E_CUDA;
+  if (cudaStreamSynchronize(st) != cudaSuccess) return MNW_E_CUDA;
   return e ? MNW_E_CUDA : MNW_OK;
 }
 
@@ -429,4 +433,17 @@ int mnw_moe_read_error(const uint32_t* err, uint32_t* out_host, mnw_stream strea
 
 namespace mnw {
 int gemm_path() { return g_gemm_path; }
+
+int current_sm_count() {
+  constexpr int kMaxDevices = 64;
+  static std::atomic<int> cache[kMaxDevices];  // 0 = not looked up yet
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return 148;
+  int n = cache[dev].load(std::memory_order_relaxed);
+  if (n == 0) {
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) n = 148;
+    cache[dev].store(n, std::memory_order_relaxed);
+  }
+  return n;
+}
 }  // namespace mnw

@@ -23,6 +23,9 @@ namespace mnw {
 
 inline bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
 
+// Number of SMs of the current device, looked up once per device.
+int current_sm_count();
+
 // Launch a kernel of this library with programmatic stream serialisation: it
 // may start while the previous kernel on the stream finishes (its set-up
 // overlaps that kernel's tail), and waits for that kernel's completion with

@@ -148,9 +148,7 @@ __global__ void __launch_bounds__(256) quant_nvfp4_g16_kernel(const __nv_bfloat1
 
 cudaError_t launch_quantize(int act, const void* x, int R, int K, const int32_t* row_index, int index_div,
                             void* codes, void* scales, float* row_outer, cudaStream_t st) {
-  int dev = 0, sms = 148;
-  cudaGetDevice(&dev);
-  cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  const int sms = current_sm_count();
   if (act == MNW_ACT_INT8_G128) {
     const long long warps = static_cast<long long>(R) * (K / 128);
     long long blocks = (warps + 7) / 8;

@@ -368,9 +368,7 @@ cudaError_t launch_permute(const int32_t* ids, int T, int k, int E, int32_t* off
   }
   if (e != cudaSuccess) return e;
   if (x && x_perm && P > 0) {
-    int dev = 0, sms = 148;
-    cudaGetDevice(&dev);
-    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    const int sms = current_sm_count();
     e = launch_pdl(gather_rows_kernel, dim3(grid_for(8, P, sms * 8)), dim3(256), 0, st,
                    static_cast<const uint4*>(x), H / 8, static_cast<const int32_t*>(sorted_assign), P, k,
                    static_cast<uint4*>(x_perm));
@@ -380,9 +378,7 @@ cudaError_t launch_permute(const int32_t* ids, int T, int k, int E, int32_t* off
 
 cudaError_t launch_combine(const void* y, const int32_t* assign_pos, const float* w, int T, int k, int H,
                            void* out, cudaStream_t st) {
-  int dev = 0, sms = 148;
-  cudaGetDevice(&dev);
-  cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  const int sms = current_sm_count();
   const long long threads = static_cast<long long>(T) * (H / 8);
   const int blocks = static_cast<int>(std::min<long long>((threads + 255) / 256, static_cast<long long>(sms) * 16));
   return launch_pdl(combine_kernel, dim3(blocks < 1 ? 1 : blocks), dim3(256), 0, st, static_cast<const uint4*>(y),
