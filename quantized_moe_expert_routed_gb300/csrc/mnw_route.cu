@@ -266,6 +266,178 @@ __global__ void __launch_bounds__(kW * 32, 1)
   for (int p = total_valid + tid; p < P; p += kThreads) sorted_assign[p] = -1;
 }
 
+// ---------------------------------------------------------------------------
+// Large batches: the same stable permutation over many CTAs, in three kernels.
+// CTA c owns the contiguous chunk [c*kChunk, (c+1)*kChunk) of assignments.
+//   count : per-expert counts of the chunk  -> assign_pos[c*kChunk + e]
+//   scan  : one CTA turns them into, per (c, e), the first position of chunk
+//           c's assignments to expert e (experts in order, chunks in order
+//           within an expert), written back in place, plus expert_offsets
+//   place : each CTA re-ranks its chunk and writes positions
+// The chunk's own slice of assign_pos is the scratch for its counts and
+// starts (kChunk >= E), and only that CTA overwrites it in the last pass, so
+// no other memory is needed.
+constexpr int kChunk = 1024;        // assignments per CTA (>= E)
+constexpr int kChunkThreads = 256;  // 8 warps, 4 batches of 32 per warp
+
+// Per-warp stable ranks of one chunk: ids in registers, counts in cnt[8][E].
+struct ChunkIds {
+  int id[4];
+  uint32_t peers[4];
+};
+__device__ __forceinline__ void chunk_count(const int32_t* ids, int a0, int a1, int E, int32_t* cnt, ChunkIds& c,
+                                            uint32_t* err) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  int32_t* my = cnt + warp * E;
+#pragma unroll
+  for (int b = 0; b < 4; ++b) {
+    const int a = a0 + (warp * 4 + b) * 32 + lane;
+    c.id[b] = a < a1 ? __ldg(ids + a) : INT32_MIN;
+  }
+#pragma unroll
+  for (int b = 0; b < 4; ++b) {
+    const int a = a0 + (warp * 4 + b) * 32 + lane;
+    const bool active = a < a1;
+    const bool valid = active && c.id[b] >= 0 && c.id[b] < E;
+    if (active && !valid && err) atomicOr(err, MNW_DEVERR_BAD_EXPERT_ID);
+    const uint32_t vmask = __ballot_sync(0xffffffffu, valid);
+    c.peers[b] = valid ? __match_any_sync(vmask, c.id[b]) : 0u;
+    if (valid && lane == __ffs(c.peers[b]) - 1) my[c.id[b]] += __popc(c.peers[b]);
+    __syncwarp();
+  }
+}
+
+__global__ void __launch_bounds__(kChunkThreads) permute_count_kernel(const int32_t* __restrict__ ids, int P, int E,
+                                                                      int32_t* __restrict__ assign_pos,
+                                                                      uint32_t* __restrict__ err) {
+  extern __shared__ int32_t sm[];
+  int32_t* cnt = sm;  // [8][E]
+  pdl_launch_dependents();
+  for (int i = threadIdx.x; i < 8 * E; i += kChunkThreads) cnt[i] = 0;
+  pdl_wait();
+  __syncthreads();
+  const int a0 = blockIdx.x * kChunk, a1 = min(P, a0 + kChunk);
+  ChunkIds c;
+  chunk_count(ids, a0, a1, E, cnt, c, err);
+  __syncthreads();
+  for (int e = threadIdx.x; e < E; e += kChunkThreads) {
+    int t = 0;
+#pragma unroll
+    for (int w = 0; w < 8; ++w) t += cnt[w * E + e];
+    assign_pos[a0 + e] = t;
+  }
+}
+
+// One CTA of 1024 threads; C * E counts fit in shared memory (checked by the launcher).
+__global__ void __launch_bounds__(1024, 1) permute_scan_kernel(int C, int E, int32_t* __restrict__ assign_pos,
+                                                               int32_t* __restrict__ offsets) {
+  extern __shared__ int32_t sm[];
+  int32_t* cnt = sm;          // [C][E]
+  int32_t* tot = sm + C * E;  // [E]
+  __shared__ int32_t warp_tot[32];
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  pdl_launch_dependents();
+  pdl_wait();
+  for (int i = tid; i < C * E; i += 1024) {
+    const int c = i / E, e = i - c * E;
+    cnt[i] = assign_pos[c * kChunk + e];
+  }
+  __syncthreads();
+  for (int e = tid; e < E; e += 1024) {
+    int run = 0;
+    for (int c = 0; c < C; ++c) {
+      const int v = cnt[c * E + e];
+      cnt[c * E + e] = run;
+      run += v;
+    }
+    tot[e] = run;
+  }
+  __syncthreads();
+  // exclusive scan of the totals (E <= 1024: one expert per thread)
+  const int v = tid < E ? tot[tid] : 0;
+  int incl = v;
+#pragma unroll
+  for (int d = 1; d < 32; d <<= 1) {
+    const int o = __shfl_up_sync(0xffffffffu, incl, d);
+    if (lane >= d) incl += o;
+  }
+  if (lane == 31) warp_tot[warp] = incl;
+  __syncthreads();
+  if (warp == 0) {
+    const int t = warp_tot[lane];
+    int ti = t;
+#pragma unroll
+    for (int d = 1; d < 32; d <<= 1) {
+      const int o = __shfl_up_sync(0xffffffffu, ti, d);
+      if (lane >= d) ti += o;
+    }
+    warp_tot[lane] = ti - t;
+  }
+  __syncthreads();
+  const int excl = incl - v + warp_tot[warp];
+  if (tid < E) {
+    offsets[tid] = excl;
+    tot[tid] = excl;
+    if (tid == E - 1) offsets[E] = excl + v;
+  }
+  __syncthreads();
+  for (int i = tid; i < C * E; i += 1024) {
+    const int c = i / E, e = i - c * E;
+    assign_pos[c * kChunk + e] = tot[e] + cnt[i];
+  }
+}
+
+__global__ void __launch_bounds__(kChunkThreads) permute_place_kernel(const int32_t* __restrict__ ids, int P, int E,
+                                                                      const int32_t* __restrict__ offsets,
+                                                                      int32_t* __restrict__ sorted_assign,
+                                                                      int32_t* __restrict__ assign_pos) {
+  extern __shared__ int32_t sm[];
+  int32_t* cnt = sm;          // [8][E]: counts, then start of each warp's run
+  int32_t* base = sm + 8 * E;  // [E]: first position of this chunk's assignments per expert
+  pdl_launch_dependents();
+  for (int i = threadIdx.x; i < 8 * E; i += kChunkThreads) cnt[i] = 0;
+  pdl_wait();
+  const int a0 = blockIdx.x * kChunk, a1 = min(P, a0 + kChunk);
+  for (int e = threadIdx.x; e < E; e += kChunkThreads) base[e] = assign_pos[a0 + e];
+  __syncthreads();  // starts read before this chunk's positions overwrite them
+  ChunkIds c;
+  chunk_count(ids, a0, a1, E, cnt, c, nullptr);
+  __syncthreads();
+  for (int e = threadIdx.x; e < E; e += kChunkThreads) {
+    int run = base[e];
+#pragma unroll
+    for (int w = 0; w < 8; ++w) {
+      const int v = cnt[w * E + e];
+      cnt[w * E + e] = run;
+      run += v;
+    }
+  }
+  __syncthreads();
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const uint32_t lt_mask = (1u << lane) - 1u;
+  int32_t* my = cnt + warp * E;
+#pragma unroll
+  for (int b = 0; b < 4; ++b) {
+    const int a = a0 + (warp * 4 + b) * 32 + lane;
+    const bool active = a < a1;
+    if (c.peers[b] != 0u) {
+      const int pos = my[c.id[b]] + __popc(c.peers[b] & lt_mask);
+      assign_pos[a] = pos;
+      sorted_assign[pos] = a;
+    } else if (active) {
+      assign_pos[a] = -1;
+    }
+    __syncwarp();
+    if (c.peers[b] != 0u && lane == __ffs(c.peers[b]) - 1) my[c.id[b]] += __popc(c.peers[b]);
+    __syncwarp();
+  }
+  // the tail of dropped assignments
+  const int total = __ldg(offsets + E);
+  const int per = (P - total + gridDim.x - 1) / gridDim.x;
+  const int t0 = total + blockIdx.x * per, t1 = min(P, t0 + per);
+  for (int p = t0 + threadIdx.x; p < t1; p += kChunkThreads) sorted_assign[p] = -1;
+}
+
 // x_perm[p] = x[sorted_assign[p] / k], zeros where sorted_assign[p] < 0.  One
 // warp per row, 16-byte vectors.
 __global__ void __launch_bounds__(256) gather_rows_kernel(const uint4* __restrict__ x, int H8,
@@ -352,6 +524,9 @@ cudaError_t launch_permute(const int32_t* ids, int T, int k, int E, int32_t* off
     if (e == cudaSuccess)
       e = cudaFuncSetAttribute(permute_small_kernel<16, 16>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                static_cast<int>(17 * 1024 * sizeof(int32_t)));
+    if (e == cudaSuccess)
+      e = cudaFuncSetAttribute(permute_scan_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               static_cast<int>((48 * 1024) * sizeof(int32_t)));
     if (e != cudaSuccess) return e;
     attr_set = true;
   }
@@ -362,6 +537,19 @@ cudaError_t launch_permute(const int32_t* ids, int T, int k, int E, int32_t* off
   } else if (P <= 16 * 16 * 32) {
     e = launch_pdl(permute_small_kernel<16, 16>, dim3(1), dim3(16 * 32), static_cast<size_t>(17) * E * sizeof(int32_t),
                    st, ids, P, E, offsets, sorted_assign, assign_pos, err);
+  } else if (static_cast<long long>((P + kChunk - 1) / kChunk) * E + E <= 48 * 1024 && E <= kChunk &&
+             (P % kChunk == 0 || P % kChunk >= E)) {
+    // (every chunk, the last included, has room for its E counts in its own slice)
+    // many CTAs: count, scan (counts of all chunks in shared memory), place
+    const int C = (P + kChunk - 1) / kChunk;
+    const size_t chunk_smem = static_cast<size_t>(9) * E * sizeof(int32_t);
+    const size_t scan_smem = (static_cast<size_t>(C) * E + E) * sizeof(int32_t);
+    e = launch_pdl(permute_count_kernel, dim3(C), dim3(kChunkThreads), chunk_smem, st, ids, P, E, assign_pos, err);
+    if (e == cudaSuccess)
+      e = launch_pdl(permute_scan_kernel, dim3(1), dim3(1024), scan_smem, st, C, E, assign_pos, offsets);
+    if (e == cudaSuccess)
+      e = launch_pdl(permute_place_kernel, dim3(C), dim3(kChunkThreads), chunk_smem, st, ids, P, E,
+                     static_cast<const int32_t*>(offsets), sorted_assign, assign_pos);
   } else {
     e = launch_pdl(permute_kernel, dim3(1), dim3(kPermThreads), static_cast<size_t>(kPermWarps + 1) * E * sizeof(int32_t),
                    st, ids, P, E, offsets, sorted_assign, assign_pos, err);

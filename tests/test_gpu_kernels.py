@@ -24,7 +24,8 @@ DEV = "cuda"
 @pytest.mark.parametrize("T,k,E,bad", [(1, 1, 1, False), (37, 2, 8, False), (256, 8, 256, False),
                                        (255, 8, 128, True), (257, 8, 64, False), (512, 8, 256, True),
                                        (1024, 8, 1024, True), (1025, 8, 256, False),
-                                       (2048, 8, 256, True), (8192, 8, 256, False), (33, 3, 1024, True)])
+                                       (2048, 8, 256, True), (8192, 8, 256, False), (33, 3, 1024, True),
+                                       (2048, 8, 1024, True), (1100, 8, 256, True), (1030, 9, 256, False)])
 def test_permute_bitexact(M, T, k, E, bad):
     ids = S.routing_uniform(T, E, k, seed=T + E) if k <= E else None
     ids = ids.clone()
