@@ -381,8 +381,8 @@ int mnw_moe_forward(const mnw_moe_layer* L, int act, const void* x, const int32_
     if (rc) return rc;
     float* xo = act == MNW_ACT_NVFP4_G16 ? reinterpret_cast<float*>(b + W.xc) : nullptr;
     float* ho = act == MNW_ACT_NVFP4_G16 ? reinterpret_cast<float*>(b + W.hc) : nullptr;
-    rc = mnw_moe_quantize_act(act, x, P, H, sorted, k, b + W.xa, b + W.xb, xo, stream);
-    if (rc) return rc;
+    // each token row quantised once, its codes written to its k positions
+    if (launch_quantize_scatter(act, x, T, H, pos, k, b + W.xa, b + W.xb, xo, st) != cudaSuccess) return MNW_E_CUDA;
     rc = gemm_for(L, act, MNW_KIND_GATE_UP, b + W.xa, b + W.xb, xo, offs, P, b + W.h, err, sched_gu, st);
     if (rc) return rc;
     rc = mnw_moe_quantize_act(act, b + W.h, P, I, nullptr, 1, b + W.ha, b + W.hb, ho, stream);

@@ -59,6 +59,11 @@ cudaError_t launch_combine(const void* y, const int32_t* assign_pos, const float
                            void* out, cudaStream_t st);
 cudaError_t launch_quantize(int act, const void* x, int R, int K, const int32_t* row_index, int index_div,
                             void* codes, void* scales, float* row_outer, cudaStream_t st);
+// The forward path's form: each of the R source rows (tokens) is quantised
+// once and written to the output rows row_index[r * index_div + j] >= 0
+// (row_index = assign_pos, index_div = k).
+cudaError_t launch_quantize_scatter(int act, const void* x, int R, int K, const int32_t* row_index, int index_div,
+                            void* codes, void* scales, float* row_outer, cudaStream_t st);
 // Grouped GEMM for weight format wfmt and activation mode act.
 // sched (nullable): a zeroed device counter that lets the kernel's CTAs claim
 // work units dynamically; NULL gives a static round-robin order.

@@ -22,6 +22,11 @@ __device__ __forceinline__ int source_row(int r, const int32_t* row_index, int i
   return a < 0 ? -1 : a / index_div;
 }
 
+// kScatter = false: output row r is the quantised source row source_row(r)
+// (R output rows).  kScatter = true: source row r (R source rows, r = token)
+// is quantised once and written to output rows assign_pos[r * k + j], j < k,
+// that are >= 0 (row_index = assign_pos, index_div = k).
+template <bool kScatter>
 __global__ void __launch_bounds__(256) quant_int8_g128_kernel(const __nv_bfloat16* __restrict__ x, int R, int K,
                                                               const int32_t* __restrict__ row_index,
                                                               int index_div, int8_t* __restrict__ codes,
@@ -34,7 +39,7 @@ __global__ void __launch_bounds__(256) quant_int8_g128_kernel(const __nv_bfloat1
   for (long long wg = static_cast<long long>(blockIdx.x) * 8 + (threadIdx.x >> 5); wg < total;
        wg += static_cast<long long>(gridDim.x) * 8) {
     const int r = static_cast<int>(wg / G), g = static_cast<int>(wg % G);
-    const int src = source_row(r, row_index, index_div);
+    const int src = kScatter ? r : source_row(r, row_index, index_div);
     float v[4] = {0.f, 0.f, 0.f, 0.f};
     if (src >= 0) {
       const uint2 raw = __ldg(reinterpret_cast<const uint2*>(x + static_cast<size_t>(src) * K + g * 128) + lane);
@@ -56,8 +61,17 @@ __global__ void __launch_bounds__(256) quant_int8_g128_kernel(const __nv_bfloat1
         packed |= (static_cast<uint32_t>(q) & 0xFFu) << (8 * i);
       }
     }
-    reinterpret_cast<uint32_t*>(codes + static_cast<size_t>(r) * K + g * 128)[lane] = packed;
-    if (lane == 0) scales[static_cast<size_t>(r) * G + g] = scale;
+    if constexpr (kScatter) {
+      for (int j = 0; j < index_div; ++j) {
+        const int d = __ldg(row_index + static_cast<size_t>(r) * index_div + j);
+        if (d < 0) continue;
+        reinterpret_cast<uint32_t*>(codes + static_cast<size_t>(d) * K + g * 128)[lane] = packed;
+        if (lane == 0) scales[static_cast<size_t>(d) * G + g] = scale;
+      }
+    } else {
+      reinterpret_cast<uint32_t*>(codes + static_cast<size_t>(r) * K + g * 128)[lane] = packed;
+      if (lane == 0) scales[static_cast<size_t>(r) * G + g] = scale;
+    }
   }
 }
 
@@ -81,6 +95,8 @@ __device__ __forceinline__ uint32_t e2m1x2_rn_satfinite(float lo, float hi) {
   return out;
 }
 
+// kScatter as for quant_int8_g128_kernel.
+template <bool kScatter>
 __global__ void __launch_bounds__(256) quant_nvfp4_g16_kernel(const __nv_bfloat16* __restrict__ x, int R, int K,
                                                               const int32_t* __restrict__ row_index,
                                                               int index_div, uint8_t* __restrict__ codes,
@@ -90,9 +106,8 @@ __global__ void __launch_bounds__(256) quant_nvfp4_g16_kernel(const __nv_bfloat1
   const int lane = threadIdx.x & 31;
   const int nb = K / 16;
   for (int r = blockIdx.x * 8 + (threadIdx.x >> 5); r < R; r += gridDim.x * 8) {
-    const int src = source_row(r, row_index, index_div);
-    uint8_t* crow = codes + static_cast<size_t>(r) * (K / 2);
-    uint8_t* srow = sf + static_cast<size_t>(r) * nb;
+    const int src = kScatter ? r : source_row(r, row_index, index_div);
+    const int ndst = kScatter ? index_div : 1;  // output rows this source row goes to
     const __nv_bfloat16* xr = src >= 0 ? x + static_cast<size_t>(src) * K : nullptr;
     // row amax
     float amax = 0.f;
@@ -111,7 +126,12 @@ __global__ void __launch_bounds__(256) quant_nvfp4_g16_kernel(const __nv_bfloat1
 #pragma unroll
     for (int d = 16; d > 0; d >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, d));
     const float o = __fdiv_rn(amax, 2688.0f);
-    if (lane == 0) outer[r] = o;
+    if (lane == 0) {
+      for (int j = 0; j < ndst; ++j) {
+        const int d = kScatter ? __ldg(row_index + static_cast<size_t>(r) * index_div + j) : r;
+        if (d >= 0) outer[d] = o;
+      }
+    }
     for (int b = lane; b < nb; b += 32) {
       uint2 packed = make_uint2(0, 0);
       uint8_t sbyte = 0;
@@ -140,8 +160,12 @@ __global__ void __launch_bounds__(256) quant_nvfp4_g16_kernel(const __nv_bfloat1
           packed = make_uint2(lo, hi);
         }
       }
-      reinterpret_cast<uint2*>(crow)[b] = packed;
-      srow[b] = sbyte;
+      for (int j = 0; j < ndst; ++j) {
+        const int d = kScatter ? __ldg(row_index + static_cast<size_t>(r) * index_div + j) : r;
+        if (d < 0) continue;
+        reinterpret_cast<uint2*>(codes + static_cast<size_t>(d) * (K / 2))[b] = packed;
+        sf[static_cast<size_t>(d) * nb + b] = sbyte;
+      }
     }
   }
 }
@@ -154,14 +178,36 @@ cudaError_t launch_quantize(int act, const void* x, int R, int K, const int32_t*
     long long blocks = (warps + 7) / 8;
     if (blocks > static_cast<long long>(sms) * 16) blocks = static_cast<long long>(sms) * 16;
     if (blocks < 1) blocks = 1;
-    return launch_pdl(quant_int8_g128_kernel, dim3(static_cast<int>(blocks)), dim3(256), 0, st,
+    return launch_pdl(quant_int8_g128_kernel<false>, dim3(static_cast<int>(blocks)), dim3(256), 0, st,
                       static_cast<const __nv_bfloat16*>(x), R, K, row_index, index_div, static_cast<int8_t*>(codes),
                       static_cast<float*>(scales));
   } else {
     long long blocks = (static_cast<long long>(R) + 7) / 8;
     if (blocks > static_cast<long long>(sms) * 16) blocks = static_cast<long long>(sms) * 16;
     if (blocks < 1) blocks = 1;
-    return launch_pdl(quant_nvfp4_g16_kernel, dim3(static_cast<int>(blocks)), dim3(256), 0, st,
+    return launch_pdl(quant_nvfp4_g16_kernel<false>, dim3(static_cast<int>(blocks)), dim3(256), 0, st,
+                      static_cast<const __nv_bfloat16*>(x), R, K, row_index, index_div, static_cast<uint8_t*>(codes),
+                      static_cast<uint8_t*>(scales), row_outer);
+  }
+  return cudaGetLastError();
+}
+
+cudaError_t launch_quantize_scatter(int act, const void* x, int R, int K, const int32_t* row_index, int index_div,
+                            void* codes, void* scales, float* row_outer, cudaStream_t st) {
+  const int sms = current_sm_count();
+  if (act == MNW_ACT_INT8_G128) {
+    const long long warps = static_cast<long long>(R) * (K / 128);
+    long long blocks = (warps + 7) / 8;
+    if (blocks > static_cast<long long>(sms) * 16) blocks = static_cast<long long>(sms) * 16;
+    if (blocks < 1) blocks = 1;
+    return launch_pdl(quant_int8_g128_kernel<true>, dim3(static_cast<int>(blocks)), dim3(256), 0, st,
+                      static_cast<const __nv_bfloat16*>(x), R, K, row_index, index_div, static_cast<int8_t*>(codes),
+                      static_cast<float*>(scales));
+  } else {
+    long long blocks = (static_cast<long long>(R) + 7) / 8;
+    if (blocks > static_cast<long long>(sms) * 16) blocks = static_cast<long long>(sms) * 16;
+    if (blocks < 1) blocks = 1;
+    return launch_pdl(quant_nvfp4_g16_kernel<true>, dim3(static_cast<int>(blocks)), dim3(256), 0, st,
                       static_cast<const __nv_bfloat16*>(x), R, K, row_index, index_div, static_cast<uint8_t*>(codes),
                       static_cast<uint8_t*>(scales), row_outer);
   }
