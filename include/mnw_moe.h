@@ -29,6 +29,14 @@
  *    are OR-ed into a caller-provided 32-bit device error word (MNW_DEVERR_*)
  *    that the caller zeroes beforehand and reads with mnw_moe_read_error().
  *  - Results are deterministic: no floating-point atomics.
+ *  - Kernels are launched with programmatic stream serialisation: one may
+ *    start its set-up while the kernel before it on the stream finishes, but
+ *    waits for that kernel's completion before it reads or writes any global
+ *    memory, so ordering against the caller's own work on the stream is the
+ *    usual one.  They also allow the next kernel to start early; a caller
+ *    that launches its next kernel with the same attribute must wait
+ *    (griddepcontrol.wait / cudaGridDependencySynchronize) before reading
+ *    this library's outputs.
  *
  * Expert blob layout (defined by this library; little-endian):
  *   bytes [0, 256): header.  char[4] "MNWB"; u32 version = 1; u32 wfmt
