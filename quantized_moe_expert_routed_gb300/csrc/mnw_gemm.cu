@@ -66,13 +66,14 @@ constexpr int kThreads = (kWarpEpi0 + kEpiWarps) * 32;
 constexpr int kMaxStages = 8;
 constexpr int kMaxASlots = 8;   // operand-A ring slots in TMEM (runtime count <= this)
 constexpr int kMaxAcc = 8;      // accumulator slots (runtime count <= this)
+constexpr int kBSlots = 4;      // converted-token ring slots (INT8 / FP4 activations)
 constexpr int kTmemCols = 512;
 
 
 struct GemmArgs {
   const int32_t* offsets;
   int E, P, K, N, BN, n_tiles, stages, nmat, acc_slots, acc_base, aslots, sum_base;
-  uint32_t stage_bytes, off_a[2], off_asf[2], off_b, off_braw, off_bsf;
+  uint32_t stage_bytes, off_a[2], off_asf[2], off_b, off_braw, off_bsf, off_bring;
   uint32_t off_scales, scale_mat_bytes, off_tab, off_sa, off_bars;
   const uint8_t* experts;
   uint64_t expert_stride;
@@ -85,7 +86,8 @@ struct GemmArgs {
 };
 
 struct Bars {
-  uint64_t full[kMaxStages], empty[kMaxStages], bconv[kMaxStages];
+  uint64_t full[kMaxStages], empty[kMaxStages];
+  uint64_t bfull[kBSlots], bempty[kBSlots];  // converted-token ring
   uint64_t afull[kMaxASlots], aempty[kMaxASlots];
   uint64_t accfull[kMaxAcc], accempty[kMaxAcc];
   uint64_t sfull[2], sempty[2];
@@ -185,7 +187,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int s = 0; s < kMaxStages; ++s) {
       mbar_init(&bars->full[s], 1);
       mbar_init(&bars->empty[s], ((T::kTs || kBconv) ? kConvWarps : 0) + 1);
-      mbar_init(&bars->bconv[s], kConvWarps);
+    }
+    for (int i = 0; i < kBSlots; ++i) {
+      mbar_init(&bars->bfull[i], kConvWarps);
+      mbar_init(&bars->bempty[i], 1);
     }
     for (int i = 0; i < kMaxASlots; ++i) {
       mbar_init(&bars->afull[i], kConvWarps);
@@ -318,7 +323,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint32_t idesc = idesc_f16(kBM, BN, kBf16Mma);
       const uint32_t S_ = static_cast<uint32_t>(S), na = static_cast<uint32_t>(args.aslots),
                      nacc = static_cast<uint32_t>(args.acc_slots);
-      RingPos sp, ap, cp;  // stages, operand-A slots, accumulator slots
+      RingPos sp, ap, cp, bp;  // stages, operand-A slots, accumulator slots, token slots
       bool ok = true, issued = false;
       uint32_t d_base = 0;
       for (int u = blockIdx.x; ok && u < units; u += gridDim.x) {
@@ -332,8 +337,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         for (int ks = 0; ok && ks < nks; ++ks, sp.advance(S_)) {
           const int s = sp.slot;
-          if (!bounded_wait(kBconv ? &bars->bconv[s] : &bars->full[s], sp.phase, abort, args.err)) { ok = false; break; }
-          tc_fence_after();
+          // with converted tokens both operands come from rings; the stage itself is not read here
+          if (!kBconv) {
+            if (!bounded_wait(&bars->full[s], sp.phase, abort, args.err)) { ok = false; break; }
+            tc_fence_after();
+          }
           const uint32_t st = smem_u32(smem + s * args.stage_bytes);
           for (int sc = 0; sc < T::kSub; ++sc) {
             const int kg = ks * T::kStage + sc * 64;
@@ -352,7 +360,13 @@ __global__ void __launch_bounds__(kThreads, 1)
               if (!bounded_wait(&bars->afull[aslot], ap.phase, abort, args.err)) { ok = false; break; }
               tc_fence_after();
             }
-            const uint32_t b_tile = st + args.off_b + sc * BN * 128;
+            uint32_t b_tile = st + args.off_b + sc * BN * 128;
+            const uint32_t bslot = bp.slot;
+            if (kBconv) {
+              if (!bounded_wait(&bars->bfull[bslot], bp.phase, abort, args.err)) { ok = false; break; }
+              tc_fence_after();
+              b_tile = smem_u32(smem + args.off_bring) + bslot * BN * 128;
+            }
             const uint32_t a_tmem = tmem + aslot * (kNmat * 32);
 #pragma unroll
             for (int kk = 0; kk < 4; ++kk) {
@@ -371,6 +385,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (T::kTs) {
               mma_commit(&bars->aempty[aslot]);
               ap.advance(na);
+            }
+            if (kBconv) {
+              mma_commit(&bars->bempty[bslot]);
+              bp.advance(kBSlots);
             }
             if (kGrouped && ((kg + 64) & 127) == 0) {
               mma_commit(&bars->accfull[cp.slot]);
@@ -398,7 +416,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int r = q * 32 + lane;        // weight row within the tile
     const int ctid = cw * 32 + lane;    // 0..255
     const uint32_t S_ = static_cast<uint32_t>(S), na = static_cast<uint32_t>(args.aslots);
-    RingPos sp, ap;  // stages, operand-A slots
+    RingPos sp, ap, bp;  // stages, operand-A slots, token slots
     bool ok = true;
     if (T::kTs || kBconv) {
       for (int u = blockIdx.x; ok && u < units; u += gridDim.x) {
@@ -406,44 +424,49 @@ __global__ void __launch_bounds__(kThreads, 1)
           const int s = sp.slot;
           if (!bounded_wait(&bars->full[s], sp.phase, abort, args.err)) { ok = false; break; }
           const uint32_t st = smem_u32(smem + s * args.stage_bytes);
-          if (kBconv) {
-            // token codes -> FP16 operand tile (128-byte swizzle, BN rows per 64-K box)
-            const uint32_t braw = st + args.off_braw, bdst = st + args.off_b;
-            if (AM == AM_INT8) {
-              const int chunks = (T::kStage / 128) * BN * 8;
-              for (int i = ctid; i < chunks; i += kConvWarps * 32) {
-                const int rb = i / (BN * 8), rem = i - rb * BN * 8, row = rem >> 3, c = rem & 7;
-                const uint4 v = lds128(sw128(braw + rb * BN * 128, row, c));
-                uint32_t o[16];
-                const uint4 zero = make_uint4(0, 0, 0, 0);
-                cvt_int8x32<false>(v, zero, o);  // first 8 words hold the 16 converted values
-                const int kk = rb * 128 + c * 16, cb = kk >> 6, cc = (kk & 63) >> 3;
-                const uint32_t tile = bdst + cb * BN * 128;
-                sts128(sw128(tile, row, cc), o[0], o[1], o[2], o[3]);
-                sts128(sw128(tile, row, cc + 1), o[4], o[5], o[6], o[7]);
-              }
-            } else {
-              const uint32_t bsf = st + args.off_bsf;
-              const int chunks = BN * 8;
-              for (int i = ctid; i < chunks; i += kConvWarps * 32) {
-                const int row = i >> 3, c = i & 7;
-                const uint4 v = lds128(sw128(braw, row, c));
-                uint32_t sfp;
-                asm volatile("ld.shared.u16 %0, [%1];" : "=r"(sfp) : "r"(bsf + row * 16 + c * 2));
-                uint32_t o[16];
-                cvt_fp4x32(v, sfp & 0xFF, (sfp >> 8) & 0xFF, o);
-                const int cb = c >> 1, cc = (c & 1) * 4;
-                const uint32_t tile = bdst + cb * BN * 128;
-#pragma unroll
-                for (int j = 0; j < 4; ++j) sts128(sw128(tile, row, cc + j), o[4 * j], o[4 * j + 1], o[4 * j + 2], o[4 * j + 3]);
-              }
-            }
-            fence_proxy_async_smem();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&bars->bconv[s]);
-          }
           if (T::kTs) {
             for (int sc = 0; sc < T::kSub; ++sc, ap.advance(na)) {
+              if (kBconv) {
+                // this sub-chunk's token codes -> FP16 operand tile in the next token slot
+                // (128-byte swizzle, BN rows of 64 K)
+                const uint32_t bslot = bp.slot;
+                if (!bounded_wait(&bars->bempty[bslot], bp.phase ^ 1, abort, args.err)) { ok = false; break; }
+                tc_fence_after();
+                const uint32_t tile = smem_u32(smem + args.off_bring) + bslot * BN * 128;
+                const uint32_t braw = st + args.off_braw;
+                if (AM == AM_INT8) {
+                  // 64 K = four 16-code chunks of raw box sc / 2 (128 codes per row)
+                  for (int i = ctid; i < BN * 4; i += kConvWarps * 32) {
+                    const int row = i >> 2, c = 4 * (sc & 1) + (i & 3);
+                    const uint4 v = lds128(sw128(braw + (sc >> 1) * BN * 128, row, c));
+                    uint32_t o[16];
+                    const uint4 zero = make_uint4(0, 0, 0, 0);
+                    cvt_int8x32<false>(v, zero, o);  // first 8 words hold the 16 converted values
+                    const int cc = (c & 3) * 2;
+                    sts128(sw128(tile, row, cc), o[0], o[1], o[2], o[3]);
+                    sts128(sw128(tile, row, cc + 1), o[4], o[5], o[6], o[7]);
+                  }
+                } else {
+                  // 64 K = two 32-code chunks of the raw row (256 codes per row), scales 2 bytes each
+                  const uint32_t bsf = st + args.off_bsf;
+                  for (int i = ctid; i < BN * 2; i += kConvWarps * 32) {
+                    const int row = i >> 1, c = 2 * sc + (i & 1);
+                    const uint4 v = lds128(sw128(braw, row, c));
+                    uint32_t sfp;
+                    asm volatile("ld.shared.u16 %0, [%1];" : "=r"(sfp) : "r"(bsf + row * 16 + c * 2));
+                    uint32_t o[16];
+                    cvt_fp4x32(v, sfp & 0xFF, (sfp >> 8) & 0xFF, o);
+                    const int cc = (c & 1) * 4;
+#pragma unroll
+                    for (int j = 0; j < 4; ++j)
+                      sts128(sw128(tile, row, cc + j), o[4 * j], o[4 * j + 1], o[4 * j + 2], o[4 * j + 3]);
+                  }
+                }
+                fence_proxy_async_smem();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&bars->bfull[bslot]);
+                bp.advance(kBSlots);
+              }
               const uint32_t aslot = ap.slot;
               if (!bounded_wait(&bars->aempty[aslot], ap.phase ^ 1, abort, args.err)) {
                 ok = false;
@@ -679,7 +702,7 @@ bool plan_smem(int wf, int am, bool gate_up, int K, int E, int BN, Plan* p) {
   }
   off = align_up(off, 1024);
   a.off_b = off;
-  off += (kstage / 64) * BN * 128;
+  if (am == AM_BF16) off += (kstage / 64) * BN * 128;  // BF16 tokens are copied in operand layout
   off = align_up(off, 1024);
   a.off_braw = off;
   if (am == AM_INT8) off += (kstage / 128) * BN * 128;
@@ -698,13 +721,16 @@ bool plan_smem(int wf, int am, bool gate_up, int K, int E, int BN, Plan* p) {
   const uint32_t cpw = BN >= 32 ? BN / 2 : BN;  // token columns per epilogue warp
   const uint32_t sa = am == AM_INT8 ? align_up(kEpiWarps * cpw * G * 4u, 16) : 0u;
   const uint32_t bars = align_up(sizeof(Bars), 16);
-  fixed = scales + tab + sa + bars;
+  const uint32_t bring = am != AM_BF16 ? kBSlots * BN * 128u : 0u;  // converted-token ring
+  fixed = bring + scales + tab + sa + bars;
   const size_t budget = kSmemLimit - 1024;  // alignment slack
   if (fixed + 2 * a.stage_bytes > budget) return false;
   int stages = static_cast<int>((budget - fixed) / a.stage_bytes);
   if (stages > kMaxStages) stages = kMaxStages;
   a.stages = stages;
   uint32_t o = stages * a.stage_bytes;
+  a.off_bring = o;  // a multiple of 1024: stage_bytes is
+  o += bring;
   a.off_scales = o;
   o += scales;
   a.off_tab = o;
@@ -769,7 +795,7 @@ int run_gemm(const mnw_moe_layer* L, int wfmt, int act, int kind, const void* a0
   // Token tile: the power of two (16..max) nearest above the mean rows per expert.
   const bool grouped = am == AM_INT8 || (am == AM_BF16 && (wf == WF_INT8 || wf == WF_INT4));
   // TMEM budget (512 columns): operand-A ring + accumulators (+ running sums when grouped).
-  const int max_bn = grouped ? (gate_up ? 64 : 128) : (am == AM_FP4 ? 64 : 128);
+  const int max_bn = grouped ? (gate_up ? 64 : 128) : 128;
   const int mean = (P + L->E - 1) / L->E;
   int BN = 16;
   while (BN < mean && BN < max_bn) BN *= 2;
