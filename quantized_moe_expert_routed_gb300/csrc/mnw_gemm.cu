@@ -799,6 +799,10 @@ int run_gemm(const mnw_moe_layer* L, int wfmt, int act, int kind, const void* a0
   const int mean = (P + L->E - 1) / L->E;
   int BN = 16;
   while (BN < mean && BN < max_bn) BN *= 2;
+  // A non-grouped gate/up tile of 128 tokens leaves TMEM room for one
+  // accumulator slot only (the MMA then stalls while the epilogue drains);
+  // 96 tokens fit two slots beside a two-slot operand-A ring.
+  if (!grouped && gate_up && BN == 128 && wf != WF_BF16) BN = 96;
   Plan plan{};
   while (!plan_smem(wf, am, gate_up, K, L->E, BN, &plan)) {
     if (BN == 16) return MNW_E_UNSUPPORTED;
