@@ -27,6 +27,7 @@ _lib = None
 
 FMT_BF16, FMT_INT8_G128, FMT_INT4_G128, FMT_NVFP4_G16 = 0, 1, 2, 3
 ACT_BF16, ACT_INT8_G128, ACT_NVFP4_G16 = 0, 1, 2
+ACT_F16_ROWS = 3  # FP16 rows with a power-of-two row factor (see encode_f16_rows)
 KIND_GATE_UP, KIND_DOWN = 0, 1
 
 
@@ -59,14 +60,17 @@ def _load():
             "mnwo_e2m1_to_double": (f64, [u8]),
             "mnwo_e4m3_to_double": (i32, [u8, P]),
             "mnwo_bf16_from_double": (u16, [f64]),
+            "mnwo_fp16_from_double": (u16, [f64]),
             "mnwo_e4m3_rn_satfinite": (u8, [f32]),
             "mnwo_e2m1_rn_satfinite": (u8, [f32]),
             "mnwo_quant_int8_g128": (i32, [P, i32, i32, P, P]),
             "mnwo_quant_nvfp4_g16": (i32, [P, i32, i32, P, P, P]),
+            "mnwo_encode_f16_rows": (i32, [P, i32, i32, P, P]),
             "mnwo_permute": (i32, [P, i32, i32, i32, P, P, P]),
             "mnwo_gemm_a16": (i32, [P, ctypes.c_size_t, i32, P, P, i32, P]),
             "mnwo_gemm_a8": (i32, [P, ctypes.c_size_t, i32, P, P, P, i32, P, P]),
             "mnwo_gemm_a4": (i32, [P, ctypes.c_size_t, i32, P, P, P, P, i32, P]),
+            "mnwo_gemm_f16rows": (i32, [P, ctypes.c_size_t, i32, P, P, P, i32, P]),
             "mnwo_combine": (None, [P, P, P, i32, i32, i32, P]),
             "mnwo_moe_forward": (i32, [P, ctypes.c_size_t, i32, P, P, P, i32, i32, P, i32, P]),
         }
@@ -125,6 +129,10 @@ def bf16_from_double(v: float) -> int:
     return _load().mnwo_bf16_from_double(v)
 
 
+def fp16_from_double(v: float) -> int:
+    return _load().mnwo_fp16_from_double(v)
+
+
 def e4m3_rn_satfinite(v: float) -> int:
     return _load().mnwo_e4m3_rn_satfinite(v)
 
@@ -152,6 +160,16 @@ def quant_nvfp4_g16(x_bf16: np.ndarray):
     outer = np.zeros((R,), np.float32)
     _check(_load().mnwo_quant_nvfp4_g16(_p(x), R, K, _p(codes), _p(sf), _p(outer)), "quant_nvfp4_g16")
     return codes, sf, outer
+
+
+def encode_f16_rows(x_bf16: np.ndarray):
+    """FP16 codes (uint16 bits) and power-of-two row factors of BF16 rows."""
+    x = _c(x_bf16, np.uint16)
+    R, K = x.shape
+    codes = np.zeros((R, K), np.uint16)
+    factor = np.zeros((R,), np.float32)
+    _check(_load().mnwo_encode_f16_rows(_p(x), R, K, _p(codes), _p(factor)), "encode_f16_rows")
+    return codes, factor
 
 
 def permute(ids: np.ndarray, E: int):
@@ -209,6 +227,19 @@ def gemm_a4(blob: np.ndarray, kind: int, a_codes, a_sf, a_outer, offsets):
     out = np.zeros((P, I if kind == KIND_GATE_UP else H), np.uint16)
     _check(_load().mnwo_gemm_a4(_p(blob), blob.nbytes, kind, _p(c), _p(sf), _p(o), _p(off), P, _p(out)),
            "gemm_a4")
+    return out
+
+
+def gemm_f16rows(blob: np.ndarray, kind: int, a_f16: np.ndarray, factor, offsets):
+    blob = _c(blob, np.uint8)
+    a = _c(a_f16, np.uint16)
+    f = _c(factor, np.float32)
+    off = _c(offsets, np.int32)
+    E, H, I = _dims(blob)
+    P = a.shape[0]
+    out = np.zeros((P, I if kind == KIND_GATE_UP else H), np.uint16)
+    _check(_load().mnwo_gemm_f16rows(_p(blob), blob.nbytes, kind, _p(a), _p(f), _p(off), P, _p(out)),
+           "gemm_f16rows")
     return out
 
 

@@ -121,6 +121,23 @@ uint16_t mnwo_bf16_from_double(double v) {
   return (uint16_t)u;
 }
 
+/* IEEE binary16 encoder: RNE, 10 stored mantissa bits, emin -14 with
+ * subnormals below it, overflow to Inf. */
+uint16_t mnwo_fp16_from_double(double v) {
+  double a = fabs(v), r;
+  int e2, code;
+  if (isnan(v)) return 0x7e00;
+  r = round_to_format(a, 10, -14);
+  if (r > 65504.0) code = 0x7c00;
+  else if (r < ldexp(1.0, -14)) code = (int)(r / ldexp(1.0, -24)); /* subnormal: m * 2^-24 */
+  else {
+    double f = frexp(r, &e2);          /* r = f * 2^e2, f in [0.5,1) */
+    int m = (int)((2.0 * f - 1.0) * 1024.0);
+    code = ((e2 - 1 + 15) << 10) | m;
+  }
+  return (uint16_t)((signbit(v) ? 0x8000 : 0) | code);
+}
+
 /* E4M3 encoder: RNE, saturating to the largest finite magnitude 448.  The
  * sign of the input is kept, also for results that round to zero. */
 uint8_t mnwo_e4m3_rn_satfinite(float v) {
@@ -262,6 +279,36 @@ int mnwo_quant_nvfp4_g16(const uint16_t* x, int R, int K, uint8_t* codes, uint8_
  * position of a = offsets[e] + number of earlier assignments to the same
  * expert (stable in a).  Out-of-range ids are dropped: assign_pos[a] = -1.
  * sorted_assign[pos] = a; unused tail slots hold -1. */
+/* Not a step of the pages: the CUDA path's FP16 operand form of a BF16 row
+ * (W8A16/W4A16 gate/up on FP16 tensor cores).  A power-of-two factor moves
+ * the row's largest magnitude into [2^14, 2^15), so no value overflows FP16
+ * and values down to 2^-28 of the maximum stay normal.  The clamp keeps 2^e
+ * and 2^-e normal binary32 numbers (every finite BF16 row has e <= 113). */
+int mnwo_encode_f16_rows(const uint16_t* x, int R, int K, uint16_t* codes, float* factor) {
+  int r, k;
+  if (!x || !codes || !factor || R < 0 || K <= 0) return MNWO_E_ARG;
+  for (r = 0; r < R; ++r) {
+    const uint16_t* row = x + (size_t)r * K;
+    double amax = 0.0;
+    int e;
+    for (k = 0; k < K; ++k) {
+      double v = mnwo_bf16_to_double(row[k]);
+      if (!isfinite(v)) return MNWO_E_NONFINITE;
+      if (fabs(v) > amax) amax = fabs(v);
+    }
+    if (amax == 0.0) e = -110;
+    else {
+      frexp(amax, &e);  /* amax = f * 2^e, f in [0.5, 1): floor(log2 amax) = e - 1 */
+      e = e - 1 - 14;
+      if (e < -110) e = -110;
+      if (e > 113) e = 113;
+    }
+    factor[r] = (float)ldexp(1.0, e);
+    for (k = 0; k < K; ++k) codes[(size_t)r * K + k] = mnwo_fp16_from_double(ldexp(mnwo_bf16_to_double(row[k]), -e));
+  }
+  return MNWO_OK;
+}
+
 int mnwo_permute(const int32_t* ids, int T, int k, int E,
                  int32_t* expert_offsets, int32_t* sorted_assign, int32_t* assign_pos) {
   int P, a, e, dropped = 0;
@@ -423,6 +470,7 @@ static double silu(double g) { return g / (1.0 + exp(-g)); }
 typedef struct {
   int act, K;
   const uint16_t* bf16;                                   /* A16 */
+  const uint16_t* f16;                                    /* FP16 rows (factor in outer) */
   const int8_t* q; const float* s;                        /* A8: codes, scales [K/128] */
   const uint8_t* c4; const uint8_t* sf; float outer;      /* A4 */
 } act_row;
@@ -438,6 +486,16 @@ static int row_dot(const uint8_t* blob, const mnwo_blob_info* in, int e, int m, 
       if (rc) return rc;
       acc += mnwo_bf16_to_double(a->bf16[k]) * w;
     }
+  } else if (a->act == MNWO_ACT_F16_ROWS) {
+    for (k = 0; k < K; ++k) {
+      double v;
+      rc = mnwo_weight(blob, in, e, m, n, k, &w);
+      if (rc) return rc;
+      rc = mnwo_fp16_to_double(a->f16[k], &v);
+      if (rc) return rc;
+      acc += v * w;
+    }
+    acc *= (double)a->outer;
   } else if (a->act == MNWO_ACT_INT8_G128) {
     /* INT32 group dot products of the integer codes, each scaled by
      * (weight scale * activation scale) and summed ([card] W8A8 paragraph). */
@@ -492,6 +550,7 @@ static int mode_ok(uint32_t wfmt, int act) {
   if (act == MNWO_ACT_BF16) return wfmt != MNWO_FMT_NVFP4_G16;
   if (act == MNWO_ACT_INT8_G128) return wfmt == MNWO_FMT_INT8_G128 || wfmt == MNWO_FMT_INT4_G128;
   if (act == MNWO_ACT_NVFP4_G16) return wfmt == MNWO_FMT_NVFP4_G16;
+  if (act == MNWO_ACT_F16_ROWS) return wfmt == MNWO_FMT_INT8_G128 || wfmt == MNWO_FMT_INT4_G128;
   return 0;
 }
 
@@ -537,7 +596,10 @@ static int gemm_common(const uint8_t* blob, size_t bytes, int kind, int act, con
       r.act = act;
       r.K = K;
       if (act == MNWO_ACT_BF16) r.bf16 = (const uint16_t*)a0 + (size_t)p * K;
-      else if (act == MNWO_ACT_INT8_G128) {
+      else if (act == MNWO_ACT_F16_ROWS) {
+        r.f16 = (const uint16_t*)a0 + (size_t)p * K;
+        r.outer = ((const float*)a1)[p];
+      } else if (act == MNWO_ACT_INT8_G128) {
         r.q = (const int8_t*)a0 + (size_t)p * K;
         r.s = (const float*)a1 + (size_t)p * (K / 128);
       } else {
@@ -567,6 +629,11 @@ int mnwo_gemm_a4(const uint8_t* blob, size_t bytes, int kind, const uint8_t* a_c
                  const uint8_t* a_sf, const float* a_outer, const int32_t* offsets, int P,
                  uint16_t* out) {
   return gemm_common(blob, bytes, kind, MNWO_ACT_NVFP4_G16, a_codes, a_sf, a_outer, offsets, P, out, NULL);
+}
+
+int mnwo_gemm_f16rows(const uint8_t* blob, size_t bytes, int kind, const uint16_t* a,
+                      const float* factor, const int32_t* offsets, int P, uint16_t* out) {
+  return gemm_common(blob, bytes, kind, MNWO_ACT_F16_ROWS, a, factor, NULL, offsets, P, out, NULL);
 }
 
 /* ------------------------------------------------------------------------- */
@@ -607,7 +674,7 @@ int mnwo_moe_forward(const uint8_t* blob, size_t bytes, int act, const uint16_t*
   uint8_t *c4 = NULL, *sf = NULL;
   double* acc = NULL;
   if ((rc = mnwo_blob_parse(blob, bytes, &in))) return rc;
-  if (!mode_ok(in.wfmt, act)) return MNWO_E_MODE;
+  if (act == MNWO_ACT_F16_ROWS || !mode_ok(in.wfmt, act)) return MNWO_E_MODE; /* not a layer mode */
   if (T < 0 || k <= 0) return MNWO_E_ARG;
   if (!rows) nrows = T;
   H = (int)in.H;

@@ -29,8 +29,10 @@ extern "C" {
 
 /* Weight formats of the expert blob ([card] precision table). */
 enum { MNWO_FMT_BF16 = 0, MNWO_FMT_INT8_G128 = 1, MNWO_FMT_INT4_G128 = 2, MNWO_FMT_NVFP4_G16 = 3 };
-/* Activation modes: BF16 (A16), dynamic INT8 per 128 (A8), dynamic NVFP4 (A4). */
-enum { MNWO_ACT_BF16 = 0, MNWO_ACT_INT8_G128 = 1, MNWO_ACT_NVFP4_G16 = 2 };
+/* Activation modes: BF16 (A16), dynamic INT8 per 128 (A8), dynamic NVFP4 (A4),
+ * and FP16 rows with a power-of-two row factor (an exact re-encoding of BF16
+ * rows for FP16 tensor cores; not a mode of the pages, see mnwo_encode_f16_rows). */
+enum { MNWO_ACT_BF16 = 0, MNWO_ACT_INT8_G128 = 1, MNWO_ACT_NVFP4_G16 = 2, MNWO_ACT_F16_ROWS = 3 };
 /* Grouped GEMM kinds. */
 enum { MNWO_KIND_GATE_UP = 0, MNWO_KIND_DOWN = 1 };
 /* Matrices of one expert. */
@@ -49,6 +51,7 @@ int    mnwo_e4m3_to_double(uint8_t byte, double* out);       /* OCP E4M3FN; reje
 
 /* ---- scalar encoders: round to nearest, ties to even ---- */
 uint16_t mnwo_bf16_from_double(double v);                    /* overflow -> Inf */
+uint16_t mnwo_fp16_from_double(double v);                    /* overflow -> Inf */
 uint8_t  mnwo_e4m3_rn_satfinite(float v);                    /* saturates at +-448 */
 uint8_t  mnwo_e2m1_rn_satfinite(float v);                    /* saturates at +-6   */
 
@@ -58,6 +61,13 @@ int mnwo_quant_int8_g128(const uint16_t* x, int R, int K, int8_t* codes, float* 
 /* NVFP4: E2M1 codes (two per byte, low nibble = even index), E4M3 scale per 16,
  * FP32 outer scale per row ([card] NVFP4 row, activation column). */
 int mnwo_quant_nvfp4_g16(const uint16_t* x, int R, int K, uint8_t* codes, uint8_t* sf, float* outer);
+
+/* FP16 rows: e = clamp(floor(log2 amax_row) - 14, -110, 113) (e = -110 for an
+ * all-zero row), factor = 2^e, code = fp16_rn(x * 2^-e).  The row's largest
+ * magnitude lands in [2^14, 2^15) (unless clamped); every value at most 2^28
+ * below it is kept exactly (BF16's 8 significant bits fit FP16's 11).
+ * MNWO_E_NONFINITE for a row holding Inf or NaN. */
+int mnwo_encode_f16_rows(const uint16_t* x, int R, int K, uint16_t* codes, float* factor);
 
 /* ---- token permutation into expert-sorted order ---- */
 /* Returns the number of dropped (out-of-range) ids, or -1 on bad arguments. */
@@ -89,6 +99,10 @@ int mnwo_gemm_a8(const uint8_t* blob, size_t bytes, int kind, const int8_t* a_co
 int mnwo_gemm_a4(const uint8_t* blob, size_t bytes, int kind, const uint8_t* a_codes,
                  const uint8_t* a_sf, const float* a_outer, const int32_t* offsets, int P,
                  uint16_t* out);
+/* FP16 rows (INT8/INT4 weights): dot = factor[p] * sum_k fp16(a[p,k]) * w[n,k],
+ * the weights decoded exactly as in mnwo_gemm_a16. */
+int mnwo_gemm_f16rows(const uint8_t* blob, size_t bytes, int kind, const uint16_t* a,
+                      const float* factor, const int32_t* offsets, int P, uint16_t* out);
 
 /* ---- combine ---- */
 void mnwo_combine(const uint16_t* y, const int32_t* assign_pos, const float* w, int T, int k,
