@@ -170,16 +170,42 @@ def run_ours(args, wl):
         if rc != 0:
             raise RuntimeError(f"{what} failed: {lib.mnw_status_string(rc).decode()}")
 
+    # INT weights with BF16 activations and enough tokens per expert for the
+    # tcgen05 kernel: the forward runs gate/up on FP16 rows (row factor in xf),
+    # so the stepwise sequence and the roofline loop do the same.
+    f16_gate_up = f16_down = None
+    if wl.act == S.ACT_BF16 and wl.wfmt in (S.FMT_INT8_G128, S.FMT_INT4_G128) and -(-P // E) >= 32:
+        f16 = getattr(lib, f"mnw_moe_grouped_gemm_{gemm_name}_f16rows")
+        # a zero-row call reports whether the layer's scales allow the FP16 form
+        allowed = [f16(layer.handle, kind, None, None, None, 0, None, None, sp) == 0 for kind in (0, 1)]
+        if allowed[0]:
+            f16_gate_up = f16
+            xa = torch.empty((P, wl.H), dtype=torch.float16, device=dev)
+            xf = torch.empty((P,), dtype=torch.float32, device=dev)
+        if allowed[1]:
+            f16_down = f16
+            ha = torch.empty((P, wl.I), dtype=torch.float16, device=dev)
+            hf = torch.empty((P,), dtype=torch.float32, device=dev)
+
     def step():
         """The layer's kernels called one by one (prepares the gate/up inputs)."""
-        launches = 0
         if wl.act == S.ACT_BF16:
-            chk(lib.mnw_moe_permute(ptr(ids), T, k, E, ptr(offsets), ptr(sorted_assign), ptr(assign_pos), ptr(x),
-                                    wl.H, ptr(xa), ptr(err), sp), "permute")
-            launches += 2
-            chk(gemm(layer.handle, 0, ptr(xa), ptr(offsets), P, ptr(h), ptr(err), sp), "gate_up")
-            chk(gemm(layer.handle, 1, ptr(h), ptr(offsets), P, ptr(y), ptr(err), sp), "down")
-            launches += 2
+            if f16_gate_up is not None:
+                chk(lib.mnw_moe_permute(ptr(ids), T, k, E, ptr(offsets), ptr(sorted_assign), ptr(assign_pos), None,
+                                        0, None, ptr(err), sp), "permute")
+                chk(lib.mnw_moe_quantize_act(M.ACT_F16_ROWS, ptr(x), P, wl.H, ptr(sorted_assign), k, ptr(xa), None,
+                                             ptr(xf), sp), "encode x")
+                chk(f16_gate_up(layer.handle, 0, ptr(xa), ptr(xf), ptr(offsets), P, ptr(h), ptr(err), sp), "gate_up")
+            else:
+                chk(lib.mnw_moe_permute(ptr(ids), T, k, E, ptr(offsets), ptr(sorted_assign), ptr(assign_pos), ptr(x),
+                                        wl.H, ptr(xa), ptr(err), sp), "permute")
+                chk(gemm(layer.handle, 0, ptr(xa), ptr(offsets), P, ptr(h), ptr(err), sp), "gate_up")
+            if f16_down is not None:
+                chk(lib.mnw_moe_quantize_act(M.ACT_F16_ROWS, ptr(h), P, wl.I, None, 1, ptr(ha), None, ptr(hf), sp),
+                    "encode h")
+                chk(f16_down(layer.handle, 1, ptr(ha), ptr(hf), ptr(offsets), P, ptr(y), ptr(err), sp), "down")
+            else:
+                chk(gemm(layer.handle, 1, ptr(h), ptr(offsets), P, ptr(y), ptr(err), sp), "down")
         else:
             chk(lib.mnw_moe_permute(ptr(ids), T, k, E, ptr(offsets), ptr(sorted_assign), ptr(assign_pos), None, 0,
                                     None, ptr(err), sp), "permute")
@@ -196,9 +222,7 @@ def run_ours(args, wl):
                 chk(gemm(layer.handle, 1, ptr(hq), ptr(hs), ptr(offsets), P, ptr(y), None, ptr(err), sp), "down")
             else:
                 chk(gemm(layer.handle, 1, ptr(hq), ptr(hs), o2, ptr(offsets), P, ptr(y), ptr(err), sp), "down")
-            launches += 5
         chk(lib.mnw_moe_combine(ptr(y), ptr(assign_pos), ptr(w), T, k, wl.H, ptr(out), sp), "combine")
-        return launches + 1
 
     # Headline: whole layer steps through the library's one-call entry point
     # (its kernels launch back to back with programmatic dependent launch; no
@@ -208,10 +232,11 @@ def run_ours(args, wl):
 
     def layer_step():
         chk(fwd(layer.handle, wl.act, ptr(x), ptr(ids), ptr(w), T, k, ptr(out), ptr(ws), ws_bytes, sp), "forward")
-        return 5 if wl.act == S.ACT_BF16 else 6  # permute, (gather | quantise x), gate/up, (quantise h), down, combine
 
     def gate_up_only():
-        if wl.act == S.ACT_BF16:
+        if f16_gate_up is not None:
+            chk(f16_gate_up(layer.handle, 0, ptr(xa), ptr(xf), ptr(offsets), P, ptr(h), ptr(err), sp), "gate_up")
+        elif wl.act == S.ACT_BF16:
             chk(gemm(layer.handle, 0, ptr(xa), ptr(offsets), P, ptr(h), ptr(err), sp), "gate_up")
         elif wl.act == S.ACT_INT8_G128:
             chk(gemm(layer.handle, 0, ptr(xq), ptr(xs), ptr(offsets), P, ptr(h), None, ptr(err), sp), "gate_up")
@@ -233,7 +258,9 @@ def run_ours(args, wl):
             l2_flush()  # between timed iterations, outside the events
             e0, e1 = ev[i]
             e0.record(stream)
-            launches += layer_step()
+            n0 = lib.mnw_moe_launch_count()
+            layer_step()
+            launches += lib.mnw_moe_launch_count() - n0  # the library's own kernels, counted by the library
             e1.record(stream)
         torch.cuda.synchronize()
     step_ms = [a.elapsed_time(b) for a, b in ev]

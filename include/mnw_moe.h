@@ -84,7 +84,10 @@ enum mnw_status {
 #define MNW_DEVERR_TIMEOUT 0x2u        /* a kernel-internal wait ran out; its output is invalid */
 
 enum mnw_wfmt { MNW_FMT_BF16 = 0, MNW_FMT_INT8_G128 = 1, MNW_FMT_INT4_G128 = 2, MNW_FMT_NVFP4_G16 = 3 };
-enum mnw_afmt { MNW_ACT_BF16 = 0, MNW_ACT_INT8_G128 = 1, MNW_ACT_NVFP4_G16 = 2 };
+/* MNW_ACT_F16_ROWS is an operand form, not a layer mode: BF16 rows re-encoded
+ * as FP16 with a power-of-two factor per row (mnw_moe_quantize_act), read by
+ * the *_f16rows gate/up GEMMs.  mnw_moe_forward picks it by itself. */
+enum mnw_afmt { MNW_ACT_BF16 = 0, MNW_ACT_INT8_G128 = 1, MNW_ACT_NVFP4_G16 = 2, MNW_ACT_F16_ROWS = 3 };
 enum mnw_kind { MNW_KIND_GATE_UP = 0, MNW_KIND_DOWN = 1 };
 
 typedef struct mnw_moe_layer mnw_moe_layer;
@@ -131,7 +134,13 @@ int mnw_moe_permute(const int32_t* ids, int T, int k, int E, int32_t* expert_off
  * codes u8 [R, K/2] (even element in the low nibble), scales E4M3 u8
  * [R, K/16], row_outer f32 [R].  Every step is one IEEE binary32 operation
  * with round-to-nearest-even; the results are bit-exact.  K must be a
- * multiple of 128 (INT8) or 16 (NVFP4). */
+ * multiple of 128 (INT8) or 16 (NVFP4).
+ * act = MNW_ACT_F16_ROWS (an exact re-encoding, not a quantiser of the
+ * pages): e = clamp(floor(log2 amax_row) - 14, -110, 113) (-110 for a zero
+ * row), row_outer = 2^e, codes fp16 [R, K] = fp16_rn(x * 2^-e); scales
+ * unused (may be NULL); a negative row_index gives codes 0 and row_outer 1.
+ * Every BF16 value of a row no more than 2^28 below its largest magnitude
+ * is kept exactly.  K must be a multiple of 8. */
 int mnw_moe_quantize_act(int act, const void* x, int R, int K, const int32_t* row_index,
                          int index_div, void* codes, void* scales, float* row_outer,
                          mnw_stream stream);
@@ -160,6 +169,22 @@ int mnw_moe_grouped_gemm_w8a16(const mnw_moe_layer* layer, int kind, const void*
 int mnw_moe_grouped_gemm_w4a16(const mnw_moe_layer* layer, int kind, const void* a,
                                const int32_t* expert_offsets, int P, void* out, uint32_t* err,
                                mnw_stream stream);
+/* w8a16_f16rows / w4a16_f16rows: the grouped GEMMs of the W8A16/W4A16 modes
+ * on FP16 tensor cores.  a: device fp16 [P, K] and row_outer device f32 [P]
+ * from mnw_moe_quantize_act(MNW_ACT_F16_ROWS); each weight enters as
+ * fp16_rn(q * s) (its code times its FP16 group scale, one rounding), one
+ * FP32 accumulator spans all of K, and the row factor f multiplies each dot
+ * product: GATE_UP out = bf16(SiLU(f * (a . Wg^T)) * (f * (a . Wu^T))), DOWN
+ * out = bf16(f * (a . Wd^T)).  MNW_E_UNSUPPORTED when some q * s of the
+ * matrices used would leave FP16's normal range (a scale above 65504 / qmax,
+ * qmax = 127 or 8, or a non-zero scale below 2^-14); mnw_moe_forward then
+ * keeps the BF16 form for that GEMM.  Always the tcgen05 kernel. */
+int mnw_moe_grouped_gemm_w8a16_f16rows(const mnw_moe_layer* layer, int kind, const void* a,
+                                       const float* row_outer, const int32_t* expert_offsets, int P,
+                                       void* out, uint32_t* err, mnw_stream stream);
+int mnw_moe_grouped_gemm_w4a16_f16rows(const mnw_moe_layer* layer, int kind, const void* a,
+                                       const float* row_outer, const int32_t* expert_offsets, int P,
+                                       void* out, uint32_t* err, mnw_stream stream);
 /* w8a8 / w4a8 (model card, W8A8/W4A8 paragraph): a_codes device int8 [P, K]
  * and a_scales device f32 [P, K/128] from mnw_moe_quantize_act(INT8_G128).
  * For every 128-wide group g the exact integer dot product D_g of the codes is
@@ -210,6 +235,10 @@ size_t mnw_moe_workspace_size_host(const mnw_moe_layer* layer, int act, int T, i
 int mnw_moe_forward_host(const mnw_moe_layer* layer, int act, const void* x_host,
                          const int32_t* ids_host, const float* w_host, int T, int k,
                          void* out_host, void* ws, size_t ws_bytes, mnw_stream stream);
+
+/* Number of kernels this library has enqueued since it was loaded (every
+ * successful launch, all threads and streams; a host-side count). */
+uint64_t mnw_moe_launch_count(void);
 
 /* Grouped-GEMM kernel selection, process-wide (a tuning and testing knob;
  * results agree to FP32 rounding order either way).  MNW_PATH_AUTO: INT8/INT4

@@ -19,7 +19,7 @@ _HERE = os.path.dirname(os.path.abspath(__file__))
 
 MNW_OK = 0
 FMT_BF16, FMT_INT8_G128, FMT_INT4_G128, FMT_NVFP4_G16 = 0, 1, 2, 3
-ACT_BF16, ACT_INT8_G128, ACT_NVFP4_G16 = 0, 1, 2
+ACT_BF16, ACT_INT8_G128, ACT_NVFP4_G16, ACT_F16_ROWS = 0, 1, 2, 3
 KIND_GATE_UP, KIND_DOWN = 0, 1
 DEVERR_BAD_EXPERT_ID, DEVERR_TIMEOUT = 0x1, 0x2
 PATH_AUTO, PATH_TCGEN05, PATH_WARP_MMA = 0, 1, 2
@@ -36,6 +36,8 @@ SIGNATURES = {
     "mnw_moe_grouped_gemm_bf16": (_I, [_P, _I, _P, _P, _I, _P, _U32P, _P]),
     "mnw_moe_grouped_gemm_w8a16": (_I, [_P, _I, _P, _P, _I, _P, _U32P, _P]),
     "mnw_moe_grouped_gemm_w4a16": (_I, [_P, _I, _P, _P, _I, _P, _U32P, _P]),
+    "mnw_moe_grouped_gemm_w8a16_f16rows": (_I, [_P, _I, _P, _P, _P, _I, _P, _U32P, _P]),
+    "mnw_moe_grouped_gemm_w4a16_f16rows": (_I, [_P, _I, _P, _P, _P, _I, _P, _U32P, _P]),
     "mnw_moe_grouped_gemm_w8a8": (_I, [_P, _I, _P, _P, _P, _I, _P, _P, _U32P, _P]),
     "mnw_moe_grouped_gemm_w4a8": (_I, [_P, _I, _P, _P, _P, _I, _P, _P, _U32P, _P]),
     "mnw_moe_grouped_gemm_nvfp4": (_I, [_P, _I, _P, _P, _P, _P, _I, _P, _U32P, _P]),
@@ -47,6 +49,7 @@ SIGNATURES = {
     "mnw_moe_forward_host": (_I, [_P, _I, _P, _P, _P, _I, _I, _P, _P, _SZ, _P]),
     "mnw_moe_read_error": (_I, [_P, _P, _P]),
     "mnw_moe_set_gemm_path": (_I, [_I]),
+    "mnw_moe_launch_count": (ctypes.c_uint64, []),
     "mnw_moe_forward_static": (_I, [_P, _I, _P, _P, _P, _I, _I, _P, _U32P, _P]),
     "mnw_moe_selftest_wait_timeout": (_I, [ctypes.c_uint32, _U32P, _U32P, _P]),
 }
@@ -137,10 +140,17 @@ def mnw_moe_permute(ids, E, x=None, stream=None, err=None):
 
 def mnw_moe_quantize_act(act, x, row_index=None, index_div=1, rows=None, stream=None):
     """INT8_G128 -> (codes int8 [R,K], scales f32 [R,K/128]);
-    NVFP4_G16 -> (codes u8 [R,K/2], sf u8 [R,K/16], outer f32 [R])."""
+    NVFP4_G16 -> (codes u8 [R,K/2], sf u8 [R,K/16], outer f32 [R]);
+    F16_ROWS -> (codes fp16 [R,K], factor f32 [R])."""
     R = rows if rows is not None else (row_index.numel() if row_index is not None else x.shape[0])
     K = x.shape[1]
     dev = x.device
+    if act == ACT_F16_ROWS:
+        codes = torch.empty((R, K), dtype=torch.float16, device=dev)
+        outer = torch.empty((R,), dtype=torch.float32, device=dev)
+        _check(load().mnw_moe_quantize_act(act, _ptr(x), R, K, _ptr(row_index), index_div, _ptr(codes), None,
+                                           _ptr(outer), _stream(stream)), "mnw_moe_quantize_act")
+        return codes, outer
     if act == ACT_INT8_G128:
         codes = torch.empty((R, K), dtype=torch.int8, device=dev)
         scales = torch.empty((R, K // 128), dtype=torch.float32, device=dev)
@@ -177,6 +187,25 @@ def mnw_moe_grouped_gemm_w8a16(layer, kind, a, expert_offsets, err=None, stream=
 
 def mnw_moe_grouped_gemm_w4a16(layer, kind, a, expert_offsets, err=None, stream=None):
     return _gemm_a16("mnw_moe_grouped_gemm_w4a16", layer, kind, a, expert_offsets, err, stream)
+
+
+def _gemm_f16rows(name, layer, kind, a, row_outer, expert_offsets, err=None, stream=None):
+    P = a.shape[0]
+    out = _gemm_out(layer, kind, P, a.device)
+    fn = getattr(load(), name)
+    _check(fn(layer.handle, kind, _ptr(a), _ptr(row_outer), _ptr(expert_offsets), P, _ptr(out), _ptr(err),
+              _stream(stream)), name)
+    return out
+
+
+def mnw_moe_grouped_gemm_w8a16_f16rows(layer, kind, a, row_outer, expert_offsets, err=None, stream=None):
+    return _gemm_f16rows("mnw_moe_grouped_gemm_w8a16_f16rows", layer, kind, a, row_outer, expert_offsets, err,
+                         stream)
+
+
+def mnw_moe_grouped_gemm_w4a16_f16rows(layer, kind, a, row_outer, expert_offsets, err=None, stream=None):
+    return _gemm_f16rows("mnw_moe_grouped_gemm_w4a16_f16rows", layer, kind, a, row_outer, expert_offsets, err,
+                         stream)
 
 
 def _gemm_a8(name, layer, kind, a_codes, a_scales, expert_offsets, want_dots=False, err=None, stream=None):
@@ -264,6 +293,11 @@ def mnw_moe_read_error(err, stream=None) -> int:
     out = ctypes.c_uint32()
     _check(load().mnw_moe_read_error(_ptr(err), ctypes.byref(out), _stream(stream)), "mnw_moe_read_error")
     return out.value
+
+
+def mnw_moe_launch_count() -> int:
+    """Kernels this library has enqueued since it was loaded (host-side count)."""
+    return int(load().mnw_moe_launch_count())
 
 
 def mnw_moe_set_gemm_path(path: int) -> None:

@@ -1,6 +1,7 @@
 // mnw_api.cu -- the C ABI of include/mnw_moe.h: argument checks, the expert
 // blob header, workspace layout and the whole-layer orchestration.  No call
 // here synchronises except mnw_moe_read_error() and mnw_moe_forward_host().
+#include <cuda_fp16.h>
 #include <cudaTypedefs.h>
 
 #include <atomic>
@@ -10,6 +11,9 @@
 #include "mnw_internal.h"
 
 namespace mnw {
+
+static std::atomic<uint64_t> g_launch_count{0};
+void note_launch() { g_launch_count.fetch_add(1, std::memory_order_relaxed); }
 
 // ---- tensor maps ------------------------------------------------------------
 
@@ -42,6 +46,68 @@ bool encode_map(CUtensorMap* map, CUtensorMapDataType dtype, int rank, const voi
   CUresult r = fn(map, dtype, rank, const_cast<void*>(base), d, s, b, es, CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle,
                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS;
+}
+
+// ---- weight scale range ------------------------------------------------------
+
+// Largest |s| and smallest non-zero |s| over the FP16 group scales of
+// `nmat` matrices of every expert (scale arrays at off0 and, for a second
+// matrix, off1), as the bits of non-negative FP16 values (their order is the
+// order of magnitudes; a NaN compares above every finite value).
+static __device__ uint32_t g_scale_max_bits;
+static __device__ uint32_t g_scale_min_bits;
+__global__ void scale_range_kernel(const uint8_t* experts, uint64_t expert_stride, uint64_t off0, uint64_t off1,
+                                   int nmat, uint64_t halfs_per_matrix, int E) {
+  uint32_t m = 0, lo = 0xFFFFu;
+  const uint64_t per_expert = static_cast<uint64_t>(nmat) * halfs_per_matrix;
+  const uint64_t total = static_cast<uint64_t>(E) * per_expert;
+  for (uint64_t i = blockIdx.x * static_cast<uint64_t>(blockDim.x) + threadIdx.x; i < total;
+       i += static_cast<uint64_t>(gridDim.x) * blockDim.x) {
+    const uint64_t e = i / per_expert, rem = i - e * per_expert;
+    const uint64_t mat = rem / halfs_per_matrix, j = rem - mat * halfs_per_matrix;
+    const uint16_t* sc = reinterpret_cast<const uint16_t*>(experts + e * expert_stride + (mat ? off1 : off0));
+    const uint32_t a = __ldg(sc + j) & 0x7FFFu;
+    m = max(m, a);
+    if (a) lo = min(lo, a);
+  }
+#pragma unroll
+  for (int d = 16; d > 0; d >>= 1) {
+    m = max(m, __shfl_xor_sync(0xffffffffu, m, d));
+    lo = min(lo, __shfl_xor_sync(0xffffffffu, lo, d));
+  }
+  if ((threadIdx.x & 31) == 0) {
+    atomicMax(&g_scale_max_bits, m);
+    atomicMin(&g_scale_min_bits, lo);
+  }
+}
+
+// True when fp16(q * s) is finite and, for q != 0 and s != 0, a normal FP16
+// number (so it keeps 11 significant bits) for every code q and scale s of the
+// gate and up matrices (down = false) or of the down matrix (down = true).
+static bool scales_fit_f16(const mnw_moe_layer& L, bool down) {
+  if (L.wfmt != MNW_FMT_INT8_G128 && L.wfmt != MNW_FMT_INT4_G128) return false;
+  const uint32_t zero = 0, top = 0xFFFFu;
+  if (cudaMemcpyToSymbol(g_scale_max_bits, &zero, sizeof(zero)) != cudaSuccess ||
+      cudaMemcpyToSymbol(g_scale_min_bits, &top, sizeof(top)) != cudaSuccess)
+    return false;
+  // gate/up: [I rows][H/128 groups] each; down: [H rows][I/128 groups]
+  const uint64_t halfs = static_cast<uint64_t>(L.I) * (L.H / 128);
+  if (down)
+    scale_range_kernel<<<256, 256>>>(L.blob + L.data_offset, L.expert_stride, L.scales_off[2], L.scales_off[2], 1,
+                                     halfs, L.E);
+  else
+    scale_range_kernel<<<256, 256>>>(L.blob + L.data_offset, L.expert_stride, L.scales_off[0], L.scales_off[1], 2,
+                                     halfs, L.E);
+  note_launch();
+  uint32_t bits = 0xFFFF, lo_bits = 0;
+  if (cudaGetLastError() != cudaSuccess || cudaMemcpyFromSymbol(&bits, g_scale_max_bits, sizeof(bits)) != cudaSuccess ||
+      cudaMemcpyFromSymbol(&lo_bits, g_scale_min_bits, sizeof(lo_bits)) != cudaSuccess)
+    return false;
+  if (bits >= 0x7C00u) return false;     // an infinite or NaN scale
+  if (lo_bits < 0x0400u) return false;   // a subnormal scale: below 2^-14
+  const float smax = __half2float(__ushort_as_half(static_cast<unsigned short>(bits)));
+  const float qmax = L.wfmt == MNW_FMT_INT8_G128 ? 127.f : 8.f;
+  return smax * qmax < 65504.f;
 }
 
 // ---- blob header ------------------------------------------------------------
@@ -113,7 +179,8 @@ static WsLayout ws_layout(const mnw_moe_layer* L, int act, int T, int k) {
   w.sorted = o; o = al(o + P * 4);
   w.pos = o; o = al(o + P * 4);
   if (act == MNW_ACT_BF16) {
-    w.xa = o; o = al(o + P * H * 2);
+    w.xa = o; o = al(o + P * H * 2);  // BF16 rows, or FP16 rows for the FP16 operand path
+    w.xc = o; o = al(o + P * 4);      // their row factors (FP16 operand path)
   } else if (act == MNW_ACT_INT8_G128) {
     w.xa = o; o = al(o + P * H);
     w.xb = o; o = al(o + P * (H / 128) * 4);
@@ -123,7 +190,10 @@ static WsLayout ws_layout(const mnw_moe_layer* L, int act, int T, int k) {
     w.xc = o; o = al(o + P * 4);
   }
   w.h = o; o = al(o + P * I * 2);
-  if (act == MNW_ACT_INT8_G128) {
+  if (act == MNW_ACT_BF16 && (L->wfmt == MNW_FMT_INT8_G128 || L->wfmt == MNW_FMT_INT4_G128)) {
+    w.ha = o; o = al(o + P * I * 2);  // h as FP16 rows (FP16 operand down GEMM)
+    w.hc = o; o = al(o + P * 4);      // their row factors
+  } else if (act == MNW_ACT_INT8_G128) {
     w.ha = o; o = al(o + P * I);
     w.hb = o; o = al(o + P * (I / 128) * 4);
   } else if (act == MNW_ACT_NVFP4_G16) {
@@ -161,6 +231,8 @@ int mnw_moe_set_gemm_path(int path) {
   g_gemm_path = path;
   return MNW_OK;
 }
+
+uint64_t mnw_moe_launch_count(void) { return g_launch_count.load(std::memory_order_relaxed); }
 
 const char* mnw_status_string(int status) {
   switch (status) {
@@ -248,6 +320,9 @@ int mnw_moe_layer_init(const void* header_host, const void* blob_dev, size_t blo
     }
     if (!ok) return MNW_E_CUDA;
   }
+  // one small reduction over the gate/up scales (reads the blob, synchronises)
+  L.f16_gate_up_ok = scales_fit_f16(L, false);
+  L.f16_down_ok = scales_fit_f16(L, true);
   mnw_moe_layer* p = new (std::nothrow) mnw_moe_layer(L);
   if (!p) return MNW_E_INVALID_ARG;
   *out = p;
@@ -281,6 +356,16 @@ int mnw_moe_permute(const int32_t* ids, int T, int k, int E, int32_t* expert_off
 int mnw_moe_quantize_act(int act, const void* x, int R, int K, const int32_t* row_index, int index_div, void* codes,
                          void* scales, float* row_outer, mnw_stream stream) {
   if (R < 0 || K <= 0) return MNW_E_INVALID_ARG;
+  if (row_index && index_div < 1) return MNW_E_INVALID_ARG;
+  if (act == MNW_ACT_F16_ROWS) {
+    if (K % 8) return MNW_E_UNSUPPORTED;
+    if (R == 0) return MNW_OK;
+    if (!x || !codes || !row_outer || !aligned(x, 16) || !aligned(codes, 16) || !aligned(row_outer, 4))
+      return MNW_E_INVALID_ARG;
+    cudaError_t e = launch_gather_f16(x, K, row_index, R, row_index ? index_div : 1, codes, row_outer,
+                                      static_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? MNW_OK : MNW_E_CUDA;
+  }
   if (act == MNW_ACT_INT8_G128) {
     if (K % 128) return MNW_E_UNSUPPORTED;
   } else if (act == MNW_ACT_NVFP4_G16) {
@@ -289,7 +374,6 @@ int mnw_moe_quantize_act(int act, const void* x, int R, int K, const int32_t* ro
   } else {
     return MNW_E_INVALID_ARG;
   }
-  if (row_index && index_div < 1) return MNW_E_INVALID_ARG;
   if (R == 0) return MNW_OK;
   if (!x || !codes || !scales || !aligned(x, 16) || !aligned(codes, 16) || !aligned(scales, 4))
     return MNW_E_INVALID_ARG;
@@ -312,6 +396,21 @@ int mnw_moe_grouped_gemm_w4a16(const mnw_moe_layer* L, int kind, const void* a, 
                                uint32_t* err, mnw_stream stream) {
   return run_gemm(L, MNW_FMT_INT4_G128, MNW_ACT_BF16, kind, a, nullptr, nullptr, offs, P, out, nullptr, err,
                   static_cast<cudaStream_t>(stream));
+}
+static int gemm_f16rows(const mnw_moe_layer* L, int wfmt, int kind, const void* a, const float* f,
+                        const int32_t* offs, int P, void* out, uint32_t* err, cudaStream_t st) {
+  if (!L || (kind != MNW_KIND_GATE_UP && kind != MNW_KIND_DOWN)) return MNW_E_INVALID_ARG;
+  if (L->wfmt != wfmt) return MNW_E_MODE;
+  if (!(kind == MNW_KIND_GATE_UP ? L->f16_gate_up_ok : L->f16_down_ok)) return MNW_E_UNSUPPORTED;
+  return run_gemm(L, wfmt, kActF16Rows, kind, a, f, nullptr, offs, P, out, nullptr, err, st);
+}
+int mnw_moe_grouped_gemm_w8a16_f16rows(const mnw_moe_layer* L, int kind, const void* a, const float* f,
+                                       const int32_t* offs, int P, void* out, uint32_t* err, mnw_stream stream) {
+  return gemm_f16rows(L, MNW_FMT_INT8_G128, kind, a, f, offs, P, out, err, static_cast<cudaStream_t>(stream));
+}
+int mnw_moe_grouped_gemm_w4a16_f16rows(const mnw_moe_layer* L, int kind, const void* a, const float* f,
+                                       const int32_t* offs, int P, void* out, uint32_t* err, mnw_stream stream) {
+  return gemm_f16rows(L, MNW_FMT_INT4_G128, kind, a, f, offs, P, out, err, static_cast<cudaStream_t>(stream));
 }
 int mnw_moe_grouped_gemm_w8a8(const mnw_moe_layer* L, int kind, const int8_t* q, const float* s, const int32_t* offs,
                               int P, void* out, int32_t* dots, uint32_t* err, mnw_stream stream) {
@@ -370,11 +469,34 @@ int mnw_moe_forward(const mnw_moe_layer* L, int act, const void* x, const int32_
   if (cudaMemsetAsync(err, 0, 256, st) != cudaSuccess) return MNW_E_CUDA;
   int rc;
   if (act == MNW_ACT_BF16) {
-    rc = mnw_moe_permute(ids, T, k, L->E, offs, sorted, pos, x, H, b + W.xa, err, stream);
+    // INT weights on the tcgen05 kernel (enough tokens per expert): the GEMMs
+    // run on FP16 operands -- rows scaled into FP16 range by a power of two,
+    // weights dequantised on chip to fp16(q * s) -- so one accumulator spans
+    // all of K instead of one per 128-K group.
+    const int mean_rows = (P + L->E - 1) / L->E;
+    const int path = gemm_path();
+    const bool tc = path != MNW_PATH_WARP_MMA && (path == MNW_PATH_TCGEN05 || mean_rows >= 32);
+    if (tc && L->f16_gate_up_ok) {
+      rc = mnw_moe_permute(ids, T, k, L->E, offs, sorted, pos, nullptr, 0, nullptr, err, stream);
+      if (rc) return rc;
+      float* factor = reinterpret_cast<float*>(b + W.xc);
+      rc = mnw_moe_quantize_act(MNW_ACT_F16_ROWS, x, P, H, sorted, k, b + W.xa, nullptr, factor, stream);
+      if (rc) return rc;
+      rc = gemm_for(L, kActF16Rows, MNW_KIND_GATE_UP, b + W.xa, factor, nullptr, offs, P, b + W.h, err, sched_gu, st);
+    } else {
+      rc = mnw_moe_permute(ids, T, k, L->E, offs, sorted, pos, x, H, b + W.xa, err, stream);
+      if (rc) return rc;
+      rc = gemm_for(L, act, MNW_KIND_GATE_UP, b + W.xa, nullptr, nullptr, offs, P, b + W.h, err, sched_gu, st);
+    }
     if (rc) return rc;
-    rc = gemm_for(L, act, MNW_KIND_GATE_UP, b + W.xa, nullptr, nullptr, offs, P, b + W.h, err, sched_gu, st);
-    if (rc) return rc;
-    rc = gemm_for(L, act, MNW_KIND_DOWN, b + W.h, nullptr, nullptr, offs, P, b + W.y, err, sched_dn, st);
+    if (tc && L->f16_down_ok) {
+      float* hf = reinterpret_cast<float*>(b + W.hc);
+      rc = mnw_moe_quantize_act(MNW_ACT_F16_ROWS, b + W.h, P, I, nullptr, 1, b + W.ha, nullptr, hf, stream);
+      if (rc) return rc;
+      rc = gemm_for(L, kActF16Rows, MNW_KIND_DOWN, b + W.ha, hf, nullptr, offs, P, b + W.y, err, sched_dn, st);
+    } else {
+      rc = gemm_for(L, act, MNW_KIND_DOWN, b + W.h, nullptr, nullptr, offs, P, b + W.y, err, sched_dn, st);
+    }
     if (rc) return rc;
   } else {
     rc = mnw_moe_permute(ids, T, k, L->E, offs, sorted, pos, nullptr, 0, nullptr, err, stream);

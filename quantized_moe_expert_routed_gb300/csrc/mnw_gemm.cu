@@ -56,7 +56,10 @@
 namespace mnw {
 
 enum { WF_BF16 = 0, WF_INT8 = 1, WF_INT4 = 2, WF_NVFP4 = 3 };
-enum { AM_BF16 = 0, AM_INT8 = 1, AM_FP4 = 2 };
+// AM_F16S: activations already in FP16 with a power-of-two factor per row
+// (launch_gather_f16); INT weights are dequantised to FP16 q * s by the
+// converters, so one accumulator covers the whole K (used by the forward path).
+enum { AM_BF16 = 0, AM_INT8 = 1, AM_FP4 = 2, AM_F16S = 3 };
 
 constexpr int kBM = 128;
 constexpr int kConvWarps = 8;
@@ -164,7 +167,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                     const GemmArgs args) {
   using T = WT<WF>;
   constexpr int kNmat = kGateUp ? 2 : 1;
-  constexpr bool kBconv = AM != AM_BF16;
+  constexpr bool kBconv = AM == AM_INT8 || AM == AM_FP4;  // tokens converted by the converter warps
+  constexpr bool kScaleConv = AM == AM_F16S;              // converters apply the FP16 group scales
   // Grouped: one accumulator per 128-wide K group, rescaled in FP32 (INT weights).
   constexpr bool kGrouped = AM == AM_INT8 || (AM == AM_BF16 && T::kScales);
   constexpr bool kBf16Mma = AM == AM_BF16;
@@ -202,7 +206,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(&bars->sfull[i], 1);
-      mbar_init(&bars->sempty[i], kEpiWarps);
+      mbar_init(&bars->sempty[i], kScaleConv ? kConvWarps : kEpiWarps);
     }
     mbar_init(&bars->final_mma, 1);
     bars->abort = 0;
@@ -265,7 +269,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       bool ok = true;
       const uint32_t a_bytes = kNmat * 16384u + (WF == WF_NVFP4 ? kNmat * 2048u : 0u);
       uint32_t b_bytes;
-      if (AM == AM_BF16) b_bytes = T::kSub * BN * 128u;
+      if (AM == AM_BF16 || AM == AM_F16S) b_bytes = T::kSub * BN * 128u;
       else if (AM == AM_INT8) b_bytes = (T::kStage / 128) * BN * 128u;
       else b_bytes = BN * 128u + BN * 16u;
       const uint32_t tx = a_bytes + b_bytes;
@@ -296,7 +300,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             tma_load_3d(st + args.off_asf[0], &tmS0, &bars->full[s], ks * 16, n0, x.e);
             if (kGateUp) tma_load_3d(st + args.off_asf[1], &tmS1, &bars->full[s], ks * 16, n0, x.e);
           }
-          if (AM == AM_BF16) {
+          if (AM == AM_BF16 || AM == AM_F16S) {
             for (int b = 0; b < T::kSub; ++b)
               tma_load_2d(st + args.off_b + b * BN * 128, &tmB, &bars->full[s], ks * T::kStage + b * 64, x.row0);
           } else if (AM == AM_INT8) {
@@ -419,7 +423,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     RingPos sp, ap, bp;  // stages, operand-A slots, token slots
     bool ok = true;
     if (T::kTs || kBconv) {
-      for (int u = blockIdx.x; ok && u < units; u += gridDim.x) {
+      for (uint32_t uit = 0, u = blockIdx.x; ok && static_cast<int>(u) < units; u += gridDim.x, ++uit) {
+        // FP16 operand mode: this unit's FP16 group scales, applied here to the weights
+        const uint32_t sbuf = uit & 1;
+        if (kScaleConv && !bounded_wait(&bars->sfull[sbuf], (uit >> 1) & 1, abort, args.err)) { ok = false; break; }
         for (int ks = 0; ks < nks; ++ks, sp.advance(S_)) {
           const int s = sp.slot;
           if (!bounded_wait(&bars->full[s], sp.phase, abort, args.err)) { ok = false; break; }
@@ -485,7 +492,17 @@ __global__ void __launch_bounds__(kThreads, 1)
                   const uint4 v0 = lds128(sw128(abase, r, kin >> 4));  // 32 codes = two chunks
                   const uint4 v1 = lds128(sw128(abase, r, (kin >> 4) + 1));
                   cvt_int8x32<AM == AM_BF16>(v0, v1, o);
-                } else {  // NVFP4
+                }
+                if (kScaleConv && (WF == WF_INT4 || WF == WF_INT8)) {
+                  // exact FP16 integers q -> fp16(q * s), s the row's scale of this 128-K group
+                  const __half* scl = reinterpret_cast<const __half*>(smem + args.off_scales +
+                                                                      (sbuf * kNmat + m) * args.scale_mat_bytes);
+                  const uint32_t sh = __half_as_ushort(scl[r * G + ((ks * T::kStage + kin) >> 7)]);
+                  const uint32_t s2 = sh | (sh << 16);
+#pragma unroll
+                  for (int i = 0; i < 16; ++i) o[i] = f16x2_mul(o[i], s2);
+                }
+                if (WF == WF_NVFP4) {  // NVFP4
                   const uint4 v = lds128(sw128(abase, r, kin >> 5));
                   uint32_t sfp;
                   asm volatile("ld.shared.u16 %0, [%1];" : "=r"(sfp) : "r"(st + args.off_asf[m] + r * 16 + (kin >> 4)));
@@ -502,6 +519,10 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           __syncwarp();
           if (lane == 0) mbar_arrive(&bars->empty[s]);
+        }
+        if (kScaleConv && ok) {
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&bars->sempty[sbuf]);
         }
       }
     }
@@ -556,10 +577,14 @@ __global__ void __launch_bounds__(kThreads, 1)
               if (AM == AM_FP4) {
                 oa = __ldg(args.a_outer + x.row0 + j);
                 gv = gv * (ow[0] * oa);
+              } else if (AM == AM_F16S) {
+                oa = __ldg(args.a_outer + x.row0 + j);  // the row's 2^e
+                gv = gv * oa;
               }
               if (kGateUp) {
                 float uv = __uint_as_float(up[i]);
                 if (AM == AM_FP4) uv = uv * (ow[1] * oa);
+                else if (AM == AM_F16S) uv = uv * oa;
                 val = __fdividef(gv, 1.f + __expf(-gv)) * uv;
               } else {
                 val = gv;
@@ -702,7 +727,7 @@ bool plan_smem(int wf, int am, bool gate_up, int K, int E, int BN, Plan* p) {
   }
   off = align_up(off, 1024);
   a.off_b = off;
-  if (am == AM_BF16) off += (kstage / 64) * BN * 128;  // BF16 tokens are copied in operand layout
+  if (am == AM_BF16 || am == AM_F16S) off += (kstage / 64) * BN * 128;  // 16-bit tokens copied in operand layout
   off = align_up(off, 1024);
   a.off_braw = off;
   if (am == AM_INT8) off += (kstage / 128) * BN * 128;
@@ -721,7 +746,7 @@ bool plan_smem(int wf, int am, bool gate_up, int K, int E, int BN, Plan* p) {
   const uint32_t cpw = BN >= 32 ? BN / 2 : BN;  // token columns per epilogue warp
   const uint32_t sa = am == AM_INT8 ? align_up(kEpiWarps * cpw * G * 4u, 16) : 0u;
   const uint32_t bars = align_up(sizeof(Bars), 16);
-  const uint32_t bring = am != AM_BF16 ? kBSlots * BN * 128u : 0u;  // converted-token ring
+  const uint32_t bring = (am == AM_INT8 || am == AM_FP4) ? kBSlots * BN * 128u : 0u;  // converted-token ring
   fixed = bring + scales + tab + sa + bars;
   const size_t budget = kSmemLimit - 1024;  // alignment slack
   if (fixed + 2 * a.stage_bytes > budget) return false;
@@ -773,6 +798,9 @@ int run_gemm(const mnw_moe_layer* L, int wfmt, int act, int kind, const void* a0
   if (!a0 || !offsets || !out || !aligned(a0, 16) || !aligned(out, 16)) return MNW_E_INVALID_ARG;
   if (act == MNW_ACT_INT8_G128 && (!a1 || !aligned(a1, 16))) return MNW_E_INVALID_ARG;
   if (act == MNW_ACT_NVFP4_G16 && (!a1 || !a2 || !aligned(a1, 16) || !aligned(a2, 16))) return MNW_E_INVALID_ARG;
+  // the FP16 operand mode: INT weights, row factors in a1
+  if (act == kActF16Rows && ((wfmt != MNW_FMT_INT8_G128 && wfmt != MNW_FMT_INT4_G128) || !a1 || !aligned(a1, 4)))
+    return MNW_E_INVALID_ARG;
   // INT8/INT4 weights with few tokens per expert: the warp-MMA kernel (see
   // mnw_gemm_warp.cu for why).  From 32 tokens per expert on average the
   // tcgen05 kernel below is as fast or faster (measured on GB300: 64 tokens
@@ -780,7 +808,7 @@ int run_gemm(const mnw_moe_layer* L, int wfmt, int act, int kind, const void* a0
   // 1036 vs 1463 us), and BF16/NVFP4 weights always use it.
   const int mean_rows = (P + L->E - 1) / L->E;
   const int path = gemm_path();
-  const bool warp_ok = warp_gemm_applicable(L, wfmt, act, kind);
+  const bool warp_ok = act != kActF16Rows && warp_gemm_applicable(L, wfmt, act, kind);
   if (warp_ok && (path == MNW_PATH_WARP_MMA || (path == MNW_PATH_AUTO && mean_rows < 32))) {
     const int nt = mean_rows <= 4 ? 1 : (mean_rows <= 16 ? 2 : 4);
     return run_gemm_warp(L, wfmt, act, kind, a0, a1, offsets, P, nt, out, dots, err, sched, st);
@@ -789,7 +817,7 @@ int run_gemm(const mnw_moe_layer* L, int wfmt, int act, int kind, const void* a0
   const int K = gate_up ? L->H : L->I;
   const int N = gate_up ? L->I : L->H;
   const int nmat = gate_up ? 2 : 1;
-  const int am = act;  // MNW_ACT_* match AM_*
+  const int am = act;  // MNW_ACT_* match AM_*; kActF16Rows is AM_F16S
   const int wf = wfmt;
 
   // Token tile: the power of two (16..max) nearest above the mean rows per expert.
@@ -847,7 +875,7 @@ int run_gemm(const mnw_moe_layer* L, int wfmt, int act, int kind, const void* a0
     a.outer_off[m] = L->outer_off[m0 + m];
   }
   a.a_scales = am == AM_INT8 ? static_cast<const float*>(a1) : nullptr;
-  a.a_outer = am == AM_FP4 ? static_cast<const float*>(a2) : nullptr;
+  a.a_outer = am == AM_FP4 ? static_cast<const float*>(a2) : (am == AM_F16S ? static_cast<const float*>(a1) : nullptr);
   a.out = static_cast<__nv_bfloat16*>(out);
   a.dots = am == AM_INT8 ? dots : nullptr;
   a.err = err;
@@ -863,11 +891,12 @@ int run_gemm(const mnw_moe_layer* L, int wfmt, int act, int kind, const void* a0
   }
   const uint64_t Pu = static_cast<uint64_t>(P);
   bool ok;
-  if (am == AM_BF16) {
+  if (am == AM_BF16 || am == AM_F16S) {
     const uint64_t dims[2] = {static_cast<uint64_t>(K), Pu};
     const uint64_t strides[1] = {static_cast<uint64_t>(K) * 2};
     const uint32_t box[2] = {64, static_cast<uint32_t>(BN)};
-    ok = encode_map(&maps[4], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, a0, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_128B);
+    ok = encode_map(&maps[4], am == AM_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, a0,
+                    dims, strides, box, CU_TENSOR_MAP_SWIZZLE_128B);
   } else if (am == AM_INT8) {
     const uint64_t dims[2] = {static_cast<uint64_t>(K), Pu};
     const uint64_t strides[1] = {static_cast<uint64_t>(K)};
@@ -888,13 +917,15 @@ int run_gemm(const mnw_moe_layer* L, int wfmt, int act, int kind, const void* a0
 
   const int grid = L->num_sms;
   cudaError_t e = cudaErrorInvalidValue;
-  switch (wf * 3 + am) {
-    case WF_BF16 * 3 + AM_BF16: e = launch_kind<WF_BF16, AM_BF16>(gate_up, maps, a, plan.smem, grid, st); break;
-    case WF_INT8 * 3 + AM_BF16: e = launch_kind<WF_INT8, AM_BF16>(gate_up, maps, a, plan.smem, grid, st); break;
-    case WF_INT4 * 3 + AM_BF16: e = launch_kind<WF_INT4, AM_BF16>(gate_up, maps, a, plan.smem, grid, st); break;
-    case WF_INT8 * 3 + AM_INT8: e = launch_kind<WF_INT8, AM_INT8>(gate_up, maps, a, plan.smem, grid, st); break;
-    case WF_INT4 * 3 + AM_INT8: e = launch_kind<WF_INT4, AM_INT8>(gate_up, maps, a, plan.smem, grid, st); break;
-    case WF_NVFP4 * 3 + AM_FP4: e = launch_kind<WF_NVFP4, AM_FP4>(gate_up, maps, a, plan.smem, grid, st); break;
+  switch (wf * 4 + am) {
+    case WF_BF16 * 4 + AM_BF16: e = launch_kind<WF_BF16, AM_BF16>(gate_up, maps, a, plan.smem, grid, st); break;
+    case WF_INT8 * 4 + AM_BF16: e = launch_kind<WF_INT8, AM_BF16>(gate_up, maps, a, plan.smem, grid, st); break;
+    case WF_INT4 * 4 + AM_BF16: e = launch_kind<WF_INT4, AM_BF16>(gate_up, maps, a, plan.smem, grid, st); break;
+    case WF_INT8 * 4 + AM_INT8: e = launch_kind<WF_INT8, AM_INT8>(gate_up, maps, a, plan.smem, grid, st); break;
+    case WF_INT4 * 4 + AM_INT8: e = launch_kind<WF_INT4, AM_INT8>(gate_up, maps, a, plan.smem, grid, st); break;
+    case WF_NVFP4 * 4 + AM_FP4: e = launch_kind<WF_NVFP4, AM_FP4>(gate_up, maps, a, plan.smem, grid, st); break;
+    case WF_INT8 * 4 + AM_F16S: e = launch_kind<WF_INT8, AM_F16S>(gate_up, maps, a, plan.smem, grid, st); break;
+    case WF_INT4 * 4 + AM_F16S: e = launch_kind<WF_INT4, AM_F16S>(gate_up, maps, a, plan.smem, grid, st); break;
     default: return MNW_E_MODE;
   }
   return e == cudaSuccess ? MNW_OK : MNW_E_CUDA;

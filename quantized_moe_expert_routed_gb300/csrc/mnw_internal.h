@@ -14,6 +14,10 @@ struct mnw_moe_layer {
   uint64_t data_offset, expert_stride;
   uint64_t codes_off[3], scales_off[3], outer_off[3];
   int device, num_sms;
+  // INT weights: every fp16(q * s) of the gate/up (resp. down) matrices is
+  // finite and normal (checked once at init), so those GEMMs may run on FP16
+  // operands.
+  bool f16_gate_up_ok, f16_down_ok;
   // Weight tensor maps (built once): codes per matrix, NVFP4 block scales per matrix.
   CUtensorMap tm_codes[3];
   CUtensorMap tm_sf[3];
@@ -31,6 +35,9 @@ int current_sm_count();
 // overlaps that kernel's tail), and waits for that kernel's completion with
 // pdl_wait() before it touches global memory.  After a non-kernel stream
 // operation (a copy, a memset, an event) the launch is an ordinary one.
+// Count of kernels this library has enqueued (mnw_moe_launch_count).
+void note_launch();
+
 template <typename... KArgs, typename... Args>
 cudaError_t launch_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t st,
                        Args&&... args) {
@@ -44,7 +51,9 @@ cudaError_t launch_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t sme
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, kern, static_cast<Args&&>(args)...);
+  const cudaError_t e = cudaLaunchKernelEx(&cfg, kern, static_cast<Args&&>(args)...);
+  if (e == cudaSuccess) note_launch();
+  return e;
 }
 
 // Encode a tiled tensor map; returns false on failure.
@@ -55,6 +64,10 @@ bool encode_map(CUtensorMap* map, CUtensorMapDataType dtype, int rank, const voi
 cudaError_t launch_permute(const int32_t* ids, int T, int k, int E, int32_t* offsets, int32_t* sorted_assign,
                            int32_t* assign_pos, const void* x, int H, void* x_perm, uint32_t* err,
                            cudaStream_t st);
+// MNW_ACT_F16_ROWS encoding of P rows (row p reads x[row_index[p] / div], or
+// x[p] without row_index): FP16 codes into x_perm, power-of-two factors.
+cudaError_t launch_gather_f16(const void* x, int H, const int32_t* row_index, int P, int div, void* x_perm,
+                              float* factor, cudaStream_t st);
 cudaError_t launch_combine(const void* y, const int32_t* assign_pos, const float* w, int T, int k, int H,
                            void* out, cudaStream_t st);
 cudaError_t launch_quantize(int act, const void* x, int R, int K, const int32_t* row_index, int index_div,
@@ -64,6 +77,9 @@ cudaError_t launch_quantize(int act, const void* x, int R, int K, const int32_t*
 // (row_index = assign_pos, index_div = k).
 cudaError_t launch_quantize_scatter(int act, const void* x, int R, int K, const int32_t* row_index, int index_div,
                             void* codes, void* scales, float* row_outer, cudaStream_t st);
+// Activation mode of the FP16 operand gate/up GEMM (INT weights): a0 = FP16
+// rows from launch_gather_f16, a1 = their float factors.
+constexpr int kActF16Rows = MNW_ACT_F16_ROWS;
 // Grouped GEMM for weight format wfmt and activation mode act.
 // sched (nullable): a zeroed device counter that lets the kernel's CTAs claim
 // work units dynamically; NULL gives a static round-robin order.

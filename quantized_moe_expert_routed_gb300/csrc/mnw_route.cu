@@ -10,6 +10,7 @@
 // re-walks the segment in order, ranking lanes that share an expert by lane
 // index.
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
 
 #include <algorithm>
 
@@ -458,6 +459,60 @@ __global__ void __launch_bounds__(256) gather_rows_kernel(const uint4* __restric
   }
 }
 
+// FP16 rows with a power-of-two row factor, the operand form of the FP16
+// gate/up GEMM: row p reads x[src] with src = row_index[p] / div (src = p
+// without row_index), writes x_perm[p] = fp16_rn(x[src] * 2^-e_p) and
+// factor[p] = 2^e_p, e_p = clamp(floor(log2 amax) - 14, -110, 113).  The
+// largest magnitude lands in [2^14, 2^15); FP16 holds every BF16 value of the
+// row no more than 2^28 below it exactly, so the GEMM sees the activations
+// unchanged up to the factor its epilogue multiplies back.  A negative
+// row_index gives a zero row with factor 1.  One warp per row.
+__global__ void __launch_bounds__(256) gather_rows_f16_kernel(const uint4* __restrict__ x, int H8,
+                                                              const int32_t* __restrict__ row_index, int P,
+                                                              int div, uint4* __restrict__ x_perm,
+                                                              float* __restrict__ factor) {
+  pdl_launch_dependents();
+  pdl_wait();
+  const int warps = gridDim.x * 8, lane = threadIdx.x & 31;
+  for (int p = blockIdx.x * 8 + (threadIdx.x >> 5); p < P; p += warps) {
+    const int a = row_index ? __ldg(row_index + p) : p;
+    uint4* dst = x_perm + static_cast<size_t>(p) * H8;
+    if (a < 0) {
+      for (int c = lane; c < H8; c += 32) dst[c] = make_uint4(0, 0, 0, 0);
+      if (lane == 0) factor[p] = 1.f;
+      continue;
+    }
+    const uint4* src = x + static_cast<size_t>(a / div) * H8;
+    uint32_t m = 0;  // largest |x| as BF16 bits (magnitudes order like their bit patterns)
+    for (int c = lane; c < H8; c += 32) {
+      const uint4 v = __ldg(src + c);
+      m = max(m, max(max(v.x & 0x7FFFu, v.x >> 16 & 0x7FFFu), max(v.y & 0x7FFFu, v.y >> 16 & 0x7FFFu)));
+      m = max(m, max(max(v.z & 0x7FFFu, v.z >> 16 & 0x7FFFu), max(v.w & 0x7FFFu, v.w >> 16 & 0x7FFFu)));
+    }
+#pragma unroll
+    for (int d = 16; d > 0; d >>= 1) m = max(m, __shfl_xor_sync(0xffffffffu, m, d));
+    // floor(log2 amax) - 14: the row's largest magnitude lands in [2^14, 2^15),
+    // away from both FP16 overflow and FP16 subnormals.  Clamped so that 2^e
+    // and 2^-e are normal FP32 numbers (an all-zero row gets e = -110; the
+    // largest finite BF16 needs 113).
+    const int e = min(113, max(-110, static_cast<int>(m >> 7) - 141));
+    const float down = __uint_as_float(static_cast<uint32_t>(127 - e) << 23);
+    for (int c = lane; c < H8; c += 32) {
+      const uint4 v = __ldg(src + c);
+      const uint32_t wv[4] = {v.x, v.y, v.z, v.w};
+      uint32_t o[4];
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        const float lo = __uint_as_float(wv[q] << 16) * down, hi = __uint_as_float(wv[q] & 0xFFFF0000u) * down;
+        __half2 h = __floats2half2_rn(lo, hi);
+        o[q] = *reinterpret_cast<uint32_t*>(&h);
+      }
+      dst[c] = make_uint4(o[0], o[1], o[2], o[3]);
+    }
+    if (lane == 0) factor[p] = __uint_as_float(static_cast<uint32_t>(127 + e) << 23);
+  }
+}
+
 // out[t] = bf16(sum_j w[t, j] * y[assign_pos[t*k + j]]), FP32, j ascending.
 // One thread per (token, 8 columns); the k row loads of a thread are issued
 // before any of them is consumed (up to 8 in flight), so the kernel runs at
@@ -571,6 +626,13 @@ cudaError_t launch_combine(const void* y, const int32_t* assign_pos, const float
   const int blocks = static_cast<int>(std::min<long long>((threads + 255) / 256, static_cast<long long>(sms) * 16));
   return launch_pdl(combine_kernel, dim3(blocks < 1 ? 1 : blocks), dim3(256), 0, st, static_cast<const uint4*>(y),
                     assign_pos, w, T, k, H / 8, static_cast<uint4*>(out));
+}
+
+cudaError_t launch_gather_f16(const void* x, int H, const int32_t* row_index, int P, int div, void* x_perm,
+                              float* factor, cudaStream_t st) {
+  const int sms = current_sm_count();
+  return launch_pdl(gather_rows_f16_kernel, dim3(grid_for(8, P, sms * 8)), dim3(256), 0, st, static_cast<const uint4*>(x),
+                    H / 8, row_index, P, div, static_cast<uint4*>(x_perm), factor);
 }
 
 }  // namespace mnw

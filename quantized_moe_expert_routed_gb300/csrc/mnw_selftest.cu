@@ -46,5 +46,7 @@ extern "C" int mnw_moe_selftest_wait_timeout(uint32_t limit_us, uint32_t* err, u
   if (!err || !left_early || limit_us == 0 || limit_us > 1000000u) return MNW_E_INVALID_ARG;
   mnw::wait_timeout_kernel<<<1, 64, 0, static_cast<cudaStream_t>(stream)>>>(static_cast<uint64_t>(limit_us) * 1000u,
                                                                             err, left_early);
-  return cudaGetLastError() == cudaSuccess ? MNW_OK : MNW_E_CUDA;
+  if (cudaGetLastError() != cudaSuccess) return MNW_E_CUDA;
+  mnw::note_launch();
+  return MNW_OK;
 }

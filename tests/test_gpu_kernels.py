@@ -244,3 +244,85 @@ def test_warp_and_tcgen05_paths_agree_bitwise(M, wfmt, act, T, k, E):
     else:
         oh = O.gemm_a8(blob.numpy(), O.KIND_GATE_UP, q.cpu().numpy(), s.cpu().numpy(), o_off)
     assert_close(h1, oh, what="warp path gate_up")
+
+
+# ---- FP16 row form: INT8/INT4 weights, BF16 activations on FP16 tensor cores -----
+
+def _f16_row_inputs(R, K, seed):
+    """Activations with rows far from unit scale: tiny, huge, zero, and one
+    holding the largest finite BF16 magnitude."""
+    x = S.activations(R, K, seed=seed).float()
+    for r, f in ((2, 1e-20), (4, 1e25), (6, 0.0), (9, 3e-3)):
+        if r < R:
+            x[r] *= f
+    x = x.to(torch.bfloat16)
+    if R > 7:
+        x.view(torch.int16)[7, 1] = 0x7F7F
+    return x
+
+
+@pytest.mark.parametrize("R,K,gather", [(1, 128, False), (37, 512, False), (300, 2048, True), (64, 7168, True)])
+def test_quantize_f16_rows_bitexact(M, R, K, gather):
+    x = _f16_row_inputs(R, K, seed=R + 3)
+    idx = None
+    src = x
+    if gather:
+        idx = torch.arange(R * 2, dtype=torch.int32).flip(0)[:R].contiguous()
+        idx[5] = -1
+        src = torch.zeros_like(x)
+        for r in range(R):
+            if idx[r] >= 0:
+                src[r] = x[int(idx[r]) // 2]
+    codes, outer = M.mnw_moe_quantize_act(M.ACT_F16_ROWS, x.to(DEV),
+                                          row_index=None if idx is None else idx.to(DEV), index_div=2, rows=R)
+    oc, of = O.encode_f16_rows(S.bf16_bits_np(src))
+    if idx is not None:
+        dropped = (idx < 0).numpy()
+        oc[dropped] = 0
+        of[dropped] = 1.0  # a negative row index: zero codes, factor 1
+    assert np.array_equal(codes.cpu().view(torch.int16).numpy().view(np.uint16), oc)
+    assert np.array_equal(outer.cpu().numpy().view(np.uint32), of.view(np.uint32))
+
+
+@pytest.mark.parametrize("wfmt,fn", [(S.FMT_INT8_G128, "mnw_moe_grouped_gemm_w8a16_f16rows"),
+                                     (S.FMT_INT4_G128, "mnw_moe_grouped_gemm_w4a16_f16rows")])
+@pytest.mark.parametrize("shape", SHAPES + [(16, 1024, 512, 400, 4)])
+def test_gemm_f16rows(M, wfmt, fn, shape):
+    E, H, I, T, k = shape
+    blob, hdr, ids, x = _setup(wfmt, E, H, I, T, k, seed=17 * wfmt + T)
+    layer = M.Layer(blob.to(DEV), hdr)
+    off, sa, pos, xp = M.mnw_moe_permute(ids.to(DEV), E, x=x.to(DEV))
+    a, f = M.mnw_moe_quantize_act(M.ACT_F16_ROWS, x.to(DEV), row_index=sa, index_div=k)
+    err = torch.zeros(1, dtype=torch.int32, device=DEV)
+    h = getattr(M, fn)(layer, M.KIND_GATE_UP, a, f, off, err=err)
+    assert int(err.item()) == 0
+    o_off = off.cpu().numpy()
+    oh = O.gemm_f16rows(blob.numpy(), O.KIND_GATE_UP, a.cpu().view(torch.int16).numpy().view(np.uint16),
+                        f.cpu().numpy(), o_off)
+    assert_close(h, oh, what=f"{fn} gate_up")
+    ha, hf = M.mnw_moe_quantize_act(M.ACT_F16_ROWS, h)
+    y = getattr(M, fn)(layer, M.KIND_DOWN, ha, hf, off, err=err)
+    assert int(err.item()) == 0
+    oy = O.gemm_f16rows(blob.numpy(), O.KIND_DOWN, ha.cpu().view(torch.int16).numpy().view(np.uint16),
+                        hf.cpu().numpy(), o_off)
+    assert_close(y, oy, what=f"{fn} down")
+
+
+def test_gemm_f16rows_rejects_bad_kind_format_and_out_of_range_scales(M):
+    E, H, I, T, k = 4, 256, 256, 16, 2
+    blob, hdr, ids, x = _setup(S.FMT_INT8_G128, E, H, I, T, k, seed=21)
+    layer = M.Layer(blob.to(DEV), hdr)
+    off, sa, pos, _ = M.mnw_moe_permute(ids.to(DEV), E)
+    a, f = M.mnw_moe_quantize_act(M.ACT_F16_ROWS, x.to(DEV), row_index=sa, index_div=k)
+    with pytest.raises(M.MnwError, match="invalid"):
+        M.mnw_moe_grouped_gemm_w8a16_f16rows(layer, 7, a, f, off)
+    with pytest.raises(M.MnwError, match="mode not allowed"):
+        M.mnw_moe_grouped_gemm_w4a16_f16rows(layer, M.KIND_GATE_UP, a, f, off)  # INT8 layer
+    # scales near 65504 / 127: some fp16(q * s) would overflow
+    big, hdr_b, _ = S.expert_blob(S.FMT_INT8_G128, E, H, I, seed=22, sigma=5.0e4)
+    with pytest.raises(M.MnwError, match="unsupported"):
+        M.mnw_moe_grouped_gemm_w8a16_f16rows(M.Layer(big.to(DEV), hdr_b), M.KIND_GATE_UP, a, f, off)
+    # scales below 2^-14: some fp16(q * s) would be subnormal
+    tiny, hdr_t, _ = S.expert_blob(S.FMT_INT4_G128, E, H, I, seed=23, sigma=1.0e-6)
+    with pytest.raises(M.MnwError, match="unsupported"):
+        M.mnw_moe_grouped_gemm_w4a16_f16rows(M.Layer(tiny.to(DEV), hdr_t), M.KIND_GATE_UP, a, f, off)

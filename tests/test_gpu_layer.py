@@ -82,3 +82,45 @@ def test_deterministic_and_bad_ids(M):
     ws = M.workspace(layer, wl.act, wl.T, wl.k)
     M.mnw_moe_forward(layer, wl.act, x, ids2, w, ws=ws)
     assert M.mnw_moe_read_error(M.workspace_error_word(ws)) & M.DEVERR_BAD_EXPERT_ID
+
+
+def _run_custom(M, wl, x_scale_rows=None, relative_only=False):
+    """Whole layer vs the oracle on every row.  Rows far from unit scale (the
+    rescaled ones, or all of them with relative_only) are held to the relative
+    L2 bound row by row; the others to both stated bounds."""
+    x, ids, w, blob, hdr, L = S.make_inputs(wl, device=DEV)
+    big = sorted(x_scale_rows or {})
+    for r in big:
+        x[r] = (x[r].float() * x_scale_rows[r]).to(torch.bfloat16)
+    layer = M.Layer(blob, hdr)
+    ws = M.workspace(layer, wl.act, wl.T, wl.k)
+    out = M.mnw_moe_forward(layer, wl.act, x, ids, w, ws=ws)
+    assert M.mnw_moe_read_error(M.workspace_error_word(ws)) == 0
+    want = O.moe_forward(blob.cpu().numpy(), wl.act, S.bf16_bits_np(x), ids.cpu().numpy(), w.cpu().numpy(),
+                         rows=np.arange(wl.T, dtype=np.int32))
+    got = out.detach().float().cpu().double().numpy()
+    ref = torch.from_numpy(np.ascontiguousarray(want).view(np.int16).copy()).view(torch.bfloat16).double().numpy()
+    assert np.all(np.isfinite(got)), wl.name
+    per_row = [r for r in range(wl.T) if relative_only or r in big]
+    for r in per_row:
+        rel = np.linalg.norm(got[r] - ref[r]) / max(np.linalg.norm(ref[r]), 1e-30)
+        assert rel <= REL_L2, f"{wl.name}: row {r} rel_l2={rel:.3e}"
+    normal = [r for r in range(wl.T) if r not in per_row]
+    if normal:
+        idx = torch.tensor(normal, device=DEV)
+        assert_close(out[idx], np.ascontiguousarray(want[normal]), rel_l2=REL_L2, what=wl.name)
+
+
+@pytest.mark.parametrize("wfmt", [S.FMT_INT8_G128, S.FMT_INT4_G128])
+def test_fp16_operand_path(M, wfmt):
+    """INT weights with 64 tokens per expert: the forward path runs gate/up on
+    FP16 operands (rows scaled by powers of two, weights fp16(q * s)); rows far
+    outside FP16's range exercise the row factors."""
+    wl = S.Workload("fp16_path", 256, 512, 16, 256, 4, wfmt, S.ACT_BF16, 0.02, "uniform", 11)
+    _run_custom(M, wl, x_scale_rows={3: 3.0e5, 77: 1.0e9, 200: 1.0e-6})
+
+
+def test_fp16_operand_path_falls_back_for_large_scales(M):
+    """Weights whose fp16(q * s) could overflow keep the exact grouped path."""
+    wl = S.Workload("big_scales", 256, 512, 16, 256, 4, S.FMT_INT8_G128, S.ACT_BF16, 5.0e4, "uniform", 12)
+    _run_custom(M, wl, relative_only=True)
