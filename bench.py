@@ -170,14 +170,16 @@ def run_ours(args, wl):
         if rc != 0:
             raise RuntimeError(f"{what} failed: {lib.mnw_status_string(rc).decode()}")
 
-    # INT weights with BF16 activations and enough tokens per expert for the
-    # tcgen05 kernel: the forward runs gate/up on FP16 rows (row factor in xf),
-    # so the stepwise sequence and the roofline loop do the same.
+    # INT weights with BF16 activations: the forward runs gate/up on FP16 rows
+    # (row factor in xf), and down too once there are enough tokens per expert
+    # for the tcgen05 kernel, so the stepwise sequence and the roofline loop
+    # do the same.
     f16_gate_up = f16_down = None
-    if wl.act == S.ACT_BF16 and wl.wfmt in (S.FMT_INT8_G128, S.FMT_INT4_G128) and -(-P // E) >= 32:
+    if wl.act == S.ACT_BF16 and wl.wfmt in (S.FMT_INT8_G128, S.FMT_INT4_G128):
         f16 = getattr(lib, f"mnw_moe_grouped_gemm_{gemm_name}_f16rows")
         # a zero-row call reports whether the layer's scales allow the FP16 form
         allowed = [f16(layer.handle, kind, None, None, None, 0, None, None, sp) == 0 for kind in (0, 1)]
+        allowed[1] = allowed[1] and -(-P // E) >= 32
         if allowed[0]:
             f16_gate_up = f16
             xa = torch.empty((P, wl.H), dtype=torch.float16, device=dev)

@@ -178,7 +178,10 @@ int mnw_moe_grouped_gemm_w4a16(const mnw_moe_layer* layer, int kind, const void*
  * out = bf16(f * (a . Wd^T)).  MNW_E_UNSUPPORTED when some q * s of the
  * matrices used would leave FP16's normal range (a scale above 65504 / qmax,
  * qmax = 127 or 8, or a non-zero scale below 2^-14); mnw_moe_forward then
- * keeps the BF16 form for that GEMM.  Always the tcgen05 kernel. */
+ * keeps the BF16 form for that GEMM.  Kernel choice as for the other INT
+ * entries: below 32 tokens per expert on average the warp-MMA kernel, where
+ * the codes stay exact FP16 integers and each group's FP32 dot product is
+ * scaled by s afterwards (no fp16(q * s) rounding there). */
 int mnw_moe_grouped_gemm_w8a16_f16rows(const mnw_moe_layer* layer, int kind, const void* a,
                                        const float* row_outer, const int32_t* expert_offsets, int P,
                                        void* out, uint32_t* err, mnw_stream stream);

@@ -469,14 +469,15 @@ int mnw_moe_forward(const mnw_moe_layer* L, int act, const void* x, const int32_
   if (cudaMemsetAsync(err, 0, 256, st) != cudaSuccess) return MNW_E_CUDA;
   int rc;
   if (act == MNW_ACT_BF16) {
-    // INT weights on the tcgen05 kernel (enough tokens per expert): the GEMMs
-    // run on FP16 operands -- rows scaled into FP16 range by a power of two,
-    // weights dequantised on chip to fp16(q * s) -- so one accumulator spans
-    // all of K instead of one per 128-K group.
+    // INT weights: the GEMMs run on FP16 rows (scaled into FP16 range by a
+    // power of two per row).  On the tcgen05 kernel (enough tokens per
+    // expert) the weights are dequantised on chip to fp16(q * s), so one
+    // accumulator spans all of K; on the warp-MMA kernel the INT4 codes
+    // convert to FP16 operands in fewer instructions than to BF16.
     const int mean_rows = (P + L->E - 1) / L->E;
     const int path = gemm_path();
     const bool tc = path != MNW_PATH_WARP_MMA && (path == MNW_PATH_TCGEN05 || mean_rows >= 32);
-    if (tc && L->f16_gate_up_ok) {
+    if (L->f16_gate_up_ok) {
       rc = mnw_moe_permute(ids, T, k, L->E, offs, sorted, pos, nullptr, 0, nullptr, err, stream);
       if (rc) return rc;
       float* factor = reinterpret_cast<float*>(b + W.xc);

@@ -808,7 +808,7 @@ int run_gemm(const mnw_moe_layer* L, int wfmt, int act, int kind, const void* a0
   // 1036 vs 1463 us), and BF16/NVFP4 weights always use it.
   const int mean_rows = (P + L->E - 1) / L->E;
   const int path = gemm_path();
-  const bool warp_ok = act != kActF16Rows && warp_gemm_applicable(L, wfmt, act, kind);
+  const bool warp_ok = warp_gemm_applicable(L, wfmt, act, kind);
   if (warp_ok && (path == MNW_PATH_WARP_MMA || (path == MNW_PATH_AUTO && mean_rows < 32))) {
     const int nt = mean_rows <= 4 ? 1 : (mean_rows <= 16 ? 2 : 4);
     return run_gemm_warp(L, wfmt, act, kind, a0, a1, offsets, P, nt, out, dots, err, sched, st);

@@ -27,10 +27,21 @@
 //
 // Operand mapping.  Within one 128-K group, lane (g = lane/4, t = lane%4)
 // owns K = 32t .. 32t+31 of its rows (16 contiguous code bytes for INT4, 32
-// for INT8, 64 bytes of BF16 activations).  For k-step s (0..7) its A/B
+// for INT8, 64 bytes of 16-bit activations).  For k-step s (0..7) its A/B
 // fragment slots {2t, 2t+1} hold K = 32t+4s+{0,1} and slots {2t+8, 2t+9}
 // hold K = 32t+4s+{2,3}.  A and B use the same assignment, so the dot
 // product is unchanged and no shuffle is needed.
+//
+// FP16 rows (activations fp16 with a power-of-two factor per row) with INT4
+// weights pair K differently: k-steps 2c and 2c+1 cover the 8 K of code word
+// c (K = 32t+8c .. +7, nibble i = K 8c+i), slots {2t, 2t+1} holding K
+// {0,4} / {2,6} and slots {2t+8, 2t+9} K {1,5} / {3,7} of the word.  With
+// FP16's 10-bit mantissa, one AND-XOR places nibbles 0 and 4 (or 1 and 5,
+// 16 times larger) of a word under the exponent of 1024, so a word becomes
+// four operand registers in 1 shift + 4 AND-XOR + 2 subtractions + 2 FMAs,
+// against 9 integer instructions + 4 subtractions for the BF16 operands.
+// The token fragment then takes its pairs {x_j, x_j+4} from one 16-byte load
+// by two byte permutes per register pair.
 //
 // Work unit: (expert, token tile of 8*NT rows, block of 256 weight rows).
 // gate/up: rows are 128 gate features + the same 128 up features, so each
@@ -50,7 +61,8 @@ namespace mnw {
 namespace warpmma {
 
 enum { WF_INT8 = 1, WF_INT4 = 2 };
-enum { AM_BF16 = 0, AM_INT8 = 1 };
+// AM_F16R: FP16 activation rows with a float factor per row (kActF16Rows)
+enum { AM_BF16 = 0, AM_INT8 = 1, AM_F16R = 3 };
 
 constexpr int kMmaWarps = 8;
 constexpr int kThreads = (1 + kMmaWarps) * 32;  // warp 0 = producer
@@ -72,6 +84,7 @@ struct Args {
   uint64_t scales_off[2];  // box 0 / box 1 matrices (gate, up) or (down, down)
   int box_row_off[2];      // row offset of box 1 within its matrix (0 for gate/up, 128 for down)
   const float* a_scales;   // INT8 activations: [P][K/128]
+  const float* a_outer;    // FP16 rows: the row factors [P]
   __nv_bfloat16* out;
   int32_t* dots;
   uint32_t* err;
@@ -142,6 +155,16 @@ __device__ __forceinline__ void int4_pair(uint32_t w, int p, uint32_t& lo, uint3
     hi = f16x2_sub(and_xor(x1, 0x000F000Fu, 0x64086408u), 0x64086408u);
   }
 }
+// Two FP16 operand words from INT4 code word w (nibble i = K i): K {0,4} and
+// {1,5} (odd = false) or K {2,6} and {3,7} (odd = true), exact integers.
+template <bool kOdd>
+__device__ __forceinline__ void int4_j4(uint32_t w, uint32_t& lo, uint32_t& hi) {
+  const uint32_t v = kOdd ? w >> 8 : w;
+  // 0x6400 | (n ^ 8) = 1024 + (n ^ 8); minus 1032 gives the signed code
+  lo = f16x2_sub(and_xor(v, 0x000F000Fu, 0x64086408u), 0x64086408u);
+  // 0x6400 | (n ^ 8) << 4 = 1024 + 16 (n ^ 8); times 1/16 (0x2C00) minus 72 (0xD480)
+  hi = f16x2_fma(and_xor(v, 0x00F000F0u, 0x64806480u), 0x2C002C00u, 0xD480D480u);
+}
 // Two operand words from the 4 INT8 codes of one 32-bit word.
 template <bool kBf16>
 __device__ __forceinline__ void int8_pair(uint32_t w, uint32_t& lo, uint32_t& hi) {
@@ -181,6 +204,7 @@ __device__ __forceinline__ void group_step(const Args& args, uint32_t st, uint32
                                            const __half* scl0, const __half* scl1, int w, int g, int t, int grp,
                                            int G, const Unit& x, int nb, float (&tot)[2][NT][4]) {
   constexpr bool kBf16 = AM == AM_BF16;
+  constexpr bool kJ4 = AM == AM_F16R && WF == WF_INT4;  // (j, j+4) K pairing
   // raw codes: [box i][row g / g+8]
   uint4 ar[2][2][WF == WF_INT4 ? 1 : 2];
 #pragma unroll
@@ -197,13 +221,20 @@ __device__ __forceinline__ void group_step(const Args& args, uint32_t st, uint32
     for (int j = 0; j < NTA; ++j)
 #pragma unroll
       for (int q = 0; q < 4; ++q) cg[i][j][q] = 0.f;
+  uint4 bv[NTA];  // kJ4: the 8 activations of the current code word, per n-tile
 #pragma unroll
   for (int ks = 0; ks < 8; ++ks) {
     // token operand of this k-step: K = 32t + 4ks .. +3 of each n-tile's row
+    // (kJ4: K {0,4},{1,5} or {2,6},{3,7} of K = 32t + 8(ks/2) .. +7)
     uint32_t b0[NTA], b1[NTA];
 #pragma unroll
     for (int j = 0; j < NTA; ++j) {
-      if constexpr (kBf16) {
+      if constexpr (kJ4) {
+        if ((ks & 1) == 0) bv[j] = lds128(stb + b_off[j][ks >> 1]);
+        const uint32_t p = (ks & 1) ? bv[j].y : bv[j].x, q = (ks & 1) ? bv[j].w : bv[j].z;
+        b0[j] = prmt(p, q, 0x5410u);
+        b1[j] = prmt(p, q, 0x7632u);
+      } else if constexpr (AM != AM_INT8) {
         const uint2 v = lds64(stb + b_off[j][ks >> 1] + 8 * (ks & 1));
         b0[j] = v.x;
         b1[j] = v.y;
@@ -217,8 +248,14 @@ __device__ __forceinline__ void group_step(const Args& args, uint32_t st, uint32
 #pragma unroll
       for (int hh = 0; hh < 2; ++hh) {
         uint32_t lo, hi;
-        if constexpr (WF == WF_INT4) int4_pair<kBf16>(word_of(ar[i][hh][0], ks >> 1), ks & 1, lo, hi);
-        else int8_pair<kBf16>(word_of(ar[i][hh][ks >> 2], ks & 3), lo, hi);
+        if constexpr (kJ4) {
+          if (ks & 1) int4_j4<true>(word_of(ar[i][hh][0], ks >> 1), lo, hi);
+          else int4_j4<false>(word_of(ar[i][hh][0], ks >> 1), lo, hi);
+        } else if constexpr (WF == WF_INT4) {
+          int4_pair<kBf16>(word_of(ar[i][hh][0], ks >> 1), ks & 1, lo, hi);
+        } else {
+          int8_pair<kBf16>(word_of(ar[i][hh][ks >> 2], ks & 3), lo, hi);
+        }
         a[hh] = lo;
         a[2 + hh] = hi;
       }
@@ -238,7 +275,7 @@ __device__ __forceinline__ void group_step(const Args& args, uint32_t st, uint32
     for (int j = 0; j < NTA; ++j) {
       const int tok0 = j * 8 + 2 * t;
       float f00 = sw0, f01 = sw0, f10 = sw1, f11 = sw1;
-      if constexpr (!kBf16) {
+      if constexpr (AM == AM_INT8) {
         const float sa0 = tok0 < x.nrows ? __ldg(args.a_scales + static_cast<size_t>(x.row0 + tok0) * G + grp) : 0.f;
         const float sa1 =
             tok0 + 1 < x.nrows ? __ldg(args.a_scales + static_cast<size_t>(x.row0 + tok0 + 1) * G + grp) : 0.f;
@@ -249,7 +286,7 @@ __device__ __forceinline__ void group_step(const Args& args, uint32_t st, uint32
       tot[i][j][1] = __fmaf_rn(f01, cg[i][j][1], tot[i][j][1]);
       tot[i][j][2] = __fmaf_rn(f10, cg[i][j][2], tot[i][j][2]);
       tot[i][j][3] = __fmaf_rn(f11, cg[i][j][3], tot[i][j][3]);
-      if (!kBf16 && args.dots) {
+      if (AM == AM_INT8 && args.dots) {
         // exact group dot products, layout [P][C][G]; C = 2N (gate, up) or N
         const size_t C = kGateUp ? 2 * static_cast<size_t>(args.N) : static_cast<size_t>(args.N);
 #pragma unroll
@@ -269,7 +306,7 @@ template <int WF, int AM, bool kGateUp, int NT>
 __global__ void __launch_bounds__(kThreads, ctas_per_sm(WF, NT))
     moe_gemm_warp_kernel(const __grid_constant__ CUtensorMap tmA0, const __grid_constant__ CUtensorMap tmA1,
                          const __grid_constant__ CUtensorMap tmB, const Args args) {
-  constexpr bool kBf16 = AM == AM_BF16;
+  constexpr bool k16 = AM != AM_INT8;  // 16-bit activation rows (BF16 or FP16)
   // A stage holds kGroups 128-K groups: per weight row 128 contiguous code
   // bytes (INT4) or two 128-byte pieces (INT8), 128-byte swizzled.
   constexpr int kABoxes = WF == WF_INT4 ? 1 : 2;  // 16 KB boxes per 128-row block per stage
@@ -337,7 +374,7 @@ __global__ void __launch_bounds__(kThreads, ctas_per_sm(WF, NT))
       tma_prefetch_desc(&tmA0);
       tma_prefetch_desc(&tmA1);
       tma_prefetch_desc(&tmB);
-      const uint32_t b_bytes = (kBf16 ? 4u : 2u) * BN * 128u;
+      const uint32_t b_bytes = (k16 ? 4u : 2u) * BN * 128u;
       const uint32_t tx = 2u * kABoxes * kBoxBytes + b_bytes;
       const int nstages = (G + kGroups - 1) / kGroups;
       uint32_t it = 0, uit = 0, sit = 0;
@@ -383,10 +420,10 @@ __global__ void __launch_bounds__(kThreads, ctas_per_sm(WF, NT))
             tma_load_3d(st + (1 * kABoxes + q) * kBoxBytes, &tmA1, &bars->full[s], (ss * kABoxes + q) * 128,
                         nb + args.box_row_off[1], x.e);
           }
-          // tokens: 64-element BF16 boxes or 128-element INT8 boxes covering the stage's 256 K
+          // tokens: 64-element 16-bit boxes or 128-element INT8 boxes covering the stage's 256 K
 #pragma unroll
-          for (int b = 0; b < (kBf16 ? 4 : 2); ++b)
-            tma_load_2d(st + args.off_b + b * BN * 128, &tmB, &bars->full[s], ss * 256 + b * (kBf16 ? 64 : 128),
+          for (int b = 0; b < (k16 ? 4 : 2); ++b)
+            tma_load_2d(st + args.off_b + b * BN * 128, &tmB, &bars->full[s], ss * 256 + b * (k16 ? 64 : 128),
                         x.row0);
           if (++s == S) { s = 0; ph ^= 1; }
         }
@@ -418,8 +455,8 @@ __global__ void __launch_bounds__(kThreads, ctas_per_sm(WF, NT))
     const int row = j * 8 + g;
 #pragma unroll
     for (int c = 0; c < 4; ++c)
-      b_off[j][c] = kBf16 ? args.off_b + (t >> 1) * BN * 128 + row * 128 + (((4 * (t & 1) + c) ^ (row & 7)) << 4)
-                          : args.off_b + row * 128 + (((2 * t + (c & 1)) ^ (row & 7)) << 4);
+      b_off[j][c] = k16 ? args.off_b + (t >> 1) * BN * 128 + row * 128 + (((4 * (t & 1) + c) ^ (row & 7)) << 4)
+                        : args.off_b + row * 128 + (((2 * t + (c & 1)) ^ (row & 7)) << 4);
   }
   // a_off[gi][i][hh][c]: code chunk c of row 16w+g+8hh of block i for group gi of a stage
   uint32_t a_off[kGroups][2][2][2];
@@ -436,7 +473,7 @@ __global__ void __launch_bounds__(kThreads, ctas_per_sm(WF, NT))
               WF == WF_INT4 ? i * kBoxBytes + r * 128 + (((4 * gi + t) ^ (r & 7)) << 4)
                             : (2 * i + gi) * kBoxBytes + r * 128 + (((2 * t + c) ^ (r & 7)) << 4);
       }
-  const uint32_t b_gstep = (kBf16 ? 2u : 1u) * BN * 128u;  // token boxes per group
+  const uint32_t b_gstep = (k16 ? 2u : 1u) * BN * 128u;  // token boxes per group
   for (;; ++uit) {
     const uint32_t sb = uit & 1;
     if (!bounded_wait(&bars->sfull[sb], (uit >> 1) & 1, abort, args.err)) return;
@@ -497,12 +534,13 @@ __global__ void __launch_bounds__(kThreads, ctas_per_sm(WF, NT))
         if (tok >= x.nrows || x.row0 + tok >= args.P) continue;
         const int r = 16 * w + g + 8 * (q >> 1);
         __nv_bfloat16* orow = args.out + static_cast<size_t>(x.row0 + tok) * args.N;
+        const float f = AM == AM_F16R ? __ldg(args.a_outer + x.row0 + tok) : 1.f;  // the row's 2^e
         if (kGateUp) {
-          const float gv = tot[0][j][q], uv = tot[1][j][q];
+          const float gv = tot[0][j][q] * f, uv = tot[1][j][q] * f;
           orow[nb + r] = __float2bfloat16_rn(__fdividef(gv, 1.f + __expf(-gv)) * uv);
         } else {
-          orow[nb + r] = __float2bfloat16_rn(tot[0][j][q]);
-          orow[nb + kRowsPerBox + r] = __float2bfloat16_rn(tot[1][j][q]);
+          orow[nb + r] = __float2bfloat16_rn(tot[0][j][q] * f);
+          orow[nb + kRowsPerBox + r] = __float2bfloat16_rn(tot[1][j][q] * f);
         }
       }
     }
@@ -572,7 +610,7 @@ cudaError_t launch_kind(bool gu, int nt, const CUtensorMap* maps, const Args& a,
 
 bool warp_gemm_applicable(const mnw_moe_layer* L, int wfmt, int act, int kind) {
   if (wfmt != MNW_FMT_INT8_G128 && wfmt != MNW_FMT_INT4_G128) return false;
-  if (act != MNW_ACT_BF16 && act != MNW_ACT_INT8_G128) return false;
+  if (act != MNW_ACT_BF16 && act != MNW_ACT_INT8_G128 && act != kActF16Rows) return false;
   if (kind == MNW_KIND_GATE_UP) return L->I % warpmma::kRowsPerBox == 0;
   return L->H % (2 * warpmma::kRowsPerBox) == 0;
 }
@@ -595,7 +633,8 @@ int run_gemm_warp(const mnw_moe_layer* L, int wfmt, int act, int kind, const voi
   const int a_boxes = wfmt == MNW_FMT_INT4_G128 ? 1 : 2;
   a.box_bytes = kBoxBytes;
   a.off_b = 2 * a_boxes * kBoxBytes;
-  const uint32_t b_bytes = (act == MNW_ACT_BF16 ? 4u : 2u) * BN * 128u;
+  const bool act16 = act != MNW_ACT_INT8_G128;  // BF16 or FP16 rows
+  const uint32_t b_bytes = (act16 ? 4u : 2u) * BN * 128u;
   a.stage_bytes = align_up(a.off_b + b_bytes, 1024);
   a.scale_box_bytes = kRowsPerBox * G * 2;
   const uint32_t fixed = 4 * a.scale_box_bytes + align_up(2u * (L->E + 1) * 4u, 16) + align_up(sizeof(Bars), 16);
@@ -615,6 +654,7 @@ int run_gemm_warp(const mnw_moe_layer* L, int wfmt, int act, int kind, const voi
   a.box_row_off[0] = 0;
   a.box_row_off[1] = gu ? 0 : kRowsPerBox;
   a.a_scales = act == MNW_ACT_INT8_G128 ? static_cast<const float*>(a1) : nullptr;
+  a.a_outer = act == kActF16Rows ? static_cast<const float*>(a1) : nullptr;
   a.out = static_cast<__nv_bfloat16*>(out);
   a.dots = act == MNW_ACT_INT8_G128 ? dots : nullptr;
   a.err = err;
@@ -626,10 +666,11 @@ int run_gemm_warp(const mnw_moe_layer* L, int wfmt, int act, int kind, const voi
   maps[1] = L->tm_codes[m1];
   const uint64_t dims[2] = {static_cast<uint64_t>(K), static_cast<uint64_t>(P)};
   bool ok;
-  if (act == MNW_ACT_BF16) {
+  if (act16) {
     const uint64_t strides[1] = {static_cast<uint64_t>(K) * 2};
     const uint32_t box[2] = {64, static_cast<uint32_t>(BN)};
-    ok = encode_map(&maps[2], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, a0, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_128B);
+    ok = encode_map(&maps[2], act == MNW_ACT_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2,
+                    a0, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_128B);
   } else {
     const uint64_t strides[1] = {static_cast<uint64_t>(K)};
     const uint32_t box[2] = {128, static_cast<uint32_t>(BN)};
@@ -640,6 +681,8 @@ int run_gemm_warp(const mnw_moe_layer* L, int wfmt, int act, int kind, const voi
   cudaError_t e;
   if (wfmt == MNW_FMT_INT4_G128 && act == MNW_ACT_BF16) e = launch_kind<WF_INT4, AM_BF16>(gu, nt, maps, a, smem, grid, st);
   else if (wfmt == MNW_FMT_INT8_G128 && act == MNW_ACT_BF16) e = launch_kind<WF_INT8, AM_BF16>(gu, nt, maps, a, smem, grid, st);
+  else if (wfmt == MNW_FMT_INT4_G128 && act == kActF16Rows) e = launch_kind<WF_INT4, AM_F16R>(gu, nt, maps, a, smem, grid, st);
+  else if (wfmt == MNW_FMT_INT8_G128 && act == kActF16Rows) e = launch_kind<WF_INT8, AM_F16R>(gu, nt, maps, a, smem, grid, st);
   else if (wfmt == MNW_FMT_INT4_G128) e = launch_kind<WF_INT4, AM_INT8>(gu, nt, maps, a, smem, grid, st);
   else e = launch_kind<WF_INT8, AM_INT8>(gu, nt, maps, a, smem, grid, st);
   return e == cudaSuccess ? MNW_OK : MNW_E_CUDA;
