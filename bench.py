@@ -12,6 +12,7 @@ host cores instead (a bounded sample of the same workload).
 from __future__ import annotations
 
 import argparse
+import dataclasses
 import json
 import os
 import statistics
@@ -99,6 +100,21 @@ def _dist():
     return world, rank, local
 
 
+def reduce_ranks(value: float, world: int, op: str, device=None) -> float:
+    """Whole-job value of a per-rank number: "max" (times: the slowest replica
+    sets the job's time) or "sum" (counts).  World size 1 returns the value."""
+    if world <= 1:
+        return value
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX if op == "max" else torch.distributed.ReduceOp.SUM)
+    return float(t.item())
+
+
+def replica_workload(wl: S.Workload, rank: int) -> S.Workload:
+    """Replicas run independent batches: rank r draws its inputs from seed + 1000 r."""
+    return dataclasses.replace(wl, seed=wl.seed + 1000 * rank) if rank else wl
+
+
 def gate_up_bytes(wl: S.Workload, touched: int) -> int:
     """Algorithmic bytes of one gate/up launch: each touched expert's gate and up
     matrices (codes + scales) once, the gathered activations read once, h written once."""
@@ -118,7 +134,7 @@ def run_ours(args, wl):
     world, rank, local = _dist()
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
-    x, ids, w, blob, hdr, L = S.make_inputs(wl, device=dev)
+    x, ids, w, blob, hdr, L = S.make_inputs(replica_workload(wl, rank), device=dev)
     layer = M.Layer(blob, hdr)
     E, T, k, P = wl.E, wl.T, wl.k, wl.P
     stream = torch.cuda.current_stream(dev)
@@ -266,11 +282,8 @@ def run_ours(args, wl):
             e1.record(stream)
         torch.cuda.synchronize()
     step_ms = [a.elapsed_time(b) for a, b in ev]
-    total_ms = sum(step_ms)
-    if world > 1:
-        t = torch.tensor([total_ms], device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        total_ms = float(t.item())
+    total_ms = reduce_ranks(sum(step_ms), world, "max", dev)
+    launches = int(reduce_ranks(launches, world, "sum", dev))
     e = M.mnw_moe_read_error(M.workspace_error_word(ws))
     if e:
         raise RuntimeError(f"device error word {e:#x}")
@@ -306,6 +319,7 @@ def run_ours(args, wl):
         t0 = time.perf_counter()
         M.mnw_moe_forward_host(layer, wl.act, xh, idh, wh, wsh, outh)
         e2e_ms.append((time.perf_counter() - t0) * 1e3)
+    e2e_ms = reduce_ranks(statistics.median(e2e_ms), world, "max", dev)
 
     touched = int(torch.unique(ids[(ids >= 0) & (ids < E)]).numel())
     return dict(total_ms=total_ms, step_ms=step_ms, gu_ms=gu_ms, launches=launches, world=world, rank=rank,
@@ -395,9 +409,9 @@ def main():
     gu_tflops = gu_flops / (gu_ms / 1e3) / 1e12
     tensor_bound = gu_flops / gu_bytes > bf16_peak * 1e12 / (hbm * 1e9)
     layer_bytes = S.algorithmic_bytes(wl, r["ids"].cpu())
-    e2e_ms = statistics.median(r["e2e_ms"])
-    h2d = wl.T * wl.H * 2 + wl.P * 4 * 2
-    d2h = wl.T * wl.H * 2
+    e2e_ms = r["e2e_ms"]  # the slowest replica's median
+    h2d = r["world"] * (wl.T * wl.H * 2 + wl.P * 4 * 2)  # x, ids, w of every replica
+    d2h = r["world"] * wl.T * wl.H * 2
 
     # CPU baseline: the oracle on a bounded token sample, rank 0 only
     ntok = cpu_sample_tokens(wl, args.cpu_budget)
@@ -436,7 +450,7 @@ def main():
                                  "frac": gu_tflops / bf16_peak, "flops_per_launch": gu_flops}}),
         "cpu_baseline": {"value": cpu_rate, "unit": "tokens/s", "cores": 1, "kind": "oracle",
                          "sample": f"{ntok} of {wl.T} tokens, {cpu_dt:.1f} s single-threaded"},
-        "e2e": {"value": wl.T / (e2e_ms / 1e3), "unit": "tokens/s", "h2d_bytes_per_step": h2d,
+        "e2e": {"value": r["world"] * wl.T / (e2e_ms / 1e3), "unit": "tokens/s", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h},
         "gpu_launches": r["launches"],
         "clocks": r["clocks"],

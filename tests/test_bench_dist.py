@@ -1,0 +1,75 @@
+"""The bench's multi-process path on CPU (gloo, world size 2): the whole-job
+reductions and the reference arm under torchrun.  The GPU arm's replicas use
+the same reductions; the layer itself has no exchange step (replicas only)."""
+import json
+import os
+import socket
+import subprocess
+import sys
+
+import pytest
+import torch.multiprocessing as mp
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def _free_port() -> int:
+    with socket.socket() as s:
+        s.bind(("127.0.0.1", 0))
+        return s.getsockname()[1]
+
+
+def _rank_main(rank, world, port, q):
+    import torch.distributed as dist
+    sys.path.insert(0, ROOT)
+    import bench
+    import synth as S
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port))
+    dist.init_process_group("gloo", rank=rank, world_size=world)
+    try:
+        slow = bench.reduce_ranks(10.0 + 5.0 * rank, world, "max")
+        count = bench.reduce_ranks(3.0 + rank, world, "sum")
+        wl = bench.replica_workload(S.WORKLOADS["tiny_w8a16"], rank)
+        q.put((rank, slow, count, wl.seed))
+    finally:
+        dist.destroy_process_group()
+
+
+def test_reductions_over_two_gloo_ranks():
+    ctx = mp.get_context("spawn")
+    q = ctx.Queue()
+    port = _free_port()
+    procs = [ctx.Process(target=_rank_main, args=(r, 2, port, q)) for r in range(2)]
+    for p in procs:
+        p.start()
+    for p in procs:
+        p.join(120)
+    assert all(p.exitcode == 0 for p in procs)
+    got = sorted(q.get(timeout=5) for _ in range(2))
+    # both ranks see the slowest replica's time and the summed count
+    assert [g[1] for g in got] == [15.0, 15.0]
+    assert [g[2] for g in got] == [7.0, 7.0]
+    # replicas draw independent batches
+    assert got[0][3] != got[1][3]
+
+
+def test_reduction_is_identity_at_one_rank():
+    sys.path.insert(0, ROOT)
+    import bench
+    assert bench.reduce_ranks(12.5, 1, "max") == 12.5
+    assert bench.reduce_ranks(4.0, 1, "sum") == 4.0
+
+
+@pytest.mark.timeout(300)
+def test_reference_arm_under_torchrun_prints_one_line_from_rank0():
+    env = dict(os.environ, CUDA_VISIBLE_DEVICES="")
+    cmd = [sys.executable, "-m", "torch.distributed.run", "--nnodes=1", "--nproc-per-node", "2",
+           "--master-addr", "127.0.0.1", "--master-port", str(_free_port()), "bench.py",
+           "--impl", "reference", "--workload", "tiny_w8a16", "--gpus", "2", "--steps", "1", "--warmup", "0"]
+    r = subprocess.run(cmd, cwd=ROOT, env=env, capture_output=True, text=True, timeout=280)
+    assert r.returncode == 0, r.stderr[-2000:]
+    lines = [ln for ln in r.stdout.splitlines() if ln.startswith("{")]
+    assert len(lines) == 1
+    d = json.loads(lines[0])
+    assert d["impl"] == "reference" and d["n_gpus"] == 2 and d["value"] > 0
+    assert d["cpu_baseline"]["kind"] == "oracle" and d["e2e"]["h2d_bytes_per_step"] == 0
