@@ -160,7 +160,7 @@ static bool act_allowed(int wfmt, int act) {
 // ---- workspace layout ----------------------------------------------------------
 
 struct WsLayout {
-  size_t err, offsets, sorted, pos;
+  size_t err, dep, offsets, sorted, pos;
   size_t xa, xb, xc;   // x operand: bf16 rows | codes, scales, outer
   size_t h, ha, hb, hc;
   size_t y;
@@ -175,6 +175,7 @@ static WsLayout ws_layout(const mnw_moe_layer* L, int act, int T, int k) {
   const size_t P = static_cast<size_t>(T) * k, H = L->H, I = L->I, E = L->E;
   size_t o = 0;
   w.err = o; o += 256;
+  w.dep = o; o = al(o + warp_dep_words(static_cast<int>(P), static_cast<int>(E)) * 4);  // zeroed with err
   w.offsets = o; o = al(o + (E + 1) * 4);
   w.sorted = o; o = al(o + P * 4);
   w.pos = o; o = al(o + P * 4);
@@ -466,7 +467,7 @@ int mnw_moe_forward(const mnw_moe_layer* L, int act, const void* x, const int32_
   // The first 256 bytes of ws: error word, then a [claim, done] work counter per GEMM launch.
   uint32_t* sched_gu = err + 16;
   uint32_t* sched_dn = err + 18;
-  if (cudaMemsetAsync(err, 0, 256, st) != cudaSuccess) return MNW_E_CUDA;
+  if (cudaMemsetAsync(err, 0, W.offsets - W.err, st) != cudaSuccess) return MNW_E_CUDA;  // error word, counters
   int rc;
   if (act == MNW_ACT_BF16) {
     // INT weights: the GEMMs run on FP16 rows (scaled into FP16 range by a
@@ -477,20 +478,33 @@ int mnw_moe_forward(const mnw_moe_layer* L, int act, const void* x, const int32_
     const int mean_rows = (P + L->E - 1) / L->E;
     const int path = gemm_path();
     const bool tc = path != MNW_PATH_WARP_MMA && (path == MNW_PATH_TCGEN05 || mean_rows >= 32);
+    const int gu_act = L->f16_gate_up_ok ? kActF16Rows : act;
+    // Both GEMMs on the warp-MMA kernel (same token tile): the down launch
+    // follows the gate/up launch tile by tile instead of waiting for all of it.
+    const bool warp_down = !tc && warp_gemm_applicable(L, L->wfmt, gu_act, MNW_KIND_GATE_UP) &&
+                           warp_gemm_applicable(L, L->wfmt, act, MNW_KIND_DOWN);
+    const WarpDep gu_dep{reinterpret_cast<uint32_t*>(b + W.dep), kDepProduce, 0};
     if (L->f16_gate_up_ok) {
       rc = mnw_moe_permute(ids, T, k, L->E, offs, sorted, pos, nullptr, 0, nullptr, err, stream);
       if (rc) return rc;
       float* factor = reinterpret_cast<float*>(b + W.xc);
       rc = mnw_moe_quantize_act(MNW_ACT_F16_ROWS, x, P, H, sorted, k, b + W.xa, nullptr, factor, stream);
       if (rc) return rc;
-      rc = gemm_for(L, kActF16Rows, MNW_KIND_GATE_UP, b + W.xa, factor, nullptr, offs, P, b + W.h, err, sched_gu, st);
+      rc = run_gemm(L, L->wfmt, kActF16Rows, MNW_KIND_GATE_UP, b + W.xa, factor, nullptr, offs, P, b + W.h, nullptr,
+                    err, st, sched_gu, warp_down ? &gu_dep : nullptr);
     } else {
       rc = mnw_moe_permute(ids, T, k, L->E, offs, sorted, pos, x, H, b + W.xa, err, stream);
       if (rc) return rc;
-      rc = gemm_for(L, act, MNW_KIND_GATE_UP, b + W.xa, nullptr, nullptr, offs, P, b + W.h, err, sched_gu, st);
+      rc = run_gemm(L, L->wfmt, act, MNW_KIND_GATE_UP, b + W.xa, nullptr, nullptr, offs, P, b + W.h, nullptr, err, st,
+                    sched_gu, warp_down ? &gu_dep : nullptr);
     }
     if (rc) return rc;
-    if (tc && L->f16_down_ok) {
+    if (warp_down) {
+      // both GEMMs on the warp-MMA kernel: down starts tile by tile behind gate/up
+      const WarpDep dn{reinterpret_cast<uint32_t*>(b + W.dep), kDepConsume, warp_dep_need_gate_up(L)};
+      rc = run_gemm(L, L->wfmt, act, MNW_KIND_DOWN, b + W.h, nullptr, nullptr, offs, P, b + W.y, nullptr, err, st,
+                    sched_dn, &dn);
+    } else if (tc && L->f16_down_ok) {
       float* hf = reinterpret_cast<float*>(b + W.hc);
       rc = mnw_moe_quantize_act(MNW_ACT_F16_ROWS, b + W.h, P, I, nullptr, 1, b + W.ha, nullptr, hf, stream);
       if (rc) return rc;

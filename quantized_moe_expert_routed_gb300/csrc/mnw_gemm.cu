@@ -789,9 +789,14 @@ cudaError_t launch_kind(bool gate_up, const CUtensorMap* maps, const GemmArgs& a
 
 }  // namespace
 
+int warp_gemm_nt(int P, int E) {
+  const int mean_rows = (P + E - 1) / E;
+  return mean_rows <= 4 ? 1 : (mean_rows <= 16 ? 2 : 4);
+}
+
 int run_gemm(const mnw_moe_layer* L, int wfmt, int act, int kind, const void* a0, const void* a1, const void* a2,
              const int32_t* offsets, int P, void* out, int32_t* dots, uint32_t* err, cudaStream_t st,
-             uint32_t* sched) {
+             uint32_t* sched, const WarpDep* dep) {
   if (!L || (kind != MNW_KIND_GATE_UP && kind != MNW_KIND_DOWN) || P < 0) return MNW_E_INVALID_ARG;
   if (L->wfmt != wfmt) return MNW_E_MODE;
   if (P == 0) return MNW_OK;
@@ -810,9 +815,10 @@ int run_gemm(const mnw_moe_layer* L, int wfmt, int act, int kind, const void* a0
   const int path = gemm_path();
   const bool warp_ok = warp_gemm_applicable(L, wfmt, act, kind);
   if (warp_ok && (path == MNW_PATH_WARP_MMA || (path == MNW_PATH_AUTO && mean_rows < 32))) {
-    const int nt = mean_rows <= 4 ? 1 : (mean_rows <= 16 ? 2 : 4);
-    return run_gemm_warp(L, wfmt, act, kind, a0, a1, offsets, P, nt, out, dots, err, sched, st);
+    return run_gemm_warp(L, wfmt, act, kind, a0, a1, offsets, P, warp_gemm_nt(P, L->E), out, dots, err, sched, st,
+                         dep);
   }
+  if (dep && dep->role != kDepNone) return MNW_E_INVALID_ARG;  // only the warp-MMA kernel takes a dependency
   const bool gate_up = kind == MNW_KIND_GATE_UP;
   const int K = gate_up ? L->H : L->I;
   const int N = gate_up ? L->I : L->H;

@@ -80,17 +80,37 @@ cudaError_t launch_quantize_scatter(int act, const void* x, int R, int K, const 
 // Activation mode of the FP16 operand gate/up GEMM (INT weights): a0 = FP16
 // rows from launch_gather_f16, a1 = their float factors.
 constexpr int kActF16Rows = MNW_ACT_F16_ROWS;
+// Tile-level dependency between the gate/up and the down warp-MMA launches of
+// one forward step.  The gate/up launch (kDepProduce) adds one to flags[1 + t]
+// when all its MMA warps have written token tile t's h rows of a row block,
+// and sets flags[0] once its own wait on the previous kernel has returned.  The down launch (kDepConsume) waits for flags[0] instead of for
+// the gate/up launch to complete, so its CTAs start as gate/up CTAs retire,
+// and reads token tile t only once flags[1 + t] >= need.  flags is zeroed
+// before the gate/up launch; both launches use the same token tile.
+enum { kDepNone = 0, kDepProduce = 1, kDepConsume = 2 };
+struct WarpDep {
+  uint32_t* flags;
+  int role;
+  uint32_t need;
+};
+// Token tiles of any warp-MMA launch over P rows of E experts (8-row tiles at least).
+inline size_t warp_dep_words(int P, int E) { return static_cast<size_t>(P) / 8 + E + 2; }
+// Count a token tile's counter reaches when the gate/up launch has written all its h rows
+// (its number of row blocks).
+uint32_t warp_dep_need_gate_up(const mnw_moe_layer* L);
 // Grouped GEMM for weight format wfmt and activation mode act.
 // sched (nullable): a zeroed device counter that lets the kernel's CTAs claim
 // work units dynamically; NULL gives a static round-robin order.
 int run_gemm(const mnw_moe_layer* L, int wfmt, int act, int kind, const void* a0, const void* a1,
              const void* a2, const int32_t* offsets, int P, void* out, int32_t* dots, uint32_t* err,
-             cudaStream_t st, uint32_t* sched = nullptr);
+             cudaStream_t st, uint32_t* sched = nullptr, const WarpDep* dep = nullptr);
 // Warp-MMA grouped GEMM (INT8/INT4 weights, few tokens per expert); nt = token tile / 8.
 bool warp_gemm_applicable(const mnw_moe_layer* L, int wfmt, int act, int kind);
 int run_gemm_warp(const mnw_moe_layer* L, int wfmt, int act, int kind, const void* a0, const void* a1,
                   const int32_t* offsets, int P, int nt, void* out, int32_t* dots, uint32_t* err, uint32_t* sched,
-                  cudaStream_t st);
+                  cudaStream_t st, const WarpDep* dep = nullptr);
+// Token tile (in 8-row units) the warp-MMA kernel uses for P rows over E experts.
+int warp_gemm_nt(int P, int E);
 // Process-wide GEMM path selection (MNW_PATH_*).
 int gemm_path();
 

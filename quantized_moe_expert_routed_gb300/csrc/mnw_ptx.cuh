@@ -101,6 +101,35 @@ __device__ __forceinline__ bool bounded_wait(uint64_t* bar, uint32_t parity, vol
   return bounded_wait_for(bar, parity, abort, err, kWaitLimitNs);
 }
 
+// ---- cross-kernel dependency counters ----------------------------------------
+
+__device__ __forceinline__ uint32_t ld_acquire_gpu(const uint32_t* p) {
+  uint32_t v;
+  asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+// Wait until *p >= need (a counter another kernel releases with a fence and an
+// atomic add).  Gives up like bounded_wait: abort flag or kWaitLimitNs.
+__device__ __forceinline__ bool bounded_poll_ge(const uint32_t* p, uint32_t need, volatile int* abort, uint32_t* err) {
+  if (ld_acquire_gpu(p) >= need) return true;
+  const uint64_t t0 = globaltimer();
+  for (uint32_t it = 1;; ++it) {
+    __nanosleep(256);
+    if (ld_acquire_gpu(p) >= need) return true;
+    if ((it & 15u) == 0) {
+      if (abort && *abort) return false;
+      if (globaltimer() - t0 > kWaitLimitNs) {
+        if (abort) *abort = 1;
+        if (err) atomicOr(err, MNW_DEVERR_TIMEOUT);
+        return false;
+      }
+    }
+  }
+}
+// Order this thread's earlier generic-proxy accesses (an acquire) before its
+// later async-proxy ones (TMA reads of what the other kernel wrote).
+__device__ __forceinline__ void fence_proxy_async() { asm volatile("fence.proxy.async;" ::: "memory"); }
+
 // ---- TMA (bulk tensor copies, global -> shared) ----------------------------
 
 __device__ __forceinline__ void tma_prefetch_desc(const CUtensorMap* map) {

@@ -124,3 +124,41 @@ def test_fp16_operand_path_falls_back_for_large_scales(M):
     """Weights whose fp16(q * s) could overflow keep the exact grouped path."""
     wl = S.Workload("big_scales", 256, 512, 16, 256, 4, S.FMT_INT8_G128, S.ACT_BF16, 5.0e4, "uniform", 12)
     _run_custom(M, wl, relative_only=True)
+
+
+@pytest.mark.parametrize("wfmt", [S.FMT_INT4_G128, S.FMT_INT8_G128])
+@pytest.mark.parametrize("T,E,k", [(24, 64, 2), (40, 16, 2), (200, 16, 4), (64, 8, 8)])
+def test_forward_warp_tile_dependency(M, wfmt, T, E, k):
+    """On the warp-MMA kernel the down launch follows the gate/up launch tile by
+    tile (tile counters in the workspace instead of a wait for the whole
+    launch).  Scheduling only: the layer must give the same bits as the same
+    kernels launched one after the other, on repeated calls with one
+    workspace, and match the oracle.  Token tiles of 8, 16 and 32 rows."""
+    wl = S.Workload("warp_dep", T, 512, E, 256, k, wfmt, S.ACT_BF16, 0.02, "uniform", 31 + T)
+    x, ids, w, blob, hdr, L = S.make_inputs(wl, device=DEV)
+    if T == 64:
+        ids[:, 0] = 3  # one crowded expert, some empty ones
+    M.mnw_moe_set_gemm_path(M.PATH_WARP_MMA)
+    try:
+        layer = M.Layer(blob, hdr)
+        ws = M.workspace(layer, wl.act, T, k)
+        out1 = M.mnw_moe_forward(layer, wl.act, x, ids, w, ws=ws).clone()
+        assert M.mnw_moe_read_error(M.workspace_error_word(ws)) == 0
+        out2 = M.mnw_moe_forward(layer, wl.act, x, ids, w, ws=ws)
+        assert M.mnw_moe_read_error(M.workspace_error_word(ws)) == 0
+        assert torch.equal(out1.view(torch.int16), out2.view(torch.int16))
+        # the same kernels, launched one after the other through the ABI
+        off, sa, pos, _ = M.mnw_moe_permute(ids, E)
+        a, f = M.mnw_moe_quantize_act(M.ACT_F16_ROWS, x, row_index=sa, index_div=k)
+        gu = {S.FMT_INT4_G128: M.mnw_moe_grouped_gemm_w4a16_f16rows,
+              S.FMT_INT8_G128: M.mnw_moe_grouped_gemm_w8a16_f16rows}[wfmt]
+        dn = {S.FMT_INT4_G128: M.mnw_moe_grouped_gemm_w4a16, S.FMT_INT8_G128: M.mnw_moe_grouped_gemm_w8a16}[wfmt]
+        h = gu(layer, M.KIND_GATE_UP, a, f, off)
+        y = dn(layer, M.KIND_DOWN, h, off)
+        out3 = M.mnw_moe_combine(y, pos, w)
+        assert torch.equal(out1.view(torch.int16), out3.view(torch.int16))
+    finally:
+        M.mnw_moe_set_gemm_path(M.PATH_AUTO)
+    want = O.moe_forward(blob.cpu().numpy(), wl.act, S.bf16_bits_np(x), ids.cpu().numpy(), w.cpu().numpy(),
+                         rows=np.arange(T, dtype=np.int32))
+    assert_close(out1, want, rel_l2=REL_L2, what="warp tile dependency")
