@@ -230,10 +230,14 @@ int mnw_moe_forward(const mnw_moe_layer* layer, int act, const void* x, const in
                     mnw_stream stream);
 uint32_t* mnw_moe_workspace_error_word(void* ws);
 
-/* The whole layer from and to HOST buffers (pinned memory gives overlap):
- * copies x, ids, w into ws, runs mnw_moe_forward, copies out back and
- * synchronises `stream`.  ws must hold mnw_moe_workspace_size_host() bytes.
- * Returns MNW_E_CUDA if the device error word is non-zero afterwards. */
+/* The whole layer from and to HOST buffers: copies x into ws, runs
+ * mnw_moe_forward, and synchronises `stream`.  ids, w and out are used in
+ * place when they are page-locked memory mapped into the device's address
+ * space (e.g. cudaHostAlloc on a unified-addressing system; the kernels then
+ * read ids and w and write out over the host link), otherwise they are
+ * staged through ws with copies on `stream`.  ws must hold
+ * mnw_moe_workspace_size_host() bytes.  Returns MNW_E_CUDA if the device
+ * error word is non-zero afterwards. */
 size_t mnw_moe_workspace_size_host(const mnw_moe_layer* layer, int act, int T, int k);
 int mnw_moe_forward_host(const mnw_moe_layer* layer, int act, const void* x_host,
                          const int32_t* ids_host, const float* w_host, int T, int k,
@@ -287,6 +291,13 @@ int mnw_moe_forward_static(const mnw_moe_layer* layer, int act, const void* x, c
  * usable.  Both words are caller-owned device memory, zeroed beforehand.
  * Returns MNW_E_INVALID_ARG for null pointers or a limit out of range. */
 int mnw_moe_selftest_wait_timeout(uint32_t limit_us, uint32_t* err, uint32_t* left_early, mnw_stream stream);
+/* Self-test of the wait on a token-tile counter that a dependent launch uses
+ * (the down launch behind the gate/up launch of a forward): one thread waits
+ * up to limit_us (1 us .. 1 s) for *counter (device u32) >= need.  If the
+ * counter stays below, it ORs MNW_DEVERR_TIMEOUT into *err (device u32) and
+ * returns; no fault, the context stays usable. */
+int mnw_moe_selftest_counter_timeout(uint32_t limit_us, const uint32_t* counter, uint32_t need, uint32_t* err,
+                                     mnw_stream stream);
 
 /* Synchronise `stream`, then copy the device error word to *out_host. */
 int mnw_moe_read_error(const uint32_t* err, uint32_t* out_host, mnw_stream stream);

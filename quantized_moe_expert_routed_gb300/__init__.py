@@ -52,6 +52,7 @@ SIGNATURES = {
     "mnw_moe_launch_count": (ctypes.c_uint64, []),
     "mnw_moe_forward_static": (_I, [_P, _I, _P, _P, _P, _I, _I, _P, _U32P, _P]),
     "mnw_moe_selftest_wait_timeout": (_I, [ctypes.c_uint32, _U32P, _U32P, _P]),
+    "mnw_moe_selftest_counter_timeout": (_I, [ctypes.c_uint32, _U32P, ctypes.c_uint32, _U32P, _P]),
 }
 
 _lib = None
@@ -324,3 +325,10 @@ def mnw_moe_selftest_wait_timeout(limit_us, err, left_early, stream=None):
     left_early are zeroed int32 device tensors of one element."""
     _check(load().mnw_moe_selftest_wait_timeout(limit_us, _ptr(err), _ptr(left_early), _stream(stream)),
            "mnw_moe_selftest_wait_timeout")
+
+
+def mnw_moe_selftest_counter_timeout(limit_us, counter, need, err, stream=None):
+    """Launch the token-tile counter wait self-test (see include/mnw_moe.h);
+    counter and err are int32 device tensors of one element."""
+    _check(load().mnw_moe_selftest_counter_timeout(limit_us, _ptr(counter), need, _ptr(err), _stream(stream)),
+           "mnw_moe_selftest_counter_timeout")

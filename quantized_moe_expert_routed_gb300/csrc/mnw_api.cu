@@ -530,6 +530,19 @@ int mnw_moe_forward(const mnw_moe_layer* L, int act, const void* x, const int32_
   return mnw_moe_combine(b + W.y, pos, w, T, k, H, out, stream);
 }
 
+// The device address of a host buffer the GPU can read and write in place
+// (page-locked and mapped into the unified address space), or null for
+// pageable memory, which then goes through a staging copy.
+static void* mapped_alias(const void* host, size_t align) {
+  cudaPointerAttributes a{};
+  if (cudaPointerGetAttributes(&a, host) != cudaSuccess) {
+    cudaGetLastError();  // clear the error of a pointer CUDA does not know
+    return nullptr;
+  }
+  if (a.type != cudaMemoryTypeHost || !a.devicePointer || !aligned(a.devicePointer, align)) return nullptr;
+  return a.devicePointer;
+}
+
 int mnw_moe_forward_host(const mnw_moe_layer* L, int act, const void* x_host, const int32_t* ids_host,
                          const float* w_host, int T, int k, void* out_host, void* ws, size_t ws_bytes,
                          mnw_stream stream) {
@@ -541,14 +554,26 @@ int mnw_moe_forward_host(const mnw_moe_layer* L, int act, const void* x_host, co
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   uint8_t* b = static_cast<uint8_t*>(ws);
   const size_t xb = static_cast<size_t>(T) * L->H * 2, ib = static_cast<size_t>(T) * k * 4;
-  if (cudaMemcpyAsync(b + W.hx, x_host, xb, cudaMemcpyHostToDevice, st) != cudaSuccess ||
-      cudaMemcpyAsync(b + W.hids, ids_host, ib, cudaMemcpyHostToDevice, st) != cudaSuccess ||
-      cudaMemcpyAsync(b + W.hw, w_host, ib, cudaMemcpyHostToDevice, st) != cudaSuccess)
-    return MNW_E_CUDA;
-  int rc = mnw_moe_forward(L, act, b + W.hx, reinterpret_cast<const int32_t*>(b + W.hids),
-                           reinterpret_cast<const float*>(b + W.hw), T, k, b + W.hout, ws, W.total, stream);
+  // ids and w (read once, by the permute and the combine) and out (written
+  // once, by the combine) are used in place when they are mapped page-locked
+  // memory; x is always staged, as the gather reads each row k times.
+  const void* ids_d = mapped_alias(ids_host, 4);
+  const void* w_d = mapped_alias(w_host, 4);
+  void* out_d = mapped_alias(out_host, 16);
+  if (cudaMemcpyAsync(b + W.hx, x_host, xb, cudaMemcpyHostToDevice, st) != cudaSuccess) return MNW_E_CUDA;
+  if (!ids_d) {
+    if (cudaMemcpyAsync(b + W.hids, ids_host, ib, cudaMemcpyHostToDevice, st) != cudaSuccess) return MNW_E_CUDA;
+    ids_d = b + W.hids;
+  }
+  if (!w_d) {
+    if (cudaMemcpyAsync(b + W.hw, w_host, ib, cudaMemcpyHostToDevice, st) != cudaSuccess) return MNW_E_CUDA;
+    w_d = b + W.hw;
+  }
+  int rc = mnw_moe_forward(L, act, b + W.hx, static_cast<const int32_t*>(ids_d), static_cast<const float*>(w_d), T,
+                           k, out_d ? out_d : b + W.hout, ws, W.total, stream);
   if (rc) return rc;
-  if (cudaMemcpyAsync(out_host, b + W.hout, xb, cudaMemcpyDeviceToHost, st) != cudaSuccess) return MNW_E_CUDA;
+  if (!out_d && cudaMemcpyAsync(out_host, b + W.hout, xb, cudaMemcpyDeviceToHost, st) != cudaSuccess)
+    return MNW_E_CUDA;
   // The error word goes to host stack memory: a stream-ordered copy into
   // pageable memory returns only once it, and so everything before it on the
   // stream (the output copy included), has completed -- one wait, not two.

@@ -109,8 +109,9 @@ __device__ __forceinline__ uint32_t ld_acquire_gpu(const uint32_t* p) {
   return v;
 }
 // Wait until *p >= need (a counter another kernel releases with a fence and an
-// atomic add).  Gives up like bounded_wait: abort flag or kWaitLimitNs.
-__device__ __forceinline__ bool bounded_poll_ge(const uint32_t* p, uint32_t need, volatile int* abort, uint32_t* err) {
+// atomic add).  Gives up like bounded_wait_for: abort flag (nullable) or limit_ns.
+__device__ __forceinline__ bool bounded_poll_ge_for(const uint32_t* p, uint32_t need, volatile int* abort,
+                                                    uint32_t* err, uint64_t limit_ns) {
   if (ld_acquire_gpu(p) >= need) return true;
   const uint64_t t0 = globaltimer();
   for (uint32_t it = 1;; ++it) {
@@ -118,13 +119,16 @@ __device__ __forceinline__ bool bounded_poll_ge(const uint32_t* p, uint32_t need
     if (ld_acquire_gpu(p) >= need) return true;
     if ((it & 15u) == 0) {
       if (abort && *abort) return false;
-      if (globaltimer() - t0 > kWaitLimitNs) {
+      if (globaltimer() - t0 > limit_ns) {
         if (abort) *abort = 1;
         if (err) atomicOr(err, MNW_DEVERR_TIMEOUT);
         return false;
       }
     }
   }
+}
+__device__ __forceinline__ bool bounded_poll_ge(const uint32_t* p, uint32_t need, volatile int* abort, uint32_t* err) {
+  return bounded_poll_ge_for(p, need, abort, err, kWaitLimitNs);
 }
 // Order this thread's earlier generic-proxy accesses (an acquire) before its
 // later async-proxy ones (TMA reads of what the other kernel wrote).

@@ -38,6 +38,13 @@ __global__ void __launch_bounds__(64, 1) wait_timeout_kernel(uint64_t limit_ns, 
   }
 }
 
+// One thread waits, with the caller's limit, for *counter >= need: the wait a
+// dependent launch uses for a token tile released by the launch before it.
+__global__ void __launch_bounds__(32, 1) counter_timeout_kernel(const uint32_t* counter, uint32_t need,
+                                                                uint64_t limit_ns, uint32_t* err) {
+  if (threadIdx.x == 0) bounded_poll_ge_for(counter, need, nullptr, err, limit_ns);
+}
+
 }  // namespace
 }  // namespace mnw
 
@@ -46,6 +53,16 @@ extern "C" int mnw_moe_selftest_wait_timeout(uint32_t limit_us, uint32_t* err, u
   if (!err || !left_early || limit_us == 0 || limit_us > 1000000u) return MNW_E_INVALID_ARG;
   mnw::wait_timeout_kernel<<<1, 64, 0, static_cast<cudaStream_t>(stream)>>>(static_cast<uint64_t>(limit_us) * 1000u,
                                                                             err, left_early);
+  if (cudaGetLastError() != cudaSuccess) return MNW_E_CUDA;
+  mnw::note_launch();
+  return MNW_OK;
+}
+
+extern "C" int mnw_moe_selftest_counter_timeout(uint32_t limit_us, const uint32_t* counter, uint32_t need,
+                                                uint32_t* err, mnw_stream stream) {
+  if (!counter || !err || limit_us == 0 || limit_us > 1000000u) return MNW_E_INVALID_ARG;
+  mnw::counter_timeout_kernel<<<1, 32, 0, static_cast<cudaStream_t>(stream)>>>(
+      counter, need, static_cast<uint64_t>(limit_us) * 1000u, err);
   if (cudaGetLastError() != cudaSuccess) return MNW_E_CUDA;
   mnw::note_launch();
   return MNW_OK;

@@ -60,3 +60,24 @@ def test_selftest_rejects_bad_limits(M):
         M.mnw_moe_selftest_wait_timeout(0, err, err)
     with pytest.raises(RuntimeError):
         M.mnw_moe_selftest_wait_timeout(2_000_000, err, err)
+
+
+def test_counter_wait_times_out_without_fault(M):
+    """The wait a dependent launch does on a token-tile counter: a counter that
+    nothing raises ends in MNW_DEVERR_TIMEOUT after the limit, a satisfied one
+    returns at once, and the context stays usable."""
+    counter = torch.zeros(1, dtype=torch.int32, device="cuda")
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    t0 = time.perf_counter()
+    M.mnw_moe_selftest_counter_timeout(20000, counter, 1, err)
+    torch.cuda.synchronize()
+    waited = time.perf_counter() - t0
+    assert int(err.item()) == MNW_DEVERR_TIMEOUT
+    assert waited >= 0.02
+    counter.fill_(3)
+    err.zero_()
+    M.mnw_moe_selftest_counter_timeout(1000000, counter, 3, err)
+    torch.cuda.synchronize()
+    assert int(err.item()) == 0
+    with pytest.raises(M.MnwError):
+        M.mnw_moe_selftest_counter_timeout(0, counter, 1, err)

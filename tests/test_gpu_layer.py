@@ -58,14 +58,21 @@ def test_full_size_sampled(M, name, nrows):
     _run(M, wl, rows=rows)
 
 
-def test_forward_host_buffers(M):
-    wl = S.WORKLOADS["tiny_w8a16"]
+@pytest.mark.parametrize("name", ["tiny_w8a16", "decode_w4a16"])
+@pytest.mark.parametrize("pinned", ["all", "none", "mixed"])
+def test_forward_host_buffers(M, name, pinned):
+    """Host buffers: mapped page-locked ones are used in place, pageable ones
+    staged; either way the same bits as the device-buffer call."""
+    wl = S.WORKLOADS[name]
     x, ids, w, blob, hdr, L = S.make_inputs(wl, device=DEV)
     layer = M.Layer(blob, hdr)
     ws = M.workspace(layer, wl.act, wl.T, wl.k, host=True)
-    out_h = torch.empty((wl.T, wl.H), dtype=torch.bfloat16).pin_memory()
-    M.mnw_moe_forward_host(layer, wl.act, x.cpu().pin_memory(), ids.cpu().pin_memory(), w.cpu().pin_memory(), ws,
-                           out_h)
+    pin = {"all": (True, True, True, True), "none": (False, False, False, False),
+           "mixed": (False, True, False, True)}[pinned]  # x, ids, w, out
+    host = lambda t, p: t.cpu().pin_memory() if p else t.cpu().clone()
+    out_h = torch.empty((wl.T, wl.H), dtype=torch.bfloat16)
+    out_h = out_h.pin_memory() if pin[3] else out_h
+    M.mnw_moe_forward_host(layer, wl.act, host(x, pin[0]), host(ids, pin[1]), host(w, pin[2]), ws, out_h)
     ref = M.mnw_moe_forward(layer, wl.act, x, ids, w)
     assert torch.equal(out_h.view(torch.int16), ref.cpu().view(torch.int16))
 
