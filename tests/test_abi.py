@@ -56,6 +56,20 @@ def test_bad_arguments_rejected_before_any_launch(lib):
     # bounded-wait self-test: null words, limit out of range
     assert lib.mnw_moe_selftest_wait_timeout(1000, None, None, None) == 1
     assert lib.mnw_moe_selftest_wait_timeout(0, ctypes.c_void_p(256), ctypes.c_void_p(512), None) == 1
+    # counter-wait self-test: null counter or word, limit out of range
+    assert lib.mnw_moe_selftest_counter_timeout(1000, None, 1, ctypes.c_void_p(256), None) == 1
+    assert lib.mnw_moe_selftest_counter_timeout(1000, ctypes.c_void_p(256), 1, None, None) == 1
+    assert lib.mnw_moe_selftest_counter_timeout(2_000_000, ctypes.c_void_p(256), 1, ctypes.c_void_p(512), None) == 1
+    # FP16 row form: K not a multiple of 8, missing factors, R = 0 is a no-op
+    assert lib.mnw_moe_quantize_act(3, None, 4, 100, None, 1, None, None, None, None) == 2
+    assert lib.mnw_moe_quantize_act(3, ctypes.c_void_p(256), 4, 128, None, 1, ctypes.c_void_p(512), None, None,
+                                    None) == 1
+    assert lib.mnw_moe_quantize_act(3, None, 0, 128, None, 1, None, None, None, None) == 0
+    # FP16-row GEMMs without a layer
+    assert lib.mnw_moe_grouped_gemm_w8a16_f16rows(None, 0, None, None, None, 4, None, None, None) == 1
+    assert lib.mnw_moe_grouped_gemm_w4a16_f16rows(None, 1, None, None, None, 4, None, None, None) == 1
+    # the library's launch counter is readable without a GPU
+    assert lib.mnw_moe_launch_count() >= 0
 
 
 def test_blob_header_checks(lib):
