@@ -65,6 +65,11 @@
 #ifdef __cplusplus
 extern "C" {
 #endif
+/* The library is built with hidden visibility: only what this header
+ * declares is exported. */
+#if defined(__GNUC__)
+#pragma GCC visibility push(default)
+#endif
 
 /* A CUDA stream (cudaStream_t); 0 is the legacy default stream. */
 typedef void* mnw_stream;
@@ -302,6 +307,9 @@ int mnw_moe_selftest_counter_timeout(uint32_t limit_us, const uint32_t* counter,
 /* Synchronise `stream`, then copy the device error word to *out_host. */
 int mnw_moe_read_error(const uint32_t* err, uint32_t* out_host, mnw_stream stream);
 
+#if defined(__GNUC__)
+#pragma GCC visibility pop
+#endif
 #ifdef __cplusplus
 }
 #endif

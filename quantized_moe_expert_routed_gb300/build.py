@@ -19,7 +19,7 @@ LIB = os.path.join(HERE, "libmnw_moe.so")
 SOURCES = ["mnw_api.cu", "mnw_route.cu", "mnw_quant.cu", "mnw_gemm.cu", "mnw_gemm_warp.cu", "mnw_gemm_warp_dep.cu",
            "mnw_static_ws.cu", "mnw_selftest.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
-FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-Xcompiler", "-O2",
+FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-Xcompiler", "-O2", "-Xcompiler", "-fvisibility=hidden",
          "-I", CSRC, "-I", INCLUDE]
 
 
@@ -31,7 +31,9 @@ def _nvcc() -> str:
 
 
 def _deps():
-    files = [os.path.join(CSRC, f) for f in os.listdir(CSRC)] + [os.path.join(INCLUDE, "mnw_moe.h")]
+    # sources, the public header and this file (its flags)
+    files = [os.path.join(CSRC, f) for f in os.listdir(CSRC)] + [os.path.join(INCLUDE, "mnw_moe.h"),
+                                                                 os.path.abspath(__file__)]
     return max(os.path.getmtime(f) for f in files)
 
 

@@ -313,6 +313,29 @@ __device__ __forceinline__ void group_step(const Args& args, uint32_t st, uint32
   }
 }
 
+// The releaser warp of a launch that releases token tiles (kDepProduce): per
+// unit, once all MMA warps have written its output rows, one release add on
+// the token tile's counter; CTA 0 first sets the ready flag (every thread has
+// passed the wait on the previous kernel before the roles split).  Kept out of
+// line so that its code takes no part in the MMA warps' register allocation.
+static __device__ __noinline__ void release_loop(Bars* bars, volatile int* abort, uint32_t* err, uint32_t* dep, int n_blocks,
+                                          int units) {
+  if (blockIdx.x == 0) {
+    __threadfence();
+    atomicExch(dep, 1u);
+  }
+  for (uint32_t uit = 0;; ++uit) {
+    const uint32_t sb = uit & 1, par = (uit >> 1) & 1;
+    if (!bounded_wait(&bars->sfull[sb], par, abort, err)) break;
+    const int u = *reinterpret_cast<volatile int*>(&bars->unit[sb]);
+    if (u >= units) break;
+    if (!bounded_wait(&bars->udone[sb], par, abort, err)) break;
+    __threadfence();
+    atomicAdd(dep + 1 + u / n_blocks, 1u);
+    mbar_arrive(&bars->sempty[sb]);
+  }
+}
+
 // kDep: kDepNone, or the launch's role in a gate/up -> down tile dependency
 // (WarpDep).  A template parameter so that launches without one compile to
 // the same code (and registers) as if the feature did not exist.
@@ -358,10 +381,6 @@ __global__ void __launch_bounds__(threads_for(kDep), ctas_per_sm(WF, NT))
     if (bars->abort) return;  // nothing issued yet: leave without touching memory
   } else {
     pdl_wait();
-    if (kDep == kDepProduce && blockIdx.x == 0 && threadIdx.x == 0) {
-      __threadfence();
-      atomicExch(args.dep, 1u);
-    }
   }
   if (warp == 1) {  // tile table: first tile of each expert
     const int per = (E + 31) / 32;
@@ -481,20 +500,7 @@ __global__ void __launch_bounds__(threads_for(kDep), ctas_per_sm(WF, NT))
   if constexpr (kDep == kDepProduce) {
     if (warp == 1 + kMmaWarps) {
       // ======================= releaser =======================
-      // Per unit: once all MMA warps have written its output rows, one
-      // release add on the token tile's counter for the dependent launch.
-      if (lane == 0) {
-        for (uint32_t uit = 0;; ++uit) {
-          const uint32_t sb = uit & 1, par = (uit >> 1) & 1;
-          if (!bounded_wait(&bars->sfull[sb], par, abort, args.err)) break;
-          const int u = *reinterpret_cast<volatile int*>(&bars->unit[sb]);
-          if (u >= units) break;
-          if (!bounded_wait(&bars->udone[sb], par, abort, args.err)) break;
-          __threadfence();
-          atomicAdd(args.dep + 1 + u / args.n_blocks, 1u);
-          mbar_arrive(&bars->sempty[sb]);
-        }
-      }
+      if (lane == 0) release_loop(bars, abort, args.err, args.dep, args.n_blocks, units);
       return;
     }
   }
