@@ -84,8 +84,10 @@ __global__ void scale_range_kernel(const uint8_t* experts, uint64_t expert_strid
 // True when fp16(q * s) is finite and, for q != 0 and s != 0, a normal FP16
 // number (so it keeps 11 significant bits) for every code q and scale s of the
 // gate and up matrices (down = false) or of the down matrix (down = true).
+static std::mutex g_scale_range_mu;  // the two device words above serve one check at a time
 static bool scales_fit_f16(const mnw_moe_layer& L, bool down) {
   if (L.wfmt != MNW_FMT_INT8_G128 && L.wfmt != MNW_FMT_INT4_G128) return false;
+  std::lock_guard<std::mutex> lock(g_scale_range_mu);
   const uint32_t zero = 0, top = 0xFFFFu;
   if (cudaMemcpyToSymbol(g_scale_max_bits, &zero, sizeof(zero)) != cudaSuccess ||
       cudaMemcpyToSymbol(g_scale_min_bits, &top, sizeof(top)) != cudaSuccess)

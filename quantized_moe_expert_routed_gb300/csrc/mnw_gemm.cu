@@ -771,11 +771,12 @@ bool plan_smem(int wf, int am, bool gate_up, int K, int E, int BN, Plan* p) {
 template <int WF, int AM, bool GU>
 cudaError_t launch_one(const CUtensorMap* maps, const GemmArgs& a, size_t smem, int grid, cudaStream_t st) {
   auto kern = moe_gemm_kernel<WF, AM, GU>;
-  static bool attr = false;
-  if (!attr) {
+  static std::atomic<uint64_t> attr{0};
+  uint64_t bit;
+  if (attrs_needed(attr, &bit)) {
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(kSmemLimit));
     if (e != cudaSuccess) return e;
-    attr = true;
+    attrs_done(attr, bit);
   }
   return launch_pdl(kern, dim3(grid), dim3(kThreads), smem, st, maps[0], maps[1], maps[2], maps[3], maps[4], maps[5],
                     a);

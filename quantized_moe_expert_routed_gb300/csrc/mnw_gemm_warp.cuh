@@ -619,16 +619,17 @@ __global__ void __launch_bounds__(threads_for(kDep), ctas_per_sm(WF, NT))
 constexpr size_t kSmemPerSm = 232448;
 inline size_t smem_limit(int wf, int nt) { return ctas_per_sm(wf, nt) == 2 ? kSmemPerSm / 2 - 1024 : kSmemPerSm; }
 
-// One launch of an instance (sets its shared-memory limit on first use).
+// One launch of an instance (sets its shared-memory limit on first use per device).
 template <int WF, int AM, bool GU, int NT, int DEP>
 cudaError_t launch(const CUtensorMap* maps, const Args& a, size_t smem, int grid, cudaStream_t st) {
   auto kern = moe_gemm_warp_kernel<WF, AM, GU, NT, DEP>;
-  static bool attr = false;
-  if (!attr) {
+  static std::atomic<uint64_t> attr{0};
+  uint64_t bit;
+  if (attrs_needed(attr, &bit)) {
     cudaError_t e =
         cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem_limit(WF, NT)));
     if (e != cudaSuccess) return e;
-    attr = true;
+    attrs_done(attr, bit);
   }
   return launch_pdl(kern, dim3(grid), dim3(threads_for(DEP)), smem, st, maps[0], maps[1], maps[2], a);
 }

@@ -1,5 +1,6 @@
 // mnw_internal.h -- host-side state shared by the library's translation units.
 #pragma once
+#include <atomic>
 #include <cstddef>
 #include <cstdint>
 #include <cuda.h>
@@ -35,6 +36,20 @@ int current_sm_count();
 // overlaps that kernel's tail), and waits for that kernel's completion with
 // pdl_wait() before it touches global memory.  After a non-kernel stream
 // operation (a copy, a memset, an event) the launch is an ordinary one.
+// Kernel attributes are per device: `done` keeps one bit per device (0..63)
+// on which a kernel's attributes have been set.  Setting them twice, from two
+// threads, is harmless.
+inline bool attrs_needed(const std::atomic<uint64_t>& done, uint64_t* bit) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) {
+    *bit = 0;
+    return true;  // unknown device: set them every time
+  }
+  *bit = 1ull << dev;
+  return (done.load(std::memory_order_acquire) & *bit) == 0;
+}
+inline void attrs_done(std::atomic<uint64_t>& done, uint64_t bit) { done.fetch_or(bit, std::memory_order_release); }
+
 // Count of kernels this library has enqueued (mnw_moe_launch_count).
 void note_launch();
 

@@ -571,8 +571,9 @@ cudaError_t launch_permute(const int32_t* ids, int T, int k, int E, int32_t* off
                            int32_t* assign_pos, const void* x, int H, void* x_perm, uint32_t* err,
                            cudaStream_t st) {
   const int P = T * k;
-  static bool attr_set = false;
-  if (!attr_set) {
+  static std::atomic<uint64_t> attr{0};
+  uint64_t bit;
+  if (attrs_needed(attr, &bit)) {
     // tables for up to E = 1024 experts
     cudaError_t e = cudaFuncSetAttribute(permute_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          static_cast<int>((kPermWarps + 1) * 1024 * sizeof(int32_t)));
@@ -583,7 +584,7 @@ cudaError_t launch_permute(const int32_t* ids, int T, int k, int E, int32_t* off
       e = cudaFuncSetAttribute(permute_scan_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                static_cast<int>((48 * 1024) * sizeof(int32_t)));
     if (e != cudaSuccess) return e;
-    attr_set = true;
+    attrs_done(attr, bit);
   }
   cudaError_t e;
   if (P <= 8 * 8 * 32) {
