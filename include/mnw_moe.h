@@ -126,6 +126,14 @@ int mnw_moe_layer_info(const mnw_moe_layer* layer, int* wfmt, int* E, int* H, in
 int mnw_moe_permute(const int32_t* ids, int T, int k, int E, int32_t* expert_offsets,
                     int32_t* sorted_assign, int32_t* assign_pos, const void* x, int H,
                     void* x_perm, uint32_t* err, mnw_stream stream);
+/* The same permutation computed on the host, for a host-routing comparison
+ * path ("coder543/minnow" README, "Quantization": --host-routing): ids,
+ * expert_offsets, sorted_assign and assign_pos are HOST arrays with the
+ * layouts above, and the results are identical to mnw_moe_permute's.
+ * *dropped (may be NULL) receives the number of ids outside [0, E).  Needs
+ * no GPU.  Same limits as mnw_moe_permute. */
+int mnw_moe_permute_host(const int32_t* ids, int T, int k, int E, int32_t* expert_offsets,
+                         int32_t* sorted_assign, int32_t* assign_pos, uint32_t* dropped);
 
 /* a2 -- dynamic activation quantisation of R rows of K BF16 values.
  * Row r reads x[src] with src = r, or, when row_index (device int32 [R]) is

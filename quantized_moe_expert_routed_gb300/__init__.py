@@ -33,6 +33,7 @@ SIGNATURES = {
     "mnw_moe_layer_info": (_I, [_P, _P, _P, _P, _P]),
     "mnw_moe_permute": (_I, [_P, _I, _I, _I, _P, _P, _P, _P, _I, _P, _U32P, _P]),
     "mnw_moe_quantize_act": (_I, [_I, _P, _I, _I, _P, _I, _P, _P, _P, _P]),
+    "mnw_moe_permute_host": (_I, [_P, _I, _I, _I, _P, _P, _P, _U32P]),
     "mnw_moe_grouped_gemm_bf16": (_I, [_P, _I, _P, _P, _I, _P, _U32P, _P]),
     "mnw_moe_grouped_gemm_w8a16": (_I, [_P, _I, _P, _P, _I, _P, _U32P, _P]),
     "mnw_moe_grouped_gemm_w4a16": (_I, [_P, _I, _P, _P, _I, _P, _U32P, _P]),
@@ -137,6 +138,23 @@ def mnw_moe_permute(ids, E, x=None, stream=None, err=None):
     _check(load().mnw_moe_permute(_ptr(ids), T, k, E, _ptr(offsets), _ptr(sorted_assign), _ptr(assign_pos),
                                   _ptr(x), H, _ptr(x_perm), _ptr(err), _stream(stream)), "mnw_moe_permute")
     return offsets, sorted_assign, assign_pos, x_perm
+
+
+def mnw_moe_permute_host(ids, E):
+    """Host-side permutation (numpy int32 [T, k] in): (offsets, sorted_assign,
+    assign_pos, dropped) as numpy arrays, the same as mnw_moe_permute's."""
+    import numpy as np
+    ids = np.ascontiguousarray(ids, dtype=np.int32)
+    T, k = ids.shape
+    P = T * k
+    off = np.zeros(E + 1, np.int32)
+    sa = np.zeros(P, np.int32)
+    pos = np.zeros(P, np.int32)
+    dropped = ctypes.c_uint32()
+    p = lambda a: a.ctypes.data_as(ctypes.c_void_p)
+    _check(load().mnw_moe_permute_host(p(ids), T, k, E, p(off), p(sa), p(pos), ctypes.byref(dropped)),
+           "mnw_moe_permute_host")
+    return off, sa, pos, int(dropped.value)
 
 
 def mnw_moe_quantize_act(act, x, row_index=None, index_div=1, rows=None, stream=None):

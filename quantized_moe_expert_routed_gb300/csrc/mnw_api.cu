@@ -7,6 +7,7 @@
 #include <atomic>
 #include <cstring>
 #include <mutex>
+#include <vector>
 
 #include "mnw_internal.h"
 
@@ -354,6 +355,39 @@ int mnw_moe_permute(const int32_t* ids, int T, int k, int E, int32_t* expert_off
   cudaError_t e = launch_permute(ids, T, k, E, expert_offsets, sorted_assign, assign_pos, x, H, x_perm, err,
                                  static_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? MNW_OK : MNW_E_CUDA;
+}
+
+int mnw_moe_permute_host(const int32_t* ids, int T, int k, int E, int32_t* expert_offsets, int32_t* sorted_assign,
+                         int32_t* assign_pos, uint32_t* dropped) {
+  if (T < 0 || k < 1 || k > 32 || E < 1 || E > 1024) return MNW_E_INVALID_ARG;
+  if (static_cast<long long>(T) * k > (1LL << 24)) return MNW_E_UNSUPPORTED;
+  if (dropped) *dropped = 0;
+  if (T == 0) return MNW_OK;
+  if (!ids || !expert_offsets || !sorted_assign || !assign_pos) return MNW_E_INVALID_ARG;
+  const int P = T * k;
+  // counting sort by expert: counts, exclusive offsets, then one stable pass
+  for (int e = 0; e <= E; ++e) expert_offsets[e] = 0;
+  uint32_t bad = 0;
+  for (int a = 0; a < P; ++a) {
+    const int id = ids[a];
+    if (id >= 0 && id < E) ++expert_offsets[id + 1];
+    else ++bad;
+  }
+  for (int e = 0; e < E; ++e) expert_offsets[e + 1] += expert_offsets[e];
+  std::vector<int32_t> next(expert_offsets, expert_offsets + E);
+  for (int a = 0; a < P; ++a) {
+    const int id = ids[a];
+    if (id >= 0 && id < E) {
+      const int pos = next[id]++;
+      assign_pos[a] = pos;
+      sorted_assign[pos] = a;
+    } else {
+      assign_pos[a] = -1;
+    }
+  }
+  for (int p = expert_offsets[E]; p < P; ++p) sorted_assign[p] = -1;  // slots past the valid count
+  if (dropped) *dropped = bad;
+  return MNW_OK;
 }
 
 int mnw_moe_quantize_act(int act, const void* x, int R, int K, const int32_t* row_index, int index_div, void* codes,
