@@ -191,7 +191,9 @@ int mnw_moe_grouped_gemm_w4a16(const mnw_moe_layer* layer, int kind, const void*
  * out = bf16(f * (a . Wd^T)).  MNW_E_UNSUPPORTED when some q * s of the
  * matrices used would leave FP16's normal range (a scale above 65504 / qmax,
  * qmax = 127 or 8, or a non-zero scale below 2^-14); mnw_moe_forward then
- * keeps the BF16 form for that GEMM.  Kernel choice as for the other INT
+ * keeps the BF16 form for that GEMM.  A call with P = 0 launches nothing and
+ * only reports that: MNW_OK if the layer admits the form for `kind`,
+ * MNW_E_UNSUPPORTED if not.  Kernel choice as for the other INT
  * entries: below 32 tokens per expert on average the warp-MMA kernel, where
  * the codes stay exact FP16 integers and each group's FP32 dot product is
  * scaled by s afterwards (no fp16(q * s) rounding there). */
