@@ -123,6 +123,7 @@ def gate_up_bytes(wl: S.Workload, touched: int) -> int:
     for m in (S.GATE, S.UP):
         N, K = L.dims(m)
         per_expert += S.code_bytes(wl.wfmt, N, K) + S.scale_bytes(wl.wfmt, N, K)
+        per_expert += 4 if wl.wfmt == S.FMT_NVFP4_G16 else 0  # the matrix's FP32 outer scale
     act = {S.ACT_BF16: wl.H * 2, S.ACT_INT8_G128: wl.H + wl.H // 128 * 4,
            S.ACT_NVFP4_G16: wl.H // 2 + wl.H // 16 + 4}[wl.act]
     return touched * per_expert + wl.P * act + wl.P * wl.I * 2

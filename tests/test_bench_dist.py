@@ -73,3 +73,24 @@ def test_reference_arm_under_torchrun_prints_one_line_from_rank0():
     d = json.loads(lines[0])
     assert d["impl"] == "reference" and d["n_gpus"] == 2 and d["value"] > 0
     assert d["cpu_baseline"]["kind"] == "oracle" and d["e2e"]["h2d_bytes_per_step"] == 0
+
+
+def test_gate_up_algorithmic_bytes_by_hand():
+    """The roofline numerator, counted independently from the formats' storage
+    rules: per touched expert the gate and up codes and scales, plus the
+    gathered activation rows read and h written once."""
+    sys.path.insert(0, ROOT)
+    import bench
+    import synth as S
+    wl = S.WORKLOADS["decode_w4a16"]      # INT4: 0.5 B/code, FP16 scale per 128
+    P, H, I = wl.T * wl.k, wl.H, wl.I
+    per_expert = 2 * (I * H // 2 + I * (H // 128) * 2)
+    assert bench.gate_up_bytes(wl, 256) == 256 * per_expert + P * H * 2 + P * I * 2 == 287309824
+    wl = S.WORKLOADS["w8a8_2048"]         # INT8 codes, INT8 activations with an FP32 scale per 128
+    P, H, I = wl.T * wl.k, wl.H, wl.I
+    per_expert = 2 * (I * H + I * (H // 128) * 2)
+    assert bench.gate_up_bytes(wl, 256) == 256 * per_expert + P * (H + H // 128 * 4) + P * I * 2
+    wl = S.WORKLOADS["prefill_nvfp4"]     # E2M1 codes, E4M3 per 16, FP32 outer per matrix; same for activations
+    P, H, I = wl.T * wl.k, wl.H, wl.I
+    per_expert = 2 * (I * H // 2 + I * (H // 16) + 4)
+    assert bench.gate_up_bytes(wl, 200) == 200 * per_expert + P * (H // 2 + H // 16 + 4) + P * I * 2
