@@ -14,8 +14,9 @@
  * weights dequantised to BF16 (W4A16/W8A16); the optional INT8 activation
  * mode (W4A8/W8A8: activations quantised per group of 128 with an FP32 scale,
  * INT32 group dot products, scales applied in FP32); NVFP4 W4A4 with
- * activations quantised to E2M1 / E4M3-per-16 / FP32-per-row; fused
- * gate/up/SiLU kernels and GPU routing for 32-token decode blocks.
+ * activations quantised to E2M1 / E4M3-per-16 / FP32-per-row.  The
+ * README also names a fused gate/up/SiLU step and grouping the tokens of a
+ * 32-token decode block by expert on the GPU.
  *
  * Conventions for every call below
  *  - Pointers marked "device" are CUDA device pointers owned by the caller;
@@ -111,7 +112,8 @@ void mnw_moe_layer_destroy(mnw_moe_layer* layer);
 /* Shape of a layer: any output pointer may be NULL. */
 int mnw_moe_layer_info(const mnw_moe_layer* layer, int* wfmt, int* E, int* H, int* I);
 
-/* a1 -- token permutation ("GPU routing", minnow README, "Quantization").
+/* a1 -- token permutation: grouping the assignments by expert on the GPU
+ * ("coder543/minnow" README, section "Quantization").
  * ids: device int32 [T*k], assignment a = t*k + j goes to expert ids[a].
  * Writes (device): expert_offsets int32 [E+1] (exclusive prefix of the
  * per-expert counts; expert_offsets[E] = number of valid assignments),

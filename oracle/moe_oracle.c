@@ -14,10 +14,10 @@
  *            activations with an FP32 outer scale per input row; W8A8/W4A8
  *            quantise expert inputs to signed INT8 with FP32 scales per 128
  *            values, use INT32 group dot products and combine scaled groups
- *            in FP32; expert outputs return to BF16.
+ *            in FP32; the layer's outputs are BF16 again.
  *
- * Readings where the pages are silent are listed in the repository's design
- * notes; each is restated at the point of use below.
+ * Where the pages are silent, the reading taken is stated at the point of
+ * use below.
  *
  * Build: plain C11, -ffp-contract=off (no fused multiply-add contraction), no
  * fast-math, so that every float expression rounds as written.

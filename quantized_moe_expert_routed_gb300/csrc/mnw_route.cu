@@ -1,8 +1,9 @@
 // mnw_route.cu -- token permutation into expert-sorted order, the row gather,
 // and the top-k weighted combine.
 //
-// Permutation ("GPU routing for 32-token decode blocks", coder543/minnow
-// README, "Quantization"): a single CTA ranks every assignment a = t*k + j
+// Permutation (the grouping by expert that the "coder543/minnow" README,
+// section "Quantization", runs on the GPU for decode blocks): a single CTA
+// ranks every assignment a = t*k + j
 // stably within its expert, with no atomics whose order could leak into the
 // result.  Each of the 32 warps owns a contiguous segment of assignments; a
 // first pass counts per (warp, expert) with warp match-any groups, a scan over
