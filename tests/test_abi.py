@@ -85,3 +85,27 @@ def test_blob_header_checks(lib):
     assert lib.mnw_moe_layer_init(bytes(bad), fake_dev, 1 << 30, ctypes.byref(out)) == 3
     # misaligned blob pointer
     assert lib.mnw_moe_layer_init(bytes(hdr), ctypes.c_void_p((1 << 20) + 16), 1 << 30, ctypes.byref(out)) == 1
+
+
+def test_package_fails_loudly_without_its_library(tmp_path):
+    """No CPU or PyTorch fallback: with the library absent and no compiler to
+    build it, loading the package's library raises."""
+    import subprocess
+    import sys
+    code = f"""
+import sys
+sys.path.insert(0, {ROOT!r})
+import quantized_moe_expert_routed_gb300 as M
+from quantized_moe_expert_routed_gb300 import build as B
+B.LIB = {str(tmp_path / "libmnw_moe.so")!r}
+B.BUILD = {str(tmp_path / "_build")!r}
+try:
+    M.load()
+except RuntimeError as e:
+    print("RAISED:", e)
+else:
+    print("LOADED")
+"""
+    env = dict(os.environ, NVCC=str(tmp_path / "no-such-nvcc"))
+    r = subprocess.run([sys.executable, "-c", code], env=env, capture_output=True, text=True, timeout=120)
+    assert "RAISED:" in r.stdout and "nvcc not found" in r.stdout, r.stdout + r.stderr
