@@ -252,6 +252,7 @@ const char* mnw_status_string(int status) {
 }
 
 int mnw_moe_layer_init(const void* header_host, const void* blob_dev, size_t blob_bytes, mnw_moe_layer** out) {
+  MNW_RANGE("mnw_moe_layer_init");
   if (!header_host || !blob_dev || !out) return MNW_E_INVALID_ARG;
   *out = nullptr;
   if (!aligned(blob_dev, 256)) return MNW_E_INVALID_ARG;
@@ -346,6 +347,7 @@ int mnw_moe_layer_info(const mnw_moe_layer* L, int* wfmt, int* E, int* H, int* I
 
 int mnw_moe_permute(const int32_t* ids, int T, int k, int E, int32_t* expert_offsets, int32_t* sorted_assign,
                     int32_t* assign_pos, const void* x, int H, void* x_perm, uint32_t* err, mnw_stream stream) {
+  MNW_RANGE("mnw_moe_permute");
   if (T < 0 || k < 1 || k > 32 || E < 1 || E > 1024) return MNW_E_INVALID_ARG;
   if (static_cast<long long>(T) * k > (1LL << 24)) return MNW_E_UNSUPPORTED;
   if (T == 0) return MNW_OK;
@@ -359,6 +361,7 @@ int mnw_moe_permute(const int32_t* ids, int T, int k, int E, int32_t* expert_off
 
 int mnw_moe_permute_host(const int32_t* ids, int T, int k, int E, int32_t* expert_offsets, int32_t* sorted_assign,
                          int32_t* assign_pos, uint32_t* dropped) {
+  MNW_RANGE("mnw_moe_permute_host");
   if (T < 0 || k < 1 || k > 32 || E < 1 || E > 1024) return MNW_E_INVALID_ARG;
   if (static_cast<long long>(T) * k > (1LL << 24)) return MNW_E_UNSUPPORTED;
   if (dropped) *dropped = 0;
@@ -392,6 +395,7 @@ int mnw_moe_permute_host(const int32_t* ids, int T, int k, int E, int32_t* exper
 
 int mnw_moe_quantize_act(int act, const void* x, int R, int K, const int32_t* row_index, int index_div, void* codes,
                          void* scales, float* row_outer, mnw_stream stream) {
+  MNW_RANGE("mnw_moe_quantize_act");
   if (R < 0 || K <= 0) return MNW_E_INVALID_ARG;
   if (row_index && index_div < 1) return MNW_E_INVALID_ARG;
   if (act == MNW_ACT_F16_ROWS) {
@@ -421,16 +425,19 @@ int mnw_moe_quantize_act(int act, const void* x, int R, int K, const int32_t* ro
 
 int mnw_moe_grouped_gemm_bf16(const mnw_moe_layer* L, int kind, const void* a, const int32_t* offs, int P, void* out,
                               uint32_t* err, mnw_stream stream) {
+  MNW_RANGE("mnw_moe_grouped_gemm_bf16");
   return run_gemm(L, MNW_FMT_BF16, MNW_ACT_BF16, kind, a, nullptr, nullptr, offs, P, out, nullptr, err,
                   static_cast<cudaStream_t>(stream));
 }
 int mnw_moe_grouped_gemm_w8a16(const mnw_moe_layer* L, int kind, const void* a, const int32_t* offs, int P, void* out,
                                uint32_t* err, mnw_stream stream) {
+  MNW_RANGE("mnw_moe_grouped_gemm_w8a16");
   return run_gemm(L, MNW_FMT_INT8_G128, MNW_ACT_BF16, kind, a, nullptr, nullptr, offs, P, out, nullptr, err,
                   static_cast<cudaStream_t>(stream));
 }
 int mnw_moe_grouped_gemm_w4a16(const mnw_moe_layer* L, int kind, const void* a, const int32_t* offs, int P, void* out,
                                uint32_t* err, mnw_stream stream) {
+  MNW_RANGE("mnw_moe_grouped_gemm_w4a16");
   return run_gemm(L, MNW_FMT_INT4_G128, MNW_ACT_BF16, kind, a, nullptr, nullptr, offs, P, out, nullptr, err,
                   static_cast<cudaStream_t>(stream));
 }
@@ -443,30 +450,36 @@ static int gemm_f16rows(const mnw_moe_layer* L, int wfmt, int kind, const void* 
 }
 int mnw_moe_grouped_gemm_w8a16_f16rows(const mnw_moe_layer* L, int kind, const void* a, const float* f,
                                        const int32_t* offs, int P, void* out, uint32_t* err, mnw_stream stream) {
+  MNW_RANGE("mnw_moe_grouped_gemm_w8a16_f16rows");
   return gemm_f16rows(L, MNW_FMT_INT8_G128, kind, a, f, offs, P, out, err, static_cast<cudaStream_t>(stream));
 }
 int mnw_moe_grouped_gemm_w4a16_f16rows(const mnw_moe_layer* L, int kind, const void* a, const float* f,
                                        const int32_t* offs, int P, void* out, uint32_t* err, mnw_stream stream) {
+  MNW_RANGE("mnw_moe_grouped_gemm_w4a16_f16rows");
   return gemm_f16rows(L, MNW_FMT_INT4_G128, kind, a, f, offs, P, out, err, static_cast<cudaStream_t>(stream));
 }
 int mnw_moe_grouped_gemm_w8a8(const mnw_moe_layer* L, int kind, const int8_t* q, const float* s, const int32_t* offs,
                               int P, void* out, int32_t* dots, uint32_t* err, mnw_stream stream) {
+  MNW_RANGE("mnw_moe_grouped_gemm_w8a8");
   return run_gemm(L, MNW_FMT_INT8_G128, MNW_ACT_INT8_G128, kind, q, s, nullptr, offs, P, out, dots, err,
                   static_cast<cudaStream_t>(stream));
 }
 int mnw_moe_grouped_gemm_w4a8(const mnw_moe_layer* L, int kind, const int8_t* q, const float* s, const int32_t* offs,
                               int P, void* out, int32_t* dots, uint32_t* err, mnw_stream stream) {
+  MNW_RANGE("mnw_moe_grouped_gemm_w4a8");
   return run_gemm(L, MNW_FMT_INT4_G128, MNW_ACT_INT8_G128, kind, q, s, nullptr, offs, P, out, dots, err,
                   static_cast<cudaStream_t>(stream));
 }
 int mnw_moe_grouped_gemm_nvfp4(const mnw_moe_layer* L, int kind, const uint8_t* c, const uint8_t* sf, const float* o,
                                const int32_t* offs, int P, void* out, uint32_t* err, mnw_stream stream) {
+  MNW_RANGE("mnw_moe_grouped_gemm_nvfp4");
   return run_gemm(L, MNW_FMT_NVFP4_G16, MNW_ACT_NVFP4_G16, kind, c, sf, o, offs, P, out, nullptr, err,
                   static_cast<cudaStream_t>(stream));
 }
 
 int mnw_moe_combine(const void* y, const int32_t* assign_pos, const float* w, int T, int k, int H, void* out,
                     mnw_stream stream) {
+  MNW_RANGE("mnw_moe_combine");
   if (T < 0 || k < 1 || k > 32 || H <= 0 || H % 8) return MNW_E_INVALID_ARG;
   if (T == 0) return MNW_OK;
   if (!y || !assign_pos || !w || !out || !aligned(y, 16) || !aligned(out, 16)) return MNW_E_INVALID_ARG;
@@ -486,6 +499,7 @@ uint32_t* mnw_moe_workspace_error_word(void* ws) { return static_cast<uint32_t*>
 
 int mnw_moe_forward(const mnw_moe_layer* L, int act, const void* x, const int32_t* ids, const float* w, int T, int k,
                     void* out, void* ws, size_t ws_bytes, mnw_stream stream) {
+  MNW_RANGE("mnw_moe_forward");
   if (!L || T < 0 || k < 1 || k > 32 || k > L->E) return MNW_E_INVALID_ARG;
   if (!act_allowed(L->wfmt, act)) return MNW_E_MODE;
   if (T == 0) return MNW_OK;
@@ -582,6 +596,7 @@ static void* mapped_alias(const void* host, size_t align) {
 int mnw_moe_forward_host(const mnw_moe_layer* L, int act, const void* x_host, const int32_t* ids_host,
                          const float* w_host, int T, int k, void* out_host, void* ws, size_t ws_bytes,
                          mnw_stream stream) {
+  MNW_RANGE("mnw_moe_forward_host");
   if (!L || T < 0 || k < 1) return MNW_E_INVALID_ARG;
   if (T == 0) return MNW_OK;
   if (!x_host || !ids_host || !w_host || !out_host || !ws) return MNW_E_INVALID_ARG;

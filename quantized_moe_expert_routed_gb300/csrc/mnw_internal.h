@@ -6,6 +6,8 @@
 #include <cuda.h>
 #include <cuda_runtime.h>
 
+#include <nvtx3/nvToolsExt.h>
+
 #include "../../include/mnw_moe.h"
 
 struct mnw_moe_layer {
@@ -49,6 +51,16 @@ inline bool attrs_needed(const std::atomic<uint64_t>& done, uint64_t* bit) {
   return (done.load(std::memory_order_acquire) & *bit) == 0;
 }
 inline void attrs_done(std::atomic<uint64_t>& done, uint64_t bit) { done.fetch_or(bit, std::memory_order_release); }
+
+// An NVTX range named after the C-ABI call it covers, for profiler timelines
+// (a no-op unless a tool is attached).
+struct NvtxRange {
+  explicit NvtxRange(const char* name) { nvtxRangePushA(name); }
+  ~NvtxRange() { nvtxRangePop(); }
+  NvtxRange(const NvtxRange&) = delete;
+  NvtxRange& operator=(const NvtxRange&) = delete;
+};
+#define MNW_RANGE(name) ::mnw::NvtxRange mnw_nvtx_range_(name)
 
 // Count of kernels this library has enqueued (mnw_moe_launch_count).
 void note_launch();
