@@ -349,6 +349,72 @@ def run_oracle_sample(wl: S.Workload, ntok: int, inputs=None):
     return ntok / dt, dt
 
 
+def profile_traffic(wl: S.Workload):
+    """DRAM traffic (read + write bytes) of one gate/up launch, from the ncu
+    capture summarised in profiles/ (lines "<workload> <bytes> <summary file>");
+    None for a workload without a capture of the current kernel."""
+    try:
+        with open(os.path.join(ROOT, "profiles", "gate_up_dram_traffic.txt")) as f:
+            for ln in f:
+                parts = ln.split()
+                if len(parts) >= 2 and parts[0] == wl.name:
+                    return int(parts[1])
+    except OSError:
+        pass
+    return None
+
+
+def build_line(args, wl: S.Workload, config: dict, r: dict, cpu, traffic) -> dict:
+    """The JSON line of the GPU arm from run_ours' measurements r, the CPU
+    baseline (tokens/s, seconds, sample tokens) and the captured traffic."""
+    hbm, bf16_peak, peak_kind = _peaks()
+    ms = r["total_ms"] / args.steps
+    value = r["world"] * wl.T / (r["total_ms"] / args.steps / 1e3)
+    gu_ms = statistics.mean(r["gu_ms"])
+    gu_bytes = gate_up_bytes(wl, r["touched"])
+    achieved = gu_bytes / (gu_ms / 1e3) / 1e9
+    # The gate/up launch's binding roofline: its arithmetic intensity against
+    # the ridge of the measured peaks.  Its MMAs are 16-bit (BF16, or FP16 on
+    # exact integer / block-scaled FP4 values), so the tensor peak is the
+    # measured dense BF16 one (the kernel is timed alone: the burst figure).
+    valid = int(((r["ids"] >= 0) & (r["ids"] < wl.E)).sum())
+    gu_flops = 2.0 * 2 * wl.H * wl.I * valid
+    gu_tflops = gu_flops / (gu_ms / 1e3) / 1e12
+    tensor_bound = gu_flops / gu_bytes > bf16_peak * 1e12 / (hbm * 1e9)
+    layer_bytes = S.algorithmic_bytes(wl, r["ids"].cpu())
+    e2e_ms = r["e2e_ms"]  # the slowest replica's median
+    h2d = r["world"] * (wl.T * wl.H * 2 + wl.P * 4 * 2)  # x, ids, w of every replica
+    d2h = r["world"] * wl.T * wl.H * 2
+    cpu_rate, cpu_dt, ntok = cpu
+    dtype = {S.ACT_BF16: "bf16", S.ACT_INT8_G128: "int8xint8->f32 (f16 MMA)",
+             S.ACT_NVFP4_G16: "e2m1xe2m1->f32 (f16 MMA)"}[wl.act]
+    line = {
+        "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": r["world"], "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": dtype, "data": "synthetic (seeded, shapes of the workload)",
+        "config": config,
+        "layer_effective_gbs": layer_bytes / (ms / 1e3) / 1e9,
+        "roofline": ({"kernel": "grouped gate/up/SiLU GEMM", "bound": "tensor", "achieved": gu_tflops,
+                      "peak": bf16_peak, "unit": "TFLOP/s", "frac": gu_tflops / bf16_peak, "peak_kind": peak_kind,
+                      "flops_per_launch": gu_flops, "launch_ms": gu_ms, "traffic": traffic,
+                      "hbm": {"achieved": achieved, "peak": hbm, "unit": "GB/s", "frac": achieved / hbm,
+                              "bytes_per_launch": gu_bytes}}
+                     if tensor_bound else
+                     {"kernel": "grouped gate/up/SiLU GEMM", "bound": "hbm", "achieved": achieved, "peak": hbm,
+                      "unit": "GB/s", "frac": achieved / hbm, "peak_kind": peak_kind,
+                      "bytes_per_launch": gu_bytes, "launch_ms": gu_ms, "traffic": traffic,
+                      "tensor": {"achieved": gu_tflops, "peak": bf16_peak, "unit": "TFLOP/s",
+                                 "frac": gu_tflops / bf16_peak, "flops_per_launch": gu_flops}}),
+        "cpu_baseline": {"value": cpu_rate, "unit": "tokens/s", "cores": 1, "kind": "oracle",
+                         "sample": f"{ntok} of {wl.T} tokens, {cpu_dt:.1f} s single-threaded"},
+        "e2e": {"value": r["world"] * wl.T / (e2e_ms / 1e3), "unit": "tokens/s", "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h},
+        "gpu_launches": r["launches"],
+        "clocks": r["clocks"],
+    }
+    return line
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -395,67 +461,10 @@ def main():
     r = run_ours(args, wl)
     if rank != 0:
         return
-    hbm, bf16_peak, peak_kind = _peaks()
-    ms = r["total_ms"] / args.steps
-    value = r["world"] * wl.T / (r["total_ms"] / args.steps / 1e3)
-    gu_ms = statistics.mean(r["gu_ms"])
-    gu_bytes = gate_up_bytes(wl, r["touched"])
-    achieved = gu_bytes / (gu_ms / 1e3) / 1e9
-    # The gate/up launch's binding roofline: its arithmetic intensity against
-    # the ridge of the measured peaks.  Its MMAs are 16-bit (BF16, or FP16 on
-    # exact integer / block-scaled FP4 values), so the tensor peak is the
-    # measured dense BF16 one (the kernel is timed alone: the burst figure).
-    valid = int(((r["ids"] >= 0) & (r["ids"] < wl.E)).sum())
-    gu_flops = 2.0 * 2 * wl.H * wl.I * valid
-    gu_tflops = gu_flops / (gu_ms / 1e3) / 1e12
-    tensor_bound = gu_flops / gu_bytes > bf16_peak * 1e12 / (hbm * 1e9)
-    layer_bytes = S.algorithmic_bytes(wl, r["ids"].cpu())
-    e2e_ms = r["e2e_ms"]  # the slowest replica's median
-    h2d = r["world"] * (wl.T * wl.H * 2 + wl.P * 4 * 2)  # x, ids, w of every replica
-    d2h = r["world"] * wl.T * wl.H * 2
-
     # CPU baseline: the oracle on a bounded token sample, rank 0 only
     ntok = cpu_sample_tokens(wl, args.cpu_budget)
     cpu_rate, cpu_dt = run_oracle_sample(wl, ntok)
-
-    # DRAM traffic (read + write bytes) of one gate/up launch, from the ncu
-    # capture summarised in profiles/ (lines "<workload> <bytes> <summary file>");
-    # null for a workload without a capture of the current kernel.
-    profile_traffic = None
-    try:
-        with open(os.path.join(ROOT, "profiles", "gate_up_dram_traffic.txt")) as f:
-            for ln in f:
-                parts = ln.split()
-                if len(parts) >= 2 and parts[0] == wl.name:
-                    profile_traffic = int(parts[1])
-    except OSError:
-        pass
-    dtype = {S.ACT_BF16: "bf16", S.ACT_INT8_G128: "int8xint8->f32 (f16 MMA)",
-             S.ACT_NVFP4_G16: "e2m1xe2m1->f32 (f16 MMA)"}[wl.act]
-    line = {
-        "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": r["world"], "steps": args.steps,
-        "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
-        "vs_baseline": None, "dtype": dtype, "data": "synthetic (seeded, shapes of the workload)",
-        "config": config,
-        "layer_effective_gbs": layer_bytes / (ms / 1e3) / 1e9,
-        "roofline": ({"kernel": "grouped gate/up/SiLU GEMM", "bound": "tensor", "achieved": gu_tflops,
-                      "peak": bf16_peak, "unit": "TFLOP/s", "frac": gu_tflops / bf16_peak, "peak_kind": peak_kind,
-                      "flops_per_launch": gu_flops, "launch_ms": gu_ms, "traffic": profile_traffic,
-                      "hbm": {"achieved": achieved, "peak": hbm, "unit": "GB/s", "frac": achieved / hbm,
-                              "bytes_per_launch": gu_bytes}}
-                     if tensor_bound else
-                     {"kernel": "grouped gate/up/SiLU GEMM", "bound": "hbm", "achieved": achieved, "peak": hbm,
-                      "unit": "GB/s", "frac": achieved / hbm, "peak_kind": peak_kind,
-                      "bytes_per_launch": gu_bytes, "launch_ms": gu_ms, "traffic": profile_traffic,
-                      "tensor": {"achieved": gu_tflops, "peak": bf16_peak, "unit": "TFLOP/s",
-                                 "frac": gu_tflops / bf16_peak, "flops_per_launch": gu_flops}}),
-        "cpu_baseline": {"value": cpu_rate, "unit": "tokens/s", "cores": 1, "kind": "oracle",
-                         "sample": f"{ntok} of {wl.T} tokens, {cpu_dt:.1f} s single-threaded"},
-        "e2e": {"value": r["world"] * wl.T / (e2e_ms / 1e3), "unit": "tokens/s", "h2d_bytes_per_step": h2d,
-                "d2h_bytes_per_step": d2h},
-        "gpu_launches": r["launches"],
-        "clocks": r["clocks"],
-    }
+    line = build_line(args, wl, config, r, (cpu_rate, cpu_dt, ntok), profile_traffic(wl))
     print(json.dumps(line))
 
 

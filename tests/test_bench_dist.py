@@ -94,3 +94,49 @@ def test_gate_up_algorithmic_bytes_by_hand():
     P, H, I = wl.T * wl.k, wl.H, wl.I
     per_expert = 2 * (I * H // 2 + I * (H // 16) + 4)
     assert bench.gate_up_bytes(wl, 200) == 200 * per_expert + P * (H // 2 + H // 16 + 4) + P * I * 2
+
+
+def test_gpu_arm_json_line_contract():
+    """The GPU arm's JSON line, built from fabricated measurements: every key of
+    the contract, the whole-job value, and the roofline bound chosen by
+    arithmetic intensity (HBM for the decode batch, tensor for the large
+    W4A16 batch)."""
+    import argparse
+    sys.path.insert(0, ROOT)
+    import bench
+    import synth as S
+    args = argparse.Namespace(steps=10, warmup=3)
+    hbm, bf16, kind = bench._peaks()
+    for name, step_ms, gu_ms, bound in (("decode_w4a16", 0.1351, 0.0785, "hbm"),
+                                        ("large_w4a16", 1.9172, 1.1123, "tensor")):
+        wl = S.WORKLOADS[name]
+        ids = S.routing_uniform(wl.T, wl.E, wl.k, seed=1)
+        r = dict(total_ms=10 * step_ms, gu_ms=[gu_ms] * 10, touched=wl.E, ids=ids, e2e_ms=0.174, world=2,
+                 launches=100, clocks={"sm_mhz": 2070.0, "sm_max_mhz": 2070.0, "reasons": []})
+        line = bench.build_line(args, wl, {"workload": name}, r, (4.4, 10.0, 12), 12345)
+        for key in ("metric", "value", "unit", "n_gpus", "steps", "warmup", "ms_per_step", "higher_is_better",
+                    "scaling", "vs_baseline", "dtype", "data", "config", "roofline", "cpu_baseline", "e2e",
+                    "gpu_launches", "clocks"):
+            assert key in line, key
+        assert line["value"] == pytest.approx(2 * wl.T / (step_ms / 1e3))  # whole job: both replicas
+        assert line["n_gpus"] == 2 and line["scaling"] == "weak" and line["higher_is_better"] is True
+        roof = line["roofline"]
+        for key in ("bound", "achieved", "peak", "unit", "frac", "traffic"):
+            assert key in roof, key
+        assert roof["bound"] == bound and roof["traffic"] == 12345
+        assert roof["frac"] == pytest.approx(roof["achieved"] / roof["peak"])
+        if bound == "hbm":
+            assert roof["peak"] == hbm and roof["unit"] == "GB/s"
+            assert roof["achieved"] == pytest.approx(bench.gate_up_bytes(wl, wl.E) / (gu_ms / 1e3) / 1e9)
+        else:
+            assert roof["peak"] == bf16 and roof["unit"] == "TFLOP/s"
+            assert roof["achieved"] == pytest.approx(2 * 2 * wl.H * wl.I * wl.T * wl.k / (gu_ms / 1e3) / 1e12)
+        cb = line["cpu_baseline"]
+        assert cb["kind"] == "oracle" and cb["cores"] == 1 and cb["value"] == 4.4 and "sample" in cb
+        e2e = line["e2e"]
+        assert e2e["value"] == pytest.approx(2 * wl.T / 0.174e-3)
+        assert e2e["h2d_bytes_per_step"] == 2 * (wl.T * wl.H * 2 + wl.T * wl.k * 8)
+        assert e2e["d2h_bytes_per_step"] == 2 * wl.T * wl.H * 2
+    # the captured traffic is read from the committed ncu summary table
+    assert bench.profile_traffic(S.WORKLOADS["decode_w4a16"]) == 291030784
+    assert bench.profile_traffic(S.WORKLOADS["tiny_w8a16"]) is None
