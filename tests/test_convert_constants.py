@@ -54,3 +54,70 @@ def test_every_nibble_in_every_position_decodes_exactly():
             lo, hi = _j4(w, j >= 2, consts)
             out = (lo if j % 2 == 0 else hi)[1 if pos >= 4 else 0]
             assert np.all(out.astype(np.float64) == want), (pos, n)
+
+
+CONVERT = os.path.join(ROOT, "quantized_moe_expert_routed_gb300", "csrc", "mnw_convert.cuh")
+ROUTE = os.path.join(ROOT, "quantized_moe_expert_routed_gb300", "csrc", "mnw_route.cu")
+
+
+def _prmt(a, b, sel):
+    """PTX prmt.b32 (default mode): result byte i is byte (sel >> 4i) & 7 of {b:a}."""
+    a = np.asarray(a, np.uint64)
+    b = np.asarray(b, np.uint64)
+    src = a | (b << np.uint64(32))
+    out = np.zeros_like(a)
+    for i in range(4):
+        k = (sel >> (4 * i)) & 7
+        out |= ((src >> np.uint64(8 * k)) & np.uint64(0xFF)) << np.uint64(8 * i)
+    return out.astype(np.uint32)
+
+
+def test_natural_pair_int4_and_int8_to_fp16():
+    conv = open(CONVERT).read()
+    for expr in ("prmt(w[i], hi, 0x0400u + 0x0101u * b)",
+                 "f16x2_sub(and_xor(x, 0x000F000Fu, 0x64086408u), 0x64086408u)",
+                 "f16x2_sub(prmt(u, 0x64646464u, 0x4140u), 0x64806480u)",
+                 "f16x2_sub(prmt(u, 0x64646464u, 0x4342u), 0x64806480u)",
+                 "const uint32_t u = w[i] ^ 0x80808080u;"):
+        assert expr in conv, expr   # the replay below follows these lines
+    rng = np.random.default_rng(1)
+    w = rng.integers(0, 2 ** 32, 4096, dtype=np.uint64).astype(np.uint32)
+    nib = np.stack([(w >> (4 * i)) & 0xF for i in range(8)]).astype(np.int64)
+    q4 = np.where(nib >= 8, nib - 16, nib)                      # element e = nibble e, signed
+    hi = w >> 4
+    for b in range(4):                                           # INT4: byte b -> elements 2b, 2b+1
+        x = _prmt(w, hi, 0x0400 + 0x0101 * b)
+        a = (x & 0x000F000F) ^ 0x64086408
+        lo, hh = _halves(a)
+        c0, c1 = _halves(np.uint32(0x64086408))
+        assert np.array_equal((lo - c0).astype(np.int64), q4[2 * b])
+        assert np.array_equal((hh - c1).astype(np.int64), q4[2 * b + 1])
+    u = w ^ np.uint32(0x80808080)                                # INT8: bytes 0..3 -> elements 0..3
+    q8 = np.stack([((w >> (8 * i)) & 0xFF).astype(np.int64) for i in range(4)])
+    q8 = np.where(q8 >= 128, q8 - 256, q8)
+    for sel, e0 in ((0x4140, 0), (0x4342, 2)):
+        lo, hh = _halves(_prmt(u, np.full_like(u, 0x64646464), sel))
+        c0, c1 = _halves(np.uint32(0x64806480))
+        assert np.array_equal((lo - c0).astype(np.int64), q8[e0])
+        assert np.array_equal((hh - c1).astype(np.int64), q8[e0 + 1])
+
+
+def test_fp16_row_exponent_rule_matches_the_oracle():
+    """The gather kernel derives the row exponent from the largest BF16 bit
+    pattern: e = clamp((bits >> 7) - 141, -110, 113).  Replayed on the host it
+    must give the oracle's encoding bit for bit."""
+    import torch
+    import oracle as O
+    assert "const int e = min(113, max(-110, static_cast<int>(m >> 7) - 141));" in open(ROUTE).read()
+    rng = np.random.default_rng(2)
+    x = rng.standard_normal((64, 256)) * np.exp2(rng.integers(-90, 90, (64, 1)).astype(np.float64))
+    x[3] = 0.0
+    xb = torch.tensor(x, dtype=torch.float32).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+    codes, factor = O.encode_f16_rows(xb)
+    for r in range(64):
+        m = int((xb[r] & 0x7FFF).max())
+        e = min(113, max(-110, (m >> 7) - 141))
+        vals = (xb[r].astype(np.uint32) << 16).view(np.float32)
+        got = (vals * np.float32(2.0 ** -e)).astype(np.float16).view(np.uint16)  # exact scaling, one rounding
+        assert factor[r] == np.float32(2.0 ** e)
+        assert np.array_equal(got, codes[r]), r
