@@ -261,11 +261,16 @@ def _pack_nibbles(q: torch.Tensor) -> torch.Tensor:
     return u[..., 0::2] | (u[..., 1::2] << 4)
 
 
-def _nvfp4_matrix(seed: int, stream: int, E: int, N: int, K: int, device, sigma: float):
+def _nvfp4_matrix(seed: int, stream: int, E: int, N: int, K: int, device, sigma: float,
+                  sf_range: str = "narrow"):
     """Direct draw of NVFP4 weights: E2M1 magnitude index from a fixed
-    half-normal-like table, uniform sign; E4M3 block-scale bytes uniform in
-    [0x30, 0x38] (0.5 .. 1.0); outer = sigma / 1.6 per matrix (a gentle
-    per-expert jitter keeps experts distinct)."""
+    half-normal-like table, uniform sign.  sf_range "narrow" (the workloads):
+    E4M3 block-scale bytes uniform in [0x30, 0x38] (0.5 .. 1.0), outer =
+    sigma / 1.6 per matrix with a gentle per-expert jitter.  sf_range "full"
+    (edge-case tests): block-scale bytes uniform over every non-negative
+    finite E4M3 code 0x00 .. 0x7E (zero, the subnormals 2^-9 .. 7 * 2^-9, up
+    to 448), and outer scales spread over 2^-3 .. 2^3 around a base chosen so
+    that the weights' RMS stays near sigma."""
     n = E * N * K
     b = bits32(seed, stream, _counters(n, device))
     # magnitude index 0..7 -> thresholds on 16 bits (cumulative probabilities)
@@ -275,16 +280,22 @@ def _nvfp4_matrix(seed: int, stream: int, E: int, N: int, K: int, device, sigma:
     codes = (mag | (sign << 3)).to(torch.uint8).reshape(E, N, K)
     packed = codes[..., 0::2] | (codes[..., 1::2] << 4)
     sb = bits32(seed, stream + 1, _counters(E * N * (K // 16), device))
-    sf = (0x30 + (sb % 9)).to(torch.uint8).reshape(E, N, K // 16)
     jit = bits32(seed, stream + 2, _counters(E, device)).to(torch.float64) / 4294967296.0
-    outer = ((sigma / 1.6) * (0.75 + 0.5 * jit)).to(torch.float32)
+    if sf_range == "full":
+        sf = (sb % 127).to(torch.uint8).reshape(E, N, K // 16)
+        # RMS of a block scale drawn uniformly over the 127 codes is about 110,
+        # of an E2M1 value from the table about 1.6
+        outer = ((sigma / 176.0) * torch.pow(2.0, 6.0 * jit - 3.0)).to(torch.float32)
+    else:
+        sf = (0x30 + (sb % 9)).to(torch.uint8).reshape(E, N, K // 16)
+        outer = ((sigma / 1.6) * (0.75 + 0.5 * jit)).to(torch.float32)
     return packed, sf, outer
 
 
 def expert_blob(wfmt: int, E: int, H: int, I: int, seed: int, sigma: float = 0.02,
-                device="cpu", stream: int = 1000):
+                device="cpu", stream: int = 1000, nvfp4_sf_range: str = "narrow"):
     """Build the packed expert blob.  Returns (blob uint8 tensor on `device`,
-    header bytes, BlobLayout)."""
+    header bytes, BlobLayout).  nvfp4_sf_range: see _nvfp4_matrix."""
     L = layout(wfmt, E, H, I)
     body = torch.zeros((E, L.expert_stride), dtype=torch.uint8, device=device)
     for m in (GATE, UP, DOWN):
@@ -292,7 +303,7 @@ def expert_blob(wfmt: int, E: int, H: int, I: int, seed: int, sigma: float = 0.0
         st = stream + 10 * m
         c0 = L.codes_off[m]
         if wfmt == FMT_NVFP4_G16:
-            packed, sf, outer = _nvfp4_matrix(seed, st, E, N, K, device, sigma)
+            packed, sf, outer = _nvfp4_matrix(seed, st, E, N, K, device, sigma, nvfp4_sf_range)
             body[:, c0:c0 + N * K // 2] = packed.reshape(E, -1)
             s0 = L.scales_off[m]
             body[:, s0:s0 + N * K // 16] = sf.reshape(E, -1)

@@ -48,6 +48,35 @@ def test_permute_bitexact(M, T, k, E, bad):
     assert torch.equal(xp.cpu().view(torch.int16), want)
 
 
+def _ids_with_duplicates(T, k, E, seed):
+    """Routing with repeated experts: some tokens name one expert twice or
+    more, and the first 32 assignments (one warp's batch) all name expert
+    min(3, E - 1); the rest are drawn with replacement, so most warp batches
+    hold several lanes with the same id."""
+    g = torch.Generator().manual_seed(seed)
+    ids = torch.randint(0, E, (T, k), generator=g, dtype=torch.int32)
+    ids[::5, 1 % k] = ids[::5, 0]             # a duplicate inside one token
+    ids.view(-1)[:min(32, T * k)] = min(3, E - 1)  # a whole warp batch on one expert
+    return ids
+
+
+# (T, k, E): one shape per permute variant -- one CTA of 8 warps (<= 2048
+# assignments), one CTA of 16 warps (<= 8192), count/scan/place over many CTAs,
+# and the 32-warp CTA for batches the chunked variant does not take
+@pytest.mark.parametrize("T,k,E", [(64, 8, 16), (37, 3, 4), (512, 8, 64), (2048, 8, 256), (1030, 9, 256)])
+def test_permute_duplicate_ids_bitexact(M, T, k, E):
+    """Duplicate ids within a token are separate assignments, ranked by their
+    flat index (stable), exactly as the oracle's counting sort."""
+    ids = _ids_with_duplicates(T, k, E, seed=T * 31 + E)
+    err = torch.zeros(1, dtype=torch.int32, device=DEV)
+    off, sa, pos, _ = M.mnw_moe_permute(ids.to(DEV), E, err=err)
+    o_off, o_sa, o_pos, dropped = O.permute(ids.numpy(), E)
+    assert dropped == 0 and M.mnw_moe_read_error(err) == 0
+    assert np.array_equal(off.cpu().numpy(), o_off)
+    assert np.array_equal(sa.cpu().numpy(), o_sa)
+    assert np.array_equal(pos.cpu().numpy(), o_pos)
+
+
 @pytest.mark.parametrize("R,K,gather", [(1, 128, False), (37, 512, False), (300, 2048, True)])
 def test_quantize_int8_bitexact(M, R, K, gather):
     x = S.activations(R, K, seed=R, outlier_p=0.01)
@@ -182,6 +211,32 @@ def test_gemm_nvfp4(M, shape):
     assert_close(y, oy, rel_l2=REL_L2_NVFP4, what="nvfp4 down")
 
 
+@pytest.mark.parametrize("shape", [(8, 512, 256, 40, 2), (4, 512, 512, 300, 2)])
+def test_gemm_nvfp4_full_scale_range(M, shape):
+    """NVFP4 weights whose E4M3 block scales cover every non-negative finite
+    code (zero, subnormals, up to 448) and whose per-matrix outer scales
+    spread over a factor of 256: the block-scale decode is exercised over its
+    whole range."""
+    E, H, I, T, k = shape
+    # sigma keeps |h| well below 1, where one BF16 ulp is inside the absolute bound
+    blob, hdr, L = S.expert_blob(S.FMT_NVFP4_G16, E, H, I, seed=41 + T, sigma=0.006, nvfp4_sf_range="full")
+    sf_bytes = blob.numpy()[L.data_offset + L.scales_off[0]:][:I * H // 16]
+    assert sf_bytes.min() == 0 and sf_bytes.max() == 0x7E and ((sf_bytes > 0) & (sf_bytes < 8)).any()
+    ids = S.routing_uniform(T, E, k, seed=42 + T)
+    x = S.activations(T, H, seed=43 + T)
+    layer = M.Layer(blob.to(DEV), hdr)
+    off, sa, pos, _ = M.mnw_moe_permute(ids.to(DEV), E)
+    c, sf, o = M.mnw_moe_quantize_act(M.ACT_NVFP4_G16, x.to(DEV), row_index=sa, index_div=k)
+    h = M.mnw_moe_grouped_gemm_nvfp4(layer, M.KIND_GATE_UP, c, sf, o, off)
+    o_off = off.cpu().numpy()
+    oh = O.gemm_a4(blob.numpy(), O.KIND_GATE_UP, c.cpu().numpy(), sf.cpu().numpy(), o.cpu().numpy(), o_off)
+    assert_close(h, oh, rel_l2=REL_L2_NVFP4, what="nvfp4 full-range gate_up")
+    hc, hsf, ho = M.mnw_moe_quantize_act(M.ACT_NVFP4_G16, h)
+    y = M.mnw_moe_grouped_gemm_nvfp4(layer, M.KIND_DOWN, hc, hsf, ho, off)
+    oy = O.gemm_a4(blob.numpy(), O.KIND_DOWN, hc.cpu().numpy(), hsf.cpu().numpy(), ho.cpu().numpy(), o_off)
+    assert_close(y, oy, rel_l2=REL_L2_NVFP4, what="nvfp4 full-range down")
+
+
 def test_gemm_empty_experts_and_zero_rows(M):
     E, H, I = 6, 256, 256
     blob, hdr, L = S.expert_blob(S.FMT_INT4_G128, E, H, I, seed=3)
@@ -297,12 +352,18 @@ def test_gemm_f16rows(M, wfmt, fn, shape):
     h = getattr(M, fn)(layer, M.KIND_GATE_UP, a, f, off, err=err)
     assert int(err.item()) == 0
     o_off = off.cpu().numpy()
+    # the definition: the W8A16/W4A16 GEMM of the original BF16 rows
+    oh_def = O.gemm_a16(blob.numpy(), O.KIND_GATE_UP, to_np_bits(xp), o_off)
+    assert_close(h, oh_def, what=f"{fn} gate_up vs the BF16-row definition")
+    # and the oracle's GEMM over the same encoded rows
     oh = O.gemm_f16rows(blob.numpy(), O.KIND_GATE_UP, a.cpu().view(torch.int16).numpy().view(np.uint16),
                         f.cpu().numpy(), o_off)
     assert_close(h, oh, what=f"{fn} gate_up")
     ha, hf = M.mnw_moe_quantize_act(M.ACT_F16_ROWS, h)
     y = getattr(M, fn)(layer, M.KIND_DOWN, ha, hf, off, err=err)
     assert int(err.item()) == 0
+    oy_def = O.gemm_a16(blob.numpy(), O.KIND_DOWN, to_np_bits(h), o_off)
+    assert_close(y, oy_def, what=f"{fn} down vs the BF16-row definition")
     oy = O.gemm_f16rows(blob.numpy(), O.KIND_DOWN, ha.cpu().view(torch.int16).numpy().view(np.uint16),
                         hf.cpu().numpy(), o_off)
     assert_close(y, oy, what=f"{fn} down")
@@ -326,3 +387,38 @@ def test_gemm_f16rows_rejects_bad_kind_format_and_out_of_range_scales(M):
     tiny, hdr_t, _ = S.expert_blob(S.FMT_INT4_G128, E, H, I, seed=23, sigma=1.0e-6)
     with pytest.raises(M.MnwError, match="unsupported"):
         M.mnw_moe_grouped_gemm_w4a16_f16rows(M.Layer(tiny.to(DEV), hdr_t), M.KIND_GATE_UP, a, f, off)
+
+
+def test_standalone_gemm_graph_replay_on_two_streams(M):
+    """A standalone grouped-GEMM call keeps no state between calls (on the
+    warp-MMA kernel its CTAs take work units in a static order): two captured
+    launches replayed concurrently on two streams, several times, give the
+    eager result bit for bit."""
+    E, H, I, T, k = 64, 512, 256, 96, 4  # 6 tokens per expert: the warp-MMA kernel
+    blob, hdr, ids, x = _setup(S.FMT_INT4_G128, E, H, I, T, k, seed=71)
+    layer = M.Layer(blob.to(DEV), hdr)
+    off, sa, pos, xp = M.mnw_moe_permute(ids.to(DEV), E, x=x.to(DEV))
+    ref = M.mnw_moe_grouped_gemm_w4a16(layer, M.KIND_GATE_UP, xp, off)
+    torch.cuda.synchronize()
+    lib = M.load()
+    import ctypes
+    P = T * k
+    outs = [torch.full_like(ref, float("nan")) for _ in range(2)]
+    graphs = []
+    for o in outs:
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            rc = lib.mnw_moe_grouped_gemm_w4a16(layer.handle, M.KIND_GATE_UP, ctypes.c_void_p(xp.data_ptr()),
+                                                ctypes.c_void_p(off.data_ptr()), P, ctypes.c_void_p(o.data_ptr()),
+                                                None, ctypes.c_void_p(torch.cuda.current_stream().cuda_stream))
+        assert rc == 0
+        graphs.append(g)
+    streams = [torch.cuda.Stream(), torch.cuda.Stream()]
+    for _ in range(3):
+        for g, s in zip(graphs, streams):
+            s.wait_stream(torch.cuda.current_stream())
+            with torch.cuda.stream(s):
+                g.replay()
+    torch.cuda.synchronize()
+    for o in outs:
+        assert torch.equal(o.view(torch.int16), ref.view(torch.int16))

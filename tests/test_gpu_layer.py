@@ -58,6 +58,26 @@ def test_full_size_sampled(M, name, nrows):
     _run(M, wl, rows=rows)
 
 
+@pytest.mark.parametrize("T,E,sigma", [(48, 16, 0.004), (600, 8, 0.0015)])
+def test_nvfp4_layer_full_scale_range(M, T, E, sigma):
+    """The NVFP4 layer with weight block scales over every non-negative finite
+    E4M3 code and outer scales spread over a factor of 64 (sigma keeps |h|
+    below about 2, where one BF16 ulp is inside the absolute bound)."""
+    H, I, k = 512, 512, 4
+    x = S.activations(T, H, seed=51 + T).to(DEV)
+    ids = S.routing_uniform(T, E, k, seed=52 + T).to(DEV)
+    w = S.routing_weights(T, k, seed=53 + T).to(DEV)
+    blob, hdr, L = S.expert_blob(S.FMT_NVFP4_G16, E, H, I, seed=54 + T, sigma=sigma, device=DEV,
+                                 nvfp4_sf_range="full")
+    layer = M.Layer(blob, hdr)
+    ws = M.workspace(layer, S.ACT_NVFP4_G16, T, k)
+    out = M.mnw_moe_forward(layer, S.ACT_NVFP4_G16, x, ids, w, ws=ws)
+    assert M.mnw_moe_read_error(M.workspace_error_word(ws)) == 0
+    want = O.moe_forward(blob.cpu().numpy(), S.ACT_NVFP4_G16, S.bf16_bits_np(x), ids.cpu().numpy(),
+                         w.cpu().numpy(), rows=np.arange(T, dtype=np.int32))
+    assert_close(out, want, rel_l2=REL_L2_NVFP4, what="nvfp4 layer, full scale range")
+
+
 @pytest.mark.parametrize("name", ["tiny_w8a16", "decode_w4a16"])
 @pytest.mark.parametrize("pinned", ["all", "none", "mixed"])
 def test_forward_host_buffers(M, name, pinned):

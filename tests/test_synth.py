@@ -35,18 +35,25 @@ def test_routing_shapes_and_distinctness():
     assert torch.allclose(w.sum(1), torch.ones(10))
 
 
+def _oracle_down(b, wfmt, off):
+    """One down-GEMM row through the oracle entry that matches the blob's format
+    (K = I = 256)."""
+    if wfmt == S.FMT_NVFP4_G16:
+        return O.gemm_a4(b, 1, np.zeros((1, 128), np.uint8), np.zeros((1, 16), np.uint8),
+                         np.zeros((1,), np.float32), off)
+    return O.gemm_a16(b, 1, np.zeros((1, 256), np.uint16), off)
+
+
 @pytest.mark.parametrize("wfmt", [0, 1, 2, 3])
 def test_blob_header_parses_in_oracle(wfmt):
-    blob, hdr, L = S.expert_blob(wfmt, 2, 256, 128, seed=3)
+    blob, hdr, L = S.expert_blob(wfmt, 2, 256, 256, seed=3)
     # the oracle's own parser accepts the header; a flipped byte breaks the CRC
-    O.gemm_a16 if wfmt != 3 else None
     b = blob.numpy().copy()
     off = np.array([0, 1, 1], np.int32)
-    if wfmt != 3:
-        O.gemm_a16(b, 1, np.zeros((1, 128), np.uint16), off)
-        b[20] ^= 1
-        with pytest.raises(ValueError):
-            O.gemm_a16(b, 1, np.zeros((1, 128), np.uint16), off)
+    _oracle_down(b, wfmt, off)
+    b[20] ^= 1
+    with pytest.raises(ValueError):
+        _oracle_down(b, wfmt, off)
 
 
 def _sizes():
