@@ -30,6 +30,13 @@
  *    are OR-ed into a caller-provided 32-bit device error word (MNW_DEVERR_*)
  *    that the caller zeroes beforehand and reads with mnw_moe_read_error().
  *  - Results are deterministic: no floating-point atomics.
+ *  - The grouped-GEMM entry points keep no state between calls: calls may
+ *    overlap on different streams and may be captured in a CUDA graph and
+ *    replayed on any stream.  (mnw_moe_forward keeps its work counters in the
+ *    caller's workspace: calls sharing one workspace must not overlap.)
+ *  - Per-device state (kernel attributes, the address of
+ *    mnw_moe_forward_static's array) is set up on first use; do not use the
+ *    library after cudaDeviceReset() in the same process.
  *  - Kernels are launched with programmatic stream serialisation: one may
  *    start its set-up while the kernel before it on the stream finishes, but
  *    waits for that kernel's completion before it reads or writes any global
@@ -290,7 +297,9 @@ int mnw_moe_set_gemm_path(int path);
  *  - All calls share the array: calls that overlap on the GPU race and corrupt
  *    each other's results.  Serialise them (one stream).
  *  - err (device, may be NULL) receives this call's device error word
- *    (MNW_DEVERR_*); the word is cleared by every call.
+ *    (MNW_DEVERR_*), written on `stream` by every call (0 for T = 0).
+ *  - The array's address is cached per device for the life of the process;
+ *    do not use the library after cudaDeviceReset().
  * x, ids, w, out are as for mnw_moe_forward(). */
 #define MNW_STATIC_WS_BYTES (32u * 1024u * 1024u)
 int mnw_moe_forward_static(const mnw_moe_layer* layer, int act, const void* x, const int32_t* ids,

@@ -1,8 +1,5 @@
 // mnw_gemm_warp.cu -- host side of the warp-MMA grouped GEMM (mnw_gemm_warp.cuh):
-// work-counter ring, launch shapes, shared-memory plan, tensor maps, dispatch.
-#include <atomic>
-#include <mutex>
-
+// launch shapes, shared-memory plan, tensor maps, dispatch.
 #include "mnw_gemm_warp.cuh"
 
 namespace mnw {
@@ -19,28 +16,6 @@ MNW_WARP_DEP_INSTANCES(MNW_WARP_DEP_EXTERN)
 // ---------------------------------------------------------------------------
 
 namespace {
-// Work counters for launches that bring none: a ring of [claim, done] pairs,
-// each reset to zero by the last CTA of the launch that used it.  A slot is
-// reused after kSchedSlots further launches.
-constexpr int kSchedSlots = 1024;
-static __device__ uint32_t g_sched_ring[2 * kSchedSlots];
-std::atomic<uint32_t> g_sched_next{0};
-std::mutex g_sched_mu;
-void* g_sched_addr[64] = {};
-
-uint32_t* next_sched_slot() {
-  int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
-  void* base = nullptr;
-  {
-    std::lock_guard<std::mutex> lock(g_sched_mu);
-    if (!g_sched_addr[dev] && cudaGetSymbolAddress(&g_sched_addr[dev], g_sched_ring) != cudaSuccess) return nullptr;
-    base = g_sched_addr[dev];
-  }
-  const uint32_t slot = g_sched_next.fetch_add(1) % kSchedSlots;
-  return static_cast<uint32_t*>(base) + 2 * slot;
-}
-
 inline uint32_t align_up(uint32_t x, uint32_t a) { return (x + a - 1) / a * a; }
 
 template <int WF, int AM, bool GU, int DEP>
@@ -127,8 +102,7 @@ int run_gemm_warp(const mnw_moe_layer* L, int wfmt, int act, int kind, const voi
   a.out = static_cast<__nv_bfloat16*>(out);
   a.dots = act == MNW_ACT_INT8_G128 ? dots : nullptr;
   a.err = err;
-  a.sched = sched ? sched : next_sched_slot();
-  if (!a.sched) return MNW_E_CUDA;
+  a.sched = sched;  // NULL (a standalone call): static work order
   if (dep && dep->role != kDepNone) {
     if (!dep->flags || !sched) return MNW_E_INVALID_ARG;
     a.dep = dep->flags;

@@ -95,7 +95,9 @@ struct Args {
   __nv_bfloat16* out;
   int32_t* dots;
   uint32_t* err;
-  uint32_t* sched;  // [claim, done]: zero at launch; the last CTA to finish zeroes it again
+  // [claim, done]: zero at launch; the last CTA to finish zeroes it again.
+  // NULL: units are handed out statically (CTA c takes c, c + grid, ...).
+  uint32_t* sched;
   uint32_t* dep;    // tile dependency counters (WarpDep), or null
   int dep_role;     // kDepNone / kDepProduce / kDepConsume
   uint32_t dep_need;
@@ -436,7 +438,16 @@ __global__ void __launch_bounds__(threads_for(kDep), ctas_per_sm(WF, NT))
       // current unit's last two stages are issued, so the atomic's latency
       // hides behind them and the next unit's loads follow without a gap.
       const int claim_at = nstages >= 2 ? nstages - 2 : 0;
-      int u_next = static_cast<int>(atomicAdd(args.sched, 1u));
+      // Without a counter (a standalone call) the order is static, so launches
+      // share no state and may overlap or be replayed on any stream.
+      int static_next = static_cast<int>(blockIdx.x);
+      auto claim = [&]() -> int {
+        if (args.sched) return static_cast<int>(atomicAdd(args.sched, 1u));
+        const int u = static_next;
+        static_next += static_cast<int>(gridDim.x);
+        return u;
+      };
+      int u_next = claim();
       for (;; ++uit) {
         const int u = u_next;
         const uint32_t sb = uit & 1;
@@ -463,7 +474,7 @@ __global__ void __launch_bounds__(threads_for(kDep), ctas_per_sm(WF, NT))
           fence_proxy_async();
         }
         for (int ss = 0; ss < nstages; ++ss, ++it) {
-          if (ss == claim_at) u_next = static_cast<int>(atomicAdd(args.sched, 1u));
+          if (ss == claim_at) u_next = claim();
           if (!bounded_wait(&bars->empty[s], ph ^ 1, abort, args.err)) { ok = false; break; }
           uint8_t* st = smem + s * args.stage_bytes;
           mbar_arrive_expect_tx(&bars->full[s], tx);
@@ -484,7 +495,7 @@ __global__ void __launch_bounds__(threads_for(kDep), ctas_per_sm(WF, NT))
         }
       }
       // The last CTA to stop claiming resets the counter for its next user.
-      if (atomicAdd(args.sched + 1, 1u) == gridDim.x - 1) {
+      if (args.sched && atomicAdd(args.sched + 1, 1u) == gridDim.x - 1) {
         atomicExch(args.sched, 0u);
         atomicExch(args.sched + 1, 0u);
       }

@@ -35,7 +35,9 @@ static_assert(kStaticWsBytes == MNW_STATIC_WS_BYTES, "header and library disagre
 static __device__ __align__(256) unsigned char g_static_ws[kStaticWsBytes];
 
 // Device address of g_static_ws, looked up once per device.  In host code the
-// symbol is only a host-side stand-in, never a device address.
+// symbol is only a host-side stand-in, never a device address.  The cached
+// address belongs to the device's primary context: after cudaDeviceReset the
+// library must not be used again in this process.
 constexpr int kMaxDevices = 64;
 std::mutex g_mu;
 void* g_addr[kMaxDevices] = {};
@@ -59,7 +61,12 @@ int static_ws_address(void** out) {
 extern "C" int mnw_moe_forward_static(const mnw_moe_layer* layer, int act, const void* x, const int32_t* ids,
                                       const float* w, int T, int k, void* out, uint32_t* err, mnw_stream stream) {
   if (!layer || T < 0 || k < 1) return MNW_E_INVALID_ARG;
-  if (T == 0) return MNW_OK;
+  if (T == 0) {
+    // nothing to run; the caller's error word still reports this call (no error)
+    if (err && cudaMemsetAsync(err, 0, sizeof(uint32_t), static_cast<cudaStream_t>(stream)) != cudaSuccess)
+      return MNW_E_CUDA;
+    return MNW_OK;
+  }
   const size_t need = mnw_moe_workspace_size(layer, act, T, k);
   if (need == 0) return MNW_E_INVALID_ARG;
   if (need > mnw::kStaticWsBytes) return MNW_E_WORKSPACE_TOO_SMALL;
