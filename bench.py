@@ -3,18 +3,22 @@
 One step = one pass of the whole layer (permute + gather, fused gate/up/SiLU
 grouped GEMM, down grouped GEMM, combine; plus the activation quantisers in
 the A8/A4 modes) over one batch of seeded synthetic inputs already resident in
-HBM.  The default workload is the W4A16 decode block batch (8 concurrent
-32-token blocks, H=2048, 256 experts, I=512, top-8).
+HBM.  The default workload is the largest single-GPU one: 4096 tokens,
+H=4096, 256 experts, I=1536, top-8, INT4 weights with FP16 scales per 128
+(W4A16), skewed routing.  --workload picks another.
 
 Prints one JSON line (rank 0).  --impl reference times the CPU oracle on the
-host cores instead (a bounded sample of the same workload).
+host cores instead (a bounded sample of the same workload).  --peaks runs the
+tensor-core peak microbenchmark (bench_peaks.cu) and prints its JSON.
 """
 from __future__ import annotations
 
 import argparse
 import dataclasses
+import hashlib
 import json
 import os
+import platform
 import statistics
 import subprocess
 import sys
@@ -40,6 +44,64 @@ def _peaks():
         return float(p["hbm_gbs"]), float(p["bf16_tflops"]), "measured"
     except Exception:
         return 6800.0, 1900.0, "fallback"
+
+
+# Dense tensor rates relative to BF16 on GB300 (nominal: 2.25 PFLOP/s BF16/FP16,
+# 13.5 FP4).  Used only where no measured figure of that MMA kind exists.
+NOMINAL_RATIO = {"bf16": 1.0, "f16": 1.0, "fp4": 6.0}
+
+
+def tensor_peak(mma: str, bf16_peak: float, bf16_kind: str):
+    """Peak (TFLOP/s) of the MMA kind a gate/up launch issues, and how it was
+    obtained.  BF16 and FP16: the measured cuBLAS BF16 burst peak (FP16 runs
+    at the BF16 rate).  FP4: the figure profiles/tensor_peaks_gb300.json holds
+    (written by `python bench.py --peaks` on a GB300) when present, else the
+    measured BF16 peak times the nominal FP4/BF16 ratio."""
+    if mma in ("bf16", "f16"):
+        return bf16_peak, f"{bf16_kind} (bf16 dense burst; f16 runs at the bf16 rate)"
+    try:
+        with open(os.path.join(ROOT, "profiles", "tensor_peaks_gb300.json")) as f:
+            return float(json.load(f)["mxf4nvf4_tflops"]), "measured (tcgen05 microbenchmark, bench_peaks.cu)"
+    except (OSError, KeyError, ValueError):
+        return bf16_peak * NOMINAL_RATIO[mma], f"{bf16_kind} bf16 x nominal {NOMINAL_RATIO[mma]:g}"
+
+
+def run_peaks() -> dict:
+    """Build bench_peaks.cu with nvcc and run it on the current GPU; returns its
+    JSON (dense TFLOP/s of tcgen05 kind::f16 and kind::mxf4nvf4)."""
+    exe = os.path.join("/tmp", f"bench_peaks_{os.getpid()}")
+    nvcc = os.environ.get("NVCC", "nvcc")
+    subprocess.run([nvcc, "-gencode", "arch=compute_103a,code=sm_103a", "-O3", "-std=c++17", "-o", exe,
+                    os.path.join(ROOT, "bench_peaks.cu")], check=True)
+    try:
+        out = subprocess.run([exe], check=True, capture_output=True, text=True, timeout=300).stdout
+    finally:
+        os.remove(exe)
+    return json.loads(out.strip().splitlines()[-1])
+
+
+def host_info():
+    """nproc and CPU model of the host this process runs on."""
+    model = platform.processor() or platform.machine()
+    try:
+        with open("/proc/cpuinfo") as f:
+            for ln in f:
+                key = ln.split(":")[0].strip().lower()
+                if key in ("model name", "cpu model", "hardware"):
+                    model = ln.split(":", 1)[1].strip()
+                    break
+    except OSError:
+        pass
+    if model in ("", "aarch64"):
+        try:
+            out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=5).stdout
+            for ln in out.splitlines():
+                if ln.lower().startswith("model name"):
+                    model = ln.split(":", 1)[1].strip()
+                    break
+        except Exception:
+            pass
+    return os.cpu_count(), model
 
 
 class ClockSampler:
@@ -324,6 +386,7 @@ def run_ours(args, wl):
 
     touched = int(torch.unique(ids[(ids >= 0) & (ids < E)]).numel())
     return dict(total_ms=total_ms, step_ms=step_ms, gu_ms=gu_ms, launches=launches, world=world, rank=rank,
+                f16_rows=f16_gate_up is not None,
                 clocks=clk.summary(), e2e_ms=e2e_ms, touched=touched, ids=ids)
 
 
@@ -349,24 +412,61 @@ def run_oracle_sample(wl: S.Workload, ntok: int, inputs=None):
     return ntok / dt, dt
 
 
+GEMM_SOURCES = ("mnw_gemm", "mnw_convert.cuh", "mnw_ptx.cuh")
+
+
+def gemm_source_hash() -> str:
+    """First 12 hex digits of a SHA-256 over the grouped-GEMM kernel sources
+    (every csrc file whose name starts with one of GEMM_SOURCES), in name order."""
+    csrc = os.path.join(ROOT, "quantized_moe_expert_routed_gb300", "csrc")
+    h = hashlib.sha256()
+    for name in sorted(os.listdir(csrc)):
+        if name.startswith(GEMM_SOURCES):
+            with open(os.path.join(csrc, name), "rb") as f:
+                h.update(name.encode() + b"\0" + f.read())
+    return h.hexdigest()[:12]
+
+
 def profile_traffic(wl: S.Workload):
     """DRAM traffic (read + write bytes) of one gate/up launch, from the ncu
-    capture summarised in profiles/ (lines "<workload> <bytes> <summary file>");
-    None for a workload without a capture of the current kernel."""
+    capture summarised in profiles/ (lines "<workload> <bytes> <source hash>
+    <summary file>"), and a note.  The figure is None when there is no line for
+    the workload, or when the GEMM sources changed since the capture (their
+    hash differs from the one recorded beside it)."""
     try:
         with open(os.path.join(ROOT, "profiles", "gate_up_dram_traffic.txt")) as f:
             for ln in f:
                 parts = ln.split()
-                if len(parts) >= 2 and parts[0] == wl.name:
-                    return int(parts[1])
+                if len(parts) >= 3 and parts[0] == wl.name:
+                    if parts[2] != gemm_source_hash():
+                        sys.stderr.write(f"bench: stored DRAM traffic for {wl.name} predates the current GEMM "
+                                         f"sources ({parts[2]} != {gemm_source_hash()}); reporting null\n")
+                        return None, "stale: the GEMM kernel changed since the capture"
+                    return int(parts[1]), f"ncu capture, profiles/{parts[3] if len(parts) > 3 else ''}"
     except OSError:
         pass
-    return None
+    return None, "no capture of the current kernel"
+
+
+def gate_up_mma(wl: S.Workload, f16_rows: bool) -> tuple:
+    """(MMA kind the gate/up launch issues, dtype string of the path)."""
+    if wl.act == S.ACT_NVFP4_G16:
+        return "fp4", "e2m1 x e2m1, e4m3 block scales, fp32 outer scales -> f32 (block-scaled fp4 MMA)"
+    if wl.act == S.ACT_INT8_G128:
+        return "f16", "int8 x int8 group dots exact in f16 MMA (f32 accumulate) -> f32 group combine"
+    if wl.wfmt == S.FMT_BF16:
+        return "bf16", "bf16 x bf16 -> f32"
+    w = "int4" if wl.wfmt == S.FMT_INT4_G128 else "int8"
+    if f16_rows:
+        return "f16", (f"f16 x f16 -> f32 ({w} weights dequantised on chip; bf16 rows re-encoded exactly as f16 "
+                       "with a power-of-two row factor)")
+    return "bf16", f"bf16 x bf16 -> f32 ({w} codes as exact bf16 integers, f32 group scales)"
 
 
 def build_line(args, wl: S.Workload, config: dict, r: dict, cpu, traffic) -> dict:
     """The JSON line of the GPU arm from run_ours' measurements r, the CPU
-    baseline (tokens/s, seconds, sample tokens) and the captured traffic."""
+    baseline (tokens/s, seconds, sample tokens) and the captured traffic
+    (bytes or None, note)."""
     hbm, bf16_peak, peak_kind = _peaks()
     ms = r["total_ms"] / args.steps
     value = r["world"] * wl.T / (r["total_ms"] / args.steps / 1e3)
@@ -374,38 +474,43 @@ def build_line(args, wl: S.Workload, config: dict, r: dict, cpu, traffic) -> dic
     gu_bytes = gate_up_bytes(wl, r["touched"])
     achieved = gu_bytes / (gu_ms / 1e3) / 1e9
     # The gate/up launch's binding roofline: its arithmetic intensity against
-    # the ridge of the measured peaks.  Its MMAs are 16-bit (BF16, or FP16 on
-    # exact integer / block-scaled FP4 values), so the tensor peak is the
-    # measured dense BF16 one (the kernel is timed alone: the burst figure).
+    # the ridge of the HBM peak and the dense peak of the MMA kind it issues
+    # (the kernel is timed alone: the burst figure).
+    mma, dtype = gate_up_mma(wl, r.get("f16_rows", False))
+    t_peak, t_kind = tensor_peak(mma, bf16_peak, peak_kind)
     valid = int(((r["ids"] >= 0) & (r["ids"] < wl.E)).sum())
     gu_flops = 2.0 * 2 * wl.H * wl.I * valid
     gu_tflops = gu_flops / (gu_ms / 1e3) / 1e12
-    tensor_bound = gu_flops / gu_bytes > bf16_peak * 1e12 / (hbm * 1e9)
+    tensor_bound = gu_flops / gu_bytes > t_peak * 1e12 / (hbm * 1e9)
     layer_bytes = S.algorithmic_bytes(wl, r["ids"].cpu())
     e2e_ms = r["e2e_ms"]  # the slowest replica's median
     h2d = r["world"] * (wl.T * wl.H * 2 + wl.P * 4 * 2)  # x, ids, w of every replica
     d2h = r["world"] * wl.T * wl.H * 2
     cpu_rate, cpu_dt, ntok = cpu
-    dtype = {S.ACT_BF16: "bf16", S.ACT_INT8_G128: "int8xint8->f32 (f16 MMA)",
-             S.ACT_NVFP4_G16: "e2m1xe2m1->f32 (f16 MMA)"}[wl.act]
+    nproc, cpu_model = host_info()
+    traffic_bytes, traffic_note = traffic
+    tensor = {"achieved": gu_tflops, "peak": t_peak, "unit": "TFLOP/s", "frac": gu_tflops / t_peak,
+              "peak_kind": t_kind, "mma": mma, "flops_per_launch": gu_flops}
+    hbm_part = {"achieved": achieved, "peak": hbm, "unit": "GB/s", "frac": achieved / hbm, "peak_kind": peak_kind,
+                "bytes_per_launch": gu_bytes}
+    if tensor_bound:
+        roofline = {"kernel": "grouped gate/up/SiLU GEMM", "bound": "tensor", **tensor, "launch_ms": gu_ms,
+                    "launch_ms_median": statistics.median(r["gu_ms"]), "traffic": traffic_bytes,
+                    "traffic_note": traffic_note, "hbm": hbm_part}
+    else:
+        roofline = {"kernel": "grouped gate/up/SiLU GEMM", "bound": "hbm", **hbm_part, "launch_ms": gu_ms,
+                    "launch_ms_median": statistics.median(r["gu_ms"]), "traffic": traffic_bytes,
+                    "traffic_note": traffic_note, "tensor": tensor}
     line = {
         "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": r["world"], "steps": args.steps,
-        "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
+        "warmup": args.warmup, "ms_per_step": ms, "ms_per_step_median": statistics.median(r["step_ms"]),
+        "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": dtype, "data": "synthetic (seeded, shapes of the workload)",
         "config": config,
         "layer_effective_gbs": layer_bytes / (ms / 1e3) / 1e9,
-        "roofline": ({"kernel": "grouped gate/up/SiLU GEMM", "bound": "tensor", "achieved": gu_tflops,
-                      "peak": bf16_peak, "unit": "TFLOP/s", "frac": gu_tflops / bf16_peak, "peak_kind": peak_kind,
-                      "flops_per_launch": gu_flops, "launch_ms": gu_ms, "traffic": traffic,
-                      "hbm": {"achieved": achieved, "peak": hbm, "unit": "GB/s", "frac": achieved / hbm,
-                              "bytes_per_launch": gu_bytes}}
-                     if tensor_bound else
-                     {"kernel": "grouped gate/up/SiLU GEMM", "bound": "hbm", "achieved": achieved, "peak": hbm,
-                      "unit": "GB/s", "frac": achieved / hbm, "peak_kind": peak_kind,
-                      "bytes_per_launch": gu_bytes, "launch_ms": gu_ms, "traffic": traffic,
-                      "tensor": {"achieved": gu_tflops, "peak": bf16_peak, "unit": "TFLOP/s",
-                                 "frac": gu_tflops / bf16_peak, "flops_per_launch": gu_flops}}),
+        "roofline": roofline,
         "cpu_baseline": {"value": cpu_rate, "unit": "tokens/s", "cores": 1, "kind": "oracle",
+                         "host_nproc": nproc, "host_cpu_model": cpu_model,
                          "sample": f"{ntok} of {wl.T} tokens, {cpu_dt:.1f} s single-threaded"},
         "e2e": {"value": r["world"] * wl.T / (e2e_ms / 1e3), "unit": "tokens/s", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h},
@@ -418,12 +523,16 @@ def build_line(args, wl: S.Workload, config: dict, r: dict, cpu, traffic) -> dic
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=20)
-    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
-    ap.add_argument("--workload", default="decode_w4a16", choices=sorted(S.WORKLOADS))
+    ap.add_argument("--workload", default="large_w4a16", choices=sorted(S.WORKLOADS))
     ap.add_argument("--cpu-budget", type=float, default=15.0, help="seconds of oracle time for cpu_baseline")
+    ap.add_argument("--peaks", action="store_true", help="run the tensor-core peak microbenchmark and exit")
     args = ap.parse_args()
+    if args.peaks:
+        print(json.dumps(run_peaks()))
+        return
     wl = S.WORKLOADS[args.workload]
     world, rank, local = _dist()
     if world > 1 and not torch.distributed.is_initialized():
@@ -454,7 +563,8 @@ def main():
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": statistics.median(times) * 1e3,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
             "data": "synthetic", "config": config,
-            "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": 1, "kind": "oracle", "sample": sample},
+            "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": 1, "kind": "oracle",
+                             "host_nproc": host_info()[0], "host_cpu_model": host_info()[1], "sample": sample},
             "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}))
         return
 

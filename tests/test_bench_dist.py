@@ -111,9 +111,10 @@ def test_gpu_arm_json_line_contract():
                                         ("large_w4a16", 1.9172, 1.1123, "tensor")):
         wl = S.WORKLOADS[name]
         ids = S.routing_uniform(wl.T, wl.E, wl.k, seed=1)
-        r = dict(total_ms=10 * step_ms, gu_ms=[gu_ms] * 10, touched=wl.E, ids=ids, e2e_ms=0.174, world=2,
-                 launches=100, clocks={"sm_mhz": 2070.0, "sm_max_mhz": 2070.0, "reasons": []})
-        line = bench.build_line(args, wl, {"workload": name}, r, (4.4, 10.0, 12), 12345)
+        r = dict(total_ms=10 * step_ms, step_ms=[step_ms] * 10, gu_ms=[gu_ms] * 10, touched=wl.E, ids=ids,
+                 e2e_ms=0.174, world=2, launches=100, f16_rows=True,
+                 clocks={"sm_mhz": 2070.0, "sm_max_mhz": 2070.0, "reasons": []})
+        line = bench.build_line(args, wl, {"workload": name}, r, (4.4, 10.0, 12), (12345, "test"))
         for key in ("metric", "value", "unit", "n_gpus", "steps", "warmup", "ms_per_step", "higher_is_better",
                     "scaling", "vs_baseline", "dtype", "data", "config", "roofline", "cpu_baseline", "e2e",
                     "gpu_launches", "clocks"):
@@ -131,12 +132,39 @@ def test_gpu_arm_json_line_contract():
         else:
             assert roof["peak"] == bf16 and roof["unit"] == "TFLOP/s"
             assert roof["achieved"] == pytest.approx(2 * 2 * wl.H * wl.I * wl.T * wl.k / (gu_ms / 1e3) / 1e12)
+        assert roof["launch_ms_median"] == pytest.approx(gu_ms)
+        assert line["ms_per_step_median"] == pytest.approx(step_ms)
+        assert line["dtype"].startswith("f16 x f16")  # INT4 weights on FP16 rows
         cb = line["cpu_baseline"]
         assert cb["kind"] == "oracle" and cb["cores"] == 1 and cb["value"] == 4.4 and "sample" in cb
+        assert cb["host_nproc"] == os.cpu_count() and cb["host_cpu_model"]
         e2e = line["e2e"]
         assert e2e["value"] == pytest.approx(2 * wl.T / 0.174e-3)
         assert e2e["h2d_bytes_per_step"] == 2 * (wl.T * wl.H * 2 + wl.T * wl.k * 8)
         assert e2e["d2h_bytes_per_step"] == 2 * wl.T * wl.H * 2
-    # the captured traffic is read from the committed ncu summary table
-    assert bench.profile_traffic(S.WORKLOADS["decode_w4a16"]) == 291030784
-    assert bench.profile_traffic(S.WORKLOADS["tiny_w8a16"]) is None
+    # the captured traffic is read from the committed ncu summary table, and
+    # reported only while the GEMM sources hash to the value recorded with it
+    table = os.path.join(ROOT, "profiles", "gate_up_dram_traffic.txt")
+    for ln in open(table):
+        parts = ln.split()
+        if parts and not ln.startswith("#"):
+            got, note = bench.profile_traffic(S.WORKLOADS[parts[0]])
+            if parts[2] == bench.gemm_source_hash():
+                assert got == int(parts[1])
+            else:
+                assert got is None and note.startswith("stale")
+    assert bench.profile_traffic(S.WORKLOADS["tiny_w8a16"])[0] is None
+
+
+def test_fp4_tensor_peak_is_measured_or_nominal():
+    """NVFP4 fractions are quoted against an FP4 peak: the measured figure when
+    profiles/tensor_peaks_gb300.json exists, else BF16 x the nominal 6."""
+    sys.path.insert(0, ROOT)
+    import bench
+    hbm, bf16, kind = bench._peaks()
+    peak, how = bench.tensor_peak("fp4", bf16, kind)
+    if os.path.exists(os.path.join(ROOT, "profiles", "tensor_peaks_gb300.json")):
+        assert how.startswith("measured") and peak > bf16
+    else:
+        assert peak == pytest.approx(6 * bf16) and "nominal" in how
+    assert bench.tensor_peak("f16", bf16, kind)[0] == bf16
