@@ -10,8 +10,10 @@
 //                                        scale applied in FP32)
 //   weights INT8/INT4 + INT8 per 128    (codes as exact FP16 integers in TMEM/smem,
 //                                        INT32-exact group dots, FP32 rescale by s_w*s_a)
-//   weights NVFP4 + NVFP4               (block-scaled E2M1 values as exact FP16,
-//                                        outer scales applied in the epilogue)
+//   weights NVFP4 + NVFP4               (E2M1 codes straight from shared memory into
+//                                        the block-scaled FP4 MMA, E4M3 scales per 16
+//                                        in tensor memory, FP32 outer scales applied
+//                                        in the epilogue)
 //
 // Dequantisation happens in registers on the way into the tensor cores; no
 // expanded weight copy exists in memory.  INT codes are exact in BF16/FP16, so
@@ -31,7 +33,10 @@
 //   warp 0      TMA producer: weight tiles (raw codes) + group scales + token tiles
 //   warp 1      MMA issuer (one thread); owns the TMEM allocation
 //   warps 2-9   converters: raw weight codes -> BF16/FP16 operand in TMEM
-//               (tcgen05.st); INT8/FP4 token codes -> FP16 operand in shared memory
+//               (tcgen05.st); INT8 token codes -> FP16 operand in shared memory.
+//               NVFP4: warps 2-5 move each stage's E4M3 block scales of weights
+//               and tokens into tensor memory for the block-scaled MMA; the
+//               codes themselves are MMA operands as the TMA left them.
 //   warps 10-17 epilogue: TMEM accumulators -> (group rescale) -> SiLU(g)*u or y
 //               -> BF16 global; two warps per TMEM lane quarter, each with half
 //               of the token columns
@@ -39,7 +44,8 @@
 // TMEM (512 columns): operand-A ring (slots of 64 K per matrix), then the
 // accumulators; in the grouped modes two per-group accumulators (one drains
 // while the next fills) and the FP32 running sum.  With BF16 weights A never
-// enters TMEM and the accumulators may use all 512 columns.
+// enters TMEM and the accumulators may use all 512 columns.  NVFP4: the
+// accumulators, then a ring of scale-factor slots, one per stage.
 //
 // Every wait is bounded (mnw_ptx.cuh); on a timeout all roles leave their
 // loops, outstanding copies and MMAs are drained with a time limit, TMEM is
@@ -69,13 +75,16 @@ constexpr int kThreads = (kWarpEpi0 + kEpiWarps) * 32;
 constexpr int kMaxStages = 8;
 constexpr int kMaxASlots = 8;   // operand-A ring slots in TMEM (runtime count <= this)
 constexpr int kMaxAcc = 8;      // accumulator slots (runtime count <= this)
-constexpr int kBSlots = 4;      // converted-token ring slots (INT8 / FP4 activations)
+constexpr int kBSlots = 4;      // converted-token ring slots (INT8 activations)
+constexpr int kMaxSf = 8;       // scale-factor ring slots in TMEM (NVFP4; runtime count <= this)
+constexpr int kSfWarps = 4;     // NVFP4: converter warps that move block scales into TMEM, one per lane quarter
 constexpr int kTmemCols = 512;
 
 
 struct GemmArgs {
   const int32_t* offsets;
   int E, P, K, N, BN, n_tiles, stages, nmat, acc_slots, acc_base, aslots, sum_base;
+  int sf_base, sf_slots, sf_cols;  // NVFP4: TMEM scale-factor ring (first column, slots, columns per slot)
   uint32_t stage_bytes, off_a[2], off_asf[2], off_b, off_braw, off_bsf, off_bring;
   uint32_t off_scales, scale_mat_bytes, off_tab, off_sa, off_bars;
   const uint8_t* experts;
@@ -94,6 +103,7 @@ struct Bars {
   uint64_t afull[kMaxASlots], aempty[kMaxASlots];
   uint64_t accfull[kMaxAcc], accempty[kMaxAcc];
   uint64_t sfull[2], sempty[2];
+  uint64_t sffull[kMaxSf], sfempty[kMaxSf];  // NVFP4 scale factors in TMEM
   uint64_t final_mma;
   uint32_t tmem_base;
   int abort;
@@ -103,7 +113,7 @@ template <int WF>
 struct WT {
   static constexpr int kStage = WF == WF_BF16 ? 64 : (WF == WF_INT8 ? 128 : 256);  // K per stage
   static constexpr int kSub = kStage / 64;                                          // 64-K sub-chunks
-  static constexpr bool kTs = WF != WF_BF16;                                         // A from TMEM
+  static constexpr bool kTs = WF == WF_INT8 || WF == WF_INT4;                        // A from TMEM
   static constexpr bool kScales = WF == WF_INT8 || WF == WF_INT4;                    // FP16 group scales
 };
 
@@ -167,7 +177,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                     const GemmArgs args) {
   using T = WT<WF>;
   constexpr int kNmat = kGateUp ? 2 : 1;
-  constexpr bool kBconv = AM == AM_INT8 || AM == AM_FP4;  // tokens converted by the converter warps
+  constexpr bool kBconv = AM == AM_INT8;                  // tokens converted by the converter warps
+  constexpr bool kFp4 = WF == WF_NVFP4;                   // block-scaled FP4 MMA on the raw codes
   constexpr bool kScaleConv = AM == AM_F16S;              // converters apply the FP16 group scales
   // Grouped: one accumulator per 128-wide K group, rescaled in FP32 (INT weights).
   constexpr bool kGrouped = AM == AM_INT8 || (AM == AM_BF16 && T::kScales);
@@ -190,7 +201,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (threadIdx.x == 0) {
     for (int s = 0; s < kMaxStages; ++s) {
       mbar_init(&bars->full[s], 1);
-      mbar_init(&bars->empty[s], ((T::kTs || kBconv) ? kConvWarps : 0) + 1);
+      mbar_init(&bars->empty[s], ((T::kTs || kBconv) ? kConvWarps : (kFp4 ? kSfWarps : 0)) + 1);
     }
     for (int i = 0; i < kBSlots; ++i) {
       mbar_init(&bars->bfull[i], kConvWarps);
@@ -203,6 +214,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int i = 0; i < kMaxAcc; ++i) {
       mbar_init(&bars->accfull[i], 1);
       mbar_init(&bars->accempty[i], kEpiWarps);
+    }
+    for (int i = 0; i < kMaxSf; ++i) {
+      mbar_init(&bars->sffull[i], kSfWarps);
+      mbar_init(&bars->sfempty[i], 1);
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(&bars->sfull[i], 1);
@@ -220,6 +235,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     tma_prefetch_desc(&tmA0);
     if (kGateUp) tma_prefetch_desc(&tmA1);
     tma_prefetch_desc(&tmB);
+    if (kFp4) {
+      tma_prefetch_desc(&tmS0);
+      if (kGateUp) tma_prefetch_desc(&tmS1);
+      tma_prefetch_desc(&tmBs);
+    }
   }
   // everything below reads or writes global memory the previous kernel may own
   pdl_wait();
@@ -323,7 +343,51 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else if (warp == kWarpMma) {
     // ======================= MMA issuer =======================
-    if (lane == 0) {
+    if (lane == 0 && kFp4) {
+      // Block-scaled FP4: per stage, both operands as the TMA left them (128-byte
+      // rows of 256 E2M1 codes) and the stage's scale factors in TMEM slot fp;
+      // 4 MMAs of K = 64 per matrix.
+      const uint32_t idesc = idesc_fp4(kBM, BN);
+      const uint32_t S_ = static_cast<uint32_t>(S), nacc = static_cast<uint32_t>(args.acc_slots),
+                     nsf = static_cast<uint32_t>(args.sf_slots);
+      RingPos sp, cp, fp;  // stages, accumulator slots, scale-factor slots
+      bool ok = true, issued = false;
+      for (int u = blockIdx.x; ok && u < units; u += gridDim.x) {
+        if (!bounded_wait(&bars->accempty[cp.slot], cp.phase ^ 1, abort, args.err)) { ok = false; break; }
+        tc_fence_after();
+        const uint32_t d_base = tmem + args.acc_base + cp.slot * kNmat * BN;
+        for (int ks = 0; ks < nks; ++ks, sp.advance(S_), fp.advance(nsf)) {
+          const int s = sp.slot;
+          if (!bounded_wait(&bars->full[s], sp.phase, abort, args.err) ||
+              !bounded_wait(&bars->sffull[fp.slot], fp.phase, abort, args.err)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t st = smem_u32(smem + s * args.stage_bytes);
+          const uint32_t sf = tmem + args.sf_base + fp.slot * args.sf_cols;  // [SFA m0 | SFA m1 | SFB], 16 columns each
+#pragma unroll
+          for (int kk = 0; kk < 4; ++kk) {
+            const uint64_t bdesc = sdesc_sw128(st + args.off_braw + kk * 32);
+            const uint32_t acc = (ks != 0 || kk != 0);
+#pragma unroll
+            for (int m = 0; m < kNmat; ++m)
+              mma_fp4_ss(d_base + m * BN, sdesc_sw128(st + args.off_a[m] + kk * 32), bdesc, idesc, sf + m * 16 + kk * 4,
+                         sf + kNmat * 16 + kk * 4, acc);
+          }
+          issued = true;
+          mma_commit(&bars->sfempty[fp.slot]);
+          mma_commit(&bars->empty[s]);
+        }
+        if (!ok) break;
+        mma_commit(&bars->accfull[cp.slot]);
+        cp.advance(nacc);
+      }
+      if (issued) {
+        mma_commit(&bars->final_mma);
+        drain_wait(&bars->final_mma, 0);
+      }
+    } else if (lane == 0) {
       const uint32_t idesc = idesc_f16(kBM, BN, kBf16Mma);
       const uint32_t S_ = static_cast<uint32_t>(S), na = static_cast<uint32_t>(args.aslots),
                      nacc = static_cast<uint32_t>(args.acc_slots);
@@ -422,7 +486,61 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t S_ = static_cast<uint32_t>(S), na = static_cast<uint32_t>(args.aslots);
     RingPos sp, ap, bp;  // stages, operand-A slots, token slots
     bool ok = true;
-    if (T::kTs || kBconv) {
+    if (kFp4 && cw < kSfWarps) {
+      // Block scales of one stage (256 K: four 64-K MMA steps) into TMEM slot fp.
+      // A (weights): lane quarter q holds rows 32q..32q+31; row r's four scales
+      // of step kk (one 32-bit word, first 16 K in the low byte) go to the four
+      // columns m*16 + 4kk .. +3 of lane r.  B (tokens): every lane quarter
+      // holds all BN token rows, token 32j + l in lane l of column 32 + 4kk + j
+      // (16 + 4kk + j for one matrix); rows past BN read as zero.
+      const uint32_t nsf = static_cast<uint32_t>(args.sf_slots);
+      const uint32_t lane_bits = static_cast<uint32_t>(q * 32) << 16;
+      RingPos fp;
+      for (int u = blockIdx.x; ok && u < units; u += gridDim.x) {
+        for (int ks = 0; ks < nks; ++ks, sp.advance(S_), fp.advance(nsf)) {
+          const int s = sp.slot;
+          if (!bounded_wait(&bars->full[s], sp.phase, abort, args.err) ||
+              !bounded_wait(&bars->sfempty[fp.slot], fp.phase ^ 1, abort, args.err)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t st = smem_u32(smem + s * args.stage_bytes);
+          const uint32_t sf = tmem + lane_bits + args.sf_base + fp.slot * args.sf_cols;
+          uint32_t o[16];
+#pragma unroll
+          for (int m = 0; m < kNmat; ++m) {
+            const uint4 v = lds128(st + args.off_asf[m] + r * 16);
+            const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+            for (int i = 0; i < 16; ++i) o[i] = w[i >> 2];
+            tmem_st16(sf + m * 16, o);
+          }
+          uint4 tv[4];
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            const int row = 32 * j + lane;
+            tv[j] = row < BN ? lds128(st + args.off_bsf + row * 16) : make_uint4(0, 0, 0, 0);
+          }
+#pragma unroll
+          for (int kk = 0; kk < 4; ++kk) {
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+              const uint4 v = tv[j];
+              o[kk * 4 + j] = kk == 0 ? v.x : (kk == 1 ? v.y : (kk == 2 ? v.z : v.w));
+            }
+          }
+          tmem_st16(sf + kNmat * 16, o);
+          tmem_wait_st();
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) {
+            mbar_arrive(&bars->sffull[fp.slot]);
+            mbar_arrive(&bars->empty[s]);
+          }
+        }
+      }
+    } else if (T::kTs || kBconv) {
       for (uint32_t uit = 0, u = blockIdx.x; ok && static_cast<int>(u) < units; u += gridDim.x, ++uit) {
         // FP16 operand mode: this unit's FP16 group scales, applied here to the weights
         const uint32_t sbuf = uit & 1;
@@ -441,33 +559,16 @@ __global__ void __launch_bounds__(kThreads, 1)
                 tc_fence_after();
                 const uint32_t tile = smem_u32(smem + args.off_bring) + bslot * BN * 128;
                 const uint32_t braw = st + args.off_braw;
-                if (AM == AM_INT8) {
-                  // 64 K = four 16-code chunks of raw box sc / 2 (128 codes per row)
-                  for (int i = ctid; i < BN * 4; i += kConvWarps * 32) {
-                    const int row = i >> 2, c = 4 * (sc & 1) + (i & 3);
-                    const uint4 v = lds128(sw128(braw + (sc >> 1) * BN * 128, row, c));
-                    uint32_t o[16];
-                    const uint4 zero = make_uint4(0, 0, 0, 0);
-                    cvt_int8x32<false>(v, zero, o);  // first 8 words hold the 16 converted values
-                    const int cc = (c & 3) * 2;
-                    sts128(sw128(tile, row, cc), o[0], o[1], o[2], o[3]);
-                    sts128(sw128(tile, row, cc + 1), o[4], o[5], o[6], o[7]);
-                  }
-                } else {
-                  // 64 K = two 32-code chunks of the raw row (256 codes per row), scales 2 bytes each
-                  const uint32_t bsf = st + args.off_bsf;
-                  for (int i = ctid; i < BN * 2; i += kConvWarps * 32) {
-                    const int row = i >> 1, c = 2 * sc + (i & 1);
-                    const uint4 v = lds128(sw128(braw, row, c));
-                    uint32_t sfp;
-                    asm volatile("ld.shared.u16 %0, [%1];" : "=r"(sfp) : "r"(bsf + row * 16 + c * 2));
-                    uint32_t o[16];
-                    cvt_fp4x32(v, sfp & 0xFF, (sfp >> 8) & 0xFF, o);
-                    const int cc = (c & 1) * 4;
-#pragma unroll
-                    for (int j = 0; j < 4; ++j)
-                      sts128(sw128(tile, row, cc + j), o[4 * j], o[4 * j + 1], o[4 * j + 2], o[4 * j + 3]);
-                  }
+                // 64 K = four 16-code chunks of raw box sc / 2 (128 codes per row)
+                for (int i = ctid; i < BN * 4; i += kConvWarps * 32) {
+                  const int row = i >> 2, c = 4 * (sc & 1) + (i & 3);
+                  const uint4 v = lds128(sw128(braw + (sc >> 1) * BN * 128, row, c));
+                  uint32_t o[16];
+                  const uint4 zero = make_uint4(0, 0, 0, 0);
+                  cvt_int8x32<false>(v, zero, o);  // first 8 words hold the 16 converted values
+                  const int cc = (c & 3) * 2;
+                  sts128(sw128(tile, row, cc), o[0], o[1], o[2], o[3]);
+                  sts128(sw128(tile, row, cc + 1), o[4], o[5], o[6], o[7]);
                 }
                 fence_proxy_async_smem();
                 __syncwarp();
@@ -501,12 +602,6 @@ __global__ void __launch_bounds__(kThreads, 1)
                   const uint32_t s2 = sh | (sh << 16);
 #pragma unroll
                   for (int i = 0; i < 16; ++i) o[i] = f16x2_mul(o[i], s2);
-                }
-                if (WF == WF_NVFP4) {  // NVFP4
-                  const uint4 v = lds128(sw128(abase, r, kin >> 5));
-                  uint32_t sfp;
-                  asm volatile("ld.shared.u16 %0, [%1];" : "=r"(sfp) : "r"(st + args.off_asf[m] + r * 16 + (kin >> 4)));
-                  cvt_fp4x32(v, sfp & 0xFF, (sfp >> 8) & 0xFF, o);
                 }
                 tmem_st16(tmem + (static_cast<uint32_t>(q * 32) << 16) + aslot * (kNmat * 32) + m * 32 + h * 16, o);
               }
@@ -746,7 +841,7 @@ bool plan_smem(int wf, int am, bool gate_up, int K, int E, int BN, Plan* p) {
   const uint32_t cpw = BN >= 32 ? BN / 2 : BN;  // token columns per epilogue warp
   const uint32_t sa = am == AM_INT8 ? align_up(kEpiWarps * cpw * G * 4u, 16) : 0u;
   const uint32_t bars = align_up(sizeof(Bars), 16);
-  const uint32_t bring = (am == AM_INT8 || am == AM_FP4) ? kBSlots * BN * 128u : 0u;  // converted-token ring
+  const uint32_t bring = am == AM_INT8 ? kBSlots * BN * 128u : 0u;  // converted-token ring
   fixed = bring + scales + tab + sa + bars;
   const size_t budget = kSmemLimit - 1024;  // alignment slack
   if (fixed + 2 * a.stage_bytes > budget) return false;
@@ -844,7 +939,7 @@ int run_gemm(const mnw_moe_layer* L, int wfmt, int act, int kind, const void* a0
     BN /= 2;
   }
   GemmArgs& a = plan.args;
-  const bool ts = wf != WF_BF16;
+  const bool ts = wf == WF_INT8 || wf == WF_INT4;  // A through TMEM (converted codes)
   a.offsets = offsets;
   a.E = L->E;
   a.P = P;
@@ -853,7 +948,25 @@ int run_gemm(const mnw_moe_layer* L, int wfmt, int act, int kind, const void* a0
   a.BN = BN;
   a.n_tiles = N / kBM;
   a.nmat = nmat;
-  {
+  if (wf == WF_NVFP4) {
+    // TMEM columns: [accumulator slots | scale-factor slots].  A scale-factor
+    // slot holds one stage's block scales: 16 columns per weight matrix and 16
+    // for the tokens.  At least two of each, so the epilogue drains one
+    // accumulator while the MMAs fill the other and the scale-factor warps
+    // fill one slot while the MMAs read the other.
+    const int d_cols = nmat * BN, sf_cols = 16 * (nmat + 1);
+    int nacc = 2, nsf = 2;
+    if (2 * d_cols + 2 * sf_cols > kTmemCols) return MNW_E_UNSUPPORTED;
+    while (nacc < 4 && (nacc + 1) * d_cols + 2 * sf_cols <= kTmemCols) ++nacc;
+    while (nsf < kMaxSf && nsf < a.stages && nacc * d_cols + (nsf + 1) * sf_cols <= kTmemCols) ++nsf;
+    a.aslots = 1;
+    a.acc_slots = nacc;
+    a.acc_base = 0;
+    a.sum_base = 0;
+    a.sf_base = nacc * d_cols;
+    a.sf_slots = nsf;
+    a.sf_cols = sf_cols;
+  } else {
     // TMEM columns: [A ring | accumulator slots | running sum (grouped)].
     // Deep rings hide the converter -> MMA -> epilogue hand-off latency; small
     // token tiles leave room for more slots.

@@ -205,6 +205,20 @@ __device__ __forceinline__ void mma_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_
       "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
       : "memory");
 }
+// D[tmem] (+)= (A * SFA)[smem desc] * (B * SFB)[smem desc]^T, kind::mxf4nvf4:
+// E2M1 operands packed two per byte (K = 64 per instruction), one UE4M3
+// scale per 16 K for every row of A and of B, read from tensor memory at
+// sfa_tmem / sfb_tmem (four scales of a row in one 32-bit column, the first
+// 16 K in the low byte).  One CTA.
+__device__ __forceinline__ void mma_fp4_ss(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
+                                           uint32_t sfa_tmem, uint32_t sfb_tmem, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %6, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::mxf4nvf4.block_scale.scale_vec::4X [%0], %1, %2, %3, [%4], [%5], p;\n\t}" ::"r"(
+          d_tmem),
+      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(sfa_tmem), "r"(sfb_tmem), "r"(accumulate)
+      : "memory");
+}
 // Arrive once on `bar` when every tcgen05 operation issued so far by this thread has completed.
 __device__ __forceinline__ void mma_commit(uint64_t* bar) {
   asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
@@ -217,6 +231,13 @@ __device__ __forceinline__ void mma_commit(uint64_t* bar) {
 __host__ __device__ constexpr uint32_t idesc_f16(int M, int N, bool ab_bf16) {
   return (1u << 4) | ((ab_bf16 ? 1u : 0u) << 7) | ((ab_bf16 ? 1u : 0u) << 10) |
          (static_cast<uint32_t>(N >> 3) << 17) | (static_cast<uint32_t>(M >> 4) << 24);
+}
+
+// Instruction descriptor of kind::mxf4nvf4 with block scaling: A and B E2M1
+// (format code 1), UE4M3 scale factors (bit 23 clear), both K-major, FP32
+// accumulation, scale-factor selectors 0.
+__host__ __device__ constexpr uint32_t idesc_fp4(int M, int N) {
+  return (1u << 7) | (1u << 10) | (static_cast<uint32_t>(N >> 3) << 17) | (static_cast<uint32_t>(M >> 4) << 24);
 }
 
 // Shared-memory descriptor of a K-major operand tile in the 128-byte swizzle
