@@ -144,6 +144,33 @@ int mnw_moe_permute(const int32_t* ids, int T, int k, int E, int32_t* expert_off
 int mnw_moe_permute_host(const int32_t* ids, int T, int k, int E, int32_t* expert_offsets,
                          int32_t* sorted_assign, int32_t* assign_pos, uint32_t* dropped);
 
+/* GPU routing fused with the permutation (the step before a1 on the decode
+ * path): the "coder543/minnow" README, section "Quantization", routes the
+ * 32-token decode blocks on the GPU; the "LLaDA2.2-flash-minnow" model card,
+ * "Checkpoints and precision", keeps routers in their source floating point.
+ * The pages give no formula; the rule used here:
+ *   logits[t, e] = x[t] . w_router[e]   (BF16 inputs, FP32 accumulation in a
+ *                                        fixed order: reproducible bits)
+ *   ids[t, 0..k) = the k largest logits of row t, largest first, the lower
+ *                  expert index first among equal logits (NaN ranks last)
+ *   w[t, j]      = exp(l_j - l_0) / sum_i exp(l_i - l_0) over the k chosen (FP32)
+ * then expert_offsets, sorted_assign and assign_pos exactly as
+ * mnw_moe_permute() gives for those ids.
+ * x: device bf16 [T, H]; w_router: device bf16 [E, H]; ids: device int32
+ * [T, k]; w: device f32 [T, k]; the permutation outputs as mnw_moe_permute.
+ * scratch: device, 256-byte aligned, >= mnw_moe_route_scratch_size(T, E)
+ * bytes.  It starts with arrival counters that must be zero before the first
+ * call (a zero-filled buffer) and that every completed call leaves at zero;
+ * the rest receives the logits [T, E] (f32, row-major).  Calls sharing one
+ * scratch must not overlap.  err (device, nullable) as for mnw_moe_permute.
+ * One kernel launch when T*k <= 4096 (the permutation runs in its last CTA);
+ * larger batches add the permutation's own launches.  Limits: H % 128 == 0,
+ * 1 <= k <= min(E, 32), E <= 1024.  T = 0 is a no-op. */
+size_t mnw_moe_route_scratch_size(int T, int E);
+int mnw_moe_route(const void* x, const void* w_router, int T, int H, int E, int k, int32_t* ids, float* w,
+                  int32_t* expert_offsets, int32_t* sorted_assign, int32_t* assign_pos, void* scratch,
+                  size_t scratch_bytes, uint32_t* err, mnw_stream stream);
+
 /* a2 -- dynamic activation quantisation of R rows of K BF16 values.
  * Row r reads x[src] with src = r, or, when row_index (device int32 [R]) is
  * non-NULL, src = row_index[r] / index_div (a negative row_index gives a
@@ -253,6 +280,17 @@ int mnw_moe_forward(const mnw_moe_layer* layer, int act, const void* x, const in
                     const float* w, int T, int k, void* out, void* ws, size_t ws_bytes,
                     mnw_stream stream);
 uint32_t* mnw_moe_workspace_error_word(void* ws);
+
+/* The whole layer with GPU routing: mnw_moe_route() on x and w_router (device
+ * bf16 [E, H]), then the layer exactly as mnw_moe_forward() with those ids and
+ * weights (the router's launch already holds the permutation).  ids_out
+ * (device int32 [T, k]) and w_out (device f32 [T, k]) receive the router's
+ * choices.  ws: >= mnw_moe_workspace_size_routed() bytes; the router's
+ * counters live in it and are cleared by every call. */
+size_t mnw_moe_workspace_size_routed(const mnw_moe_layer* layer, int act, int T, int k);
+int mnw_moe_forward_routed(const mnw_moe_layer* layer, int act, const void* x, const void* w_router, int T,
+                           int k, int32_t* ids_out, float* w_out, void* out, void* ws, size_t ws_bytes,
+                           mnw_stream stream);
 
 /* The whole layer from and to HOST buffers: copies x into ws, runs
  * mnw_moe_forward, and synchronises `stream`.  ids, w and out are used in

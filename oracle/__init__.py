@@ -67,6 +67,7 @@ def _load():
             "mnwo_quant_nvfp4_g16": (i32, [P, i32, i32, P, P, P]),
             "mnwo_encode_f16_rows": (i32, [P, i32, i32, P, P]),
             "mnwo_permute": (i32, [P, i32, i32, i32, P, P, P]),
+            "mnwo_route": (i32, [P, P, i32, i32, i32, i32, P, P, P]),
             "mnwo_gemm_a16": (i32, [P, ctypes.c_size_t, i32, P, P, i32, P]),
             "mnwo_gemm_a8": (i32, [P, ctypes.c_size_t, i32, P, P, P, i32, P, P]),
             "mnwo_gemm_a4": (i32, [P, ctypes.c_size_t, i32, P, P, P, P, i32, P]),
@@ -170,6 +171,20 @@ def encode_f16_rows(x_bf16: np.ndarray):
     factor = np.zeros((R,), np.float32)
     _check(_load().mnwo_encode_f16_rows(_p(x), R, K, _p(codes), _p(factor)), "encode_f16_rows")
     return codes, factor
+
+
+def route(x_bf16: np.ndarray, wr_bf16: np.ndarray, k: int):
+    """Router of the GPU-routing path: (ids int32 [T,k], w float32 [T,k],
+    logits float64 [T,E]); see mnwo_route for the reading of the pages."""
+    x = _c(x_bf16, np.uint16)
+    wr = _c(wr_bf16, np.uint16)
+    T, H = x.shape
+    E = wr.shape[0]
+    ids = np.zeros((T, k), np.int32)
+    w = np.zeros((T, k), np.float32)
+    logits = np.zeros((T, E), np.float64)
+    _check(_load().mnwo_route(_p(x), _p(wr), T, H, E, k, _p(ids), _p(w), _p(logits)), "route")
+    return ids, w, logits
 
 
 def permute(ids: np.ndarray, E: int):

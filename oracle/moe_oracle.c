@@ -309,6 +309,45 @@ int mnwo_encode_f16_rows(const uint16_t* x, int R, int K, uint16_t* codes, float
   return MNWO_OK;
 }
 
+/* Router: logits by the plain dot product, then the k largest by selection
+ * (each pass takes the largest logit not yet chosen; on equal logits the
+ * first expert in index order), then a softmax over the chosen logits. */
+int mnwo_route(const uint16_t* x, const uint16_t* wr, int T, int H, int E, int k, int32_t* ids, float* w,
+               double* logits) {
+  if (T < 0 || H <= 0 || E <= 0 || k < 1 || k > E || !x || !wr || !ids || !w) return MNWO_E_ARG;
+  double* l = (double*)malloc(sizeof(double) * (size_t)E);
+  unsigned char* taken = (unsigned char*)malloc((size_t)E);
+  if (!l || !taken) {
+    free(l);
+    free(taken);
+    return MNWO_E_ARG;
+  }
+  for (int t = 0; t < T; ++t) {
+    for (int e = 0; e < E; ++e) {
+      double acc = 0.0;
+      for (int h = 0; h < H; ++h)
+        acc += mnwo_bf16_to_double(x[(size_t)t * H + h]) * mnwo_bf16_to_double(wr[(size_t)e * H + h]);
+      l[e] = acc;
+      taken[e] = 0;
+      if (logits) logits[(size_t)t * E + e] = acc;
+    }
+    for (int j = 0; j < k; ++j) {
+      int best = -1;
+      for (int e = 0; e < E; ++e)
+        if (!taken[e] && (best < 0 || l[e] > l[best])) best = e;
+      taken[best] = 1;
+      ids[(size_t)t * k + j] = best;
+    }
+    const double lmax = l[ids[(size_t)t * k]];
+    double sum = 0.0;
+    for (int j = 0; j < k; ++j) sum += exp(l[ids[(size_t)t * k + j]] - lmax);
+    for (int j = 0; j < k; ++j) w[(size_t)t * k + j] = (float)(exp(l[ids[(size_t)t * k + j]] - lmax) / sum);
+  }
+  free(l);
+  free(taken);
+  return MNWO_OK;
+}
+
 int mnwo_permute(const int32_t* ids, int T, int k, int E,
                  int32_t* expert_offsets, int32_t* sorted_assign, int32_t* assign_pos) {
   int P, a, e, dropped = 0;

@@ -69,6 +69,18 @@ int mnwo_quant_nvfp4_g16(const uint16_t* x, int R, int K, uint8_t* codes, uint8_
  * MNWO_E_NONFINITE for a row holding Inf or NaN. */
 int mnwo_encode_f16_rows(const uint16_t* x, int R, int K, uint16_t* codes, float* factor);
 
+/* ---- router (the step before the permutation on the GPU routing path) ----
+ * [minnow] "Quantization": GPU routing for 32-token decode blocks; [card]:
+ * routers keep their source floating-point (BF16) weights.  Reading of the
+ * pages (they give no formula): logits[t, e] = sum_h x[t, h] * wr[e, h]
+ * (FP64 here); ids[t, 0..k) = the k largest logits of row t, largest first,
+ * the lower expert index first among equal logits; w[t, j] = softmax of the k
+ * chosen logits, exp(l_j - l_max) / sum_i exp(l_i - l_max) in FP64, stored
+ * as float.  x: [T, H] BF16 bits; wr: [E, H] BF16 bits; logits (nullable):
+ * [T, E] FP64.  Returns MNWO_E_ARG for k outside [1, E]. */
+int mnwo_route(const uint16_t* x, const uint16_t* wr, int T, int H, int E, int k, int32_t* ids, float* w,
+               double* logits);
+
 /* ---- token permutation into expert-sorted order ---- */
 /* Returns the number of dropped (out-of-range) ids, or -1 on bad arguments. */
 int mnwo_permute(const int32_t* ids, int T, int k, int E,

@@ -34,6 +34,10 @@ SIGNATURES = {
     "mnw_moe_permute": (_I, [_P, _I, _I, _I, _P, _P, _P, _P, _I, _P, _U32P, _P]),
     "mnw_moe_quantize_act": (_I, [_I, _P, _I, _I, _P, _I, _P, _P, _P, _P]),
     "mnw_moe_permute_host": (_I, [_P, _I, _I, _I, _P, _P, _P, _U32P]),
+    "mnw_moe_route_scratch_size": (_SZ, [_I, _I]),
+    "mnw_moe_route": (_I, [_P, _P, _I, _I, _I, _I, _P, _P, _P, _P, _P, _P, _SZ, _U32P, _P]),
+    "mnw_moe_workspace_size_routed": (_SZ, [_P, _I, _I, _I]),
+    "mnw_moe_forward_routed": (_I, [_P, _I, _P, _P, _I, _I, _P, _P, _P, _P, _SZ, _P]),
     "mnw_moe_grouped_gemm_bf16": (_I, [_P, _I, _P, _P, _I, _P, _U32P, _P]),
     "mnw_moe_grouped_gemm_w8a16": (_I, [_P, _I, _P, _P, _I, _P, _U32P, _P]),
     "mnw_moe_grouped_gemm_w4a16": (_I, [_P, _I, _P, _P, _I, _P, _U32P, _P]),
@@ -138,6 +142,52 @@ def mnw_moe_permute(ids, E, x=None, stream=None, err=None):
     _check(load().mnw_moe_permute(_ptr(ids), T, k, E, _ptr(offsets), _ptr(sorted_assign), _ptr(assign_pos),
                                   _ptr(x), H, _ptr(x_perm), _ptr(err), _stream(stream)), "mnw_moe_permute")
     return offsets, sorted_assign, assign_pos, x_perm
+
+
+def mnw_moe_route(x, w_router, k, scratch=None, stream=None, err=None):
+    """GPU routing fused with the permutation (see include/mnw_moe.h).
+    x: bf16 [T, H]; w_router: bf16 [E, H].  Returns (ids int32 [T,k], w f32
+    [T,k], expert_offsets, sorted_assign, assign_pos, logits f32 [T,E]).
+    scratch: a uint8 device tensor reused across calls (zero-filled when new)."""
+    T, H = x.shape
+    E = w_router.shape[0]
+    dev = x.device
+    need = load().mnw_moe_route_scratch_size(T, E)
+    if scratch is None:
+        scratch = torch.zeros(need + 256, dtype=torch.uint8, device=dev)
+    base = (-scratch.data_ptr()) % 256
+    view = scratch[base:base + need]
+    ids = torch.empty((T, k), dtype=torch.int32, device=dev)
+    w = torch.empty((T, k), dtype=torch.float32, device=dev)
+    off = torch.empty(E + 1, dtype=torch.int32, device=dev)
+    sa = torch.empty(T * k, dtype=torch.int32, device=dev)
+    pos = torch.empty(T * k, dtype=torch.int32, device=dev)
+    _check(load().mnw_moe_route(_ptr(x), _ptr(w_router), T, H, E, k, _ptr(ids), _ptr(w), _ptr(off), _ptr(sa),
+                                _ptr(pos), _ptr(view), need, _ptr(err), _stream(stream)), "mnw_moe_route")
+    cb = (((1 + (T + 15) // 16) * 4 + 255) // 256) * 256  # the counters come first
+    logits = view[cb:cb + T * E * 4].view(torch.float32).view(T, E)
+    return ids, w, off, sa, pos, logits
+
+
+def mnw_moe_workspace_size_routed(layer, act, T, k) -> int:
+    return load().mnw_moe_workspace_size_routed(layer.handle, act, T, k)
+
+
+def mnw_moe_forward_routed(layer, act, x, w_router, k, ws=None, out=None, stream=None):
+    """The layer with GPU routing; returns (out bf16 [T,H], ids int32 [T,k], w f32 [T,k])."""
+    T = x.shape[0]
+    if ws is None:
+        n = mnw_moe_workspace_size_routed(layer, act, T, k)
+        ws = torch.empty(n + 256, dtype=torch.uint8, device=x.device)
+    base = (-ws.data_ptr()) % 256
+    ids = torch.empty((T, k), dtype=torch.int32, device=x.device)
+    w = torch.empty((T, k), dtype=torch.float32, device=x.device)
+    if out is None:
+        out = torch.empty((T, layer.H), dtype=torch.bfloat16, device=x.device)
+    _check(load().mnw_moe_forward_routed(layer.handle, act, _ptr(x), _ptr(w_router), T, k, _ptr(ids), _ptr(w),
+                                         _ptr(out), ctypes.c_void_p(ws.data_ptr() + base), ws.numel() - base,
+                                         _stream(stream)), "mnw_moe_forward_routed")
+    return out, ids, w
 
 
 def mnw_moe_permute_host(ids, E):

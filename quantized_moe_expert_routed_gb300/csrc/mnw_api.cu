@@ -163,7 +163,7 @@ static bool act_allowed(int wfmt, int act) {
 // ---- workspace layout ----------------------------------------------------------
 
 struct WsLayout {
-  size_t err, dep, offsets, sorted, pos;
+  size_t err, dep, rt, rt_zero_end, offsets, sorted, pos;
   size_t xa, xb, xc;   // x operand: bf16 rows | codes, scales, outer
   size_t h, ha, hb, hc;
   size_t y;
@@ -173,12 +173,17 @@ struct WsLayout {
 
 static size_t al(size_t x) { return (x + 255) / 256 * 256; }
 
-static WsLayout ws_layout(const mnw_moe_layer* L, int act, int T, int k) {
+// routed: room for the GPU router's scratch (arrival counters, zeroed with the
+// error word, then the logits [T, E]).
+static WsLayout ws_layout(const mnw_moe_layer* L, int act, int T, int k, bool routed = false) {
   WsLayout w{};
   const size_t P = static_cast<size_t>(T) * k, H = L->H, I = L->I, E = L->E;
   size_t o = 0;
   w.err = o; o += 256;
   w.dep = o; o = al(o + warp_dep_words(static_cast<int>(P), static_cast<int>(E)) * 4);  // zeroed with err
+  w.rt = o;
+  if (routed) o = al(o + route_scratch_bytes(T, L->E));
+  w.rt_zero_end = routed ? w.rt + route_counter_bytes(T) : w.rt;  // [err, rt_zero_end) is zeroed per call
   w.offsets = o; o = al(o + (E + 1) * 4);
   w.sorted = o; o = al(o + P * 4);
   w.pos = o; o = al(o + P * 4);
@@ -497,15 +502,23 @@ size_t mnw_moe_workspace_size_host(const mnw_moe_layer* L, int act, int T, int k
 }
 uint32_t* mnw_moe_workspace_error_word(void* ws) { return static_cast<uint32_t*>(ws); }
 
-int mnw_moe_forward(const mnw_moe_layer* L, int act, const void* x, const int32_t* ids, const float* w, int T, int k,
-                    void* out, void* ws, size_t ws_bytes, mnw_stream stream) {
-  MNW_RANGE("mnw_moe_forward");
+}  // extern "C"
+
+// The layer.  With wr (router weights) non-null the ids and weights come from
+// the GPU router (written to ids_out / w_out), whose launch also produces the
+// permutation; the steps that would permute then only gather rows.
+static int forward_impl(const mnw_moe_layer* L, int act, const void* x, const int32_t* ids, const float* w,
+                        const void* wr, int32_t* ids_out, float* w_out, int T, int k, void* out, void* ws,
+                        size_t ws_bytes, mnw_stream stream) {
   if (!L || T < 0 || k < 1 || k > 32 || k > L->E) return MNW_E_INVALID_ARG;
   if (!act_allowed(L->wfmt, act)) return MNW_E_MODE;
   if (T == 0) return MNW_OK;
-  if (!x || !ids || !w || !out || !ws || !aligned(x, 16) || !aligned(out, 16) || !aligned(ws, 256))
+  const bool routed = wr != nullptr;
+  if (routed && (!ids_out || !w_out || !aligned(wr, 16) || !route_shape_ok(T, L->H, L->E, k)))
     return MNW_E_INVALID_ARG;
-  const WsLayout W = ws_layout(L, act, T, k);
+  if (!routed && (!ids || !w)) return MNW_E_INVALID_ARG;
+  if (!x || !out || !ws || !aligned(x, 16) || !aligned(out, 16) || !aligned(ws, 256)) return MNW_E_INVALID_ARG;
+  const WsLayout W = ws_layout(L, act, T, k, routed);
   if (ws_bytes < W.total) return MNW_E_WORKSPACE_TOO_SMALL;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   uint8_t* b = static_cast<uint8_t*>(ws);
@@ -517,7 +530,19 @@ int mnw_moe_forward(const mnw_moe_layer* L, int act, const void* x, const int32_
   // The first 256 bytes of ws: error word, then a [claim, done] work counter per GEMM launch.
   uint32_t* sched_gu = err + 16;
   uint32_t* sched_dn = err + 18;
-  if (cudaMemsetAsync(err, 0, W.offsets - W.err, st) != cudaSuccess) return MNW_E_CUDA;  // error word, counters
+  if (cudaMemsetAsync(err, 0, W.rt_zero_end - W.err, st) != cudaSuccess) return MNW_E_CUDA;  // error word, counters
+  if (routed) {
+    if (launch_route(x, wr, T, L->H, L->E, k, ids_out, w_out, offs, sorted, pos, b + W.rt, err, st) != cudaSuccess)
+      return MNW_E_CUDA;
+    ids = ids_out;
+    w = w_out;
+  }
+  // the permutation, optionally gathering x rows (routed: already permuted, gather only)
+  auto permute = [&](const void* gx, void* gx_perm) -> int {
+    if (!routed) return mnw_moe_permute(ids, T, k, L->E, offs, sorted, pos, gx, gx ? H : 0, gx_perm, err, stream);
+    if (!gx) return MNW_OK;
+    return launch_gather_rows(gx, H, sorted, P, k, gx_perm, st) == cudaSuccess ? MNW_OK : MNW_E_CUDA;
+  };
   int rc;
   if (act == MNW_ACT_BF16) {
     // INT weights: the GEMMs run on FP16 rows (scaled into FP16 range by a
@@ -535,7 +560,7 @@ int mnw_moe_forward(const mnw_moe_layer* L, int act, const void* x, const int32_
                            warp_gemm_applicable(L, L->wfmt, act, MNW_KIND_DOWN);
     const WarpDep gu_dep{reinterpret_cast<uint32_t*>(b + W.dep), kDepProduce, 0};
     if (L->f16_gate_up_ok) {
-      rc = mnw_moe_permute(ids, T, k, L->E, offs, sorted, pos, nullptr, 0, nullptr, err, stream);
+      rc = permute(nullptr, nullptr);
       if (rc) return rc;
       float* factor = reinterpret_cast<float*>(b + W.xc);
       rc = mnw_moe_quantize_act(MNW_ACT_F16_ROWS, x, P, H, sorted, k, b + W.xa, nullptr, factor, stream);
@@ -543,7 +568,7 @@ int mnw_moe_forward(const mnw_moe_layer* L, int act, const void* x, const int32_
       rc = run_gemm(L, L->wfmt, kActF16Rows, MNW_KIND_GATE_UP, b + W.xa, factor, nullptr, offs, P, b + W.h, nullptr,
                     err, st, sched_gu, warp_down ? &gu_dep : nullptr);
     } else {
-      rc = mnw_moe_permute(ids, T, k, L->E, offs, sorted, pos, x, H, b + W.xa, err, stream);
+      rc = permute(x, b + W.xa);
       if (rc) return rc;
       rc = run_gemm(L, L->wfmt, act, MNW_KIND_GATE_UP, b + W.xa, nullptr, nullptr, offs, P, b + W.h, nullptr, err, st,
                     sched_gu, warp_down ? &gu_dep : nullptr);
@@ -564,7 +589,7 @@ int mnw_moe_forward(const mnw_moe_layer* L, int act, const void* x, const int32_
     }
     if (rc) return rc;
   } else {
-    rc = mnw_moe_permute(ids, T, k, L->E, offs, sorted, pos, nullptr, 0, nullptr, err, stream);
+    rc = permute(nullptr, nullptr);
     if (rc) return rc;
     float* xo = act == MNW_ACT_NVFP4_G16 ? reinterpret_cast<float*>(b + W.xc) : nullptr;
     float* ho = act == MNW_ACT_NVFP4_G16 ? reinterpret_cast<float*>(b + W.hc) : nullptr;
@@ -578,6 +603,47 @@ int mnw_moe_forward(const mnw_moe_layer* L, int act, const void* x, const int32_
     if (rc) return rc;
   }
   return mnw_moe_combine(b + W.y, pos, w, T, k, H, out, stream);
+}
+
+extern "C" {
+
+int mnw_moe_forward(const mnw_moe_layer* L, int act, const void* x, const int32_t* ids, const float* w, int T, int k,
+                    void* out, void* ws, size_t ws_bytes, mnw_stream stream) {
+  MNW_RANGE("mnw_moe_forward");
+  if (T > 0 && (!ids || !w)) return MNW_E_INVALID_ARG;
+  return forward_impl(L, act, x, ids, w, nullptr, nullptr, nullptr, T, k, out, ws, ws_bytes, stream);
+}
+
+size_t mnw_moe_workspace_size_routed(const mnw_moe_layer* L, int act, int T, int k) {
+  if (!L || T < 0 || k < 1) return 0;
+  return ws_layout(L, act, T, k, true).total;
+}
+
+int mnw_moe_forward_routed(const mnw_moe_layer* L, int act, const void* x, const void* w_router, int T, int k,
+                           int32_t* ids_out, float* w_out, void* out, void* ws, size_t ws_bytes, mnw_stream stream) {
+  MNW_RANGE("mnw_moe_forward_routed");
+  if (T > 0 && !w_router) return MNW_E_INVALID_ARG;
+  return forward_impl(L, act, x, nullptr, nullptr, w_router, ids_out, w_out, T, k, out, ws, ws_bytes, stream);
+}
+
+size_t mnw_moe_route_scratch_size(int T, int E) {
+  if (T < 0 || E < 1) return 0;
+  return route_scratch_bytes(T, E);
+}
+
+int mnw_moe_route(const void* x, const void* w_router, int T, int H, int E, int k, int32_t* ids, float* w,
+                  int32_t* expert_offsets, int32_t* sorted_assign, int32_t* assign_pos, void* scratch,
+                  size_t scratch_bytes, uint32_t* err, mnw_stream stream) {
+  MNW_RANGE("mnw_moe_route");
+  if (!route_shape_ok(T, H, E, k)) return MNW_E_INVALID_ARG;
+  if (T == 0) return MNW_OK;
+  if (!x || !w_router || !ids || !w || !expert_offsets || !sorted_assign || !assign_pos || !scratch ||
+      !aligned(x, 16) || !aligned(w_router, 16) || !aligned(scratch, 256))
+    return MNW_E_INVALID_ARG;
+  if (scratch_bytes < route_scratch_bytes(T, E)) return MNW_E_WORKSPACE_TOO_SMALL;
+  const cudaError_t e = launch_route(x, w_router, T, H, E, k, ids, w, expert_offsets, sorted_assign, assign_pos,
+                                     scratch, err, static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? MNW_OK : MNW_E_CUDA;
 }
 
 // The device address of a host buffer the GPU can read and write in place

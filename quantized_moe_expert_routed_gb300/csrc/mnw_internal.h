@@ -91,6 +91,18 @@ bool encode_map(CUtensorMap* map, CUtensorMapDataType dtype, int rank, const voi
 cudaError_t launch_permute(const int32_t* ids, int T, int k, int E, int32_t* offsets, int32_t* sorted_assign,
                            int32_t* assign_pos, const void* x, int H, void* x_perm, uint32_t* err,
                            cudaStream_t st);
+// x_perm[p] = x[sorted_assign[p] / k] (zero rows where sorted_assign[p] < 0).
+cudaError_t launch_gather_rows(const void* x, int H, const int32_t* sorted_assign, int P, int k, void* x_perm,
+                               cudaStream_t st);
+// GPU routing fused with the permutation (mnw_router.cu): ids/w for every
+// token and the permutation of them; scratch = [arrival counters | logits].
+size_t route_scratch_bytes(int T, int E);
+bool route_shape_ok(int T, int H, int E, int k);
+cudaError_t launch_route(const void* x, const void* wr, int T, int H, int E, int k, int32_t* ids, float* w,
+                         int32_t* offsets, int32_t* sorted_assign, int32_t* assign_pos, void* scratch, uint32_t* err,
+                         cudaStream_t st);
+// Bytes at the start of the route scratch that hold its arrival counters.
+inline size_t route_counter_bytes(int T) { return ((1 + (static_cast<size_t>(T) + 15) / 16) * 4 + 255) / 256 * 256; }
 // MNW_ACT_F16_ROWS encoding of P rows (row p reads x[row_index[p] / div], or
 // x[p] without row_index): FP16 codes into x_perm, power-of-two factors.
 cudaError_t launch_gather_f16(const void* x, int H, const int32_t* row_index, int P, int div, void* x_perm,

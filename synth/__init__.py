@@ -160,6 +160,12 @@ def routing_hot_cold(T: int, E: int, k: int, seed: int, hot_frac: float = 0.10, 
     return ids.to(torch.int32)
 
 
+def router_weights(E: int, H: int, seed: int, device="cpu", stream: int = 400) -> torch.Tensor:
+    """Router matrix [E, H] bf16 ~N(0, 1/H), so that logits of N(0,1) tokens are ~N(0, 1)."""
+    v = normal_f64(seed, stream, E * H, device) / math.sqrt(H)
+    return v.to(torch.float32).to(torch.bfloat16).reshape(E, H)
+
+
 def routing_weights(T: int, k: int, seed: int, device="cpu", stream: int = 300) -> torch.Tensor:
     """float32 [T, k]: softmax over k N(0,1) logits."""
     logits = normal_f64(seed, stream, T * k, device).reshape(T, k)
