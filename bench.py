@@ -199,6 +199,8 @@ def run_ours(args, wl):
     dev = torch.device("cuda", local)
     x, ids, w, blob, hdr, L = S.make_inputs(replica_workload(wl, rank), device=dev)
     layer = M.Layer(blob, hdr)
+    M.mnw_moe_set_gemm_path({"auto": M.PATH_AUTO, "tcgen05": M.PATH_TCGEN05, "warp": M.PATH_WARP_MMA,
+                             "rows": M.PATH_ROWS}[args.gemm_path])
     E, T, k, P = wl.E, wl.T, wl.k, wl.P
     stream = torch.cuda.current_stream(dev)
     ws = M.workspace(layer, wl.act, T, k, device=dev)
@@ -258,7 +260,7 @@ def run_ours(args, wl):
         f16 = getattr(lib, f"mnw_moe_grouped_gemm_{gemm_name}_f16rows")
         # a zero-row call reports whether the layer's scales allow the FP16 form
         allowed = [f16(layer.handle, kind, None, None, None, 0, None, None, sp) == 0 for kind in (0, 1)]
-        allowed[1] = allowed[1] and -(-P // E) >= 32
+        allowed[1] = allowed[1] and (-(-P // E) >= 32 or args.gemm_path in ("tcgen05", "rows"))
         if allowed[0]:
             f16_gate_up = f16
             xa = torch.empty((P, wl.H), dtype=torch.float16, device=dev)
@@ -529,6 +531,8 @@ def main():
     ap.add_argument("--workload", default="large_w4a16", choices=sorted(S.WORKLOADS))
     ap.add_argument("--cpu-budget", type=float, default=15.0, help="seconds of oracle time for cpu_baseline")
     ap.add_argument("--peaks", action="store_true", help="run the tensor-core peak microbenchmark and exit")
+    ap.add_argument("--gemm-path", default="auto", choices=["auto", "tcgen05", "warp", "rows"],
+                    help="grouped-GEMM kernel selection (mnw_moe_set_gemm_path)")
     args = ap.parse_args()
     if args.peaks:
         print(json.dumps(run_peaks()))
@@ -537,7 +541,7 @@ def main():
     world, rank, local = _dist()
     if world > 1 and not torch.distributed.is_initialized():
         torch.distributed.init_process_group("nccl" if torch.cuda.is_available() else "gloo")
-    config = {"workload": wl.name, "T": wl.T, "H": wl.H, "E": wl.E, "I": wl.I, "k": wl.k,
+    config = {"workload": wl.name, "T": wl.T, "H": wl.H, "E": wl.E, "I": wl.I, "k": wl.k, "gemm_path": args.gemm_path,
               "weights": ["bf16", "int8_g128", "int4_g128", "nvfp4_g16"][wl.wfmt],
               "activations": ["bf16", "int8_g128", "nvfp4_g16"][wl.act], "routing": wl.routing,
               "l2": "flushed between timed steps outside the events: a 2x L2 buffer written, then another 2x L2 buffer read"}

@@ -101,7 +101,11 @@ enum mnw_wfmt { MNW_FMT_BF16 = 0, MNW_FMT_INT8_G128 = 1, MNW_FMT_INT4_G128 = 2, 
  * as FP16 with a power-of-two factor per row (mnw_moe_quantize_act), read by
  * the *_f16rows gate/up GEMMs.  mnw_moe_forward picks it by itself. */
 enum mnw_afmt { MNW_ACT_BF16 = 0, MNW_ACT_INT8_G128 = 1, MNW_ACT_NVFP4_G16 = 2, MNW_ACT_F16_ROWS = 3 };
-enum mnw_kind { MNW_KIND_GATE_UP = 0, MNW_KIND_DOWN = 1 };
+/* GATE / UP: the gate or the up matrix alone, out (bf16 [P, I]) = bf16(a .
+ * W^T) -- the unfused-activation comparison path ("coder543/minnow" README,
+ * "Quantization": --unfused-activation), whose activation then runs as
+ * mnw_moe_silu_mul(). */
+enum mnw_kind { MNW_KIND_GATE_UP = 0, MNW_KIND_DOWN = 1, MNW_KIND_GATE = 2, MNW_KIND_UP = 3 };
 
 typedef struct mnw_moe_layer mnw_moe_layer;
 
@@ -260,6 +264,14 @@ int mnw_moe_grouped_gemm_nvfp4(const mnw_moe_layer* layer, int kind, const uint8
                                const int32_t* expert_offsets, int P, void* out, uint32_t* err,
                                mnw_stream stream);
 
+/* The activation step of the unfused comparison path ("coder543/minnow"
+ * README, "Quantization": --unfused-activation): h[i] = bf16(SiLU(g[i]) *
+ * u[i]), SiLU(g) = g / (1 + e^-g), in FP32 from BF16 g and u (device bf16
+ * arrays of n values, n % 8 == 0; h device bf16 [n]).  The fused GEMMs
+ * evaluate the same expression on the FP32 dot products instead of their BF16
+ * roundings. */
+int mnw_moe_silu_mul(const void* g, const void* u, size_t n, void* h, mnw_stream stream);
+
 /* a5 -- combine: out[t] = bf16(sum_j w[t, j] * y[assign_pos[t*k + j]]) with
  * FP32 accumulation in ascending j; assignments with assign_pos < 0 are
  * skipped.  y: device bf16 [P, H]; assign_pos: device int32 [T*k];
@@ -288,6 +300,16 @@ uint32_t* mnw_moe_workspace_error_word(void* ws);
  * choices.  ws: >= mnw_moe_workspace_size_routed() bytes; the router's
  * counters live in it and are cleared by every call. */
 size_t mnw_moe_workspace_size_routed(const mnw_moe_layer* layer, int act, int T, int k);
+/* Host routing, process-wide (the "coder543/minnow" README, "Quantization":
+ * --host-routing, a comparison path; default 0): mnw_moe_forward_routed then
+ * computes the logits on the GPU, copies them to the host, picks the top-k and
+ * the softmax weights (same rule, FP32 host arithmetic) and the permutation
+ * (as mnw_moe_permute_host) on the host, and copies ids, weights and the
+ * permutation back before running the layer.  The call then synchronises
+ * `stream` twice and uses host memory of its own (T*E floats and the routing
+ * arrays) for the duration of the call.  Not synchronised with calls in flight
+ * on other threads. */
+int mnw_moe_set_host_routing(int on);
 int mnw_moe_forward_routed(const mnw_moe_layer* layer, int act, const void* x, const void* w_router, int T,
                            int k, int32_t* ids_out, float* w_out, void* out, void* ws, size_t ws_bytes,
                            mnw_stream stream);
@@ -310,14 +332,27 @@ int mnw_moe_forward_host(const mnw_moe_layer* layer, int act, const void* x_host
 uint64_t mnw_moe_launch_count(void);
 
 /* Grouped-GEMM kernel selection, process-wide (a tuning and testing knob;
- * results agree to FP32 rounding order either way).  MNW_PATH_AUTO: INT8/INT4
- * weights with fewer than 32 tokens per expert on average (P / E) use the
- * warp-level MMA kernel (operands dequantised straight into registers),
- * everything else the tcgen05 kernel.  MNW_PATH_TCGEN05 / MNW_PATH_WARP_MMA force one of them
- * (the warp kernel only covers INT8/INT4 weights with BF16 or INT8
- * activations).  Not synchronised with calls in flight on other threads. */
-enum mnw_path { MNW_PATH_AUTO = 0, MNW_PATH_TCGEN05 = 1, MNW_PATH_WARP_MMA = 2 };
+ * results agree to FP32 rounding order either way).  Three kernels:
+ *  - warp-level MMA (operands dequantised straight into registers): INT8/INT4
+ *    weights with BF16, FP16-row or INT8 activations;
+ *  - tcgen05 row tiles (tokens as M = 128, 256 weight rows as N, both from
+ *    shared memory): FP16 rows on INT8/INT4 weights, BF16 on BF16 weights;
+ *  - tcgen05 weight tiles (128 weight rows as M, the tokens of one expert as
+ *    N): every format and mode.
+ * MNW_PATH_AUTO: INT8/INT4 weights with fewer than 32 tokens per expert on
+ * average (P / E) take the warp kernel, otherwise the row-tile kernel where it
+ * applies and the weight-tile kernel elsewhere.  MNW_PATH_TCGEN05 forces the
+ * weight-tile kernel, MNW_PATH_WARP_MMA the warp kernel where it applies,
+ * MNW_PATH_ROWS the row-tile kernel where it applies (the weight-tile kernel
+ * elsewhere).  Not synchronised with calls in flight on other threads. */
+enum mnw_path { MNW_PATH_AUTO = 0, MNW_PATH_TCGEN05 = 1, MNW_PATH_WARP_MMA = 2, MNW_PATH_ROWS = 3 };
 int mnw_moe_set_gemm_path(int path);
+/* The forward's gate/up step, process-wide: 1 (default) fused -- SiLU(g) * u
+ * in the GEMM epilogue; 0 -- the unfused comparison path: gate and up as two
+ * single-matrix GEMMs (BF16 g and u in the workspace), then
+ * mnw_moe_silu_mul().  Not synchronised with calls in flight on other
+ * threads. */
+int mnw_moe_set_fused_activation(int fused);
 
 /* The whole layer with no device allocation and no caller workspace (the
  * pages have no counterpart; this is an integration convenience).  For

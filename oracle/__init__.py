@@ -28,7 +28,7 @@ _lib = None
 FMT_BF16, FMT_INT8_G128, FMT_INT4_G128, FMT_NVFP4_G16 = 0, 1, 2, 3
 ACT_BF16, ACT_INT8_G128, ACT_NVFP4_G16 = 0, 1, 2
 ACT_F16_ROWS = 3  # FP16 rows with a power-of-two row factor (see encode_f16_rows)
-KIND_GATE_UP, KIND_DOWN = 0, 1
+KIND_GATE_UP, KIND_DOWN, KIND_GATE, KIND_UP = 0, 1, 2, 3
 
 
 def build(force: bool = False) -> str:
@@ -68,6 +68,7 @@ def _load():
             "mnwo_encode_f16_rows": (i32, [P, i32, i32, P, P]),
             "mnwo_permute": (i32, [P, i32, i32, i32, P, P, P]),
             "mnwo_route": (i32, [P, P, i32, i32, i32, i32, P, P, P]),
+            "mnwo_silu_mul": (None, [P, P, ctypes.c_size_t, P]),
             "mnwo_gemm_a16": (i32, [P, ctypes.c_size_t, i32, P, P, i32, P]),
             "mnwo_gemm_a8": (i32, [P, ctypes.c_size_t, i32, P, P, P, i32, P, P]),
             "mnwo_gemm_a4": (i32, [P, ctypes.c_size_t, i32, P, P, P, P, i32, P]),
@@ -211,7 +212,7 @@ def gemm_a16(blob: np.ndarray, kind: int, a_bf16: np.ndarray, offsets: np.ndarra
     off = _c(offsets, np.int32)
     E, H, I = _dims(blob)
     P = a.shape[0]
-    out = np.zeros((P, I if kind == KIND_GATE_UP else H), np.uint16)
+    out = np.zeros((P, H if kind == KIND_DOWN else I), np.uint16)
     _check(_load().mnwo_gemm_a16(_p(blob), blob.nbytes, kind, _p(a), _p(off), P, _p(out)), "gemm_a16")
     return out
 
@@ -223,7 +224,7 @@ def gemm_a8(blob: np.ndarray, kind: int, a_codes, a_scales, offsets, want_dots: 
     off = _c(offsets, np.int32)
     E, H, I = _dims(blob)
     P, K = q.shape
-    N = I if kind == KIND_GATE_UP else H
+    N = H if kind == KIND_DOWN else I
     out = np.zeros((P, N), np.uint16)
     dots = np.zeros((P, (2 if kind == KIND_GATE_UP else 1) * N, K // 128), np.int32) if want_dots else None
     _check(_load().mnwo_gemm_a8(_p(blob), blob.nbytes, kind, _p(q), _p(s), _p(off), P, _p(out), _p(dots)),
@@ -239,7 +240,7 @@ def gemm_a4(blob: np.ndarray, kind: int, a_codes, a_sf, a_outer, offsets):
     off = _c(offsets, np.int32)
     E, H, I = _dims(blob)
     P = c.shape[0]
-    out = np.zeros((P, I if kind == KIND_GATE_UP else H), np.uint16)
+    out = np.zeros((P, H if kind == KIND_DOWN else I), np.uint16)
     _check(_load().mnwo_gemm_a4(_p(blob), blob.nbytes, kind, _p(c), _p(sf), _p(o), _p(off), P, _p(out)),
            "gemm_a4")
     return out
@@ -252,9 +253,19 @@ def gemm_f16rows(blob: np.ndarray, kind: int, a_f16: np.ndarray, factor, offsets
     off = _c(offsets, np.int32)
     E, H, I = _dims(blob)
     P = a.shape[0]
-    out = np.zeros((P, I if kind == KIND_GATE_UP else H), np.uint16)
+    out = np.zeros((P, H if kind == KIND_DOWN else I), np.uint16)
     _check(_load().mnwo_gemm_f16rows(_p(blob), blob.nbytes, kind, _p(a), _p(f), _p(off), P, _p(out)),
            "gemm_f16rows")
+    return out
+
+
+def silu_mul(g_bf16, u_bf16):
+    """bf16(SiLU(g) * u) of BF16 g and u (the unfused activation), FP64 inside."""
+    g = _c(g_bf16, np.uint16)
+    u = _c(u_bf16, np.uint16)
+    assert g.shape == u.shape
+    out = np.zeros(g.shape, np.uint16)
+    _load().mnwo_silu_mul(_p(g), _p(u), g.size, _p(out))
     return out
 
 

@@ -594,10 +594,11 @@ static int mode_ok(uint32_t wfmt, int act) {
 }
 
 /* One grouped-GEMM output row: GATE_UP writes I values bf16(SiLU(g)*u),
- * DOWN writes H values bf16(dot). */
+ * DOWN writes H values bf16(dot), GATE / UP write I values bf16(dot) of the
+ * gate / up matrix alone (the unfused-activation comparison path). */
 static int expert_row(const uint8_t* blob, const mnwo_blob_info* in, int kind, int e,
                       const act_row* a, uint16_t* out, int32_t* dots) {
-  int n, rc, N = kind == MNWO_KIND_GATE_UP ? (int)in->I : (int)in->H;
+  int n, rc, N = kind == MNWO_KIND_DOWN ? (int)in->H : (int)in->I;
   int G = a->K / 128;
   for (n = 0; n < N; ++n) {
     double g, u;
@@ -608,7 +609,8 @@ static int expert_row(const uint8_t* blob, const mnwo_blob_info* in, int kind, i
       if (rc) return rc;
       out[n] = mnwo_bf16_from_double(silu(g) * u);
     } else {
-      rc = row_dot(blob, in, e, MNWO_DOWN, n, a, &g, dots ? dots + (size_t)n * G : NULL);
+      const int m = kind == MNWO_KIND_DOWN ? MNWO_DOWN : (kind == MNWO_KIND_GATE ? MNWO_GATE : MNWO_UP);
+      rc = row_dot(blob, in, e, m, n, a, &g, dots ? dots + (size_t)n * G : NULL);
       if (rc) return rc;
       out[n] = mnwo_bf16_from_double(g);
     }
@@ -623,9 +625,9 @@ static int gemm_common(const uint8_t* blob, size_t bytes, int kind, int act, con
   int rc, e, p, K, N;
   if ((rc = mnwo_blob_parse(blob, bytes, &in))) return rc;
   if (!mode_ok(in.wfmt, act)) return MNWO_E_MODE;
-  if (kind != MNWO_KIND_GATE_UP && kind != MNWO_KIND_DOWN) return MNWO_E_ARG;
-  K = kind == MNWO_KIND_GATE_UP ? (int)in.H : (int)in.I;
-  N = kind == MNWO_KIND_GATE_UP ? (int)in.I : (int)in.H;
+  if (kind < MNWO_KIND_GATE_UP || kind > MNWO_KIND_UP) return MNWO_E_ARG;
+  K = kind == MNWO_KIND_DOWN ? (int)in.I : (int)in.H;
+  N = kind == MNWO_KIND_DOWN ? (int)in.H : (int)in.I;
   if (offsets[0] < 0 || offsets[in.E] > P) return MNWO_E_ARG;
   for (e = 0; e < (int)in.E; ++e) {
     if (offsets[e + 1] < offsets[e]) return MNWO_E_ARG;
@@ -673,6 +675,14 @@ int mnwo_gemm_a4(const uint8_t* blob, size_t bytes, int kind, const uint8_t* a_c
 int mnwo_gemm_f16rows(const uint8_t* blob, size_t bytes, int kind, const uint16_t* a,
                       const float* factor, const int32_t* offsets, int P, uint16_t* out) {
   return gemm_common(blob, bytes, kind, MNWO_ACT_F16_ROWS, a, factor, NULL, offsets, P, out, NULL);
+}
+
+/* The activation of the unfused comparison path: out[i] = bf16(SiLU(g[i]) *
+ * u[i]) from BF16 g and u, in FP64. */
+void mnwo_silu_mul(const uint16_t* g, const uint16_t* u, size_t n, uint16_t* out) {
+  size_t i;
+  for (i = 0; i < n; ++i)
+    out[i] = mnwo_bf16_from_double(silu(mnwo_bf16_to_double(g[i])) * mnwo_bf16_to_double(u[i]));
 }
 
 /* ------------------------------------------------------------------------- */

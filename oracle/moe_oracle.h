@@ -33,8 +33,10 @@ enum { MNWO_FMT_BF16 = 0, MNWO_FMT_INT8_G128 = 1, MNWO_FMT_INT4_G128 = 2, MNWO_F
  * and FP16 rows with a power-of-two row factor (an exact re-encoding of BF16
  * rows for FP16 tensor cores; not a mode of the pages, see mnwo_encode_f16_rows). */
 enum { MNWO_ACT_BF16 = 0, MNWO_ACT_INT8_G128 = 1, MNWO_ACT_NVFP4_G16 = 2, MNWO_ACT_F16_ROWS = 3 };
-/* Grouped GEMM kinds. */
-enum { MNWO_KIND_GATE_UP = 0, MNWO_KIND_DOWN = 1 };
+/* Grouped GEMM kinds: the fused gate/up/SiLU, down, and the gate or up
+ * matrix alone (the unfused-activation comparison path of [minnow]
+ * "Quantization": the activation then runs as its own step, mnwo_silu_mul). */
+enum { MNWO_KIND_GATE_UP = 0, MNWO_KIND_DOWN = 1, MNWO_KIND_GATE = 2, MNWO_KIND_UP = 3 };
 /* Matrices of one expert. */
 enum { MNWO_GATE = 0, MNWO_UP = 1, MNWO_DOWN = 2 };
 
@@ -115,6 +117,9 @@ int mnwo_gemm_a4(const uint8_t* blob, size_t bytes, int kind, const uint8_t* a_c
  * the weights decoded exactly as in mnwo_gemm_a16. */
 int mnwo_gemm_f16rows(const uint8_t* blob, size_t bytes, int kind, const uint16_t* a,
                       const float* factor, const int32_t* offsets, int P, uint16_t* out);
+
+/* ---- the unfused activation: out = bf16(SiLU(g) * u), FP64 from BF16 g, u ---- */
+void mnwo_silu_mul(const uint16_t* g, const uint16_t* u, size_t n, uint16_t* out);
 
 /* ---- combine ---- */
 void mnwo_combine(const uint16_t* y, const int32_t* assign_pos, const float* w, int T, int k,

@@ -20,9 +20,9 @@ _HERE = os.path.dirname(os.path.abspath(__file__))
 MNW_OK = 0
 FMT_BF16, FMT_INT8_G128, FMT_INT4_G128, FMT_NVFP4_G16 = 0, 1, 2, 3
 ACT_BF16, ACT_INT8_G128, ACT_NVFP4_G16, ACT_F16_ROWS = 0, 1, 2, 3
-KIND_GATE_UP, KIND_DOWN = 0, 1
+KIND_GATE_UP, KIND_DOWN, KIND_GATE, KIND_UP = 0, 1, 2, 3
 DEVERR_BAD_EXPERT_ID, DEVERR_TIMEOUT = 0x1, 0x2
-PATH_AUTO, PATH_TCGEN05, PATH_WARP_MMA = 0, 1, 2
+PATH_AUTO, PATH_TCGEN05, PATH_WARP_MMA, PATH_ROWS = 0, 1, 2, 3
 
 # Symbols of include/mnw_moe.h, with their ctypes signatures.
 _P, _I, _SZ, _U32P = ctypes.c_void_p, ctypes.c_int, ctypes.c_size_t, ctypes.c_void_p
@@ -54,6 +54,9 @@ SIGNATURES = {
     "mnw_moe_forward_host": (_I, [_P, _I, _P, _P, _P, _I, _I, _P, _P, _SZ, _P]),
     "mnw_moe_read_error": (_I, [_P, _P, _P]),
     "mnw_moe_set_gemm_path": (_I, [_I]),
+    "mnw_moe_set_fused_activation": (_I, [_I]),
+    "mnw_moe_set_host_routing": (_I, [_I]),
+    "mnw_moe_silu_mul": (_I, [_P, _P, _SZ, _P, _P]),
     "mnw_moe_launch_count": (ctypes.c_uint64, []),
     "mnw_moe_forward_static": (_I, [_P, _I, _P, _P, _P, _I, _I, _P, _U32P, _P]),
     "mnw_moe_selftest_wait_timeout": (_I, [ctypes.c_uint32, _U32P, _U32P, _P]),
@@ -233,8 +236,23 @@ def mnw_moe_quantize_act(act, x, row_index=None, index_div=1, rows=None, stream=
     return (codes, scales) if act == ACT_INT8_G128 else (codes, scales, outer)
 
 
+def mnw_moe_set_fused_activation(fused: bool) -> None:
+    _check(load().mnw_moe_set_fused_activation(1 if fused else 0), "mnw_moe_set_fused_activation")
+
+
+def mnw_moe_set_host_routing(on: bool) -> None:
+    _check(load().mnw_moe_set_host_routing(1 if on else 0), "mnw_moe_set_host_routing")
+
+
+def mnw_moe_silu_mul(g, u, stream=None):
+    """bf16(SiLU(g) * u) of two bf16 tensors of the same shape."""
+    h = torch.empty_like(g)
+    _check(load().mnw_moe_silu_mul(_ptr(g), _ptr(u), g.numel(), _ptr(h), _stream(stream)), "mnw_moe_silu_mul")
+    return h
+
+
 def _gemm_out(layer, kind, P, dev):
-    N = layer.I if kind == KIND_GATE_UP else layer.H
+    N = layer.H if kind == KIND_DOWN else layer.I
     return torch.empty((P, N), dtype=torch.bfloat16, device=dev)
 
 
@@ -282,7 +300,7 @@ def _gemm_a8(name, layer, kind, a_codes, a_scales, expert_offsets, want_dots=Fal
     out = _gemm_out(layer, kind, P, a_codes.device)
     dots = None
     if want_dots:
-        C = (2 * layer.I) if kind == KIND_GATE_UP else layer.H
+        C = (2 * layer.I) if kind == KIND_GATE_UP else (layer.H if kind == KIND_DOWN else layer.I)
         dots = torch.zeros((P, C, K // 128), dtype=torch.int32, device=a_codes.device)
     fn = getattr(load(), name)
     _check(fn(layer.handle, kind, _ptr(a_codes), _ptr(a_scales), _ptr(expert_offsets), P, _ptr(out), _ptr(dots),

@@ -210,7 +210,7 @@ static WsLayout ws_layout(const mnw_moe_layer* L, int act, int T, int k, bool ro
     w.hb = o; o = al(o + P * I / 16);
     w.hc = o; o = al(o + P * 4);
   }
-  w.y = o; o = al(o + P * H * 2);
+  w.y = o; o = al(o + P * (H > 2 * I ? H : 2 * I) * 2);  // y, or g and u of the unfused gate/up
   w.total = o;
   w.hx = o; o = al(o + static_cast<size_t>(T) * H * 2);
   w.hids = o; o = al(o + P * 4);
@@ -235,8 +235,27 @@ using namespace mnw;
 extern "C" {
 
 static int g_gemm_path = MNW_PATH_AUTO;
+static std::atomic<int> g_fused_activation{1};
+static std::atomic<int> g_host_routing{0};
+int mnw_moe_set_host_routing(int on) {
+  if (on != 0 && on != 1) return MNW_E_INVALID_ARG;
+  g_host_routing.store(on);
+  return MNW_OK;
+}
+int mnw_moe_set_fused_activation(int fused) {
+  if (fused != 0 && fused != 1) return MNW_E_INVALID_ARG;
+  g_fused_activation.store(fused);
+  return MNW_OK;
+}
+
+int mnw_moe_silu_mul(const void* g, const void* u, size_t n, void* h, mnw_stream stream) {
+  MNW_RANGE("mnw_moe_silu_mul");
+  if (n == 0) return MNW_OK;
+  if (!g || !u || !h || n % 8 || !aligned(g, 16) || !aligned(u, 16) || !aligned(h, 16)) return MNW_E_INVALID_ARG;
+  return launch_silu_mul(g, u, n, h, static_cast<cudaStream_t>(stream)) == cudaSuccess ? MNW_OK : MNW_E_CUDA;
+}
 int mnw_moe_set_gemm_path(int path) {
-  if (path < MNW_PATH_AUTO || path > MNW_PATH_WARP_MMA) return MNW_E_INVALID_ARG;
+  if (path < MNW_PATH_AUTO || path > MNW_PATH_ROWS) return MNW_E_INVALID_ARG;
   g_gemm_path = path;
   return MNW_OK;
 }
@@ -448,9 +467,9 @@ int mnw_moe_grouped_gemm_w4a16(const mnw_moe_layer* L, int kind, const void* a, 
 }
 static int gemm_f16rows(const mnw_moe_layer* L, int wfmt, int kind, const void* a, const float* f,
                         const int32_t* offs, int P, void* out, uint32_t* err, cudaStream_t st) {
-  if (!L || (kind != MNW_KIND_GATE_UP && kind != MNW_KIND_DOWN)) return MNW_E_INVALID_ARG;
+  if (!L || kind < MNW_KIND_GATE_UP || kind > MNW_KIND_UP) return MNW_E_INVALID_ARG;
   if (L->wfmt != wfmt) return MNW_E_MODE;
-  if (!(kind == MNW_KIND_GATE_UP ? L->f16_gate_up_ok : L->f16_down_ok)) return MNW_E_UNSUPPORTED;
+  if (!(kind == MNW_KIND_DOWN ? L->f16_down_ok : L->f16_gate_up_ok)) return MNW_E_UNSUPPORTED;
   return run_gemm(L, wfmt, kActF16Rows, kind, a, f, nullptr, offs, P, out, nullptr, err, st);
 }
 int mnw_moe_grouped_gemm_w8a16_f16rows(const mnw_moe_layer* L, int kind, const void* a, const float* f,
@@ -531,12 +550,51 @@ static int forward_impl(const mnw_moe_layer* L, int act, const void* x, const in
   uint32_t* sched_gu = err + 16;
   uint32_t* sched_dn = err + 18;
   if (cudaMemsetAsync(err, 0, W.rt_zero_end - W.err, st) != cudaSuccess) return MNW_E_CUDA;  // error word, counters
-  if (routed) {
+  int rc0;
+  if (routed && !host_routing()) {
     if (launch_route(x, wr, T, L->H, L->E, k, ids_out, w_out, offs, sorted, pos, b + W.rt, err, st) != cudaSuccess)
       return MNW_E_CUDA;
+  } else if (routed) {
+    // Host routing: logits on the GPU, copied to the host; top-k, softmax and
+    // the permutation on the host; the results copied back (synchronises).
+    float* logits = reinterpret_cast<float*>(b + W.rt + route_counter_bytes(T));
+    const size_t TE = static_cast<size_t>(T) * L->E, Pk = static_cast<size_t>(P);
+    std::vector<float> lg(TE), wh(Pk);
+    std::vector<int32_t> ih(Pk), oh(L->E + 1), sh(Pk), ph(Pk);
+    if (launch_route_logits(x, wr, T, L->H, L->E, logits, st) != cudaSuccess ||
+        cudaMemcpyAsync(lg.data(), logits, TE * 4, cudaMemcpyDeviceToHost, st) != cudaSuccess ||
+        cudaStreamSynchronize(st) != cudaSuccess)
+      return MNW_E_CUDA;
+    route_topk_host(lg.data(), T, L->E, k, ih.data(), wh.data());
+    rc0 = mnw_moe_permute_host(ih.data(), T, k, L->E, oh.data(), sh.data(), ph.data(), nullptr);
+    if (rc0) return rc0;
+    if (cudaMemcpyAsync(ids_out, ih.data(), Pk * 4, cudaMemcpyHostToDevice, st) != cudaSuccess ||
+        cudaMemcpyAsync(w_out, wh.data(), Pk * 4, cudaMemcpyHostToDevice, st) != cudaSuccess ||
+        cudaMemcpyAsync(offs, oh.data(), (L->E + 1) * 4, cudaMemcpyHostToDevice, st) != cudaSuccess ||
+        cudaMemcpyAsync(sorted, sh.data(), Pk * 4, cudaMemcpyHostToDevice, st) != cudaSuccess ||
+        cudaMemcpyAsync(pos, ph.data(), Pk * 4, cudaMemcpyHostToDevice, st) != cudaSuccess ||
+        cudaStreamSynchronize(st) != cudaSuccess)  // the host vectors go out of scope below
+      return MNW_E_CUDA;
+  }
+  if (routed) {
     ids = ids_out;
     w = w_out;
   }
+  // gate/up: fused (SiLU in the GEMM epilogue), or the unfused comparison path:
+  // gate and up as single-matrix GEMMs into the y region, then the activation
+  const bool fused = fused_activation();
+  auto gate_up = [&](int gact, const void* a0, const void* a1, const void* a2, const WarpDep* dep) -> int {
+    if (fused)
+      return run_gemm(L, L->wfmt, gact, MNW_KIND_GATE_UP, a0, a1, a2, offs, P, b + W.h, nullptr, err, st, sched_gu,
+                      dep);
+    uint8_t* g = b + W.y;
+    uint8_t* u = g + static_cast<size_t>(P) * I * 2;
+    int r = run_gemm(L, L->wfmt, gact, MNW_KIND_GATE, a0, a1, a2, offs, P, g, nullptr, err, st);
+    if (r) return r;
+    r = run_gemm(L, L->wfmt, gact, MNW_KIND_UP, a0, a1, a2, offs, P, u, nullptr, err, st);
+    if (r) return r;
+    return launch_silu_mul(g, u, static_cast<size_t>(P) * I, b + W.h, st) == cudaSuccess ? MNW_OK : MNW_E_CUDA;
+  };
   // the permutation, optionally gathering x rows (routed: already permuted, gather only)
   auto permute = [&](const void* gx, void* gx_perm) -> int {
     if (!routed) return mnw_moe_permute(ids, T, k, L->E, offs, sorted, pos, gx, gx ? H : 0, gx_perm, err, stream);
@@ -552,11 +610,11 @@ static int forward_impl(const mnw_moe_layer* L, int act, const void* x, const in
     // convert to FP16 operands in fewer instructions than to BF16.
     const int mean_rows = (P + L->E - 1) / L->E;
     const int path = gemm_path();
-    const bool tc = path != MNW_PATH_WARP_MMA && (path == MNW_PATH_TCGEN05 || mean_rows >= 32);
+    const bool tc = path != MNW_PATH_WARP_MMA && (path == MNW_PATH_TCGEN05 || path == MNW_PATH_ROWS || mean_rows >= 32);
     const int gu_act = L->f16_gate_up_ok ? kActF16Rows : act;
     // Both GEMMs on the warp-MMA kernel (same token tile): the down launch
     // follows the gate/up launch tile by tile instead of waiting for all of it.
-    const bool warp_down = !tc && warp_gemm_applicable(L, L->wfmt, gu_act, MNW_KIND_GATE_UP) &&
+    const bool warp_down = fused && !tc && warp_gemm_applicable(L, L->wfmt, gu_act, MNW_KIND_GATE_UP) &&
                            warp_gemm_applicable(L, L->wfmt, act, MNW_KIND_DOWN);
     const WarpDep gu_dep{reinterpret_cast<uint32_t*>(b + W.dep), kDepProduce, 0};
     if (L->f16_gate_up_ok) {
@@ -565,13 +623,11 @@ static int forward_impl(const mnw_moe_layer* L, int act, const void* x, const in
       float* factor = reinterpret_cast<float*>(b + W.xc);
       rc = mnw_moe_quantize_act(MNW_ACT_F16_ROWS, x, P, H, sorted, k, b + W.xa, nullptr, factor, stream);
       if (rc) return rc;
-      rc = run_gemm(L, L->wfmt, kActF16Rows, MNW_KIND_GATE_UP, b + W.xa, factor, nullptr, offs, P, b + W.h, nullptr,
-                    err, st, sched_gu, warp_down ? &gu_dep : nullptr);
+      rc = gate_up(kActF16Rows, b + W.xa, factor, nullptr, warp_down ? &gu_dep : nullptr);
     } else {
       rc = permute(x, b + W.xa);
       if (rc) return rc;
-      rc = run_gemm(L, L->wfmt, act, MNW_KIND_GATE_UP, b + W.xa, nullptr, nullptr, offs, P, b + W.h, nullptr, err, st,
-                    sched_gu, warp_down ? &gu_dep : nullptr);
+      rc = gate_up(act, b + W.xa, nullptr, nullptr, warp_down ? &gu_dep : nullptr);
     }
     if (rc) return rc;
     if (warp_down) {
@@ -595,7 +651,7 @@ static int forward_impl(const mnw_moe_layer* L, int act, const void* x, const in
     float* ho = act == MNW_ACT_NVFP4_G16 ? reinterpret_cast<float*>(b + W.hc) : nullptr;
     // each token row quantised once, its codes written to its k positions
     if (launch_quantize_scatter(act, x, T, H, pos, k, b + W.xa, b + W.xb, xo, st) != cudaSuccess) return MNW_E_CUDA;
-    rc = gemm_for(L, act, MNW_KIND_GATE_UP, b + W.xa, b + W.xb, xo, offs, P, b + W.h, err, sched_gu, st);
+    rc = gate_up(act, b + W.xa, b + W.xb, xo, nullptr);
     if (rc) return rc;
     rc = mnw_moe_quantize_act(act, b + W.h, P, I, nullptr, 1, b + W.ha, b + W.hb, ho, stream);
     if (rc) return rc;
@@ -712,6 +768,8 @@ int mnw_moe_read_error(const uint32_t* err, uint32_t* out_host, mnw_stream strea
 
 namespace mnw {
 int gemm_path() { return g_gemm_path; }
+bool fused_activation() { return g_fused_activation.load() != 0; }
+bool host_routing() { return g_host_routing.load() != 0; }
 
 int current_sm_count() {
   constexpr int kMaxDevices = 64;

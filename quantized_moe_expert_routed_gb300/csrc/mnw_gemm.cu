@@ -893,7 +893,7 @@ int warp_gemm_nt(int P, int E) {
 int run_gemm(const mnw_moe_layer* L, int wfmt, int act, int kind, const void* a0, const void* a1, const void* a2,
              const int32_t* offsets, int P, void* out, int32_t* dots, uint32_t* err, cudaStream_t st,
              uint32_t* sched, const WarpDep* dep) {
-  if (!L || (kind != MNW_KIND_GATE_UP && kind != MNW_KIND_DOWN) || P < 0) return MNW_E_INVALID_ARG;
+  if (!L || kind < MNW_KIND_GATE_UP || kind > MNW_KIND_UP || P < 0) return MNW_E_INVALID_ARG;
   if (L->wfmt != wfmt) return MNW_E_MODE;
   if (P == 0) return MNW_OK;
   if (!a0 || !offsets || !out || !aligned(a0, 16) || !aligned(out, 16)) return MNW_E_INVALID_ARG;
@@ -910,14 +910,19 @@ int run_gemm(const mnw_moe_layer* L, int wfmt, int act, int kind, const void* a0
   const int mean_rows = (P + L->E - 1) / L->E;
   const int path = gemm_path();
   const bool warp_ok = warp_gemm_applicable(L, wfmt, act, kind);
-  if (warp_ok && (path == MNW_PATH_WARP_MMA || (path == MNW_PATH_AUTO && mean_rows < 32))) {
+  if (warp_ok && (path == MNW_PATH_WARP_MMA || (path != MNW_PATH_TCGEN05 && path != MNW_PATH_ROWS && mean_rows < 32))) {
     return run_gemm_warp(L, wfmt, act, kind, a0, a1, offsets, P, warp_gemm_nt(P, L->E), out, dots, err, sched, st,
                          dep);
   }
   if (dep && dep->role != kDepNone) return MNW_E_INVALID_ARG;  // only the warp-MMA kernel takes a dependency
+  // FP16 rows on INT weights, and BF16 on BF16: the row-tile kernel (tokens as
+  // M, 256 weight rows as N; mnw_gemm_rows.cu) unless the swap-AB kernel below
+  // is forced.
+  if (path != MNW_PATH_TCGEN05 && rows_gemm_applicable(L, wfmt, act, kind))
+    return run_gemm_rows(L, wfmt, act, kind, a0, a1, offsets, P, out, err, st);
   const bool gate_up = kind == MNW_KIND_GATE_UP;
-  const int K = gate_up ? L->H : L->I;
-  const int N = gate_up ? L->I : L->H;
+  const int K = kind == MNW_KIND_DOWN ? L->I : L->H;
+  const int N = kind == MNW_KIND_DOWN ? L->H : L->I;
   const int nmat = gate_up ? 2 : 1;
   const int am = act;  // MNW_ACT_* match AM_*; kActF16Rows is AM_F16S
   const int wf = wfmt;
@@ -989,7 +994,7 @@ int run_gemm(const mnw_moe_layer* L, int wfmt, int act, int kind, const void* a0
   }
   a.experts = L->blob + L->data_offset;
   a.expert_stride = L->expert_stride;
-  const int m0 = gate_up ? 0 : 2;
+  const int m0 = kind_matrix(kind);  // first (or only) matrix of the launch
   for (int m = 0; m < nmat; ++m) {
     a.scales_off[m] = L->scales_off[m0 + m];
     a.outer_off[m] = L->outer_off[m0 + m];

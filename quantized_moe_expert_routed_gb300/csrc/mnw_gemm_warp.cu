@@ -56,7 +56,7 @@ bool warp_gemm_applicable(const mnw_moe_layer* L, int wfmt, int act, int kind) {
   if (wfmt != MNW_FMT_INT8_G128 && wfmt != MNW_FMT_INT4_G128) return false;
   if (act != MNW_ACT_BF16 && act != MNW_ACT_INT8_G128 && act != kActF16Rows) return false;
   if (kind == MNW_KIND_GATE_UP) return L->I % warpmma::kRowsPerBox == 0;
-  return L->H % (2 * warpmma::kRowsPerBox) == 0;
+  return (kind == MNW_KIND_DOWN ? L->H : L->I) % (2 * warpmma::kRowsPerBox) == 0;
 }
 
 int run_gemm_warp(const mnw_moe_layer* L, int wfmt, int act, int kind, const void* a0, const void* a1,
@@ -64,7 +64,7 @@ int run_gemm_warp(const mnw_moe_layer* L, int wfmt, int act, int kind, const voi
                   cudaStream_t st, const WarpDep* dep) {
   using namespace warpmma;
   const bool gu = kind == MNW_KIND_GATE_UP;
-  const int K = gu ? L->H : L->I, N = gu ? L->I : L->H, G = K / 128;
+  const int K = kind == MNW_KIND_DOWN ? L->I : L->H, N = kind == MNW_KIND_DOWN ? L->H : L->I, G = K / 128;
   const int BN = 8 * nt;
   Args a{};
   a.offsets = offsets;
@@ -92,7 +92,7 @@ int run_gemm_warp(const mnw_moe_layer* L, int wfmt, int act, int kind, const voi
   const size_t smem = a.off_bars + sizeof(Bars) + 1024;
   a.experts = L->blob + L->data_offset;
   a.expert_stride = L->expert_stride;
-  const int m0 = gu ? 0 : 2, m1 = gu ? 1 : 2;
+  const int m0 = kind_matrix(kind), m1 = gu ? 1 : m0;
   a.scales_off[0] = L->scales_off[m0];
   a.scales_off[1] = L->scales_off[m1];
   a.box_row_off[0] = 0;

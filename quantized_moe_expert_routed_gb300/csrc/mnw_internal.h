@@ -28,6 +28,9 @@ struct mnw_moe_layer {
 
 namespace mnw {
 
+// The expert matrix a grouped GEMM of `kind` reads first (gate/up: gate, then up).
+inline int kind_matrix(int kind) { return kind == MNW_KIND_DOWN ? 2 : (kind == MNW_KIND_UP ? 1 : 0); }
+
 inline bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
 
 // Number of SMs of the current device, looked up once per device.
@@ -91,6 +94,11 @@ bool encode_map(CUtensorMap* map, CUtensorMapDataType dtype, int rank, const voi
 cudaError_t launch_permute(const int32_t* ids, int T, int k, int E, int32_t* offsets, int32_t* sorted_assign,
                            int32_t* assign_pos, const void* x, int H, void* x_perm, uint32_t* err,
                            cudaStream_t st);
+// h = bf16(SiLU(g) * u) elementwise over n BF16 values (n % 8 == 0, 16-byte aligned).
+cudaError_t launch_silu_mul(const void* g, const void* u, size_t n, void* h, cudaStream_t st);
+// Process-wide: the forward's gate/up runs fused (SiLU in the GEMM epilogue) or
+// as two single-matrix GEMMs and the activation step.
+bool fused_activation();
 // x_perm[p] = x[sorted_assign[p] / k] (zero rows where sorted_assign[p] < 0).
 cudaError_t launch_gather_rows(const void* x, int H, const int32_t* sorted_assign, int P, int k, void* x_perm,
                                cudaStream_t st);
@@ -101,6 +109,11 @@ bool route_shape_ok(int T, int H, int E, int k);
 cudaError_t launch_route(const void* x, const void* wr, int T, int H, int E, int k, int32_t* ids, float* w,
                          int32_t* offsets, int32_t* sorted_assign, int32_t* assign_pos, void* scratch, uint32_t* err,
                          cudaStream_t st);
+// Host routing (a comparison path): the router's logits only, then the top-k
+// and softmax on the host with the same rule.
+cudaError_t launch_route_logits(const void* x, const void* wr, int T, int H, int E, float* logits, cudaStream_t st);
+void route_topk_host(const float* logits, int T, int E, int k, int32_t* ids, float* w);
+bool host_routing();
 // Bytes at the start of the route scratch that hold its arrival counters.
 inline size_t route_counter_bytes(int T) { return ((1 + (static_cast<size_t>(T) + 15) / 16) * 4 + 255) / 256 * 256; }
 // MNW_ACT_F16_ROWS encoding of P rows (row p reads x[row_index[p] / div], or
@@ -148,6 +161,11 @@ bool warp_gemm_applicable(const mnw_moe_layer* L, int wfmt, int act, int kind);
 int run_gemm_warp(const mnw_moe_layer* L, int wfmt, int act, int kind, const void* a0, const void* a1,
                   const int32_t* offsets, int P, int nt, void* out, int32_t* dots, uint32_t* err, uint32_t* sched,
                   cudaStream_t st, const WarpDep* dep = nullptr);
+// Row-tile tcgen05 GEMM (tokens as M, 256 weight rows as N; mnw_gemm_rows.cu):
+// FP16 rows on INT8/INT4 weights, BF16 rows on BF16 weights.
+bool rows_gemm_applicable(const mnw_moe_layer* L, int wfmt, int act, int kind);
+int run_gemm_rows(const mnw_moe_layer* L, int wfmt, int act, int kind, const void* a0, const void* a1,
+                  const int32_t* offsets, int P, void* out, uint32_t* err, cudaStream_t st);
 // Token tile (in 8-row units) the warp-MMA kernel uses for P rows over E experts.
 int warp_gemm_nt(int P, int E);
 // Process-wide GEMM path selection (MNW_PATH_*).

@@ -515,6 +515,42 @@ cudaError_t launch_gather_rows(const void* x, int H, const int32_t* sorted_assig
                     H / 8, sorted_assign, P, k, static_cast<uint4*>(x_perm));
 }
 
+// The activation of the unfused comparison path: h = bf16(SiLU(g) * u) from
+// BF16 g and u (the same FP32 expression as the fused epilogues), 8 values
+// per thread.
+__global__ void __launch_bounds__(256) silu_mul_kernel(const uint4* __restrict__ g, const uint4* __restrict__ u,
+                                                       size_t n8, uint4* __restrict__ h) {
+  pdl_launch_dependents();
+  pdl_wait();
+  for (size_t i = blockIdx.x * static_cast<size_t>(blockDim.x) + threadIdx.x; i < n8;
+       i += static_cast<size_t>(gridDim.x) * blockDim.x) {
+    const uint4 gv = __ldg(g + i), uv = __ldg(u + i);
+    const uint32_t gw[4] = {gv.x, gv.y, gv.z, gv.w}, uw[4] = {uv.x, uv.y, uv.z, uv.w};
+    uint32_t o[4];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      float r[2];
+#pragma unroll
+      for (int e = 0; e < 2; ++e) {
+        const float a = __uint_as_float(e ? (gw[j] & 0xFFFF0000u) : (gw[j] << 16));
+        const float b = __uint_as_float(e ? (uw[j] & 0xFFFF0000u) : (uw[j] << 16));
+        r[e] = __fdividef(a, 1.f + __expf(-a)) * b;
+      }
+      __nv_bfloat162 p = __floats2bfloat162_rn(r[0], r[1]);
+      o[j] = *reinterpret_cast<uint32_t*>(&p);
+    }
+    h[i] = make_uint4(o[0], o[1], o[2], o[3]);
+  }
+}
+
+cudaError_t launch_silu_mul(const void* g, const void* u, size_t n, void* h, cudaStream_t st) {
+  const int sms = current_sm_count();
+  const size_t n8 = n / 8;
+  const int blocks = static_cast<int>(std::min<size_t>((n8 + 255) / 256, static_cast<size_t>(sms) * 8));
+  return launch_pdl(silu_mul_kernel, dim3(blocks < 1 ? 1 : blocks), dim3(256), 0, st, static_cast<const uint4*>(g),
+                    static_cast<const uint4*>(u), n8, static_cast<uint4*>(h));
+}
+
 cudaError_t launch_combine(const void* y, const int32_t* assign_pos, const float* w, int T, int k, int H,
                            void* out, cudaStream_t st) {
   const int sms = current_sm_count();

@@ -28,6 +28,7 @@
 #include <atomic>
 #include <cfloat>
 #include <climits>
+#include <cmath>
 
 #include "mnw_internal.h"
 #include "mnw_permute.cuh"
@@ -55,7 +56,7 @@ __global__ void __launch_bounds__(kRtThreads) route_kernel(const uint32_t* __res
                                                           int T, int H, int E, int k, float* logits, int32_t* ids,
                                                           float* w, int32_t* offsets, int32_t* sorted_assign,
                                                           int32_t* assign_pos, uint32_t* counters, uint32_t* err,
-                                                          int fuse_permute) {
+                                                          int fuse_permute, int logits_only) {
   extern __shared__ __align__(16) int32_t rt_smem[];
   __shared__ int32_t warp_tot[32];
   __shared__ int32_t total_valid;
@@ -121,6 +122,8 @@ __global__ void __launch_bounds__(kRtThreads) route_kernel(const uint32_t* __res
     const int t = t0 + i / kRtExp, e = e0 + i % kRtExp;
     if (t < T && e < E) logits[static_cast<size_t>(t) * E + e] = s;
   }
+
+  if (logits_only) return;  // host routing: the host picks the experts
 
   // ---- 2. the last expert tile of this token tile picks the top-k ----
   __threadfence();
@@ -222,9 +225,46 @@ cudaError_t launch_route(const void* x, const void* wr, int T, int H, int E, int
   const dim3 grid(tiles, (E + kRtExp - 1) / kRtExp);
   cudaError_t e = launch_pdl(route_kernel, grid, dim3(kRtThreads), smem, st, static_cast<const uint32_t*>(x),
                              static_cast<const uint32_t*>(wr), T, H, E, k, logits, ids, w, offsets, sorted_assign,
-                             assign_pos, counters, err, fuse ? 1 : 0);
+                             assign_pos, counters, err, fuse ? 1 : 0, 0);
   if (e != cudaSuccess || fuse) return e;
   return launch_permute(ids, T, k, E, offsets, sorted_assign, assign_pos, nullptr, 0, nullptr, err, st);
+}
+
+cudaError_t launch_route_logits(const void* x, const void* wr, int T, int H, int E, float* logits, cudaStream_t st) {
+  const int tiles = (T + kRtTok - 1) / kRtTok;
+  const size_t smem = static_cast<size_t>(kRtWarps) * kRtTok * kRtExp * 4;
+  return launch_pdl(route_kernel, dim3(tiles, (E + kRtExp - 1) / kRtExp), dim3(kRtThreads), smem, st,
+                    static_cast<const uint32_t*>(x), static_cast<const uint32_t*>(wr), T, H, E, 1, logits,
+                    static_cast<int32_t*>(nullptr), static_cast<float*>(nullptr), static_cast<int32_t*>(nullptr),
+                    static_cast<int32_t*>(nullptr), static_cast<int32_t*>(nullptr), static_cast<uint32_t*>(nullptr),
+                    static_cast<uint32_t*>(nullptr), 0, 1);
+}
+
+void route_topk_host(const float* logits, int T, int E, int k, int32_t* ids, float* w) {
+  for (int t = 0; t < T; ++t) {
+    const float* l = logits + static_cast<size_t>(t) * E;
+    uint64_t taken[kRtMaxE / 64] = {};
+    float l0 = 0.f, den = 0.f;
+    for (int j = 0; j < k; ++j) {
+      float bv = -INFINITY;
+      int be = -1;
+      for (int e = 0; e < E; ++e) {
+        if ((taken[e >> 6] >> (e & 63)) & 1u) continue;
+        const float v = l[e] != l[e] ? -INFINITY : l[e];  // a NaN logit ranks last
+        if (be < 0 || v > bv) {
+          bv = v;
+          be = e;
+        }
+      }
+      taken[be >> 6] |= 1ull << (be & 63);
+      if (j == 0) l0 = bv;
+      const float p = bv == l0 ? 1.f : std::exp(bv - l0);
+      den += p;
+      ids[static_cast<size_t>(t) * k + j] = be;
+      w[static_cast<size_t>(t) * k + j] = p;
+    }
+    for (int j = 0; j < k; ++j) w[static_cast<size_t>(t) * k + j] /= den;
+  }
 }
 
 }  // namespace mnw

@@ -422,3 +422,36 @@ def test_standalone_gemm_graph_replay_on_two_streams(M):
     torch.cuda.synchronize()
     for o in outs:
         assert torch.equal(o.view(torch.int16), ref.view(torch.int16))
+
+
+@pytest.mark.parametrize("wfmt", [S.FMT_INT4_G128, S.FMT_INT8_G128, S.FMT_BF16])
+@pytest.mark.parametrize("T,k,E,H,I", [(300, 4, 8, 512, 256), (40, 2, 8, 512, 256), (700, 2, 16, 512, 256),
+                                       (33, 8, 64, 512, 768)])
+def test_row_tile_kernel_forced_matches_oracle(M, wfmt, T, k, E, H, I):
+    """The row-tile tcgen05 kernel (tokens as M, 256 weight rows as N) forced on
+    every shape: token tiles of 1..128 rows, experts with several tiles, empty
+    experts, feature tiles of 128 (gate/up) and 256 (down) columns.  INT
+    weights take FP16 rows, BF16 weights BF16 rows."""
+    blob, hdr, ids, x = _setup(wfmt, E, H, I, T, k, seed=5 * T + wfmt)
+    ids[: T // 3, 0] = 1  # a crowded expert (several token tiles)
+    if E > 8:
+        ids[ids == 5] = 6  # an empty expert
+    layer = M.Layer(blob.to(DEV), hdr)
+    off, sa, pos, xp = M.mnw_moe_permute(ids.to(DEV), E, x=x.to(DEV))
+    o_off = off.cpu().numpy()
+    M.mnw_moe_set_gemm_path(M.PATH_ROWS)
+    try:
+        if wfmt == S.FMT_BF16:
+            h = M.mnw_moe_grouped_gemm_bf16(layer, M.KIND_GATE_UP, xp, off)
+            y = M.mnw_moe_grouped_gemm_bf16(layer, M.KIND_DOWN, h, off)
+        else:
+            fn = M.mnw_moe_grouped_gemm_w4a16_f16rows if wfmt == S.FMT_INT4_G128 else \
+                M.mnw_moe_grouped_gemm_w8a16_f16rows
+            a, f = M.mnw_moe_quantize_act(M.ACT_F16_ROWS, x.to(DEV), row_index=sa, index_div=k)
+            h = fn(layer, M.KIND_GATE_UP, a, f, off)
+            ha, hf = M.mnw_moe_quantize_act(M.ACT_F16_ROWS, h)
+            y = fn(layer, M.KIND_DOWN, ha, hf, off)
+    finally:
+        M.mnw_moe_set_gemm_path(M.PATH_AUTO)
+    assert_close(h, O.gemm_a16(blob.numpy(), O.KIND_GATE_UP, to_np_bits(xp), o_off), what="row tiles gate_up")
+    assert_close(y, O.gemm_a16(blob.numpy(), O.KIND_DOWN, to_np_bits(h), o_off), what="row tiles down")

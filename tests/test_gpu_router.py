@@ -130,3 +130,29 @@ def test_forward_routed_matches_forward_on_the_routers_choice(M, name):
                          rows=np.arange(wl.T, dtype=np.int32))
     tol = REL_L2_NVFP4 if wl.act == S.ACT_NVFP4_G16 else REL_L2
     assert_close(out, want, rel_l2=tol, what=f"{name} routed")
+
+
+@pytest.mark.parametrize("name", ["decode_w4a16", "prefill_nvfp4"])
+def test_host_routing_comparison_path(M, name):
+    """Host routing: the same logits, the same rule and the same permutation
+    computed on the host, so ids and the permutation agree with GPU routing
+    exactly and the weights to the last FP32 bits of exp."""
+    wl = S.WORKLOADS[name]
+    wl = S.Workload(**{**wl.__dict__, "T": 300, "E": 64, "H": 512,
+                       "I": 512 if wl.wfmt == S.FMT_NVFP4_G16 else 256})
+    x, _, _, blob, hdr, L = S.make_inputs(wl, device=DEV)
+    wr = S.router_weights(wl.E, wl.H, seed=wl.seed + 9).to(DEV)
+    layer = M.Layer(blob, hdr)
+    out_gpu, ids_gpu, w_gpu = M.mnw_moe_forward_routed(layer, wl.act, x, wr, wl.k)
+    M.mnw_moe_set_host_routing(True)
+    try:
+        out_host, ids_host, w_host = M.mnw_moe_forward_routed(layer, wl.act, x, wr, wl.k)
+    finally:
+        M.mnw_moe_set_host_routing(False)
+    assert torch.equal(ids_gpu, ids_host)
+    assert torch.allclose(w_gpu, w_host, rtol=1e-6, atol=1e-7)
+    tol = REL_L2_NVFP4 if wl.act == S.ACT_NVFP4_G16 else REL_L2
+    want = O.moe_forward(blob.cpu().numpy(), wl.act, S.bf16_bits_np(x), ids_host.cpu().numpy(),
+                         w_host.cpu().numpy(), rows=np.arange(wl.T, dtype=np.int32))
+    assert_close(out_host, want, rel_l2=tol, what=f"{name} host routing")
+    assert (out_host.double() - out_gpu.double()).norm() <= 1e-3 * out_gpu.double().norm()
