@@ -189,3 +189,37 @@ def test_forward_warp_tile_dependency(M, wfmt, T, E, k):
     want = O.moe_forward(blob.cpu().numpy(), wl.act, S.bf16_bits_np(x), ids.cpu().numpy(), w.cpu().numpy(),
                          rows=np.arange(T, dtype=np.int32))
     assert_close(out1, want, rel_l2=REL_L2, what="warp tile dependency")
+
+
+@pytest.mark.parametrize("name", ["decode_w4a16", "w8a8_2048", "prefill_nvfp4"])
+def test_forward_replays_from_a_cuda_graph(M, name):
+    """The layer's launches (memset, permute, quantisers, GEMMs chained with
+    programmatic dependent launch, the linked decode GEMMs, combine) captured
+    once in a CUDA graph and replayed: the same bits as the eager call, replay
+    after replay, with new inputs copied into the captured buffers between
+    replays."""
+    wl = S.WORKLOADS[name]
+    if name != "decode_w4a16":
+        wl = S.Workload(**{**wl.__dict__, "T": 256, "E": 64, "H": 512, "I": 512})
+    x, ids, w, blob, hdr, L = S.make_inputs(wl, device=DEV)
+    layer = M.Layer(blob, hdr)
+    ws = M.workspace(layer, wl.act, wl.T, wl.k)
+    out = torch.empty((wl.T, wl.H), dtype=torch.bfloat16, device=DEV)
+    ref = M.mnw_moe_forward(layer, wl.act, x, ids, w, ws=ws, out=out).clone()  # eager (also the one-time set-up)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        M.mnw_moe_forward(layer, wl.act, x, ids, w, ws=ws, out=out)
+    for _ in range(3):
+        out.zero_()
+        g.replay()
+        torch.cuda.synchronize()
+        assert M.mnw_moe_read_error(M.workspace_error_word(ws)) == 0
+        assert torch.equal(out.view(torch.int16), ref.view(torch.int16))
+    # new inputs in the captured buffers
+    x2 = S.activations(wl.T, wl.H, seed=wl.seed + 77).to(DEV)
+    x.copy_(x2)
+    g.replay()
+    torch.cuda.synchronize()
+    eager = M.mnw_moe_forward(layer, wl.act, x, ids, w)
+    assert torch.equal(out.view(torch.int16), eager.view(torch.int16))
