@@ -533,11 +533,17 @@ def main():
     ap.add_argument("--peaks", action="store_true", help="run the tensor-core peak microbenchmark and exit")
     ap.add_argument("--gemm-path", default="auto", choices=["auto", "tcgen05", "warp", "rows"],
                     help="grouped-GEMM kernel selection (mnw_moe_set_gemm_path)")
+    ap.add_argument("--tokens", type=int, default=0, help="override the workload's token count (smaller cases)")
+    ap.add_argument("--experts", type=int, default=0, help="override the workload's expert count (smaller cases)")
     args = ap.parse_args()
     if args.peaks:
         print(json.dumps(run_peaks()))
         return
     wl = S.WORKLOADS[args.workload]
+    if args.tokens or args.experts:
+        # a smaller case gets its own name, so no figure captured on the full workload is attached to it
+        T_, E_ = args.tokens or wl.T, args.experts or wl.E
+        wl = dataclasses.replace(wl, name=f"{wl.name}_T{T_}_E{E_}", T=T_, E=E_)
     world, rank, local = _dist()
     if world > 1 and not torch.distributed.is_initialized():
         torch.distributed.init_process_group("nccl" if torch.cuda.is_available() else "gloo")
