@@ -75,6 +75,7 @@ def _load():
             "mnwo_gemm_f16rows": (i32, [P, ctypes.c_size_t, i32, P, P, P, i32, P]),
             "mnwo_combine": (None, [P, P, P, i32, i32, i32, P]),
             "mnwo_moe_forward": (i32, [P, ctypes.c_size_t, i32, P, P, P, i32, i32, P, i32, P]),
+            "mnwo_attention": (i32, [P, P, P, i32, i32, i32, i32, i32, i32, f64, P, i32, P]),
         }
         for name, (res, args) in sig.items():
             fn = getattr(lib, name)
@@ -292,3 +293,21 @@ def moe_forward(blob, act: int, x_bf16, ids, w, rows=None):
     _check(_load().mnwo_moe_forward(_p(blob), blob.nbytes, act, _p(x), _p(i), _p(ww), T, k, _p(r), n, _p(out)),
            "moe_forward")
     return out
+
+
+def attention(q_bf16, k_bf16, v_bf16, blk: int, scale: float, rows=None):
+    """Block attention (FP64) of BF16 q [B, T, Hq, d] with k, v [B, T, Hkv, d]:
+    key j is allowed for token t when j / blk <= t / blk.  Returns FP64
+    [B, T, Hq, d], or [len(rows), Hq, d] for the flat token indices in rows."""
+    q = _c(q_bf16, np.uint16)
+    k = _c(k_bf16, np.uint16)
+    v = _c(v_bf16, np.uint16)
+    B, T, Hq, d = q.shape
+    Hkv = k.shape[2]
+    assert k.shape == (B, T, Hkv, d) and v.shape == k.shape
+    r = None if rows is None else _c(rows, np.int32)
+    n = B * T if r is None else r.size
+    out = np.zeros((n, Hq, d), np.float64)
+    _check(_load().mnwo_attention(_p(q), _p(k), _p(v), B, T, Hq, Hkv, d, int(blk), float(scale), _p(r),
+                                  0 if r is None else n, _p(out)), "attention")
+    return out.reshape(B, T, Hq, d) if r is None else out

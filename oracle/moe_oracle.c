@@ -776,3 +776,63 @@ done:
   free(h); free(y); free(q8); free(s8); free(c4); free(sf); free(acc);
   return rc;
 }
+
+/* ------------------------------------------------------------------------- */
+/* Block attention for prefill (the second workload)                          */
+/* ------------------------------------------------------------------------- */
+
+/* [minnow] "Quantization": Block FlashAttention computes prompt attention
+ * with the scores kept on chip; this is the result it computes, written out
+ * directly.  For each selected token t of sequence b and query head h (kv
+ * head g = h / (Hq / Hkv)):
+ *   s_j = scale * sum_c q[b,t,h,c] * k[b,j,g,c]   for every allowed key j,
+ *   out[b,t,h,:] = sum_j exp(s_j - max s) v[b,j,g,:] / sum_j exp(s_j - max s),
+ * key j allowed iff j < T and j / blk <= t / blk (the block-causal mask of a
+ * block-diffusion model's prompt: blk = 1 is causal, blk >= T bidirectional).
+ * Everything in FP64 from the BF16 inputs.  q, out: [B, T, Hq, d]; k, v:
+ * [B, T, Hkv, d]; rows (nullable) lists flat token indices b*T + t, and out
+ * then holds [nrows, Hq, d]. */
+int mnwo_attention(const uint16_t* q, const uint16_t* k, const uint16_t* v, int B, int T, int Hq, int Hkv,
+                   int d, int blk, double scale, const int32_t* rows, int nrows, double* out) {
+  int i, h, j, c;
+  double *s = NULL, *qd = NULL;
+  if (B <= 0 || T <= 0 || Hq <= 0 || Hkv <= 0 || d <= 0 || blk <= 0 || Hq % Hkv) return MNWO_E_ARG;
+  if (!rows) nrows = B * T;
+  s = (double*)malloc(sizeof(double) * T);
+  qd = (double*)malloc(sizeof(double) * d);
+  if (!s || !qd) { free(s); free(qd); return MNWO_E_ARG; }
+  for (i = 0; i < nrows; ++i) {
+    const int flat = rows ? rows[i] : i;
+    int b, t, kmax;
+    long long km;
+    if (flat < 0 || flat >= B * T) { free(s); free(qd); return MNWO_E_ARG; }
+    b = flat / T;
+    t = flat % T;
+    km = ((long long)(t / blk) + 1) * blk; /* keys 0 .. kmax-1 are allowed */
+    kmax = km > T ? T : (int)km;
+    for (h = 0; h < Hq; ++h) {
+      const int g = h / (Hq / Hkv);
+      double m = -INFINITY, l = 0.0;
+      double* o = out + ((size_t)i * Hq + h) * d;
+      for (c = 0; c < d; ++c) qd[c] = mnwo_bf16_to_double(q[(((size_t)b * T + t) * Hq + h) * d + c]);
+      for (j = 0; j < kmax; ++j) {
+        const uint16_t* kr = k + (((size_t)b * T + j) * Hkv + g) * d;
+        double acc = 0.0;
+        for (c = 0; c < d; ++c) acc += qd[c] * mnwo_bf16_to_double(kr[c]);
+        s[j] = scale * acc;
+        if (s[j] > m) m = s[j];
+      }
+      for (c = 0; c < d; ++c) o[c] = 0.0;
+      for (j = 0; j < kmax; ++j) {
+        const uint16_t* vr = v + (((size_t)b * T + j) * Hkv + g) * d;
+        const double p = exp(s[j] - m);
+        l += p;
+        for (c = 0; c < d; ++c) o[c] += p * mnwo_bf16_to_double(vr[c]);
+      }
+      for (c = 0; c < d; ++c) o[c] /= l;
+    }
+  }
+  free(s);
+  free(qd);
+  return 0;
+}

@@ -131,6 +131,17 @@ int mnwo_moe_forward(const uint8_t* blob, size_t bytes, int act, const uint16_t*
                      const int32_t* ids, const float* w, int T, int k,
                      const int32_t* rows, int nrows, uint16_t* out);
 
+/* ---- block attention for prefill (the second workload) ----
+ * [minnow] "Quantization" (Block FlashAttention keeps the prompt's attention
+ * scores on chip; what it computes is plain attention): for each selected
+ * token t of sequence b and query head h, with kv head g = h / (Hq / Hkv),
+ * out = softmax_j(scale * q . k_j) weighted sum of v_j over the allowed keys
+ * j: j < T and j / blk <= t / blk (block-causal; blk = 1 causal, blk >= T
+ * bidirectional).  FP64 from BF16 q [B,T,Hq,d], k and v [B,T,Hkv,d]; rows
+ * (nullable) lists flat token indices b*T + t; out is [nrows, Hq, d] FP64. */
+int mnwo_attention(const uint16_t* q, const uint16_t* k, const uint16_t* v, int B, int T, int Hq, int Hkv,
+                   int d, int blk, double scale, const int32_t* rows, int nrows, double* out);
+
 #ifdef __cplusplus
 }
 #endif

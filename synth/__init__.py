@@ -412,3 +412,34 @@ def flops(wl: Workload, ids: torch.Tensor) -> int:
     """2 * 3 * H * I per valid assignment."""
     valid = int(((ids >= 0) & (ids < wl.E)).sum())
     return 2 * 3 * wl.H * wl.I * valid
+
+
+# ---------------------------------------------------------------------------
+# the block-attention prefill workload (the second workload)
+# ---------------------------------------------------------------------------
+
+
+@dataclass
+class AttnWorkload:
+    name: str
+    B: int       # sequences
+    T: int       # prompt tokens per sequence
+    Hq: int      # query heads
+    Hkv: int     # key/value heads (grouped queries: Hq / Hkv per kv head)
+    d: int       # head dimension
+    blk: int     # block size of the block-causal mask
+    seed: int
+
+
+ATTN_WORKLOADS = {
+    "attn_small": AttnWorkload("attn_small", 2, 300, 4, 2, 128, 32, 11),
+    "attn_prefill_8k": AttnWorkload("attn_prefill_8k", 1, 8192, 16, 4, 128, 32, 12),
+}
+
+
+def attention_inputs(B: int, T: int, Hq: int, Hkv: int, d: int, seed: int, device="cpu"):
+    """q [B,T,Hq,d], k and v [B,T,Hkv,d] bf16, each element ~N(0,1)."""
+    q = normal_f64(seed, 500, B * T * Hq * d, device).to(torch.float32).to(torch.bfloat16).reshape(B, T, Hq, d)
+    k = normal_f64(seed, 501, B * T * Hkv * d, device).to(torch.float32).to(torch.bfloat16).reshape(B, T, Hkv, d)
+    v = normal_f64(seed, 502, B * T * Hkv * d, device).to(torch.float32).to(torch.bfloat16).reshape(B, T, Hkv, d)
+    return q, k, v
