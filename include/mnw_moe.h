@@ -398,6 +398,26 @@ int mnw_moe_selftest_wait_timeout(uint32_t limit_us, uint32_t* err, uint32_t* le
 int mnw_moe_selftest_counter_timeout(uint32_t limit_us, const uint32_t* counter, uint32_t need, uint32_t* err,
                                      mnw_stream stream);
 
+/* ---- block attention for prompt prefill (the second workload) ----
+ * "coder543/minnow" README, "Quantization": Block FlashAttention serves
+ * long-prompt prefill with the attention scores kept on chip.  For every
+ * token t of sequence b and query head h (kv head g = h / (Hq / Hkv)):
+ *   out[b,t,h,:] = sum_j softmax_j(scale * q[b,t,h,:] . k[b,j,g,:]) v[b,j,g,:]
+ * over the allowed keys j: j / blk <= t / blk (block-causal with blocks of
+ * blk tokens; blk = 1 is causal, blk >= T bidirectional).  q and out are
+ * [B, T, Hq, d] BF16, k and v [B, T, Hkv, d] BF16, all contiguous, 16-byte
+ * aligned device memory; d must be 128.  Scores and the softmax are FP32,
+ * the probabilities enter the second product as BF16 (FP32 accumulation),
+ * out is rounded to BF16.  ws (device, caller-owned, at least
+ * mnw_attn_workspace_size bytes, 256-byte aligned) holds a transposed copy
+ * of v.  Returns MNW_E_INVALID_ARG (null or misaligned pointers, Hq not a
+ * multiple of Hkv, blk < 1, scale not positive and finite),
+ * MNW_E_UNSUPPORTED (d != 128), MNW_E_WORKSPACE_TOO_SMALL; B or T = 0 is a
+ * no-op.  Device-side timeouts are OR-ed into *err (device u32, nullable). */
+size_t mnw_attn_workspace_size(int B, int T, int Hkv, int d);
+int mnw_attn_prefill(const void* q, const void* k, const void* v, int B, int T, int Hq, int Hkv, int d, int blk,
+                     float scale, void* out, void* ws, size_t ws_bytes, uint32_t* err, mnw_stream stream);
+
 /* Synchronise `stream`, then copy the device error word to *out_host. */
 int mnw_moe_read_error(const uint32_t* err, uint32_t* out_host, mnw_stream stream);
 

@@ -61,6 +61,8 @@ SIGNATURES = {
     "mnw_moe_forward_static": (_I, [_P, _I, _P, _P, _P, _I, _I, _P, _U32P, _P]),
     "mnw_moe_selftest_wait_timeout": (_I, [ctypes.c_uint32, _U32P, _U32P, _P]),
     "mnw_moe_selftest_counter_timeout": (_I, [ctypes.c_uint32, _U32P, ctypes.c_uint32, _U32P, _P]),
+    "mnw_attn_workspace_size": (_SZ, [_I, _I, _I, _I]),
+    "mnw_attn_prefill": (_I, [_P, _P, _P, _I, _I, _I, _I, _I, _I, ctypes.c_float, _P, _P, _SZ, _U32P, _P]),
 }
 
 _lib = None
@@ -249,6 +251,21 @@ def mnw_moe_silu_mul(g, u, stream=None):
     h = torch.empty_like(g)
     _check(load().mnw_moe_silu_mul(_ptr(g), _ptr(u), g.numel(), _ptr(h), _stream(stream)), "mnw_moe_silu_mul")
     return h
+
+
+def mnw_attn_prefill(q, k, v, blk: int, scale: float, out=None, ws=None, err=None, stream=None):
+    """Block attention of bf16 q [B, T, Hq, d] over k, v [B, T, Hkv, d]; key j
+    is allowed for token t when j // blk <= t // blk.  Returns out [B, T, Hq, d]."""
+    B, T, Hq, d = q.shape
+    Hkv = k.shape[2]
+    L = load()
+    if out is None:
+        out = torch.empty_like(q)
+    if ws is None:
+        ws = torch.empty((max(1, L.mnw_attn_workspace_size(B, T, Hkv, d)),), dtype=torch.uint8, device=q.device)
+    _check(L.mnw_attn_prefill(_ptr(q), _ptr(k), _ptr(v), B, T, Hq, Hkv, d, int(blk), float(scale), _ptr(out),
+                              _ptr(ws), ws.numel(), _ptr(err), _stream(stream)), "mnw_attn_prefill")
+    return out
 
 
 def _gemm_out(layer, kind, P, dev):

@@ -1,0 +1,481 @@
+// mnw_attention.cu -- block attention for prompt prefill on tcgen05, with the
+// scores kept on chip (the "coder543/minnow" README, "Quantization": Block
+// FlashAttention for long-prompt prefill; its alternative materialises the
+// score matrix).
+//
+// What it computes: for token t of sequence b and query head h (kv head
+// g = h / (Hq / Hkv)), the softmax over the allowed keys j of
+// scale * q[b,t,h] . k[b,j,g], applied to v[b,j,g]; key j is allowed when
+// j / blk <= t / blk (block-causal: a block-diffusion model's prompt attends
+// within its own 32-token block and to every earlier block).
+//
+// One CTA per (128-query tile, query head, sequence), heaviest query tiles
+// first.  Roles (192 threads):
+//   warp 0      TMA producer: the Q tile once, then 128-key K and V^T tiles
+//               into two-slot rings
+//   warp 1      MMA issuer (one thread), owns the tensor memory:
+//               S_j = Q K_j^T into one of two 128-column TMEM buffers
+//               (tcgen05.mma kind::f16, both operands in shared memory), and
+//               O += P_j V_j with P_j read from tensor memory (the A operand
+//               of tcgen05.mma may live there) and V_j^T from shared memory.
+//               S_{j+1} is issued before O += P_j V_j, so the tensor pipe
+//               computes the next scores while the softmax runs.
+//   warps 2-5   softmax: thread r owns query row r (its TMEM lane).  Per key
+//               tile: row maximum of the scaled scores, P = 2^(s*log2e*scale
+//               - m) rounded to BF16 and written over the first 64 columns of
+//               the same S buffer (two keys per column), the row sum of the
+//               rounded P.  The running maximum m moves, and O and the row
+//               sum are rescaled, only when a tile's maximum exceeds it by
+//               more than 2^8 (rare after the first tiles); every other tile
+//               uses the old m, whose P values stay below 2^8.
+// Tensor memory (512 columns): S0 | S1 | O | unused.
+// V is transposed into the workspace first (keys contiguous per head
+// dimension) so that both products read K-major operands.
+#include <cuda_bf16.h>
+
+#include <atomic>
+
+#include "mnw_convert.cuh"
+#include "mnw_internal.h"
+#include "mnw_ptx.cuh"
+
+namespace mnw {
+namespace attn {
+
+constexpr int kD = 128;    // head dimension
+constexpr int kBQ = 128;   // queries per tile (the MMAs' M)
+constexpr int kBK = 128;   // keys per tile
+constexpr int kSlots = 2;  // K and V^T ring depth
+constexpr int kWarpTma = 0, kWarpMma = 1, kWarpSm0 = 2, kSmWarps = 4;
+constexpr int kThreads = (kWarpSm0 + kSmWarps) * 32;
+constexpr uint32_t kBoxBytes = 128 * 128;           // 128 rows x 64 BF16 (128 bytes, 128-byte swizzle)
+constexpr uint32_t kTileBytes = 2 * kBoxBytes;      // 128 rows x 128 BF16
+constexpr uint32_t kOffQ = 0, kOffK = kTileBytes, kOffV = kOffK + kSlots * kTileBytes;
+constexpr uint32_t kOffBars = kOffV + kSlots * kTileBytes;
+constexpr int kTmemCols = 512;
+constexpr uint32_t kColO = 256;
+constexpr float kRescaleLog2 = 8.f;
+
+struct Args {
+  int B, T, Hq, Hkv, blk, n_qt;
+  float scale_log2;  // softmax scale times log2(e)
+  __nv_bfloat16* out;
+  uint32_t* err;
+};
+
+struct Bars {
+  uint64_t q_full;
+  uint64_t k_full[kSlots], k_empty[kSlots], v_full[kSlots], v_empty[kSlots];
+  uint64_t s_full[2], p_full[2], o_done, o_final, mma_drain;
+  uint32_t tmem_base;
+  int abort;
+};
+
+constexpr size_t kSmemBytes = kOffBars + sizeof(Bars) + 1024;
+
+struct RingPos {
+  uint32_t slot = 0, phase = 0;
+  __device__ __forceinline__ void advance(uint32_t n) {
+    if (++slot == n) {
+      slot = 0;
+      phase ^= 1u;
+    }
+  }
+};
+
+__device__ __forceinline__ float ex2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+// One lane waits, the warp follows (tcgen05.ld/st are warp-collective, so
+// the whole warp takes the same branch).
+__device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, volatile int* abort, uint32_t* err) {
+  int ok = 1;
+  if ((threadIdx.x & 31) == 0) ok = bounded_wait(bar, parity, abort, err) ? 1 : 0;
+  ok = __shfl_sync(0xffffffffu, ok, 0);
+  __syncwarp();
+  return ok != 0;
+}
+
+__device__ __forceinline__ void drain_wait(uint64_t* bar, uint32_t parity) {
+  const uint64_t t0 = globaltimer();
+  while (!mbar_try_wait(bar, parity)) {
+    if (globaltimer() - t0 > kWaitLimitNs) return;
+  }
+}
+
+__device__ __forceinline__ void stg128(void* p, uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
+  asm volatile("st.global.v4.u32 [%0], {%1,%2,%3,%4};" ::"l"(p), "r"(a), "r"(b), "r"(c), "r"(d) : "memory");
+}
+
+// Keys 0 .. kend-1 are allowed for query t (block-causal, clipped to T).
+__device__ __forceinline__ int key_end(int t, int blk, int T) {
+  const long long km = (static_cast<long long>(t / blk) + 1) * blk;
+  return km > T ? T : static_cast<int>(km);
+}
+
+__global__ void __launch_bounds__(kThreads, 1)
+    attn_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
+                    const __grid_constant__ CUtensorMap tmV, const Args args) {
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  Bars* bars = reinterpret_cast<Bars*>(smem + kOffBars);
+  volatile int* abort = &bars->abort;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int T = args.T, Hq = args.Hq;
+
+  // work item: query tiles in decreasing order (most keys first), then head, then sequence
+  const int per_qt = Hq * args.B;
+  const int qt = args.n_qt - 1 - static_cast<int>(blockIdx.x) / per_qt;
+  const int rem = static_cast<int>(blockIdx.x) % per_qt;
+  const int h = rem % Hq, b = rem / Hq;
+  const int g = h / (Hq / args.Hkv);
+  const int q0 = qt * kBQ;
+  const int kend_tile = key_end(min(q0 + kBQ, T) - 1, args.blk, T);
+  const int nt = (kend_tile + kBK - 1) / kBK;  // key tiles this query tile needs (>= 1)
+
+  pdl_launch_dependents();
+  if (threadIdx.x == 0) {
+    mbar_init(&bars->q_full, 1);
+    for (int i = 0; i < kSlots; ++i) {
+      mbar_init(&bars->k_full[i], 1);
+      mbar_init(&bars->k_empty[i], 1);
+      mbar_init(&bars->v_full[i], 1);
+      mbar_init(&bars->v_empty[i], 1);
+    }
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&bars->s_full[i], 1);
+      mbar_init(&bars->p_full[i], kSmWarps);
+    }
+    mbar_init(&bars->o_done, 1);
+    mbar_init(&bars->o_final, 1);
+    mbar_init(&bars->mma_drain, 1);
+    bars->abort = 0;
+    fence_barrier_init();
+  }
+  if (warp == kWarpMma) {
+    tmem_alloc(&bars->tmem_base, kTmemCols);
+    tmem_relinquish();
+  }
+  if (warp == kWarpTma && lane == 0) {
+    tma_prefetch_desc(&tmQ);
+    tma_prefetch_desc(&tmK);
+    tma_prefetch_desc(&tmV);
+  }
+  pdl_wait();  // q, k and the transposed v are written by earlier work on the stream
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = bars->tmem_base;
+
+  if (warp == kWarpTma) {
+    // ======================= producer =======================
+    if (lane == 0) {
+      bool ok = true;
+      uint32_t k_issued = 0, v_issued = 0;
+      mbar_arrive_expect_tx(&bars->q_full, kTileBytes);
+      tma_load_4d(smem + kOffQ, &tmQ, &bars->q_full, 0, h, q0, b);
+      tma_load_4d(smem + kOffQ + kBoxBytes, &tmQ, &bars->q_full, 64, h, q0, b);
+      RingPos kp, vp;
+      for (int j = 0; ok && j < nt; ++j) {
+        if (!bounded_wait(&bars->k_empty[kp.slot], kp.phase ^ 1, abort, args.err)) { ok = false; break; }
+        uint8_t* kd = smem + kOffK + kp.slot * kTileBytes;
+        mbar_arrive_expect_tx(&bars->k_full[kp.slot], kTileBytes);
+        tma_load_4d(kd, &tmK, &bars->k_full[kp.slot], 0, g, j * kBK, b);
+        tma_load_4d(kd + kBoxBytes, &tmK, &bars->k_full[kp.slot], 64, g, j * kBK, b);
+        ++k_issued;
+        kp.advance(kSlots);
+        if (!bounded_wait(&bars->v_empty[vp.slot], vp.phase ^ 1, abort, args.err)) { ok = false; break; }
+        uint8_t* vd = smem + kOffV + vp.slot * kTileBytes;
+        mbar_arrive_expect_tx(&bars->v_full[vp.slot], kTileBytes);
+        tma_load_4d(vd, &tmV, &bars->v_full[vp.slot], j * kBK, 0, g, b);
+        tma_load_4d(vd + kBoxBytes, &tmV, &bars->v_full[vp.slot], j * kBK + 64, 0, g, b);
+        ++v_issued;
+        vp.advance(kSlots);
+      }
+      if (!ok || *abort) {
+        // let every copy already issued land before the CTA exits
+        drain_wait(&bars->q_full, 0);
+        for (uint32_t i = k_issued > kSlots ? k_issued - kSlots : 0; i < k_issued; ++i)
+          drain_wait(&bars->k_full[i % kSlots], (i / kSlots) & 1);
+        for (uint32_t i = v_issued > kSlots ? v_issued - kSlots : 0; i < v_issued; ++i)
+          drain_wait(&bars->v_full[i % kSlots], (i / kSlots) & 1);
+      }
+    }
+  } else if (warp == kWarpMma) {
+    // ======================= MMA issuer =======================
+    if (lane == 0) {
+      const uint32_t idesc = idesc_f16(kBQ, kBK, true);
+      const uint32_t idesc_pv = idesc_f16(kBQ, kD, true);
+      const uint32_t q_s = smem_u32(smem + kOffQ);
+      bool ok = bounded_wait(&bars->q_full, 0, abort, args.err);
+      bool issued = false;
+      RingPos kp, vp;
+      auto issue_s = [&](int j) -> bool {
+        if (!bounded_wait(&bars->k_full[kp.slot], kp.phase, abort, args.err)) return false;
+        tc_fence_after();
+        const uint32_t k_s = smem_u32(smem + kOffK + kp.slot * kTileBytes);
+        const uint32_t d = tmem + static_cast<uint32_t>(j & 1) * kBK;
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk) {
+          const uint32_t off = (kk >> 2) * kBoxBytes + (kk & 3) * 32;
+          mma_ss(d, sdesc_sw128(q_s + off), sdesc_sw128(k_s + off), idesc, kk > 0);
+        }
+        issued = true;
+        mma_commit(&bars->k_empty[kp.slot]);
+        mma_commit(&bars->s_full[j & 1]);
+        kp.advance(kSlots);
+        return true;
+      };
+      auto issue_pv = [&](int j) -> bool {
+        if (!bounded_wait(&bars->p_full[j & 1], (j >> 1) & 1, abort, args.err)) return false;
+        if (!bounded_wait(&bars->v_full[vp.slot], vp.phase, abort, args.err)) return false;
+        tc_fence_after();
+        const uint32_t v_s = smem_u32(smem + kOffV + vp.slot * kTileBytes);
+        const uint32_t p = tmem + static_cast<uint32_t>(j & 1) * kBK;  // P_j: 64 columns, two keys each
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk) {
+          const uint32_t off = (kk >> 2) * kBoxBytes + (kk & 3) * 32;
+          mma_ts(tmem + kColO, p + kk * 8, sdesc_sw128(v_s + off), idesc_pv, (j > 0 || kk > 0));
+        }
+        mma_commit(&bars->v_empty[vp.slot]);
+        mma_commit(&bars->o_done);
+        vp.advance(kSlots);
+        return true;
+      };
+      if (ok) ok = issue_s(0);
+      for (int j = 1; ok && j < nt; ++j) {
+        ok = issue_s(j);
+        if (ok) ok = issue_pv(j - 1);
+      }
+      if (ok) ok = issue_pv(nt - 1);
+      if (ok) mma_commit(&bars->o_final);
+      if (issued) {
+        // every MMA has finished with shared and tensor memory before the CTA tears down
+        mma_commit(&bars->mma_drain);
+        drain_wait(&bars->mma_drain, 0);
+      }
+    }
+  } else {
+    // ======================= softmax =======================
+    const int q = warp & 3;  // TMEM lane quarter
+    const int r = q * 32 + lane;
+    const int t = q0 + r;
+    const uint32_t lane_bits = static_cast<uint32_t>(q * 32) << 16;
+    const int kend = key_end(min(t, T - 1), args.blk, T);
+    const float sl2 = args.scale_log2;
+    float m_used = 0.f, l = 0.f;
+    bool ok = true;
+    for (int j = 0; j < nt; ++j) {
+      if (!warp_wait(&bars->s_full[j & 1], (j >> 1) & 1, abort, args.err)) { ok = false; break; }
+      tc_fence_after();
+      const uint32_t sa = tmem + lane_bits + static_cast<uint32_t>(j & 1) * kBK;
+      const int lim = kend - j * kBK;  // keys c < lim of this tile are allowed for row r
+      float mx = -INFINITY;
+#pragma unroll 1
+      for (int c0 = 0; c0 < kBK; c0 += 16) {
+        uint32_t v[16];
+        tmem_ld16(sa + c0, v);
+        tmem_wait_ld();
+#pragma unroll
+        for (int e = 0; e < 16; ++e)
+          if (c0 + e < lim) mx = fmaxf(mx, __uint_as_float(v[e]));
+      }
+      mx *= sl2;  // the scale is positive
+      bool resc = false;
+      if (j == 0) {
+        m_used = mx;  // key 0 is allowed for every row, so mx is finite
+      } else {
+        resc = mx > m_used + kRescaleLog2;
+        if (__any_sync(0xffffffffu, resc)) {
+          // O holds the products of tiles 0 .. j-1: wait for the last of them
+          if (!warp_wait(&bars->o_done, (j - 1) & 1, abort, args.err)) { ok = false; break; }
+          tc_fence_after();
+          const float alpha = resc ? ex2(m_used - mx) : 1.f;
+#pragma unroll 1
+          for (int c0 = 0; c0 < kD; c0 += 16) {
+            uint32_t o[16];
+            tmem_ld16(tmem + lane_bits + kColO + c0, o);
+            tmem_wait_ld();
+#pragma unroll
+            for (int e = 0; e < 16; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
+            tmem_st16(tmem + lane_bits + kColO + c0, o);
+          }
+          tmem_wait_st();
+          if (resc) {
+            l *= alpha;
+            m_used = mx;
+          }
+        }
+      }
+      // P as BF16 pairs over columns 0..63 of this S buffer; each chunk of 32
+      // keys is read before its 16 columns of P are written (below it).
+      const float mneg = -m_used;
+#pragma unroll 1
+      for (int c0 = 0; c0 < kBK; c0 += 32) {
+        uint32_t s0[16], s1[16];
+        tmem_ld16(sa + c0, s0);
+        tmem_ld16(sa + c0 + 16, s1);
+        tmem_wait_ld();
+        uint32_t pk[16];
+#pragma unroll
+        for (int e = 0; e < 16; ++e) {
+          const uint32_t* src = e < 8 ? s0 : s1;
+          const int i0 = 2 * (e & 7);
+          const int key = c0 + 2 * e;
+          const float p0 = key < lim ? ex2(fmaf(__uint_as_float(src[i0]), sl2, mneg)) : 0.f;
+          const float p1 = key + 1 < lim ? ex2(fmaf(__uint_as_float(src[i0 + 1]), sl2, mneg)) : 0.f;
+          const __nv_bfloat162 pb = __floats2bfloat162_rn(p0, p1);
+          const float2 pr = __bfloat1622float2(pb);
+          l += pr.x + pr.y;
+          pk[e] = *reinterpret_cast<const uint32_t*>(&pb);
+        }
+        tmem_st16(sa + c0 / 2, pk);
+      }
+      tmem_wait_st();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&bars->p_full[j & 1]);
+    }
+    if (ok && warp_wait(&bars->o_final, 0, abort, args.err)) {
+      tc_fence_after();
+      const float inv = 1.f / l;
+      __nv_bfloat16* dst = args.out + ((static_cast<size_t>(b) * T + t) * Hq + h) * kD;
+#pragma unroll 1
+      for (int c0 = 0; c0 < kD; c0 += 16) {
+        uint32_t o[16];
+        tmem_ld16(tmem + lane_bits + kColO + c0, o);
+        tmem_wait_ld();
+        uint32_t pk[8];
+#pragma unroll
+        for (int e = 0; e < 8; ++e)
+          pk[e] = pack_bf16x2(__uint_as_float(o[2 * e]) * inv, __uint_as_float(o[2 * e + 1]) * inv);
+        if (t < T) {
+          stg128(dst + c0, pk[0], pk[1], pk[2], pk[3]);
+          stg128(dst + c0 + 8, pk[4], pk[5], pk[6], pk[7]);
+        }
+      }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == kWarpMma) {
+    tc_fence_after();
+    tmem_dealloc(tmem, kTmemCols);
+  }
+}
+
+// v [B, T, Hkv, 128] -> vt [B, Hkv, 128, Tp] (keys contiguous); 64 keys per CTA.
+__global__ void __launch_bounds__(256) attn_vt_kernel(const __nv_bfloat16* __restrict__ v, int T, int Hkv, int Tp,
+                                                       __nv_bfloat16* __restrict__ vt) {
+  __shared__ __nv_bfloat16 tile[kD][64 + 2];
+  pdl_launch_dependents();
+  pdl_wait();
+  const int t0 = blockIdx.x * 64, g = blockIdx.y, b = blockIdx.z;
+  for (int i = threadIdx.x; i < 64 * kD; i += blockDim.x) {
+    const int tt = i / kD, c = i % kD;
+    const int t = t0 + tt;
+    tile[c][tt] = t < T ? v[((static_cast<size_t>(b) * T + t) * Hkv + g) * kD + c] : __float2bfloat16_rn(0.f);
+  }
+  __syncthreads();
+  for (int i = threadIdx.x; i < 64 * kD; i += blockDim.x) {
+    const int c = i / 64, tt = i % 64;
+    const int t = t0 + tt;
+    if (t < T) vt[((static_cast<size_t>(b) * Hkv + g) * kD + c) * Tp + t] = tile[c][tt];
+  }
+}
+
+inline int padded_keys(int T) { return (T + 7) / 8 * 8; }
+
+}  // namespace attn
+}  // namespace mnw
+
+using namespace mnw;
+
+extern "C" {
+
+size_t mnw_attn_workspace_size(int B, int T, int Hkv, int d) {
+  if (B <= 0 || T <= 0 || Hkv <= 0 || d <= 0) return 0;
+  const size_t bytes = static_cast<size_t>(B) * Hkv * d * attn::padded_keys(T) * 2;
+  return (bytes + 255) / 256 * 256;
+}
+
+int mnw_attn_prefill(const void* q, const void* k, const void* v, int B, int T, int Hq, int Hkv, int d, int blk,
+                     float scale, void* out, void* ws, size_t ws_bytes, uint32_t* err, mnw_stream stream) {
+  MNW_RANGE("mnw_attn_prefill");
+  using namespace attn;
+  if (B < 0 || T < 0 || Hq <= 0 || Hkv <= 0 || d <= 0 || blk < 1 || Hq % Hkv) return MNW_E_INVALID_ARG;
+  if (!(scale > 0.f) || !(scale < 3.0e38f)) return MNW_E_INVALID_ARG;
+  if (d != kD) return MNW_E_UNSUPPORTED;
+  if (B == 0 || T == 0) return MNW_OK;
+  if (static_cast<long long>(B) * T * Hq > (1ll << 31) / kD) return MNW_E_UNSUPPORTED;
+  if (!q || !k || !v || !out || !ws || !aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(out, 16) ||
+      !aligned(ws, 256))
+    return MNW_E_INVALID_ARG;
+  if (ws_bytes < mnw_attn_workspace_size(B, T, Hkv, d)) return MNW_E_WORKSPACE_TOO_SMALL;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  const int Tp = padded_keys(T);
+  auto* vt = static_cast<__nv_bfloat16*>(ws);
+
+  cudaError_t e = launch_pdl(attn_vt_kernel, dim3((T + 63) / 64, Hkv, B), dim3(256), 0, st,
+                             static_cast<const __nv_bfloat16*>(v), T, Hkv, Tp, vt);
+  if (e != cudaSuccess) return MNW_E_CUDA;
+
+  CUtensorMap maps[3];
+  memset(maps, 0, sizeof(maps));
+  const uint32_t box_qk[4] = {64, 1, static_cast<uint32_t>(kBQ), 1};
+  {
+    const uint64_t dims[4] = {static_cast<uint64_t>(kD), static_cast<uint64_t>(Hq), static_cast<uint64_t>(T),
+                              static_cast<uint64_t>(B)};
+    const uint64_t strides[3] = {static_cast<uint64_t>(kD) * 2, static_cast<uint64_t>(Hq) * kD * 2,
+                                 static_cast<uint64_t>(T) * Hq * kD * 2};
+    if (!encode_map(&maps[0], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, q, dims, strides, box_qk, CU_TENSOR_MAP_SWIZZLE_128B))
+      return MNW_E_INVALID_ARG;
+  }
+  {
+    const uint64_t dims[4] = {static_cast<uint64_t>(kD), static_cast<uint64_t>(Hkv), static_cast<uint64_t>(T),
+                              static_cast<uint64_t>(B)};
+    const uint64_t strides[3] = {static_cast<uint64_t>(kD) * 2, static_cast<uint64_t>(Hkv) * kD * 2,
+                                 static_cast<uint64_t>(T) * Hkv * kD * 2};
+    if (!encode_map(&maps[1], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, k, dims, strides, box_qk, CU_TENSOR_MAP_SWIZZLE_128B))
+      return MNW_E_INVALID_ARG;
+  }
+  {
+    // keys beyond T read as zero (the map ends at T; the rows are Tp long)
+    const uint64_t dims[4] = {static_cast<uint64_t>(T), static_cast<uint64_t>(kD), static_cast<uint64_t>(Hkv),
+                              static_cast<uint64_t>(B)};
+    const uint64_t strides[3] = {static_cast<uint64_t>(Tp) * 2, static_cast<uint64_t>(kD) * Tp * 2,
+                                 static_cast<uint64_t>(Hkv) * kD * Tp * 2};
+    const uint32_t box[4] = {64, static_cast<uint32_t>(kD), 1, 1};
+    if (!encode_map(&maps[2], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, vt, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_128B))
+      return MNW_E_INVALID_ARG;
+  }
+  Args a{};
+  a.B = B;
+  a.T = T;
+  a.Hq = Hq;
+  a.Hkv = Hkv;
+  a.blk = blk;
+  a.n_qt = (T + kBQ - 1) / kBQ;
+  a.scale_log2 = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634);
+  a.out = static_cast<__nv_bfloat16*>(out);
+  a.err = err;
+
+  static std::atomic<uint64_t> attr{0};
+  uint64_t bit;
+  if (attrs_needed(attr, &bit)) {
+    e = cudaFuncSetAttribute(attn_fwd_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(kSmemBytes));
+    if (e != cudaSuccess) return MNW_E_CUDA;
+    attrs_done(attr, bit);
+  }
+  const long long grid = static_cast<long long>(a.n_qt) * Hq * B;
+  if (grid > 0x7fffffffll) return MNW_E_UNSUPPORTED;
+  e = launch_pdl(attn_fwd_kernel, dim3(static_cast<unsigned>(grid)), dim3(kThreads), kSmemBytes, st, maps[0], maps[1],
+                 maps[2], a);
+  return e == cudaSuccess ? MNW_OK : MNW_E_CUDA;
+}
+
+}  // extern "C"

@@ -109,3 +109,22 @@ else:
     env = dict(os.environ, NVCC=str(tmp_path / "no-such-nvcc"))
     r = subprocess.run([sys.executable, "-c", code], env=env, capture_output=True, text=True, timeout=120)
     assert "RAISED:" in r.stdout and "nvcc not found" in r.stdout, r.stdout + r.stderr
+
+
+def test_attention_arguments_checked_before_any_launch(lib):
+    F = ctypes.c_float
+    assert lib.mnw_attn_workspace_size(1, 300, 2, 128) == ((2 * 128 * 304 * 2 + 255) // 256) * 256
+    assert lib.mnw_attn_workspace_size(0, 300, 2, 128) == 0
+    # B = 0 or T = 0: nothing to do
+    assert lib.mnw_attn_prefill(None, None, None, 0, 16, 2, 1, 128, 32, F(0.1), None, None, 0, None, None) == 0
+    assert lib.mnw_attn_prefill(None, None, None, 1, 0, 2, 1, 128, 32, F(0.1), None, None, 0, None, None) == 0
+    # query heads not a multiple of the kv heads, blk < 1, scale not positive
+    assert lib.mnw_attn_prefill(None, None, None, 1, 16, 3, 2, 128, 32, F(0.1), None, None, 0, None, None) == 1
+    assert lib.mnw_attn_prefill(None, None, None, 1, 16, 2, 1, 128, 0, F(0.1), None, None, 0, None, None) == 1
+    assert lib.mnw_attn_prefill(None, None, None, 1, 16, 2, 1, 128, 32, F(0.0), None, None, 0, None, None) == 1
+    assert lib.mnw_attn_prefill(None, None, None, 1, 16, 2, 1, 128, 32, F(float("nan")), None, None, 0, None,
+                                None) == 1
+    # head dimension other than 128
+    assert lib.mnw_attn_prefill(None, None, None, 1, 16, 2, 1, 64, 32, F(0.1), None, None, 0, None, None) == 2
+    # null tensors
+    assert lib.mnw_attn_prefill(None, None, None, 1, 16, 2, 1, 128, 32, F(0.1), None, None, 0, None, None) == 1
