@@ -34,6 +34,7 @@ import torch  # noqa: E402
 import synth as S  # noqa: E402
 
 METRIC = "MoE-layer tokens/s and achieved HBM GB/s or tensor-pipe % vs GB300 peak, 1 GPU"
+ATTN_METRIC = "Block-attention prefill tokens/s and achieved tensor-pipe % vs GB300 peak, 1 GPU"
 L2_BYTES = 129 * 1024 * 1024
 
 
@@ -417,33 +418,38 @@ def run_oracle_sample(wl: S.Workload, ntok: int, inputs=None):
 GEMM_SOURCES = ("mnw_gemm", "mnw_convert.cuh", "mnw_ptx.cuh")
 
 
-def gemm_source_hash() -> str:
+def gemm_source_hash(prefixes=None) -> str:
     """First 12 hex digits of a SHA-256 over the grouped-GEMM kernel sources
-    (every csrc file whose name starts with one of GEMM_SOURCES), in name order."""
+    (every csrc file whose name starts with one of GEMM_SOURCES, or of the
+    prefixes given), in name order."""
     csrc = os.path.join(ROOT, "quantized_moe_expert_routed_gb300", "csrc")
     h = hashlib.sha256()
     for name in sorted(os.listdir(csrc)):
-        if name.startswith(GEMM_SOURCES):
+        if name.startswith(prefixes or GEMM_SOURCES):
             with open(os.path.join(csrc, name), "rb") as f:
                 h.update(name.encode() + b"\0" + f.read())
     return h.hexdigest()[:12]
 
 
-def profile_traffic(wl: S.Workload):
-    """DRAM traffic (read + write bytes) of one gate/up launch, from the ncu
-    capture summarised in profiles/ (lines "<workload> <bytes> <source hash>
-    <summary file>"), and a note.  The figure is None when there is no line for
-    the workload, or when the GEMM sources changed since the capture (their
-    hash differs from the one recorded beside it)."""
+ATTN_SOURCES = ("mnw_attention", "mnw_convert.cuh", "mnw_ptx.cuh")
+
+
+def profile_traffic(wl, table="gate_up_dram_traffic.txt", sources=None):
+    """DRAM traffic (read + write bytes) of one launch of the dominant kernel,
+    from the ncu capture summarised in profiles/ (lines "<workload> <bytes>
+    <source hash> <summary file>"), and a note.  The figure is None when there
+    is no line for the workload, or when the kernel sources changed since the
+    capture (their hash differs from the one recorded beside it)."""
     try:
-        with open(os.path.join(ROOT, "profiles", "gate_up_dram_traffic.txt")) as f:
+        with open(os.path.join(ROOT, "profiles", table)) as f:
             for ln in f:
                 parts = ln.split()
                 if len(parts) >= 3 and parts[0] == wl.name:
-                    if parts[2] != gemm_source_hash():
-                        sys.stderr.write(f"bench: stored DRAM traffic for {wl.name} predates the current GEMM "
-                                         f"sources ({parts[2]} != {gemm_source_hash()}); reporting null\n")
-                        return None, "stale: the GEMM kernel changed since the capture"
+                    now = gemm_source_hash(sources)
+                    if parts[2] != now:
+                        sys.stderr.write(f"bench: stored DRAM traffic for {wl.name} predates the current kernel "
+                                         f"sources ({parts[2]} != {now}); reporting null\n")
+                        return None, "stale: the kernel changed since the capture"
                     return int(parts[1]), f"ncu capture, profiles/{parts[3] if len(parts) > 3 else ''}"
     except OSError:
         pass
@@ -522,13 +528,201 @@ def build_line(args, wl: S.Workload, config: dict, r: dict, cpu, traffic) -> dic
     return line
 
 
+# ---------------------------------------------------------------------------
+# the second workload: block attention for prompt prefill
+# ---------------------------------------------------------------------------
+
+
+def attn_flops(aw) -> float:
+    """Useful FLOPs of one call: 2 products of 2*d flops per allowed (query, key)
+    pair and query head (the masked pairs inside computed tiles not counted)."""
+    t = np.arange(aw.T, dtype=np.int64)
+    kend = np.minimum(aw.T, (t // aw.blk + 1) * aw.blk)
+    return 4.0 * aw.d * aw.Hq * aw.B * float(kend.sum())
+
+
+def attn_oracle_sample(aw, nrows: int, inputs):
+    import oracle
+    q, k, v = inputs
+    rows = np.linspace(0, aw.B * aw.T - 1, nrows).astype(np.int32)
+    u = lambda t: t.detach().cpu().contiguous().view(torch.uint16).numpy()  # noqa: E731
+    qh, kh, vh = u(q), u(k), u(v)
+    t0 = time.perf_counter()
+    oracle.attention(qh, kh, vh, aw.blk, 1.0 / np.sqrt(aw.d), rows=rows)
+    dt = time.perf_counter() - t0
+    return nrows / dt, dt
+
+
+def attn_cpu_rows(aw, budget_s: float) -> int:
+    """How many query rows the oracle runs in about budget_s seconds (~4e8 FP64 MAC/s)."""
+    macs_per_row = 2.0 * aw.Hq * aw.d * (aw.T / 2 + aw.blk)
+    return max(1, min(aw.B * aw.T, int(budget_s * 4.0e8 / macs_per_row)))
+
+
+def run_attn(args, aw):
+    import ctypes
+
+    import quantized_moe_expert_routed_gb300 as M
+    world, rank, local = _dist()
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    if rank:
+        aw = dataclasses.replace(aw, seed=aw.seed + 1000 * rank)
+    q, k, v = S.attention_inputs(aw.B, aw.T, aw.Hq, aw.Hkv, aw.d, aw.seed, device=dev)
+    lib = M.load()
+    out = torch.empty_like(q)
+    ws = torch.empty((lib.mnw_attn_workspace_size(aw.B, aw.T, aw.Hkv, aw.d),), dtype=torch.uint8, device=dev)
+    err = torch.zeros(1, dtype=torch.int32, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    sp = ctypes.c_void_p(stream.cuda_stream)
+    ptr = lambda t: ctypes.c_void_p(t.data_ptr())  # noqa: E731
+    scale = 1.0 / float(np.sqrt(aw.d))
+    flush = torch.empty(2 * L2_BYTES, dtype=torch.uint8, device=dev)
+    flush_clean = torch.zeros(2 * L2_BYTES // 4, dtype=torch.int32, device=dev)
+
+    def l2_flush():
+        flush.zero_()
+        flush_clean.amax()
+
+    def call(qq, kk, vv, oo):
+        rc = lib.mnw_attn_prefill(ptr(qq), ptr(kk), ptr(vv), aw.B, aw.T, aw.Hq, aw.Hkv, aw.d, aw.blk,
+                                  ctypes.c_float(scale), ptr(oo), ptr(ws), ws.numel(), ptr(err), sp)
+        if rc != 0:
+            raise RuntimeError(f"mnw_attn_prefill failed: {lib.mnw_status_string(rc).decode()}")
+
+    for _ in range(args.warmup):
+        call(q, k, v, out)
+        l2_flush()
+    torch.cuda.synchronize()
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    launches = 0
+    with ClockSampler(local) as clk:
+        for i in range(args.steps):
+            l2_flush()
+            e0, e1 = ev[i]
+            e0.record(stream)
+            n0 = lib.mnw_moe_launch_count()
+            call(q, k, v, out)
+            launches += lib.mnw_moe_launch_count() - n0
+            e1.record(stream)
+        torch.cuda.synchronize()
+    step_ms = [a.elapsed_time(b) for a, b in ev]
+    total_ms = reduce_ranks(sum(step_ms), world, "max", dev)
+    launches = int(reduce_ranks(launches, world, "sum", dev))
+    if int(err.item()):
+        raise RuntimeError(f"device error word {int(err.item()):#x}")
+
+    # end to end: q, k, v from page-locked host memory, out back to it, inside the timed region
+    qh, kh, vh = q.cpu().pin_memory(), k.cpu().pin_memory(), v.cpu().pin_memory()
+    oh = torch.empty(out.shape, dtype=out.dtype).pin_memory()
+    qd, kd, vd, od = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v), torch.empty_like(out)
+
+    def e2e_step():
+        qd.copy_(qh, non_blocking=True)
+        kd.copy_(kh, non_blocking=True)
+        vd.copy_(vh, non_blocking=True)
+        call(qd, kd, vd, od)
+        oh.copy_(od, non_blocking=True)
+        stream.synchronize()
+
+    for _ in range(max(1, args.warmup)):
+        e2e_step()
+    e2e_ms = []
+    for _ in range(args.steps):
+        l2_flush()
+        torch.cuda.synchronize()
+        t0 = time.perf_counter()
+        e2e_step()
+        e2e_ms.append((time.perf_counter() - t0) * 1e3)
+    e2e_ms = reduce_ranks(statistics.median(e2e_ms), world, "max", dev)
+    return dict(total_ms=total_ms, step_ms=step_ms, launches=launches, world=world, rank=rank,
+                clocks=clk.summary(), e2e_ms=e2e_ms, inputs=(q, k, v),
+                h2d=q.numel() * 2 + k.numel() * 2 + v.numel() * 2, d2h=out.numel() * 2)
+
+
+def attn_line(args, aw, r, cpu, traffic=(None, "no capture of the current kernel")) -> dict:
+    hbm, bf16_peak, peak_kind = _peaks()
+    ms = r["total_ms"] / args.steps
+    flops = attn_flops(aw)
+    achieved = flops / (ms / 1e3) / 1e12
+    cpu_rate, cpu_dt, nrows = cpu
+    nproc, cpu_model = host_info()
+    tokens = aw.B * aw.T
+    return {
+        "metric": ATTN_METRIC, "value": r["world"] * tokens / (ms / 1e3), "unit": "tokens/s", "n_gpus": r["world"],
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
+        "ms_per_step_median": statistics.median(r["step_ms"]), "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16 x bf16 -> f32 scores, f32 softmax, bf16 probabilities x bf16 -> f32",
+        "data": "synthetic (seeded, shapes of the workload)",
+        "config": {"workload": aw.name, "B": aw.B, "T": aw.T, "Hq": aw.Hq, "Hkv": aw.Hkv, "d": aw.d,
+                   "mask": f"block-causal, {aw.blk}-token blocks",
+                   "l2": "flushed between timed steps outside the events: a 2x L2 buffer written, then another "
+                         "2x L2 buffer read"},
+        "roofline": {"kernel": "block attention (the call: V transpose, then the attention kernel)",
+                     "bound": "tensor", "achieved": achieved, "peak": bf16_peak, "unit": "TFLOP/s",
+                     "frac": achieved / bf16_peak, "peak_kind": f"{peak_kind} (bf16 dense burst)",
+                     "flops_per_launch": flops, "launch_ms": ms, "launch_ms_median": statistics.median(r["step_ms"]),
+                     "traffic": traffic[0], "traffic_note": traffic[1]},
+        "cpu_baseline": {"value": cpu_rate, "unit": "tokens/s", "cores": 1, "kind": "oracle",
+                         "host_nproc": nproc, "host_cpu_model": cpu_model,
+                         "sample": f"{nrows} of {tokens} query rows (all heads), {cpu_dt:.1f} s single-threaded"},
+        "e2e": {"value": r["world"] * tokens / (r["e2e_ms"] / 1e3), "unit": "tokens/s",
+                "h2d_bytes_per_step": r["world"] * r["h2d"], "d2h_bytes_per_step": r["world"] * r["d2h"]},
+        "gpu_launches": r["launches"],
+        "clocks": r["clocks"],
+    }
+
+
+def main_attn(args, aw):
+    world, rank, local = _dist()
+    if world > 1 and not torch.distributed.is_initialized():
+        torch.distributed.init_process_group("nccl" if torch.cuda.is_available() else "gloo")
+    if args.impl == "reference":
+        if rank != 0:
+            return
+        dev = "cuda" if torch.cuda.is_available() else "cpu"
+        inputs = S.attention_inputs(aw.B, aw.T, aw.Hq, aw.Hkv, aw.d, aw.seed, device=dev)
+        per_step = max(2.0, min(20.0, 120.0 / max(1, args.steps + args.warmup)))
+        nrows = attn_cpu_rows(aw, per_step)
+        for _ in range(min(args.warmup, 1)):
+            attn_oracle_sample(aw, max(1, nrows // 4), inputs)
+        rates, times = [], []
+        for _ in range(args.steps):
+            rr, dt = attn_oracle_sample(aw, nrows, inputs)
+            rates.append(rr)
+            times.append(dt)
+        value = statistics.median(rates)
+        nproc, cpu_model = host_info()
+        print(json.dumps({
+            "impl": "reference", "metric": ATTN_METRIC, "value": value, "unit": "tokens/s", "n_gpus": args.gpus,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": statistics.median(times) * 1e3,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": aw.name, "B": aw.B, "T": aw.T, "Hq": aw.Hq, "Hkv": aw.Hkv, "d": aw.d,
+                       "mask": f"block-causal, {aw.blk}-token blocks"},
+            "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": 1, "kind": "oracle", "host_nproc": nproc,
+                             "host_cpu_model": cpu_model,
+                             "sample": f"{nrows} of {aw.B * aw.T} query rows per step (all heads)"},
+            "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}))
+        return
+    r = run_attn(args, aw)
+    if rank != 0:
+        return
+    nrows = attn_cpu_rows(aw, args.cpu_budget)
+    cpu = attn_oracle_sample(aw, nrows, r["inputs"])
+    traffic = profile_traffic(aw, "attn_dram_traffic.txt", ATTN_SOURCES)
+    print(json.dumps(attn_line(args, aw, r, (cpu[0], cpu[1], nrows), traffic)))
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=50)
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
-    ap.add_argument("--workload", default="large_w4a16", choices=sorted(S.WORKLOADS))
+    ap.add_argument("--workload", default="large_w4a16", choices=sorted(S.WORKLOADS) + sorted(S.ATTN_WORKLOADS))
     ap.add_argument("--cpu-budget", type=float, default=15.0, help="seconds of oracle time for cpu_baseline")
     ap.add_argument("--peaks", action="store_true", help="run the tensor-core peak microbenchmark and exit")
     ap.add_argument("--gemm-path", default="auto", choices=["auto", "tcgen05", "warp", "rows"],
@@ -538,6 +732,12 @@ def main():
     args = ap.parse_args()
     if args.peaks:
         print(json.dumps(run_peaks()))
+        return
+    if args.workload in S.ATTN_WORKLOADS:
+        aw = S.ATTN_WORKLOADS[args.workload]
+        if args.tokens:
+            aw = dataclasses.replace(aw, name=f"{aw.name}_T{args.tokens}", T=args.tokens)
+        main_attn(args, aw)
         return
     wl = S.WORKLOADS[args.workload]
     if args.tokens or args.experts:

@@ -10,7 +10,7 @@
 // within its own 32-token block and to every earlier block).
 //
 // One CTA per (128-query tile, query head, sequence), heaviest query tiles
-// first.  Roles (192 threads):
+// first.  Roles (576 threads):
 //   warp 0      TMA producer: the Q tile once, then 128-key K and V^T tiles
 //               into two-slot rings
 //   warp 1      MMA issuer (one thread), owns the tensor memory:
@@ -20,14 +20,19 @@
 //               of tcgen05.mma may live there) and V_j^T from shared memory.
 //               S_{j+1} is issued before O += P_j V_j, so the tensor pipe
 //               computes the next scores while the softmax runs.
-//   warps 2-5   softmax: thread r owns query row r (its TMEM lane).  Per key
-//               tile: row maximum of the scaled scores, P = 2^(s*log2e*scale
-//               - m) rounded to BF16 and written over the first 64 columns of
-//               the same S buffer (two keys per column), the row sum of the
-//               rounded P.  The running maximum m moves, and O and the row
-//               sum are rescaled, only when a tile's maximum exceeds it by
-//               more than 2^8 (rare after the first tiles); every other tile
-//               uses the old m, whose P values stay below 2^8.
+//   warps 2-17  softmax: four warps per TMEM lane quarter, warp part p of a
+//               quarter owns keys 32p..32p+31 of each tile (and O columns
+//               32p..32p+31) for the quarter's 32 query rows, one row per
+//               lane.  Per key tile: the row maximum of the scaled scores
+//               (the four parts' maxima meet through a shared-memory slot and
+//               an mbarrier), P = 2^(s*log2e*scale - m) rounded to BF16 and
+//               written over the first 16 of the part's own 32 S columns (two
+//               keys per column), the part's row sum of the rounded P.  The
+//               running maximum m moves, and O and the row sums are
+//               rescaled, only when a tile's maximum exceeds it by more than
+//               2^8 (rare after the first tiles); other tiles keep the old m,
+//               whose P values stay below 2^8.  Sixteen warps (four per
+//               scheduler) hide the latency of each warp's dependent chain.
 // Tensor memory (512 columns): S0 | S1 | O | unused.
 // V is transposed into the workspace first (keys contiguous per head
 // dimension) so that both products read K-major operands.
@@ -46,7 +51,7 @@ constexpr int kD = 128;    // head dimension
 constexpr int kBQ = 128;   // queries per tile (the MMAs' M)
 constexpr int kBK = 128;   // keys per tile
 constexpr int kSlots = 2;  // K and V^T ring depth
-constexpr int kWarpTma = 0, kWarpMma = 1, kWarpSm0 = 2, kSmWarps = 4;
+constexpr int kWarpTma = 0, kWarpMma = 1, kWarpSm0 = 2, kSmWarps = 16;
 constexpr int kThreads = (kWarpSm0 + kSmWarps) * 32;
 constexpr uint32_t kBoxBytes = 128 * 128;           // 128 rows x 64 BF16 (128 bytes, 128-byte swizzle)
 constexpr uint32_t kTileBytes = 2 * kBoxBytes;      // 128 rows x 128 BF16
@@ -67,6 +72,9 @@ struct Bars {
   uint64_t q_full;
   uint64_t k_full[kSlots], k_empty[kSlots], v_full[kSlots], v_empty[kSlots];
   uint64_t s_full[2], p_full[2], o_done, o_final, mma_drain;
+  uint64_t xmax[4][2], xsum[4];  // per lane quarter: the four parts' row maxima (per tile parity), row sums
+  float pmax[2][4][4][32];       // [tile parity][quarter][part][lane]
+  float psum[4][4][32];
   uint32_t tmem_base;
   int abort;
 };
@@ -152,6 +160,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(&bars->o_done, 1);
     mbar_init(&bars->o_final, 1);
     mbar_init(&bars->mma_drain, 1);
+    for (int i = 0; i < 4; ++i) {
+      mbar_init(&bars->xmax[i][0], 4);
+      mbar_init(&bars->xmax[i][1], 4);
+      mbar_init(&bars->xsum[i], 4);
+    }
     bars->abort = 0;
     fence_barrier_init();
   }
@@ -234,11 +247,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (!bounded_wait(&bars->v_full[vp.slot], vp.phase, abort, args.err)) return false;
         tc_fence_after();
         const uint32_t v_s = smem_u32(smem + kOffV + vp.slot * kTileBytes);
-        const uint32_t p = tmem + static_cast<uint32_t>(j & 1) * kBK;  // P_j: 64 columns, two keys each
+        // P_j: keys 32p..32p+31 in columns 32p..32p+15 of the S buffer, two keys each
+        const uint32_t p = tmem + static_cast<uint32_t>(j & 1) * kBK;
 #pragma unroll
         for (int kk = 0; kk < 8; ++kk) {
           const uint32_t off = (kk >> 2) * kBoxBytes + (kk & 3) * 32;
-          mma_ts(tmem + kColO, p + kk * 8, sdesc_sw128(v_s + off), idesc_pv, (j > 0 || kk > 0));
+          mma_ts(tmem + kColO, p + (kk >> 1) * 32 + (kk & 1) * 8, sdesc_sw128(v_s + off), idesc_pv, (j > 0 || kk > 0));
         }
         mma_commit(&bars->v_empty[vp.slot]);
         mma_commit(&bars->o_done);
@@ -260,10 +274,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else {
     // ======================= softmax =======================
-    const int q = warp & 3;  // TMEM lane quarter
+    const int q = warp & 3;                  // TMEM lane quarter: query rows 32q .. 32q+31
+    const int part = (warp - kWarpSm0) >> 2;  // keys (and O columns) 32 part .. 32 part + 31
     const int r = q * 32 + lane;
     const int t = q0 + r;
     const uint32_t lane_bits = static_cast<uint32_t>(q * 32) << 16;
+    const uint32_t ocol = tmem + lane_bits + kColO + part * 32;
     const int kend = key_end(min(t, T - 1), args.blk, T);
     const float sl2 = args.scale_log2;
     float m_used = 0.f, l = 0.f;
@@ -271,38 +287,44 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int j = 0; j < nt; ++j) {
       if (!warp_wait(&bars->s_full[j & 1], (j >> 1) & 1, abort, args.err)) { ok = false; break; }
       tc_fence_after();
-      const uint32_t sa = tmem + lane_bits + static_cast<uint32_t>(j & 1) * kBK;
-      const int lim = kend - j * kBK;  // keys c < lim of this tile are allowed for row r
+      const uint32_t sa = tmem + lane_bits + static_cast<uint32_t>(j & 1) * kBK + part * 32;
+      const int lim = kend - j * kBK - part * 32;  // keys e < lim of this part are allowed for the row
+      uint32_t sv[32];
+      tmem_ld32(sa, sv);
+      tmem_wait_ld();
       float mx = -INFINITY;
-#pragma unroll 1
-      for (int c0 = 0; c0 < kBK; c0 += 16) {
-        uint32_t v[16];
-        tmem_ld16(sa + c0, v);
-        tmem_wait_ld();
+      if (lim >= 32) {
 #pragma unroll
-        for (int e = 0; e < 16; ++e)
-          if (c0 + e < lim) mx = fmaxf(mx, __uint_as_float(v[e]));
+        for (int e = 0; e < 32; ++e) mx = fmaxf(mx, __uint_as_float(sv[e]));
+      } else {
+#pragma unroll
+        for (int e = 0; e < 32; ++e)
+          if (e < lim) mx = fmaxf(mx, __uint_as_float(sv[e]));
       }
+      // the row's maximum over the four parts
+      bars->pmax[j & 1][q][part][lane] = mx;
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&bars->xmax[q][j & 1]);
+      if (!warp_wait(&bars->xmax[q][j & 1], (j >> 1) & 1, abort, args.err)) { ok = false; break; }
+      mx = fmaxf(fmaxf(bars->pmax[j & 1][q][0][lane], bars->pmax[j & 1][q][1][lane]),
+                 fmaxf(bars->pmax[j & 1][q][2][lane], bars->pmax[j & 1][q][3][lane]));
       mx *= sl2;  // the scale is positive
-      bool resc = false;
       if (j == 0) {
         m_used = mx;  // key 0 is allowed for every row, so mx is finite
       } else {
-        resc = mx > m_used + kRescaleLog2;
+        const bool resc = mx > m_used + kRescaleLog2;
         if (__any_sync(0xffffffffu, resc)) {
           // O holds the products of tiles 0 .. j-1: wait for the last of them
           if (!warp_wait(&bars->o_done, (j - 1) & 1, abort, args.err)) { ok = false; break; }
           tc_fence_after();
           const float alpha = resc ? ex2(m_used - mx) : 1.f;
-#pragma unroll 1
-          for (int c0 = 0; c0 < kD; c0 += 16) {
-            uint32_t o[16];
-            tmem_ld16(tmem + lane_bits + kColO + c0, o);
-            tmem_wait_ld();
+          uint32_t o[32];
+          tmem_ld32(ocol, o);
+          tmem_wait_ld();
 #pragma unroll
-            for (int e = 0; e < 16; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
-            tmem_st16(tmem + lane_bits + kColO + c0, o);
-          }
+          for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
+          tmem_st16(ocol, *reinterpret_cast<uint32_t(*)[16]>(&o[0]));
+          tmem_st16(ocol + 16, *reinterpret_cast<uint32_t(*)[16]>(&o[16]));
           tmem_wait_st();
           if (resc) {
             l *= alpha;
@@ -310,52 +332,49 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         }
       }
-      // P as BF16 pairs over columns 0..63 of this S buffer; each chunk of 32
-      // keys is read before its 16 columns of P are written (below it).
+      // P as BF16 pairs over the first 16 of this part's 32 S columns (already read)
       const float mneg = -m_used;
-#pragma unroll 1
-      for (int c0 = 0; c0 < kBK; c0 += 32) {
-        uint32_t s0[16], s1[16];
-        tmem_ld16(sa + c0, s0);
-        tmem_ld16(sa + c0 + 16, s1);
-        tmem_wait_ld();
-        uint32_t pk[16];
+      uint32_t pk[16];
 #pragma unroll
-        for (int e = 0; e < 16; ++e) {
-          const uint32_t* src = e < 8 ? s0 : s1;
-          const int i0 = 2 * (e & 7);
-          const int key = c0 + 2 * e;
-          const float p0 = key < lim ? ex2(fmaf(__uint_as_float(src[i0]), sl2, mneg)) : 0.f;
-          const float p1 = key + 1 < lim ? ex2(fmaf(__uint_as_float(src[i0 + 1]), sl2, mneg)) : 0.f;
-          const __nv_bfloat162 pb = __floats2bfloat162_rn(p0, p1);
-          const float2 pr = __bfloat1622float2(pb);
-          l += pr.x + pr.y;
-          pk[e] = *reinterpret_cast<const uint32_t*>(&pb);
-        }
-        tmem_st16(sa + c0 / 2, pk);
+      for (int e = 0; e < 16; ++e) {
+        const float p0 = 2 * e < lim ? ex2(fmaf(__uint_as_float(sv[2 * e]), sl2, mneg)) : 0.f;
+        const float p1 = 2 * e + 1 < lim ? ex2(fmaf(__uint_as_float(sv[2 * e + 1]), sl2, mneg)) : 0.f;
+        const __nv_bfloat162 pb = __floats2bfloat162_rn(p0, p1);
+        const float2 pr = __bfloat1622float2(pb);
+        l += pr.x + pr.y;
+        pk[e] = *reinterpret_cast<const uint32_t*>(&pb);
       }
+      tmem_st16(sa, pk);
       tmem_wait_st();
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(&bars->p_full[j & 1]);
     }
+    if (ok) {
+      // the row sum over the four parts
+      bars->psum[q][part][lane] = l;
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&bars->xsum[q]);
+      ok = warp_wait(&bars->xsum[q], 0, abort, args.err);
+    }
     if (ok && warp_wait(&bars->o_final, 0, abort, args.err)) {
       tc_fence_after();
-      const float inv = 1.f / l;
-      __nv_bfloat16* dst = args.out + ((static_cast<size_t>(b) * T + t) * Hq + h) * kD;
-#pragma unroll 1
-      for (int c0 = 0; c0 < kD; c0 += 16) {
-        uint32_t o[16];
-        tmem_ld16(tmem + lane_bits + kColO + c0, o);
-        tmem_wait_ld();
-        uint32_t pk[8];
+      const float lsum = (bars->psum[q][0][lane] + bars->psum[q][1][lane]) +
+                         (bars->psum[q][2][lane] + bars->psum[q][3][lane]);
+      const float inv = 1.f / lsum;
+      uint32_t o[32];
+      tmem_ld32(ocol, o);
+      tmem_wait_ld();
+      uint32_t pk[16];
 #pragma unroll
-        for (int e = 0; e < 8; ++e)
-          pk[e] = pack_bf16x2(__uint_as_float(o[2 * e]) * inv, __uint_as_float(o[2 * e + 1]) * inv);
-        if (t < T) {
-          stg128(dst + c0, pk[0], pk[1], pk[2], pk[3]);
-          stg128(dst + c0 + 8, pk[4], pk[5], pk[6], pk[7]);
-        }
+      for (int e = 0; e < 16; ++e)
+        pk[e] = pack_bf16x2(__uint_as_float(o[2 * e]) * inv, __uint_as_float(o[2 * e + 1]) * inv);
+      if (t < T) {
+        __nv_bfloat16* dst = args.out + ((static_cast<size_t>(b) * T + t) * Hq + h) * kD + part * 32;
+        stg128(dst, pk[0], pk[1], pk[2], pk[3]);
+        stg128(dst + 8, pk[4], pk[5], pk[6], pk[7]);
+        stg128(dst + 16, pk[8], pk[9], pk[10], pk[11]);
+        stg128(dst + 24, pk[12], pk[13], pk[14], pk[15]);
       }
     }
   }

@@ -168,3 +168,13 @@ def test_fp4_tensor_peak_is_measured_or_nominal():
     else:
         assert peak == pytest.approx(6 * bf16) and "nominal" in how
     assert bench.tensor_peak("f16", bf16, kind)[0] == bf16
+
+
+def test_attention_flop_count_matches_brute_force():
+    import bench
+    import synth as S
+    aw = S.AttnWorkload("t", 2, 70, 3, 1, 16, 32, 0)
+    allowed = sum(1 for t in range(aw.T) for j in range(aw.T) if j // aw.blk <= t // aw.blk)
+    assert bench.attn_flops(aw) == 4.0 * aw.d * aw.Hq * aw.B * allowed
+    assert 1 <= bench.attn_cpu_rows(aw, 1e-9) <= aw.B * aw.T
+    assert bench.attn_cpu_rows(aw, 1e9) == aw.B * aw.T
