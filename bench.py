@@ -354,6 +354,31 @@ def run_ours(args, wl):
     if e:
         raise RuntimeError(f"device error word {e:#x}")
 
+    # The same forward captured once in a CUDA graph and replayed: the host's
+    # launch work leaves the step (the kernels and their order are unchanged).
+    graph = torch.cuda.CUDAGraph()
+    cap = torch.cuda.Stream(dev)
+    cap.wait_stream(stream)
+    with torch.cuda.graph(graph, stream=cap):
+        chk(fwd(layer.handle, wl.act, ptr(x), ptr(ids), ptr(w), T, k, ptr(out), ptr(ws), ws_bytes,
+                ctypes.c_void_p(cap.cuda_stream)), "forward (graph capture)")
+    stream.wait_stream(cap)
+    graph.replay()
+    torch.cuda.synchronize()
+    gr_ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    for i in range(args.steps):
+        l2_flush()
+        a0, a1 = gr_ev[i]
+        a0.record(stream)
+        graph.replay()
+        a1.record(stream)
+    torch.cuda.synchronize()
+    graph_ms = reduce_ranks(statistics.median([a.elapsed_time(b) for a, b in gr_ev]), world, "max", dev)
+    e = M.mnw_moe_read_error(M.workspace_error_word(ws))
+    if e:
+        raise RuntimeError(f"device error word {e:#x} after graph replays")
+    del graph
+
     # Roofline: the fused gate/up GEMM launch alone, on inputs prepared by the
     # same kernels as the layer (CUDA events on its stream, L2 flushed between).
     step()
@@ -389,7 +414,7 @@ def run_ours(args, wl):
 
     touched = int(torch.unique(ids[(ids >= 0) & (ids < E)]).numel())
     return dict(total_ms=total_ms, step_ms=step_ms, gu_ms=gu_ms, launches=launches, world=world, rank=rank,
-                f16_rows=f16_gate_up is not None,
+                f16_rows=f16_gate_up is not None, graph_ms=graph_ms,
                 clocks=clk.summary(), e2e_ms=e2e_ms, touched=touched, ids=ids)
 
 
@@ -525,6 +550,10 @@ def build_line(args, wl: S.Workload, config: dict, r: dict, cpu, traffic) -> dic
         "gpu_launches": r["launches"],
         "clocks": r["clocks"],
     }
+    if r.get("graph_ms"):
+        line["graph"] = {"value": r["world"] * wl.T / (r["graph_ms"] / 1e3), "unit": "tokens/s",
+                         "ms_per_step_median": r["graph_ms"],
+                         "note": "the same forward captured once in a CUDA graph and replayed (L2 flushed between)"}
     return line
 
 
