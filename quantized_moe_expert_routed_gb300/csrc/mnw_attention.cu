@@ -114,10 +114,6 @@ __device__ __forceinline__ void drain_wait(uint64_t* bar, uint32_t parity) {
   }
 }
 
-__device__ __forceinline__ void stg128(void* p, uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
-  asm volatile("st.global.v4.u32 [%0], {%1,%2,%3,%4};" ::"l"(p), "r"(a), "r"(b), "r"(c), "r"(d) : "memory");
-}
-
 // Keys 0 .. kend-1 are allowed for query t (block-causal, clipped to T).
 __device__ __forceinline__ int key_end(int t, int blk, int T) {
   const long long km = (static_cast<long long>(t / blk) + 1) * blk;

@@ -657,36 +657,45 @@ __global__ void __launch_bounds__(kThreads, 1)
             ow[m] = __ldg(reinterpret_cast<const float*>(args.experts + static_cast<uint64_t>(x.e) * args.expert_stride +
                                                          args.outer_off[m]));
         }
+        // Each 16-token chunk goes through this warp's staging tile [16 tokens][32 features]
+        // (BF16), then out as 16-byte row pieces: 64 bytes of a token's row per 4 lanes.
+        uint16_t* stage = reinterpret_cast<uint16_t*>(smem + args.off_sa) + ew * (16 * 32);
+        const uint32_t stage_s = smem_u32(stage);
         for (int j0 = c0; j0 < jend; j0 += 16) {
           uint32_t g[16], up[16];
           tmem_ld16(d + j0, g);
           if (kGateUp) tmem_ld16(d + BN + j0, up);
+          // the row factors of the chunk's 16 tokens: lane i reads token j0 + i (clamped in range)
+          float oa_l = 1.f;
+          if (AM == AM_FP4 || AM == AM_F16S) oa_l = __ldg(args.a_outer + min(x.row0 + j0 + (lane & 15), args.P - 1));
           tmem_wait_ld();
 #pragma unroll
           for (int i = 0; i < 16; ++i) {
-            const int j = j0 + i;
+            const float oa = __shfl_sync(0xffffffffu, oa_l, i);
+            float gv = __uint_as_float(g[i]);
+            if (AM == AM_FP4) gv = gv * (ow[0] * oa);
+            else if (AM == AM_F16S) gv = gv * oa;
+            float val = gv;
+            if (kGateUp) {
+              float uv = __uint_as_float(up[i]);
+              if (AM == AM_FP4) uv = uv * (ow[1] * oa);
+              else if (AM == AM_F16S) uv = uv * oa;
+              val = __fdividef(gv, 1.f + __expf(-gv)) * uv;
+            }
+            stage[i * 32 + lane] = __bfloat16_as_ushort(__float2bfloat16_rn(val));
+          }
+          __syncwarp();
+#pragma unroll
+          for (int h2 = 0; h2 < 2; ++h2) {
+            const int c = lane + 32 * h2;  // 16-byte piece: token c / 4, features 8 (c % 4) ..
+            const int j = j0 + (c >> 2);
             if (j < jend && x.row0 + j < args.P) {
-              float gv = __uint_as_float(g[i]);
-              float val;
-              float oa = 1.f;
-              if (AM == AM_FP4) {
-                oa = __ldg(args.a_outer + x.row0 + j);
-                gv = gv * (ow[0] * oa);
-              } else if (AM == AM_F16S) {
-                oa = __ldg(args.a_outer + x.row0 + j);  // the row's 2^e
-                gv = gv * oa;
-              }
-              if (kGateUp) {
-                float uv = __uint_as_float(up[i]);
-                if (AM == AM_FP4) uv = uv * (ow[1] * oa);
-                else if (AM == AM_F16S) uv = uv * oa;
-                val = __fdividef(gv, 1.f + __expf(-gv)) * uv;
-              } else {
-                val = gv;
-              }
-              args.out[static_cast<size_t>(x.row0 + j) * args.N + col] = __float2bfloat16_rn(val);
+              const uint4 v = lds128(stage_s + c * 16);
+              stg128(args.out + static_cast<size_t>(x.row0 + j) * args.N + n0 + q * 32 + (c & 3) * 8, v.x, v.y,
+                     v.z, v.w);
             }
           }
+          __syncwarp();
         }
         tc_fence_before();
         __syncwarp();
@@ -839,7 +848,9 @@ bool plan_smem(int wf, int am, bool gate_up, int K, int E, int BN, Plan* p) {
   const uint32_t scales = 2 * nmat * a.scale_mat_bytes;
   const uint32_t tab = align_up(2u * (E + 1) * 4u, 16);
   const uint32_t cpw = BN >= 32 ? BN / 2 : BN;  // token columns per epilogue warp
-  const uint32_t sa = am == AM_INT8 ? align_up(kEpiWarps * cpw * G * 4u, 16) : 0u;
+  // A8: the epilogue warps' activation scales; non-grouped modes: their BF16 staging tiles [16][32]
+  const bool grouped = am == AM_INT8 || (am == AM_BF16 && (wf == WF_INT8 || wf == WF_INT4));
+  const uint32_t sa = am == AM_INT8 ? align_up(kEpiWarps * cpw * G * 4u, 16) : (grouped ? 0u : kEpiWarps * 16u * 32u * 2u);
   const uint32_t bars = align_up(sizeof(Bars), 16);
   const uint32_t bring = am == AM_INT8 ? kBSlots * BN * 128u : 0u;  // converted-token ring
   fixed = bring + scales + tab + sa + bars;
