@@ -648,15 +648,23 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int jend = min(c1, x.nrows);  // live columns of this warp: [c0, jend)
       if (!kGrouped) {
         const uint32_t slot = cp.slot;
-        if (!bounded_wait(&bars->accfull[slot], cp.phase, abort, args.err)) { ok = false; break; }
-        tc_fence_after();
-        const uint32_t d = tmem + lane_bits + args.acc_base + slot * kNmat * BN;
+        // The unit's scale factors, loaded before the wait so their latency overlaps it:
+        // the expert matrices' outer scales, and the row factors of this warp's tokens
+        // c0 + lane and c0 + 32 + lane (up to 64 columns per warp).
         float ow[2] = {1.f, 1.f};
         if (AM == AM_FP4) {
           for (int m = 0; m < kNmat; ++m)
             ow[m] = __ldg(reinterpret_cast<const float*>(args.experts + static_cast<uint64_t>(x.e) * args.expert_stride +
                                                          args.outer_off[m]));
         }
+        float oa_r[2] = {1.f, 1.f};
+        if (AM == AM_FP4 || AM == AM_F16S) {
+#pragma unroll
+          for (int h2 = 0; h2 < 2; ++h2) oa_r[h2] = __ldg(args.a_outer + min(x.row0 + c0 + 32 * h2 + lane, args.P - 1));
+        }
+        if (!bounded_wait(&bars->accfull[slot], cp.phase, abort, args.err)) { ok = false; break; }
+        tc_fence_after();
+        const uint32_t d = tmem + lane_bits + args.acc_base + slot * kNmat * BN;
         // Each 16-token chunk goes through this warp's staging tile [16 tokens][32 features]
         // (BF16), then out as 16-byte row pieces: 64 bytes of a token's row per 4 lanes.
         uint16_t* stage = reinterpret_cast<uint16_t*>(smem + args.off_sa) + ew * (16 * 32);
@@ -665,13 +673,12 @@ __global__ void __launch_bounds__(kThreads, 1)
           uint32_t g[16], up[16];
           tmem_ld16(d + j0, g);
           if (kGateUp) tmem_ld16(d + BN + j0, up);
-          // the row factors of the chunk's 16 tokens: lane i reads token j0 + i (clamped in range)
-          float oa_l = 1.f;
-          if (AM == AM_FP4 || AM == AM_F16S) oa_l = __ldg(args.a_outer + min(x.row0 + j0 + (lane & 15), args.P - 1));
           tmem_wait_ld();
+          // the chunk's tokens j0 .. j0+15 are this warp's columns (j0 - c0) .. +15: held by lanes (j0 - c0 + i) % 32
+          const float oa_c = ((j0 - c0) & 32) ? oa_r[1] : oa_r[0];
 #pragma unroll
           for (int i = 0; i < 16; ++i) {
-            const float oa = __shfl_sync(0xffffffffu, oa_l, i);
+            const float oa = __shfl_sync(0xffffffffu, oa_c, ((j0 - c0) & 31) + i);
             float gv = __uint_as_float(g[i]);
             if (AM == AM_FP4) gv = gv * (ow[0] * oa);
             else if (AM == AM_F16S) gv = gv * oa;
