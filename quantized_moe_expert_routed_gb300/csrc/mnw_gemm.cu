@@ -365,7 +365,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           tc_fence_after();
           const uint32_t st = smem_u32(smem + s * args.stage_bytes);
-          const uint32_t sf = tmem + args.sf_base + fp.slot * args.sf_cols;  // [SFA m0 | SFA m1 | SFB], 16 columns each
+          // [SFA m0 | SFA m1]: 16 columns each; SFB: 8 columns per 64-K step
+          const uint32_t sf = tmem + args.sf_base + fp.slot * args.sf_cols;
 #pragma unroll
           for (int kk = 0; kk < 4; ++kk) {
             const uint64_t bdesc = sdesc_sw128(st + args.off_braw + kk * 32);
@@ -373,7 +374,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
             for (int m = 0; m < kNmat; ++m)
               mma_fp4_ss(d_base + m * BN, sdesc_sw128(st + args.off_a[m] + kk * 32), bdesc, idesc, sf + m * 16 + kk * 4,
-                         sf + kNmat * 16 + kk * 4, acc);
+                         sf + kNmat * 16 + kk * 8, acc);
           }
           issued = true;
           mma_commit(&bars->sfempty[fp.slot]);
@@ -491,8 +492,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       // A (weights): lane quarter q holds rows 32q..32q+31; row r's four scales
       // of step kk (one 32-bit word, first 16 K in the low byte) go to the four
       // columns m*16 + 4kk .. +3 of lane r.  B (tokens): every lane quarter
-      // holds all BN token rows, token 32j + l in lane l of column 32 + 4kk + j
-      // (16 + 4kk + j for one matrix); rows past BN read as zero.
+      // holds all BN (<= 256) token rows, token 32j + l in lane l of column
+      // 16 nmat + 8kk + j; rows past BN read as zero.
       const uint32_t nsf = static_cast<uint32_t>(args.sf_slots);
       const uint32_t lane_bits = static_cast<uint32_t>(q * 32) << 16;
       RingPos fp;
@@ -516,21 +517,25 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int i = 0; i < 16; ++i) o[i] = w[i >> 2];
             tmem_st16(sf + m * 16, o);
           }
-          uint4 tv[4];
+          uint4 tv[8];
 #pragma unroll
-          for (int j = 0; j < 4; ++j) {
+          for (int j = 0; j < 8; ++j) {
             const int row = 32 * j + lane;
             tv[j] = row < BN ? lds128(st + args.off_bsf + row * 16) : make_uint4(0, 0, 0, 0);
           }
 #pragma unroll
-          for (int kk = 0; kk < 4; ++kk) {
+          for (int hk = 0; hk < 2; ++hk) {  // steps 2hk and 2hk + 1: 16 columns
 #pragma unroll
-            for (int j = 0; j < 4; ++j) {
-              const uint4 v = tv[j];
-              o[kk * 4 + j] = kk == 0 ? v.x : (kk == 1 ? v.y : (kk == 2 ? v.z : v.w));
+            for (int k2 = 0; k2 < 2; ++k2) {
+              const int kk = 2 * hk + k2;
+#pragma unroll
+              for (int j = 0; j < 8; ++j) {
+                const uint4 v = tv[j];
+                o[k2 * 8 + j] = kk == 0 ? v.x : (kk == 1 ? v.y : (kk == 2 ? v.z : v.w));
+              }
             }
+            tmem_st16(sf + kNmat * 16 + hk * 16, o);
           }
-          tmem_st16(sf + kNmat * 16, o);
           tmem_wait_st();
           tc_fence_before();
           __syncwarp();
@@ -657,10 +662,11 @@ __global__ void __launch_bounds__(kThreads, 1)
             ow[m] = __ldg(reinterpret_cast<const float*>(args.experts + static_cast<uint64_t>(x.e) * args.expert_stride +
                                                          args.outer_off[m]));
         }
-        float oa_r[2] = {1.f, 1.f};
+        float oa_r[4] = {1.f, 1.f, 1.f, 1.f};  // row factors of tokens c0 + 32 i + lane (up to 128 columns)
         if (AM == AM_FP4 || AM == AM_F16S) {
 #pragma unroll
-          for (int h2 = 0; h2 < 2; ++h2) oa_r[h2] = __ldg(args.a_outer + min(x.row0 + c0 + 32 * h2 + lane, args.P - 1));
+          for (int h2 = 0; h2 < 4; ++h2)
+            if (32 * h2 < c1 - c0) oa_r[h2] = __ldg(args.a_outer + min(x.row0 + c0 + 32 * h2 + lane, args.P - 1));
         }
         if (!bounded_wait(&bars->accfull[slot], cp.phase, abort, args.err)) { ok = false; break; }
         tc_fence_after();
@@ -675,7 +681,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (kGateUp) tmem_ld16(d + BN + j0, up);
           tmem_wait_ld();
           // the chunk's tokens j0 .. j0+15 are this warp's columns (j0 - c0) .. +15: held by lanes (j0 - c0 + i) % 32
-          const float oa_c = ((j0 - c0) & 32) ? oa_r[1] : oa_r[0];
+          const int oc = (j0 - c0) >> 5;
+          const float oa_c = oc == 0 ? oa_r[0] : (oc == 1 ? oa_r[1] : (oc == 2 ? oa_r[2] : oa_r[3]));
 #pragma unroll
           for (int i = 0; i < 16; ++i) {
             const float oa = __shfl_sync(0xffffffffu, oa_c, ((j0 - c0) & 31) + i);
@@ -956,6 +963,10 @@ int run_gemm(const mnw_moe_layer* L, int wfmt, int act, int kind, const void* a0
   // accumulator slot only (the MMA then stalls while the epilogue drains);
   // 96 tokens fit two slots beside a two-slot operand-A ring.
   if (!grouped && gate_up && BN == 128 && wf != WF_BF16) BN = 96;
+  // NVFP4 down: the block-scaled MMA costs about the same for any N up to 256,
+  // so wider token tiles pay; 192 leaves room for two accumulators and two
+  // scale-factor slots (gate/up keeps 96: two matrices per tile).
+  if (wf == WF_NVFP4 && !gate_up && mean > 128) BN = 192;
   Plan plan{};
   while (!plan_smem(wf, am, gate_up, K, L->E, BN, &plan)) {
     if (BN == 16) return MNW_E_UNSUPPORTED;
@@ -977,7 +988,7 @@ int run_gemm(const mnw_moe_layer* L, int wfmt, int act, int kind, const void* a0
     // for the tokens.  At least two of each, so the epilogue drains one
     // accumulator while the MMAs fill the other and the scale-factor warps
     // fill one slot while the MMAs read the other.
-    const int d_cols = nmat * BN, sf_cols = 16 * (nmat + 1);
+    const int d_cols = nmat * BN, sf_cols = 16 * nmat + 32;
     int nacc = 2, nsf = 2;
     if (2 * d_cols + 2 * sf_cols > kTmemCols) return MNW_E_UNSUPPORTED;
     while (nacc < 4 && (nacc + 1) * d_cols + 2 * sf_cols <= kTmemCols) ++nacc;
