@@ -10,30 +10,36 @@
 // within its own 32-token block and to every earlier block).
 //
 // One CTA per (128-query tile, query head, sequence), heaviest query tiles
-// first.  Roles (576 threads):
+// first.  The key tiles are split between two independent softmax groups:
+// group 0 takes the even tiles, group 1 the odd ones, each with its own
+// score buffer, running maximum, row sums and output accumulator, and the two
+// partial results are merged at the end (the usual rescaled sum of two
+// softmax partitions).  While one group computes, the other's scores are in
+// the tensor pipe, and the two output accumulators form independent MMA
+// chains.  Roles (576 threads):
 //   warp 0      TMA producer: the Q tile once, then 128-key K and V^T tiles
 //               into two-slot rings
 //   warp 1      MMA issuer (one thread), owns the tensor memory:
-//               S_j = Q K_j^T into one of two 128-column TMEM buffers
-//               (tcgen05.mma kind::f16, both operands in shared memory), and
-//               O += P_j V_j with P_j read from tensor memory (the A operand
-//               of tcgen05.mma may live there) and V_j^T from shared memory.
-//               S_{j+1} is issued before O += P_j V_j, so the tensor pipe
-//               computes the next scores while the softmax runs.
-//   warps 2-17  softmax: four warps per TMEM lane quarter, warp part p of a
-//               quarter owns keys 32p..32p+31 of each tile (and O columns
-//               32p..32p+31) for the quarter's 32 query rows, one row per
-//               lane.  Per key tile: the row maximum of the scaled scores
-//               (the four parts' maxima meet through a shared-memory slot and
-//               an mbarrier), P = 2^(s*log2e*scale - m) rounded to BF16 and
-//               written over the first 16 of the part's own 32 S columns (two
-//               keys per column), the part's row sum of the rounded P.  The
-//               running maximum m moves, and O and the row sums are
-//               rescaled, only when a tile's maximum exceeds it by more than
-//               2^8 (rare after the first tiles); other tiles keep the old m,
-//               whose P values stay below 2^8.  Sixteen warps (four per
-//               scheduler) hide the latency of each warp's dependent chain.
-// Tensor memory (512 columns): S0 | S1 | O | unused.
+//               S_j = Q K_j^T (tcgen05.mma kind::f16, both operands in shared
+//               memory) into group (j % 2)'s score buffer, and O_g += P_j V_j
+//               with P_j read from tensor memory (the A operand of
+//               tcgen05.mma may live there) and V_j^T from shared memory.
+//               Order: S_0, S_1, then for each j: O += P_j V_j, S_{j+2}.
+//   warps 2-17  softmax: group g = warps 2 + 8g .. 9 + 8g; in a group, two
+//               warps per TMEM lane quarter, warp part p owning keys
+//               64p..64p+63 of the group's tiles for the quarter's 32 query
+//               rows, one row per lane.  Per tile: the row maximum of the
+//               scaled scores (the two parts' maxima meet through shared
+//               memory and an mbarrier), P = 2^(s*log2e*scale - m) rounded to
+//               BF16 and written over the first half of the part's own S
+//               columns (two keys per column), the part's row sum of the
+//               rounded P.  The group's running maximum m moves, and its O
+//               columns and row sums are rescaled, only when a tile's maximum
+//               exceeds it by more than 2^8; other tiles keep the old m, whose
+//               P values stay below 2^8.  A tile's scores being complete means
+//               the group's previous product into O is complete too (same
+//               issuing thread, in order), so a rescale needs no extra wait.
+// Tensor memory (512 columns): S_0 | S_1 | O_0 | O_1.
 // V is transposed into the workspace first (keys contiguous per head
 // dimension) so that both products read K-major operands.
 #include <cuda_bf16.h>
@@ -58,7 +64,7 @@ constexpr uint32_t kTileBytes = 2 * kBoxBytes;      // 128 rows x 128 BF16
 constexpr uint32_t kOffQ = 0, kOffK = kTileBytes, kOffV = kOffK + kSlots * kTileBytes;
 constexpr uint32_t kOffBars = kOffV + kSlots * kTileBytes;
 constexpr int kTmemCols = 512;
-constexpr uint32_t kColO = 256;
+constexpr uint32_t kColO = 256;  // O_g at kColO + 128 g
 constexpr float kRescaleLog2 = 8.f;
 
 struct Args {
@@ -71,10 +77,11 @@ struct Args {
 struct Bars {
   uint64_t q_full;
   uint64_t k_full[kSlots], k_empty[kSlots], v_full[kSlots], v_empty[kSlots];
-  uint64_t s_full[2], p_full[2], o_done, o_final, mma_drain;
-  uint64_t xmax[4][2], xsum[4];  // per lane quarter: the four parts' row maxima (per tile parity), row sums
-  float pmax[2][4][4][32];       // [tile parity][quarter][part][lane]
-  float psum[4][4][32];
+  uint64_t s_full[2], p_full[2], o_final, mma_drain;  // s_full, p_full: per softmax group
+  uint64_t xmax[2][4][2];  // [group][quarter][tile parity]: the two parts' row maxima
+  uint64_t fin[4];         // [quarter]: the four (group, part) warps' final row maxima and sums
+  float pmax[2][2][4][2][32];  // [group][tile parity][quarter][part][lane]
+  float fm[4][2][32], fl[4][2][2][32];  // final maxima [quarter][group][lane], sums [quarter][group][part][lane]
   uint32_t tmem_base;
   int abort;
 };
@@ -151,15 +158,16 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(&bars->s_full[i], 1);
-      mbar_init(&bars->p_full[i], kSmWarps);
+      mbar_init(&bars->p_full[i], kSmWarps / 2);
     }
-    mbar_init(&bars->o_done, 1);
     mbar_init(&bars->o_final, 1);
     mbar_init(&bars->mma_drain, 1);
     for (int i = 0; i < 4; ++i) {
-      mbar_init(&bars->xmax[i][0], 4);
-      mbar_init(&bars->xmax[i][1], 4);
-      mbar_init(&bars->xsum[i], 4);
+      for (int gg = 0; gg < 2; ++gg) {
+        mbar_init(&bars->xmax[gg][i][0], 2);
+        mbar_init(&bars->xmax[gg][i][1], 2);
+      }
+      mbar_init(&bars->fin[i], 4);
     }
     bars->abort = 0;
     fence_barrier_init();
@@ -243,24 +251,24 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (!bounded_wait(&bars->v_full[vp.slot], vp.phase, abort, args.err)) return false;
         tc_fence_after();
         const uint32_t v_s = smem_u32(smem + kOffV + vp.slot * kTileBytes);
-        // P_j: keys 32p..32p+31 in columns 32p..32p+15 of the S buffer, two keys each
+        // P_j: keys 64p..64p+63 in columns 64p..64p+31 of the group's S buffer, two keys each
         const uint32_t p = tmem + static_cast<uint32_t>(j & 1) * kBK;
+        const uint32_t o = tmem + kColO + static_cast<uint32_t>(j & 1) * kD;
 #pragma unroll
         for (int kk = 0; kk < 8; ++kk) {
           const uint32_t off = (kk >> 2) * kBoxBytes + (kk & 3) * 32;
-          mma_ts(tmem + kColO, p + (kk >> 1) * 32 + (kk & 1) * 8, sdesc_sw128(v_s + off), idesc_pv, (j > 0 || kk > 0));
+          mma_ts(o, p + (kk >> 2) * 64 + (kk & 3) * 8, sdesc_sw128(v_s + off), idesc_pv, (j > 1 || kk > 0));
         }
         mma_commit(&bars->v_empty[vp.slot]);
-        mma_commit(&bars->o_done);
         vp.advance(kSlots);
         return true;
       };
       if (ok) ok = issue_s(0);
-      for (int j = 1; ok && j < nt; ++j) {
-        ok = issue_s(j);
-        if (ok) ok = issue_pv(j - 1);
+      if (ok && nt > 1) ok = issue_s(1);
+      for (int j = 0; ok && j < nt; ++j) {
+        ok = issue_pv(j);
+        if (ok && j + 2 < nt) ok = issue_s(j + 2);
       }
-      if (ok) ok = issue_pv(nt - 1);
       if (ok) mma_commit(&bars->o_final);
       if (issued) {
         // every MMA has finished with shared and tensor memory before the CTA tears down
@@ -270,57 +278,62 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else {
     // ======================= softmax =======================
-    const int q = warp & 3;                  // TMEM lane quarter: query rows 32q .. 32q+31
-    const int part = (warp - kWarpSm0) >> 2;  // keys (and O columns) 32 part .. 32 part + 31
+    const int grp = (warp - kWarpSm0) >> 3;         // softmax group: key tiles grp, grp + 2, ...
+    const int q = warp & 3;                         // TMEM lane quarter: query rows 32q .. 32q+31
+    const int part = ((warp - kWarpSm0) >> 2) & 1;  // keys (and O columns) 64 part .. 64 part + 63
     const int r = q * 32 + lane;
     const int t = q0 + r;
     const uint32_t lane_bits = static_cast<uint32_t>(q * 32) << 16;
-    const uint32_t ocol = tmem + lane_bits + kColO + part * 32;
+    const uint32_t sbase = tmem + lane_bits + static_cast<uint32_t>(grp) * kBK + part * 64;
+    const uint32_t obase = tmem + lane_bits + kColO + static_cast<uint32_t>(grp) * kD + part * 64;
     const int kend = key_end(min(t, T - 1), args.blk, T);
     const float sl2 = args.scale_log2;
-    float m_used = 0.f, l = 0.f;
+    float m_used = -INFINITY, l = 0.f;
     bool ok = true;
-    for (int j = 0; j < nt; ++j) {
-      if (!warp_wait(&bars->s_full[j & 1], (j >> 1) & 1, abort, args.err)) { ok = false; break; }
+    int k = 0;  // tiles of this group done
+    for (int j = grp; j < nt; j += 2, ++k) {
+      if (!warp_wait(&bars->s_full[grp], k & 1, abort, args.err)) { ok = false; break; }
       tc_fence_after();
-      const uint32_t sa = tmem + lane_bits + static_cast<uint32_t>(j & 1) * kBK + part * 32;
-      const int lim = kend - j * kBK - part * 32;  // keys e < lim of this part are allowed for the row
-      uint32_t sv[32];
-      tmem_ld32(sa, sv);
-      tmem_wait_ld();
+      const int lim = kend - j * kBK - part * 64;  // keys e < lim of this part are allowed for the row
       float mx = -INFINITY;
-      if (lim >= 32) {
 #pragma unroll
-        for (int e = 0; e < 32; ++e) mx = fmaxf(mx, __uint_as_float(sv[e]));
-      } else {
+      for (int hh = 0; hh < 2; ++hh) {
+        uint32_t sv[32];
+        tmem_ld32(sbase + hh * 32, sv);
+        tmem_wait_ld();
+        const int lh = lim - 32 * hh;
+        if (lh >= 32) {
 #pragma unroll
-        for (int e = 0; e < 32; ++e)
-          if (e < lim) mx = fmaxf(mx, __uint_as_float(sv[e]));
+          for (int e = 0; e < 32; ++e) mx = fmaxf(mx, __uint_as_float(sv[e]));
+        } else {
+#pragma unroll
+          for (int e = 0; e < 32; ++e)
+            if (e < lh) mx = fmaxf(mx, __uint_as_float(sv[e]));
+        }
       }
-      // the row's maximum over the four parts
-      bars->pmax[j & 1][q][part][lane] = mx;
+      // the row's maximum over the two parts
+      bars->pmax[grp][k & 1][q][part][lane] = mx;
       __syncwarp();
-      if (lane == 0) mbar_arrive(&bars->xmax[q][j & 1]);
-      if (!warp_wait(&bars->xmax[q][j & 1], (j >> 1) & 1, abort, args.err)) { ok = false; break; }
-      mx = fmaxf(fmaxf(bars->pmax[j & 1][q][0][lane], bars->pmax[j & 1][q][1][lane]),
-                 fmaxf(bars->pmax[j & 1][q][2][lane], bars->pmax[j & 1][q][3][lane]));
-      mx *= sl2;  // the scale is positive
-      if (j == 0) {
-        m_used = mx;  // key 0 is allowed for every row, so mx is finite
+      if (lane == 0) mbar_arrive(&bars->xmax[grp][q][k & 1]);
+      if (!warp_wait(&bars->xmax[grp][q][k & 1], (k >> 1) & 1, abort, args.err)) { ok = false; break; }
+      mx = fmaxf(bars->pmax[grp][k & 1][q][0][lane], bars->pmax[grp][k & 1][q][1][lane]) * sl2;  // scale > 0
+      if (k == 0) {
+        m_used = mx;  // key 0 is allowed for every row, so the first tile's maximum is finite
       } else {
         const bool resc = mx > m_used + kRescaleLog2;
         if (__any_sync(0xffffffffu, resc)) {
-          // O holds the products of tiles 0 .. j-1: wait for the last of them
-          if (!warp_wait(&bars->o_done, (j - 1) & 1, abort, args.err)) { ok = false; break; }
-          tc_fence_after();
+          // O_grp holds this group's earlier products, all complete (see above)
           const float alpha = resc ? ex2(m_used - mx) : 1.f;
-          uint32_t o[32];
-          tmem_ld32(ocol, o);
-          tmem_wait_ld();
 #pragma unroll
-          for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
-          tmem_st16(ocol, *reinterpret_cast<uint32_t(*)[16]>(&o[0]));
-          tmem_st16(ocol + 16, *reinterpret_cast<uint32_t(*)[16]>(&o[16]));
+          for (int hh = 0; hh < 2; ++hh) {
+            uint32_t o[32];
+            tmem_ld32(obase + hh * 32, o);
+            tmem_wait_ld();
+#pragma unroll
+            for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
+            tmem_st16(obase + hh * 32, *reinterpret_cast<uint32_t(*)[16]>(&o[0]));
+            tmem_st16(obase + hh * 32 + 16, *reinterpret_cast<uint32_t(*)[16]>(&o[16]));
+          }
           tmem_wait_st();
           if (resc) {
             l *= alpha;
@@ -328,49 +341,73 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         }
       }
-      // P as BF16 pairs over the first 16 of this part's 32 S columns (already read)
+      // P as BF16 pairs over the first 32 of this part's 64 S columns: keys 32hh .. 32hh+31
+      // are read (again) before their 16 columns of P are written, below them
       const float mneg = -m_used;
-      uint32_t pk[16];
 #pragma unroll
-      for (int e = 0; e < 16; ++e) {
-        const float p0 = 2 * e < lim ? ex2(fmaf(__uint_as_float(sv[2 * e]), sl2, mneg)) : 0.f;
-        const float p1 = 2 * e + 1 < lim ? ex2(fmaf(__uint_as_float(sv[2 * e + 1]), sl2, mneg)) : 0.f;
-        const __nv_bfloat162 pb = __floats2bfloat162_rn(p0, p1);
-        const float2 pr = __bfloat1622float2(pb);
-        l += pr.x + pr.y;
-        pk[e] = *reinterpret_cast<const uint32_t*>(&pb);
+      for (int hh = 0; hh < 2; ++hh) {
+        uint32_t sv[32];
+        tmem_ld32(sbase + hh * 32, sv);
+        tmem_wait_ld();
+        uint32_t pk[16];
+#pragma unroll
+        for (int e = 0; e < 16; ++e) {
+          const int key = 32 * hh + 2 * e;
+          const float p0 = key < lim ? ex2(fmaf(__uint_as_float(sv[2 * e]), sl2, mneg)) : 0.f;
+          const float p1 = key + 1 < lim ? ex2(fmaf(__uint_as_float(sv[2 * e + 1]), sl2, mneg)) : 0.f;
+          const __nv_bfloat162 pb = __floats2bfloat162_rn(p0, p1);
+          const float2 pr = __bfloat1622float2(pb);
+          l += pr.x + pr.y;
+          pk[e] = *reinterpret_cast<const uint32_t*>(&pb);
+        }
+        tmem_st16(sbase + hh * 16, pk);
       }
-      tmem_st16(sa, pk);
       tmem_wait_st();
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(&bars->p_full[j & 1]);
+      if (lane == 0) mbar_arrive(&bars->p_full[grp]);
     }
+    // merge the two groups: out = sum_g 2^(m_g - M) O_g / sum_g 2^(m_g - M) l_g, M = max m_g
     if (ok) {
-      // the row sum over the four parts
-      bars->psum[q][part][lane] = l;
+      if (part == 0) bars->fm[q][grp][lane] = m_used;
+      bars->fl[q][grp][part][lane] = l;
       __syncwarp();
-      if (lane == 0) mbar_arrive(&bars->xsum[q]);
-      ok = warp_wait(&bars->xsum[q], 0, abort, args.err);
+      if (lane == 0) mbar_arrive(&bars->fin[q]);
+      ok = warp_wait(&bars->fin[q], 0, abort, args.err);
     }
     if (ok && warp_wait(&bars->o_final, 0, abort, args.err)) {
       tc_fence_after();
-      const float lsum = (bars->psum[q][0][lane] + bars->psum[q][1][lane]) +
-                         (bars->psum[q][2][lane] + bars->psum[q][3][lane]);
-      const float inv = 1.f / lsum;
-      uint32_t o[32];
-      tmem_ld32(ocol, o);
-      tmem_wait_ld();
-      uint32_t pk[16];
+      const float m0 = bars->fm[q][0][lane], m1 = bars->fm[q][1][lane];
+      const float l0 = bars->fl[q][0][0][lane] + bars->fl[q][0][1][lane];
+      const float l1 = bars->fl[q][1][0][lane] + bars->fl[q][1][1][lane];
+      const bool two = nt > 1;  // with one key tile, group 1 wrote nothing (O_1 is not read)
+      const float M = two ? fmaxf(m0, m1) : m0;
+      const float a0 = ex2(m0 - M), a1 = two ? ex2(m1 - M) : 0.f;
+      const float inv = 1.f / (l0 * a0 + l1 * a1);
+      // this warp writes O columns 32 (2 grp + part) .. +31 of its quarter's rows, 16 at a time
+      const float s0 = a0 * inv, s1 = a1 * inv;
 #pragma unroll
-      for (int e = 0; e < 16; ++e)
-        pk[e] = pack_bf16x2(__uint_as_float(o[2 * e]) * inv, __uint_as_float(o[2 * e + 1]) * inv);
-      if (t < T) {
-        __nv_bfloat16* dst = args.out + ((static_cast<size_t>(b) * T + t) * Hq + h) * kD + part * 32;
-        stg128(dst, pk[0], pk[1], pk[2], pk[3]);
-        stg128(dst + 8, pk[4], pk[5], pk[6], pk[7]);
-        stg128(dst + 16, pk[8], pk[9], pk[10], pk[11]);
-        stg128(dst + 24, pk[12], pk[13], pk[14], pk[15]);
+      for (int hh = 0; hh < 2; ++hh) {
+        const int c0 = 32 * (2 * grp + part) + 16 * hh;
+        uint32_t o0[16], o1[16];
+        tmem_ld16(tmem + lane_bits + kColO + c0, o0);
+        if (two) tmem_ld16(tmem + lane_bits + kColO + kD + c0, o1);
+        tmem_wait_ld();
+        uint32_t pk[8];
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+          float v0 = __uint_as_float(o0[2 * e]) * s0, v1 = __uint_as_float(o0[2 * e + 1]) * s0;
+          if (two) {
+            v0 = fmaf(__uint_as_float(o1[2 * e]), s1, v0);
+            v1 = fmaf(__uint_as_float(o1[2 * e + 1]), s1, v1);
+          }
+          pk[e] = pack_bf16x2(v0, v1);
+        }
+        if (t < T) {
+          __nv_bfloat16* dst = args.out + ((static_cast<size_t>(b) * T + t) * Hq + h) * kD + c0;
+          stg128(dst, pk[0], pk[1], pk[2], pk[3]);
+          stg128(dst + 8, pk[4], pk[5], pk[6], pk[7]);
+        }
       }
     }
   }
