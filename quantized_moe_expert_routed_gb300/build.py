@@ -16,7 +16,7 @@ CSRC = os.path.join(HERE, "csrc")
 INCLUDE = os.path.join(os.path.dirname(HERE), "include")
 BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(HERE, "libmnw_moe.so")
-SOURCES = ["mnw_api.cu", "mnw_route.cu", "mnw_router.cu", "mnw_quant.cu", "mnw_gemm.cu", "mnw_gemm_rows.cu", "mnw_gemm_warp.cu",
+SOURCES = ["mnw_api.cu", "mnw_route.cu", "mnw_router.cu", "mnw_quant.cu", "mnw_gemm.cu", "mnw_gemm_rows.cu", "mnw_gemm_rows_a8.cu", "mnw_gemm_warp.cu",
            "mnw_gemm_warp_dep.cu", "mnw_static_ws.cu", "mnw_selftest.cu", "mnw_attention.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-Xcompiler", "-O2", "-Xcompiler", "-fvisibility=hidden",

@@ -945,6 +945,9 @@ int run_gemm(const mnw_moe_layer* L, int wfmt, int act, int kind, const void* a0
   // is forced.
   if (path != MNW_PATH_TCGEN05 && rows_gemm_applicable(L, wfmt, act, kind))
     return run_gemm_rows(L, wfmt, act, kind, a0, a1, offsets, P, out, err, st);
+  // W8A8: the row-tile kernel with per-group accumulators (mnw_gemm_rows_a8.cu)
+  if (path != MNW_PATH_TCGEN05 && rows_a8_applicable(L, wfmt, act, kind))
+    return run_gemm_rows_a8(L, kind, a0, static_cast<const float*>(a1), offsets, P, out, dots, err, st);
   const bool gate_up = kind == MNW_KIND_GATE_UP;
   const int K = kind == MNW_KIND_DOWN ? L->I : L->H;
   const int N = kind == MNW_KIND_DOWN ? L->H : L->I;

@@ -166,6 +166,11 @@ int run_gemm_warp(const mnw_moe_layer* L, int wfmt, int act, int kind, const voi
 bool rows_gemm_applicable(const mnw_moe_layer* L, int wfmt, int act, int kind);
 int run_gemm_rows(const mnw_moe_layer* L, int wfmt, int act, int kind, const void* a0, const void* a1,
                   const int32_t* offsets, int P, void* out, uint32_t* err, cudaStream_t st);
+// Row-tile tcgen05 GEMM for INT8 weights with INT8 activations (tokens as M,
+// 128 weight rows as N, one accumulator per 128-K group; mnw_gemm_rows_a8.cu).
+bool rows_a8_applicable(const mnw_moe_layer* L, int wfmt, int act, int kind);
+int run_gemm_rows_a8(const mnw_moe_layer* L, int kind, const void* a_codes, const float* a_scales,
+                     const int32_t* offsets, int P, void* out, int32_t* dots, uint32_t* err, cudaStream_t st);
 // Token tile (in 8-row units) the warp-MMA kernel uses for P rows over E experts.
 int warp_gemm_nt(int P, int E);
 // Process-wide GEMM path selection (MNW_PATH_*).

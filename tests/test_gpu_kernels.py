@@ -455,3 +455,39 @@ def test_row_tile_kernel_forced_matches_oracle(M, wfmt, T, k, E, H, I):
         M.mnw_moe_set_gemm_path(M.PATH_AUTO)
     assert_close(h, O.gemm_a16(blob.numpy(), O.KIND_GATE_UP, to_np_bits(xp), o_off), what="row tiles gate_up")
     assert_close(y, O.gemm_a16(blob.numpy(), O.KIND_DOWN, to_np_bits(h), o_off), what="row tiles down")
+
+
+@pytest.mark.parametrize("path", ["rows", "tcgen05"])
+@pytest.mark.parametrize("T,k,E,H,I", [(300, 4, 8, 512, 512), (40, 2, 8, 1024, 512), (700, 2, 16, 2048, 512),
+                                       (33, 8, 64, 512, 1024)])
+def test_a8_kernels_forced_match_oracle(M, path, T, k, E, H, I):
+    """W8A8 on the row-tile kernel (tokens as M, 128 weight rows as N, one
+    accumulator per 128-K group, running sums in registers) and on the
+    weight-tile kernel, each forced on every shape: ragged and crowded experts,
+    an empty one, group dots bit for bit, the fused pair and the single gate
+    and up matrices of the unfused path, and down."""
+    blob, hdr, ids, x = _setup(S.FMT_INT8_G128, E, H, I, T, k, seed=7 * T + E, outlier_p=0.01)
+    ids[: T // 3, 0] = 1  # a crowded expert
+    if E > 8:
+        ids[ids == 5] = 6  # an empty expert
+    layer = M.Layer(blob.to(DEV), hdr)
+    off, sa, pos, _ = M.mnw_moe_permute(ids.to(DEV), E)
+    o_off = off.cpu().numpy()
+    valid = int(o_off[-1])
+    q, s = M.mnw_moe_quantize_act(M.ACT_INT8_G128, x.to(DEV), row_index=sa, index_div=k)
+    qn, sn = q.cpu().numpy(), s.cpu().numpy()
+    M.mnw_moe_set_gemm_path(M.PATH_ROWS if path == "rows" else M.PATH_TCGEN05)
+    try:
+        for kind, okind in ((M.KIND_GATE_UP, O.KIND_GATE_UP), (M.KIND_GATE, O.KIND_GATE), (M.KIND_UP, O.KIND_UP)):
+            h, dots = M.mnw_moe_grouped_gemm_w8a8(layer, kind, q, s, off, want_dots=True)
+            oh, odots = O.gemm_a8(blob.numpy(), okind, qn, sn, o_off, want_dots=True)
+            assert np.array_equal(dots.cpu().numpy()[:valid], odots[:valid]), (path, kind)
+            assert_close(h, oh, what=f"w8a8 {path} kind {kind}")
+        h2, _ = M.mnw_moe_grouped_gemm_w8a8(layer, M.KIND_GATE_UP, q, s, off, want_dots=True)
+        hq, hs = M.mnw_moe_quantize_act(M.ACT_INT8_G128, h2)
+        y, ydots = M.mnw_moe_grouped_gemm_w8a8(layer, M.KIND_DOWN, hq, hs, off, want_dots=True)
+        oy, oydots = O.gemm_a8(blob.numpy(), O.KIND_DOWN, hq.cpu().numpy(), hs.cpu().numpy(), o_off, want_dots=True)
+        assert np.array_equal(ydots.cpu().numpy()[:valid], oydots[:valid]), path
+        assert_close(y, oy, what=f"w8a8 {path} down")
+    finally:
+        M.mnw_moe_set_gemm_path(M.PATH_AUTO)
