@@ -53,7 +53,7 @@ constexpr int kThreads = (kWarpEpi0 + kEpiWarps) * 32;
 constexpr int kStages = 3;    // code stages (one 128-K group each)
 constexpr int kOpSlots = 2;   // converted 64-K operand slots (A and B tile)
 constexpr int kAccSlots = 4;  // per-group accumulators of 128 columns
-constexpr int kMaxG = 32;     // K <= 4096
+constexpr int kMaxG = 16;     // K <= 2048
 constexpr uint32_t kCodeTile = 128 * 128;        // 128 rows x 128 codes
 constexpr uint32_t kStageBytes = 2 * kCodeTile;  // tokens + weights
 constexpr uint32_t kOpTile = 128 * 128;          // 128 rows x 64 FP16
@@ -70,7 +70,7 @@ struct Args {
   __nv_bfloat16* out;
   int32_t* dots;           // nullable: [P][C][G], C = 2I (gate, then up) or N
   int dots_c, dots_c_off;  // dots row width C and a column offset
-  uint32_t off_op, off_sc, off_tab, off_bars, sc_w_bytes, sc_bytes;
+  uint32_t off_op, off_sc, off_swt, off_tab, off_bars, sc_w_bytes, sc_bytes;
   uint32_t* err;
 };
 
@@ -79,6 +79,7 @@ struct Bars {
   uint64_t ofull[kOpSlots], oempty[kOpSlots];
   uint64_t afull[kAccSlots], aempty[kAccSlots];
   uint64_t sfull[2], sempty[2];
+  uint64_t tpose[2];  // the epilogue warps' transposed weight scales are in place
   uint64_t final_mma;
   uint32_t tmem_base;
   int abort;
@@ -159,6 +160,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int i = 0; i < 2; ++i) {
       mbar_init(&bars->sfull[i], 1);
       mbar_init(&bars->sempty[i], kEpiWarps);
+      mbar_init(&bars->tpose[i], kEpiWarps);
     }
     mbar_init(&bars->final_mma, 1);
     bars->abort = 0;
@@ -348,6 +350,15 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (!wwait(&bars->sfull[sb], (s_used >> 1) & 1u, abort, args.err)) { ok = false; break; }
       const __half* sw = reinterpret_cast<const __half*>(sc_ring + sb * args.sc_bytes);   // [128 weight rows][G]
       const float* sa = reinterpret_cast<const float*>(sc_ring + sb * args.sc_bytes + args.sc_w_bytes) + tr * G;
+      // the weight scales transposed to FP32 [G][128 columns], so that a group's 64 column
+      // scales of a warp are 16 broadcast 16-byte loads; buffer sb is free: every epilogue
+      // warp finished unit u - 2 before the producer refilled scale buffer sb
+      float* swt = reinterpret_cast<float*>(smem + args.off_swt) + sb * (kMaxG * 128);
+      for (int i = (warp - kWarpEpi0) * 32 + lane; i < 128 * G; i += kEpiWarps * 32)
+        swt[i] = __half2float(sw[(i & 127) * G + (i >> 7)]);
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&bars->tpose[sb]);
+      if (!wwait(&bars->tpose[sb], (s_used >> 1) & 1u, abort, args.err)) { ok = false; break; }
       float sum[64];
 #pragma unroll
       for (int c = 0; c < 64; ++c) sum[c] = 0.f;
@@ -371,9 +382,10 @@ __global__ void __launch_bounds__(kThreads, 1)
               dr[static_cast<size_t>(args.dots_c_off + gcol) * G + g] = __float2int_rn(__uint_as_float(acc[i]));
             }
           }
+          const float* wg = swt + g * 128 + cbase;
 #pragma unroll
           for (int i = 0; i < 16; ++i) {
-            const float f = __fmul_rn(__half2float(sw[(cbase + i) * G + g]), s_a);
+            const float f = __fmul_rn(wg[i], s_a);
             sum[16 * ch + i] = __fmaf_rn(f, __uint_as_float(acc[i]), sum[16 * ch + i]);
           }
         }
@@ -447,7 +459,7 @@ bool rows_a8_applicable(const mnw_moe_layer* L, int wfmt, int act, int kind) {
   if (wfmt != MNW_FMT_INT8_G128 || act != MNW_ACT_INT8_G128) return false;
   const int K = kind == MNW_KIND_DOWN ? L->I : L->H;
   const int N = kind == MNW_KIND_DOWN ? L->H : L->I;
-  // K: whole 128-groups, at most kMaxG of them, and a multiple of 4 groups (the token
+  // K: whole 128-groups, at most kMaxG of them (larger K: the weight-tile kernel), and a multiple of 4 groups (the token
   // rows' FP32 group scales then fill whole 16-byte units for the bulk copy)
   if (K % 512 || K / 128 > rowsa8::kMaxG) return false;
   return kind == MNW_KIND_GATE_UP ? N % 64 == 0 : N % 128 == 0;
@@ -486,6 +498,8 @@ int run_gemm_rows_a8(const mnw_moe_layer* L, int kind, const void* a_codes, cons
   o += kOpSlots * kOpBytes;
   a.off_sc = o;
   o += 2 * a.sc_bytes;
+  a.off_swt = o;
+  o += 2 * kMaxG * 128 * 4;
   a.off_tab = o;
   o += align_up(2u * (L->E + 1) * 4u, 16);
   a.off_bars = align_up(o, 16);
