@@ -40,6 +40,22 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   return d;
 }
 
+// Two FP32 lanes in one 64-bit register: d = a * b and d = a * b + c, each
+// lane rounded to nearest exactly as the scalar operation (sm_100 family).
+__device__ __forceinline__ uint64_t f32x2_mul(uint64_t a, uint64_t b) {
+  uint64_t d;
+  asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
+}
+__device__ __forceinline__ uint64_t f32x2_fma(uint64_t a, uint64_t b, uint64_t c) {
+  uint64_t d;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+  return d;
+}
+__device__ __forceinline__ uint64_t f32x2_pack(uint32_t lo, uint32_t hi) {
+  return static_cast<uint64_t>(lo) | (static_cast<uint64_t>(hi) << 32);
+}
+
 // 32 signed INT4 codes (one 16-byte chunk, element 2c in the low nibble of
 // byte c) -> 16 words of (even, odd) pairs holding the integers q exactly, as
 // BF16 (kBf16) or FP16.  The group scale is applied later, in FP32.

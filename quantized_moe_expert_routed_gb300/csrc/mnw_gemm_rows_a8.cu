@@ -359,14 +359,15 @@ __global__ void __launch_bounds__(kThreads, 1)
       __syncwarp();
       if (lane == 0) mbar_arrive(&bars->tpose[sb]);
       if (!wwait(&bars->tpose[sb], (s_used >> 1) & 1u, abort, args.err)) { ok = false; break; }
-      float sum[64];
+      uint64_t sum2[32];  // the 64 running sums as FP32 pairs (packed FMAs, each lane as the scalar one)
 #pragma unroll
-      for (int c = 0; c < 64; ++c) sum[c] = 0.f;
+      for (int c = 0; c < 32; ++c) sum2[c] = 0ull;
       for (int g = 0; g < G; ++g) {
         if (!wwait(&bars->afull[ap.slot], ap.phase, abort, args.err)) { ok = false; break; }
         tc_fence_after();
         const uint32_t d = tmem + lane_bits + ap.slot * kBN;
         const float s_a = valid ? sa[g] : 0.f;
+        const uint64_t sa2 = f32x2_pack(__float_as_uint(s_a), __float_as_uint(s_a));
         // four chunks of 16 columns: the gate (or first) half, then the up (or second) half
 #pragma unroll
         for (int ch = 0; ch < 4; ++ch) {
@@ -382,11 +383,11 @@ __global__ void __launch_bounds__(kThreads, 1)
               dr[static_cast<size_t>(args.dots_c_off + gcol) * G + g] = __float2int_rn(__uint_as_float(acc[i]));
             }
           }
-          const float* wg = swt + g * 128 + cbase;
+          const uint64_t* wg2 = reinterpret_cast<const uint64_t*>(swt + g * 128 + cbase);
 #pragma unroll
-          for (int i = 0; i < 16; ++i) {
-            const float f = __fmul_rn(wg[i], s_a);
-            sum[16 * ch + i] = __fmaf_rn(f, __uint_as_float(acc[i]), sum[16 * ch + i]);
+          for (int i = 0; i < 8; ++i) {
+            const uint64_t f2 = f32x2_mul(wg2[i], sa2);  // fl(s_w * s_a), two columns
+            sum2[8 * ch + i] = f32x2_fma(f2, f32x2_pack(acc[2 * i], acc[2 * i + 1]), sum2[8 * ch + i]);
           }
         }
         tc_fence_before();
@@ -408,7 +409,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             float hv[2];
 #pragma unroll
             for (int e2 = 0; e2 < 2; ++e2) {
-              const float gv = sum[2 * i + e2], uv = sum[32 + 2 * i + e2];
+              const uint64_t gp = sum2[i], upp = sum2[16 + i];
+              const float gv = __uint_as_float(static_cast<uint32_t>(gp >> (32 * e2)));
+              const float uv = __uint_as_float(static_cast<uint32_t>(upp >> (32 * e2)));
               hv[e2] = __fdividef(gv, 1.f + __expf(-gv)) * uv;
             }
             pk[i] = pack_bf16x2(hv[0], hv[1]);
@@ -419,7 +422,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         } else {
           uint32_t pk[32];
 #pragma unroll
-          for (int i = 0; i < 32; ++i) pk[i] = pack_bf16x2(sum[2 * i], sum[2 * i + 1]);
+          for (int i = 0; i < 32; ++i)
+            pk[i] = pack_bf16x2(__uint_as_float(static_cast<uint32_t>(sum2[i])),
+                                __uint_as_float(static_cast<uint32_t>(sum2[i] >> 32)));
 #pragma unroll
           for (int i = 0; i < 8; ++i)
             stg128(dst + n0 + 64 * hf + 8 * i, pk[4 * i], pk[4 * i + 1], pk[4 * i + 2], pk[4 * i + 3]);
