@@ -343,7 +343,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       // P as BF16 pairs over the first 32 of this part's 64 S columns: keys 32hh .. 32hh+31
       // are read (again) before their 16 columns of P are written, below them
-      const float mneg = -m_used;
+      // two keys per packed FP32x2 operation: the exponent argument and the row sums
+      const uint64_t sl2x2 = f32x2_pack(__float_as_uint(sl2), __float_as_uint(sl2));
+      const uint64_t mneg2 = f32x2_pack(__float_as_uint(-m_used), __float_as_uint(-m_used));
+      uint64_t l2 = 0ull;  // even and odd keys' partial sums
 #pragma unroll
       for (int hh = 0; hh < 2; ++hh) {
         uint32_t sv[32];
@@ -353,15 +356,17 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int e = 0; e < 16; ++e) {
           const int key = 32 * hh + 2 * e;
-          const float p0 = key < lim ? ex2(fmaf(__uint_as_float(sv[2 * e]), sl2, mneg)) : 0.f;
-          const float p1 = key + 1 < lim ? ex2(fmaf(__uint_as_float(sv[2 * e + 1]), sl2, mneg)) : 0.f;
+          const uint64_t t2 = f32x2_fma(f32x2_pack(sv[2 * e], sv[2 * e + 1]), sl2x2, mneg2);
+          const float p0 = key < lim ? ex2(__uint_as_float(static_cast<uint32_t>(t2))) : 0.f;
+          const float p1 = key + 1 < lim ? ex2(__uint_as_float(static_cast<uint32_t>(t2 >> 32))) : 0.f;
           const __nv_bfloat162 pb = __floats2bfloat162_rn(p0, p1);
-          const float2 pr = __bfloat1622float2(pb);
-          l += pr.x + pr.y;
-          pk[e] = *reinterpret_cast<const uint32_t*>(&pb);
+          const uint32_t pw = *reinterpret_cast<const uint32_t*>(&pb);
+          l2 = f32x2_add(l2, f32x2_pack(pw << 16, pw & 0xFFFF0000u));  // the rounded P, as FP32
+          pk[e] = pw;
         }
         tmem_st16(sbase + hh * 16, pk);
       }
+      l += __uint_as_float(static_cast<uint32_t>(l2)) + __uint_as_float(static_cast<uint32_t>(l2 >> 32));
       tmem_wait_st();
       tc_fence_before();
       __syncwarp();

@@ -50,6 +50,9 @@ def _check(got, ref, v_bf16_host, Hq, Hkv):
     (1, 384, 2, 2, 64),
     (1, 130, 2, 2, 7),      # blocks that do not divide the tile
     (1, 640, 2, 1, 200),    # blocks wider than a tile
+    (1, 1, 2, 1, 32),       # one token
+    (3, 129, 8, 1, 32),     # three sequences, 8 query heads on one kv head, one row into a second tile
+    (1, 256, 2, 2, 100),    # early rows of a tile see no key of its second tile
 ])
 def test_attention_matches_oracle(B, T, Hq, Hkv, blk):
     q, k, v, out, scale = _run(B, T, Hq, Hkv, blk, seed=100 + T + blk)
