@@ -412,9 +412,72 @@ def run_ours(args, wl):
         e2e_ms.append((time.perf_counter() - t0) * 1e3)
     e2e_ms = reduce_ranks(statistics.median(e2e_ms), world, "max", dev)
 
+    # The comparison paths the pages describe, on the same input (device buffers,
+    # L2 flushed between steps, CUDA events, median): GPU routing fused with the
+    # permutation (router weights ~N(0, 1/H) in BF16), the router alone, the
+    # unfused activation, and host routing (it synchronises: wall clock).
+    variants = {}
+    nv = max(3, min(args.steps, 10))
+
+    def timed(fn, wall=False):
+        fn()
+        torch.cuda.synchronize()
+        ts = []
+        for _ in range(nv):
+            l2_flush()
+            if wall:
+                torch.cuda.synchronize()
+                t0 = time.perf_counter()
+                fn()
+                torch.cuda.synchronize()
+                ts.append((time.perf_counter() - t0) * 1e3)
+            else:
+                a0, a1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                a0.record(stream)
+                fn()
+                a1.record(stream)
+                torch.cuda.synchronize()
+                ts.append(a0.elapsed_time(a1))
+        return statistics.median(ts)
+
+    try:
+        wr = S.router_weights(E, wl.H, wl.seed, device=dev)
+        wsr = torch.empty(M.mnw_moe_workspace_size_routed(layer, wl.act, T, k) + 256, dtype=torch.uint8, device=dev)
+        outr = torch.empty_like(out)
+        scratch = torch.zeros(lib.mnw_moe_route_scratch_size(T, E) + 256, dtype=torch.uint8, device=dev)
+        routed = lambda: M.mnw_moe_forward_routed(layer, wl.act, x, wr, k, ws=wsr, out=outr)  # noqa: E731
+        variants["routed_forward_ms"] = timed(routed)
+        r_ids = torch.empty((T, k), dtype=torch.int32, device=dev)
+        r_w = torch.empty((T, k), dtype=torch.float32, device=dev)
+        r_off = torch.empty(E + 1, dtype=torch.int32, device=dev)
+        r_sa = torch.empty(P, dtype=torch.int32, device=dev)
+        r_pos = torch.empty(P, dtype=torch.int32, device=dev)
+        r_base = (-scratch.data_ptr()) % 256
+        r_need = lib.mnw_moe_route_scratch_size(T, E)
+
+        def route():
+            chk(lib.mnw_moe_route(ptr(x), ptr(wr), T, wl.H, E, k, ptr(r_ids), ptr(r_w), ptr(r_off), ptr(r_sa),
+                                  ptr(r_pos), ctypes.c_void_p(scratch.data_ptr() + r_base), r_need, ptr(err), sp),
+                "route")
+
+        variants["route_ms"] = timed(route)
+        M.mnw_moe_set_host_routing(True)
+        try:
+            variants["host_routing_forward_ms"] = timed(routed, wall=True)
+        finally:
+            M.mnw_moe_set_host_routing(False)
+    except Exception as ex:  # a shape the router does not take
+        variants["routed_note"] = f"not timed: {ex}"
+    M.mnw_moe_set_fused_activation(False)
+    try:
+        variants["unfused_forward_ms"] = timed(layer_step)
+    finally:
+        M.mnw_moe_set_fused_activation(True)
+    variants["fused_forward_ms"] = timed(layer_step)
+
     touched = int(torch.unique(ids[(ids >= 0) & (ids < E)]).numel())
     return dict(total_ms=total_ms, step_ms=step_ms, gu_ms=gu_ms, launches=launches, world=world, rank=rank,
-                f16_rows=f16_gate_up is not None, graph_ms=graph_ms,
+                f16_rows=f16_gate_up is not None, graph_ms=graph_ms, variants=variants,
                 clocks=clk.summary(), e2e_ms=e2e_ms, touched=touched, ids=ids)
 
 
@@ -550,6 +613,9 @@ def build_line(args, wl: S.Workload, config: dict, r: dict, cpu, traffic) -> dic
         "gpu_launches": r["launches"],
         "clocks": r["clocks"],
     }
+    if r.get("variants"):
+        line["variants"] = {**r["variants"], "note": "comparison paths on the same batch, median ms per forward; "
+                                                      "routed: the router's own expert choice (BF16 weights ~N(0, 1/H))"}
     if r.get("graph_ms"):
         line["graph"] = {"value": r["world"] * wl.T / (r["graph_ms"] / 1e3), "unit": "tokens/s",
                          "ms_per_step_median": r["graph_ms"],
