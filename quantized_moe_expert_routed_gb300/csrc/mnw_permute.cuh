@@ -9,6 +9,47 @@
 
 namespace mnw {
 
+// ids[a0 + 32 b + lane] -> id[b] for b < kB (INT32_MIN at or past a1), with
+// a1 - a0 <= 32 kB.  When ids + a0 is 16-byte aligned the warp reads the
+// range with 16-byte loads (each lane four consecutive ids) and puts it back
+// in lane order through its own window of 32 kB ints of shared memory (16-byte
+// aligned); otherwise with 4-byte loads.  Loads go through L2 (ld.global.cg):
+// the ids may come from other CTAs of the same launch.  Called by all 32
+// lanes of a warp.
+template <int kB>
+__device__ __forceinline__ void load_ids(const int32_t* ids, int a0, int a1, int32_t* win, int (&id)[kB]) {
+  const int lane = threadIdx.x & 31;
+  const int n = a1 - a0;
+  if ((reinterpret_cast<uintptr_t>(ids + a0) & 15u) == 0) {
+#pragma unroll
+    for (int q = 0; q < kB / 4 + (kB % 4 ? 1 : 0); ++q) {
+      const int i = q * 32 + lane;  // 16-byte word i holds ids a0 + 4i .. a0 + 4i + 3
+      if (i < kB * 8 && 4 * i < n) {
+        int4 v;
+        if (4 * i + 3 < n) {
+          v = __ldcg(reinterpret_cast<const int4*>(ids + a0) + i);
+        } else {  // the ragged end: no load past a1
+          v.x = __ldcg(ids + a0 + 4 * i);
+          v.y = 4 * i + 1 < n ? __ldcg(ids + a0 + 4 * i + 1) : INT32_MIN;
+          v.z = 4 * i + 2 < n ? __ldcg(ids + a0 + 4 * i + 2) : INT32_MIN;
+          v.w = INT32_MIN;
+        }
+        reinterpret_cast<int4*>(win)[i] = v;
+      }
+    }
+    __syncwarp();
+#pragma unroll
+    for (int b = 0; b < kB; ++b) id[b] = 32 * b + lane < n ? win[32 * b + lane] : INT32_MIN;
+    __syncwarp();  // the window may be refilled next
+  } else {
+#pragma unroll
+    for (int b = 0; b < kB; ++b) id[b] = 32 * b + lane < n ? __ldcg(ids + a0 + 32 * b + lane) : INT32_MIN;
+  }
+}
+
+// Shared-memory ints before the id windows: n rounded up to a 16-byte boundary.
+__host__ __device__ constexpr int ids_window_base(int n) { return (n + 3) & ~3; }
+
 // The same stable permutation for batches of at most kW * kB * 32
 // assignments (a decode batch: 256 tokens x top-8 = 2048): kW warps, each
 // owning a contiguous segment of at most kB * 32 assignments whose ids and
@@ -17,9 +58,10 @@ namespace mnw {
 // kW * E entries.  Only the tail [valid assignments, P) of sorted_assign is
 // filled with -1.
 // Called by all kW * 32 threads of a CTA (blockDim.x == kW * 32); sm holds
-// (kW + 1) * E ints of shared memory, warp_tot 32 ints, total_valid one.  ids
-// are read through L2 (ld.global.cg), so they may have been written earlier by
-// other CTAs of the same launch (after a fence).
+// permute_block_smem_ints(kW, kB, E) ints of shared memory (16-byte aligned):
+// the count tables, then one id window per warp; warp_tot 32 ints,
+// total_valid one.  ids are read through L2 (ld.global.cg), so they may have
+// been written earlier by other CTAs of the same launch (after a fence).
 template <int kW, int kB>
 __device__ __forceinline__ void permute_block(const int32_t* ids, int P, int E, int32_t* __restrict__ offsets,
                                               int32_t* __restrict__ sorted_assign, int32_t* __restrict__ assign_pos,
@@ -32,15 +74,12 @@ __device__ __forceinline__ void permute_block(const int32_t* ids, int P, int E, 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   for (int i = tid; i < kW * E; i += kThreads) cnt[i] = 0;
 
-  const int seg = (P + kW - 1) / kW;
+  // segments of a multiple of 4 assignments, so that each starts on a 16-byte boundary of ids
+  const int seg = ((P + kW - 1) / kW + 3) & ~3;
   const int a0 = min(P, warp * seg), a1 = min(P, a0 + seg);
   int id[kB];
   uint32_t peers[kB];
-#pragma unroll
-  for (int b = 0; b < kB; ++b) {
-    const int a = a0 + b * 32 + lane;
-    id[b] = a < a1 ? __ldcg(ids + a) : INT32_MIN;
-  }
+  load_ids<kB>(ids, a0, a1, sm + ids_window_base((kW + 1) * E) + warp * kB * 32, id);
   __syncthreads();
 
   // counting pass: per-warp counts, lanes sharing an expert grouped by match-any
@@ -131,6 +170,11 @@ __device__ __forceinline__ void permute_block(const int32_t* ids, int P, int E, 
     __syncwarp();
   }
   for (int p = total_valid + tid; p < P; p += kThreads) sorted_assign[p] = -1;
+}
+
+// Shared-memory ints permute_block needs for kW warps, kB batches and E experts.
+__host__ __device__ constexpr int permute_block_smem_ints(int kW, int kB, int E) {
+  return ids_window_base((kW + 1) * E) + kW * kB * 32;
 }
 
 }  // namespace mnw

@@ -9,7 +9,10 @@
 // first pass counts per (warp, expert) with warp match-any groups, a scan over
 // (expert, warp) turns counts into starting positions, and a second pass
 // re-walks the segment in order, ranking lanes that share an expert by lane
-// index.
+// index.  Each warp reads its ids with 16-byte loads (four consecutive ids a
+// lane) into a window of shared memory and takes them back in lane order
+// (load_ids in mnw_permute.cuh); ids off a 16-byte boundary fall back to
+// 4-byte loads.
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
@@ -29,7 +32,7 @@ __global__ void __launch_bounds__(kPermThreads, 1)
     permute_kernel(const int32_t* __restrict__ ids, int P, int E, int32_t* __restrict__ offsets,
                    int32_t* __restrict__ sorted_assign, int32_t* __restrict__ assign_pos,
                    uint32_t* __restrict__ err) {
-  extern __shared__ int32_t sm[];
+  extern __shared__ __align__(16) int32_t sm[];
   int32_t* cnt = sm;                       // [kPermWarps][E]: counts, then next position
   int32_t* tot = sm + kPermWarps * E;      // [E]
   __shared__ int32_t warp_tot[kPermWarps];
@@ -41,18 +44,16 @@ __global__ void __launch_bounds__(kPermThreads, 1)
   for (int a = tid; a < P; a += kPermThreads) sorted_assign[a] = -1;
   __syncthreads();
 
-  const int seg = (P + kPermWarps - 1) / kPermWarps;
+  // segments of a multiple of 4 assignments: each starts on a 16-byte boundary of ids
+  const int seg = ((P + kPermWarps - 1) / kPermWarps + 3) & ~3;
   const int a0 = min(P, warp * seg), a1 = min(P, a0 + seg);
   int32_t* my = cnt + warp * E;
+  int32_t* win = sm + ids_window_base((kPermWarps + 1) * E) + warp * 32 * kPermBatchesInFlight;
 
   // Pass 1: per-warp counts.
   for (int base = a0; base < a1; base += 32 * kPermBatchesInFlight) {
     int idv[kPermBatchesInFlight];
-#pragma unroll
-    for (int b = 0; b < kPermBatchesInFlight; ++b) {
-      const int a = base + b * 32 + lane;
-      idv[b] = a < a1 ? __ldg(ids + a) : INT32_MIN;
-    }
+    load_ids<kPermBatchesInFlight>(ids, base, min(a1, base + 32 * kPermBatchesInFlight), win, idv);
 #pragma unroll
     for (int b = 0; b < kPermBatchesInFlight; ++b) {
       const int a = base + b * 32 + lane;
@@ -117,11 +118,7 @@ __global__ void __launch_bounds__(kPermThreads, 1)
   const uint32_t lt_mask = (1u << lane) - 1u;
   for (int base = a0; base < a1; base += 32 * kPermBatchesInFlight) {
     int idv[kPermBatchesInFlight];
-#pragma unroll
-    for (int b = 0; b < kPermBatchesInFlight; ++b) {
-      const int a = base + b * 32 + lane;
-      idv[b] = a < a1 ? __ldg(ids + a) : INT32_MIN;
-    }
+    load_ids<kPermBatchesInFlight>(ids, base, min(a1, base + 32 * kPermBatchesInFlight), win, idv);
 #pragma unroll
     for (int b = 0; b < kPermBatchesInFlight; ++b) {
       const int a = base + b * 32 + lane;
@@ -152,7 +149,7 @@ __global__ void __launch_bounds__(kW * 32, 1)
     permute_small_kernel(const int32_t* __restrict__ ids, int P, int E, int32_t* __restrict__ offsets,
                          int32_t* __restrict__ sorted_assign, int32_t* __restrict__ assign_pos,
                          uint32_t* __restrict__ err) {
-  extern __shared__ int32_t sm[];
+  extern __shared__ __align__(16) int32_t sm[];
   __shared__ int32_t warp_tot[32];
   __shared__ int32_t total_valid;
   pdl_launch_dependents();
@@ -179,15 +176,13 @@ struct ChunkIds {
   int id[4];
   uint32_t peers[4];
 };
-__device__ __forceinline__ void chunk_count(const int32_t* ids, int a0, int a1, int E, int32_t* cnt, ChunkIds& c,
-                                            uint32_t* err) {
+// win: this warp's window of 128 ints of shared memory (16-byte aligned).
+__device__ __forceinline__ void chunk_count(const int32_t* ids, int a0, int a1, int E, int32_t* cnt, int32_t* win,
+                                            ChunkIds& c, uint32_t* err) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   int32_t* my = cnt + warp * E;
-#pragma unroll
-  for (int b = 0; b < 4; ++b) {
-    const int a = a0 + (warp * 4 + b) * 32 + lane;
-    c.id[b] = a < a1 ? __ldg(ids + a) : INT32_MIN;
-  }
+  const int w0 = a0 + warp * 128;  // this warp's 128 assignments
+  load_ids<4>(ids, w0, max(w0, min(a1, w0 + 128)), win, c.id);
 #pragma unroll
   for (int b = 0; b < 4; ++b) {
     const int a = a0 + (warp * 4 + b) * 32 + lane;
@@ -204,7 +199,7 @@ __device__ __forceinline__ void chunk_count(const int32_t* ids, int a0, int a1, 
 __global__ void __launch_bounds__(kChunkThreads) permute_count_kernel(const int32_t* __restrict__ ids, int P, int E,
                                                                       int32_t* __restrict__ assign_pos,
                                                                       uint32_t* __restrict__ err) {
-  extern __shared__ int32_t sm[];
+  extern __shared__ __align__(16) int32_t sm[];
   int32_t* cnt = sm;  // [8][E]
   pdl_launch_dependents();
   for (int i = threadIdx.x; i < 8 * E; i += kChunkThreads) cnt[i] = 0;
@@ -212,7 +207,7 @@ __global__ void __launch_bounds__(kChunkThreads) permute_count_kernel(const int3
   __syncthreads();
   const int a0 = blockIdx.x * kChunk, a1 = min(P, a0 + kChunk);
   ChunkIds c;
-  chunk_count(ids, a0, a1, E, cnt, c, err);
+  chunk_count(ids, a0, a1, E, cnt, sm + ids_window_base(8 * E) + (threadIdx.x >> 5) * 128, c, err);
   __syncthreads();
   for (int e = threadIdx.x; e < E; e += kChunkThreads) {
     int t = 0;
@@ -225,7 +220,7 @@ __global__ void __launch_bounds__(kChunkThreads) permute_count_kernel(const int3
 // One CTA of 1024 threads; C * E counts fit in shared memory (checked by the launcher).
 __global__ void __launch_bounds__(1024, 1) permute_scan_kernel(int C, int E, int32_t* __restrict__ assign_pos,
                                                                int32_t* __restrict__ offsets) {
-  extern __shared__ int32_t sm[];
+  extern __shared__ __align__(16) int32_t sm[];
   int32_t* cnt = sm;          // [C][E]
   int32_t* tot = sm + C * E;  // [E]
   __shared__ int32_t warp_tot[32];
@@ -285,7 +280,7 @@ __global__ void __launch_bounds__(kChunkThreads) permute_place_kernel(const int3
                                                                       const int32_t* __restrict__ offsets,
                                                                       int32_t* __restrict__ sorted_assign,
                                                                       int32_t* __restrict__ assign_pos) {
-  extern __shared__ int32_t sm[];
+  extern __shared__ __align__(16) int32_t sm[];
   int32_t* cnt = sm;          // [8][E]: counts, then start of each warp's run
   int32_t* base = sm + 8 * E;  // [E]: first position of this chunk's assignments per expert
   pdl_launch_dependents();
@@ -295,7 +290,7 @@ __global__ void __launch_bounds__(kChunkThreads) permute_place_kernel(const int3
   for (int e = threadIdx.x; e < E; e += kChunkThreads) base[e] = assign_pos[a0 + e];
   __syncthreads();  // starts read before this chunk's positions overwrite them
   ChunkIds c;
-  chunk_count(ids, a0, a1, E, cnt, c, nullptr);
+  chunk_count(ids, a0, a1, E, cnt, sm + ids_window_base(9 * E) + (threadIdx.x >> 5) * 128, c, nullptr);
   __syncthreads();
   for (int e = threadIdx.x; e < E; e += kChunkThreads) {
     int run = base[e];
@@ -455,6 +450,12 @@ __global__ void __launch_bounds__(256) combine_kernel(const uint4* __restrict__ 
   }
 }
 
+// permute_kernel: count tables for E experts, then one id window per warp.
+static size_t perm_kernel_smem(int E) {
+  return (static_cast<size_t>(ids_window_base((kPermWarps + 1) * E)) + kPermWarps * 32 * kPermBatchesInFlight) *
+         sizeof(int32_t);
+}
+
 static int grid_for(int rows_per_block, int n, int cap) {
   int g = (n + rows_per_block - 1) / rows_per_block;
   return g < 1 ? 1 : (g > cap ? cap : g);
@@ -469,10 +470,10 @@ cudaError_t launch_permute(const int32_t* ids, int T, int k, int E, int32_t* off
   if (attrs_needed(attr, &bit)) {
     // tables for up to E = 1024 experts
     cudaError_t e = cudaFuncSetAttribute(permute_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         static_cast<int>((kPermWarps + 1) * 1024 * sizeof(int32_t)));
+                                         static_cast<int>(perm_kernel_smem(1024)));
     if (e == cudaSuccess)
       e = cudaFuncSetAttribute(permute_small_kernel<16, 16>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                               static_cast<int>(17 * 1024 * sizeof(int32_t)));
+                               static_cast<int>(permute_block_smem_ints(16, 16, 1024) * sizeof(int32_t)));
     if (e == cudaSuccess)
       e = cudaFuncSetAttribute(permute_scan_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                static_cast<int>((48 * 1024) * sizeof(int32_t)));
@@ -481,17 +482,19 @@ cudaError_t launch_permute(const int32_t* ids, int T, int k, int E, int32_t* off
   }
   cudaError_t e;
   if (P <= 8 * 8 * 32) {
-    e = launch_pdl(permute_small_kernel<8, 8>, dim3(1), dim3(8 * 32), static_cast<size_t>(9) * E * sizeof(int32_t), st,
-                   ids, P, E, offsets, sorted_assign, assign_pos, err);
+    e = launch_pdl(permute_small_kernel<8, 8>, dim3(1), dim3(8 * 32),
+                   static_cast<size_t>(permute_block_smem_ints(8, 8, E)) * sizeof(int32_t), st, ids, P, E, offsets,
+                   sorted_assign, assign_pos, err);
   } else if (P <= 16 * 16 * 32) {
-    e = launch_pdl(permute_small_kernel<16, 16>, dim3(1), dim3(16 * 32), static_cast<size_t>(17) * E * sizeof(int32_t),
-                   st, ids, P, E, offsets, sorted_assign, assign_pos, err);
+    e = launch_pdl(permute_small_kernel<16, 16>, dim3(1), dim3(16 * 32),
+                   static_cast<size_t>(permute_block_smem_ints(16, 16, E)) * sizeof(int32_t), st, ids, P, E, offsets,
+                   sorted_assign, assign_pos, err);
   } else if (static_cast<long long>((P + kChunk - 1) / kChunk) * E + E <= 48 * 1024 && E <= kChunk &&
              (P % kChunk == 0 || P % kChunk >= E)) {
     // (every chunk, the last included, has room for its E counts in its own slice)
     // many CTAs: count, scan (counts of all chunks in shared memory), place
     const int C = (P + kChunk - 1) / kChunk;
-    const size_t chunk_smem = static_cast<size_t>(9) * E * sizeof(int32_t);
+    const size_t chunk_smem = (static_cast<size_t>(ids_window_base(9 * E)) + 8 * 128) * sizeof(int32_t);
     const size_t scan_smem = (static_cast<size_t>(C) * E + E) * sizeof(int32_t);
     e = launch_pdl(permute_count_kernel, dim3(C), dim3(kChunkThreads), chunk_smem, st, ids, P, E, assign_pos, err);
     if (e == cudaSuccess)
@@ -500,8 +503,8 @@ cudaError_t launch_permute(const int32_t* ids, int T, int k, int E, int32_t* off
       e = launch_pdl(permute_place_kernel, dim3(C), dim3(kChunkThreads), chunk_smem, st, ids, P, E,
                      static_cast<const int32_t*>(offsets), sorted_assign, assign_pos);
   } else {
-    e = launch_pdl(permute_kernel, dim3(1), dim3(kPermThreads), static_cast<size_t>(kPermWarps + 1) * E * sizeof(int32_t),
-                   st, ids, P, E, offsets, sorted_assign, assign_pos, err);
+    e = launch_pdl(permute_kernel, dim3(1), dim3(kPermThreads), perm_kernel_smem(E), st, ids, P, E, offsets,
+                   sorted_assign, assign_pos, err);
   }
   if (e != cudaSuccess) return e;
   if (x && x_perm && P > 0) e = launch_gather_rows(x, H, sorted_assign, P, k, x_perm, st);

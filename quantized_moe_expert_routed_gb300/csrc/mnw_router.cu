@@ -246,8 +246,8 @@ static cudaError_t launch_route_t(const void* x, const void* wr, int T, int H, i
                                   int32_t* assign_pos, uint32_t* counters, uint32_t* err, bool fuse, bool logits_only,
                                   cudaStream_t st) {
   constexpr size_t kRed = static_cast<size_t>(kRtWarps) * kRtTok * kMT * kRtRow * 4;
-  constexpr size_t kPermMax = static_cast<size_t>(kRtWarps + 1) * kRtMaxE * 4;
-  const size_t perm_bytes = fuse ? static_cast<size_t>(kRtWarps + 1) * E * 4 : 0;
+  constexpr size_t kPermMax = static_cast<size_t>(permute_block_smem_ints(kRtWarps, kRtPermB, kRtMaxE)) * 4;
+  const size_t perm_bytes = fuse ? static_cast<size_t>(permute_block_smem_ints(kRtWarps, kRtPermB, E)) * 4 : 0;
   const size_t smem = kRed > perm_bytes ? kRed : perm_bytes;
   static std::atomic<uint64_t> attr{0};
   uint64_t bit;

@@ -77,6 +77,24 @@ def test_permute_duplicate_ids_bitexact(M, T, k, E):
     assert np.array_equal(pos.cpu().numpy(), o_pos)
 
 
+@pytest.mark.parametrize("T,k,E", [(64, 8, 16), (37, 3, 4), (512, 8, 64), (2048, 8, 256), (1030, 9, 256)])
+@pytest.mark.parametrize("shift", [1, 2, 3])
+def test_permute_unaligned_ids_bitexact(M, T, k, E, shift):
+    """ids that start off a 16-byte boundary (the kernels then read them with
+    4-byte loads) give the same permutation as aligned ones and the oracle."""
+    ids = _ids_with_duplicates(T, k, E, seed=T * 17 + E + shift)
+    buf = torch.full((T * k + 8,), -7, dtype=torch.int32, device=DEV)
+    view = buf[shift:shift + T * k].view(T, k)
+    view.copy_(ids.to(DEV))
+    assert view.data_ptr() % 16 != 0
+    off, sa, pos, _ = M.mnw_moe_permute(view, E)
+    o_off, o_sa, o_pos, dropped = O.permute(ids.numpy(), E)
+    assert dropped == 0
+    assert np.array_equal(off.cpu().numpy(), o_off)
+    assert np.array_equal(sa.cpu().numpy(), o_sa)
+    assert np.array_equal(pos.cpu().numpy(), o_pos)
+
+
 @pytest.mark.parametrize("R,K,gather", [(1, 128, False), (37, 512, False), (300, 2048, True)])
 def test_quantize_int8_bitexact(M, R, K, gather):
     x = S.activations(R, K, seed=R, outlier_p=0.01)
