@@ -4,10 +4,14 @@
 //
 //  INT8 per 128 ("LLaDA2.2-flash-minnow" model card, W8A8/W4A8 paragraph):
 //    scale = amax / 127, code = clamp(rne(x / scale), -127, 127); amax 0 gives
-//    scale 0 and codes 0.  One warp per (row, 128-group), 4 values per lane.
+//    scale 0 and codes 0.
 //  NVFP4 (model card, NVFP4 row, activation column): outer = amax_row / 2688,
-//    sb = e4m3(amax_16 / outer / 6), code = e2m1(x / (sb * outer)).  One warp
-//    per row; lane l handles 16-blocks l, l+32, ...
+//    sb = e4m3(amax_16 / outer / 6), code = e2m1(x / (sb * outer)).
+// Rows of up to 1024 values: one warp per row, the whole row loaded first
+// with 16-byte loads (lane l holds 16-byte words l, l + 32, ...), so a warp
+// has its row's bytes in flight at once; the group or block maxima are warp
+// reductions over the lanes that hold the group.  Longer rows: one warp per
+// (row, 128-group) for INT8, and a two-pass warp per row for NVFP4.
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
@@ -170,8 +174,211 @@ __global__ void __launch_bounds__(256) quant_nvfp4_g16_kernel(const __nv_bfloat1
   }
 }
 
+// ---- rows of up to 32 * 8 * kU values, one warp per row, held in registers ----
+
+// The destination rows of source row r: lane j < index_div holds
+// row_index[r * index_div + j] (kScatter), else only r itself.
+template <bool kScatter>
+__device__ __forceinline__ int dest_of_lane(int r, const int32_t* row_index, int index_div, int lane) {
+  if (!kScatter) return lane == 0 ? r : -1;
+  return lane < index_div ? __ldg(row_index + static_cast<size_t>(r) * index_div + lane) : -1;
+}
+
+__device__ __forceinline__ void bf16x8_to_float(const uint4& q, float (&v)[8]) {
+  const uint32_t w[4] = {q.x, q.y, q.z, q.w};
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const float2 f = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&w[i]));
+    v[2 * i] = f.x;
+    v[2 * i + 1] = f.y;
+  }
+}
+
+// INT8 per 128: word i of the row (8 values) belongs to group i / 16, so the
+// lanes of a half-warp hold one group per word slot.  index_div <= 32 when kScatter.
+template <bool kScatter, int kU>
+__global__ void __launch_bounds__(256) quant_int8_rows_kernel(const __nv_bfloat16* __restrict__ x, int R, int K,
+                                                              const int32_t* __restrict__ row_index,
+                                                              int index_div, int8_t* __restrict__ codes,
+                                                              float* __restrict__ scales) {
+  pdl_launch_dependents();
+  pdl_wait();
+  const int lane = threadIdx.x & 31;
+  const int K8 = K / 8, G = K / 128;
+  for (int r = blockIdx.x * 8 + (threadIdx.x >> 5); r < R; r += gridDim.x * 8) {
+    const int src = kScatter ? r : source_row(r, row_index, index_div);
+    const uint4* xr = reinterpret_cast<const uint4*>(x) + static_cast<size_t>(src < 0 ? 0 : src) * K8;
+    uint4 raw[kU];
+#pragma unroll
+    for (int u = 0; u < kU; ++u) {
+      const int i = u * 32 + lane;
+      raw[u] = (src >= 0 && i < K8) ? __ldg(xr + i) : make_uint4(0u, 0u, 0u, 0u);
+    }
+    const int my_dst = dest_of_lane<kScatter>(r, row_index, index_div, lane);
+    const int ndst = kScatter ? index_div : 1;
+#pragma unroll
+    for (int u = 0; u < kU; ++u) {
+      if (u * 32 >= K8) break;  // (uniform)
+      const int i = u * 32 + lane;
+      float v[8];
+      bf16x8_to_float(raw[u], v);
+      float amax = 0.f;
+#pragma unroll
+      for (int e = 0; e < 8; ++e) amax = fmaxf(amax, fabsf(v[e]));
+#pragma unroll
+      for (int d = 8; d > 0; d >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, d));
+      uint2 packed = make_uint2(0u, 0u);
+      float scale = 0.f;
+      if (amax > 0.f) {
+        scale = __fdiv_rn(amax, 127.0f);
+        uint32_t lo = 0, hi = 0;
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const int q0 = max(-127, min(127, __float2int_rn(__fdiv_rn(v[e], scale))));
+          const int q1 = max(-127, min(127, __float2int_rn(__fdiv_rn(v[4 + e], scale))));
+          lo |= (static_cast<uint32_t>(q0) & 0xFFu) << (8 * e);
+          hi |= (static_cast<uint32_t>(q1) & 0xFFu) << (8 * e);
+        }
+        packed = make_uint2(lo, hi);
+      }
+      const int g = i >> 4;
+      for (int j = 0; j < ndst; ++j) {
+        const int d = __shfl_sync(0xffffffffu, my_dst, j);
+        if (d < 0 || i >= K8) continue;
+        reinterpret_cast<uint2*>(codes + static_cast<size_t>(d) * K)[i] = packed;
+        if ((lane & 15) == 0) scales[static_cast<size_t>(d) * G + g] = scale;
+      }
+    }
+  }
+}
+
+// NVFP4: 16-block b of the row is words 2b, 2b + 1; lane l holds blocks
+// l, l + 32, ... (two consecutive words each).  index_div <= 32 when kScatter.
+template <bool kScatter, int kU>
+__global__ void __launch_bounds__(256) quant_nvfp4_rows_kernel(const __nv_bfloat16* __restrict__ x, int R, int K,
+                                                               const int32_t* __restrict__ row_index,
+                                                               int index_div, uint8_t* __restrict__ codes,
+                                                               uint8_t* __restrict__ sf, float* __restrict__ outer) {
+  static_assert(kU % 2 == 0, "two words per block");
+  pdl_launch_dependents();
+  pdl_wait();
+  const int lane = threadIdx.x & 31;
+  const int K8 = K / 8, nb = K / 16;
+  for (int r = blockIdx.x * 8 + (threadIdx.x >> 5); r < R; r += gridDim.x * 8) {
+    const int src = kScatter ? r : source_row(r, row_index, index_div);
+    const uint4* xr = reinterpret_cast<const uint4*>(x) + static_cast<size_t>(src < 0 ? 0 : src) * K8;
+    uint4 raw[kU];
+#pragma unroll
+    for (int u = 0; u < kU / 2; ++u) {
+      const int b = u * 32 + lane;
+      const bool ok = src >= 0 && b < nb;
+      raw[2 * u] = ok ? __ldg(xr + 2 * b) : make_uint4(0u, 0u, 0u, 0u);
+      raw[2 * u + 1] = ok ? __ldg(xr + 2 * b + 1) : make_uint4(0u, 0u, 0u, 0u);
+    }
+    const int my_dst = dest_of_lane<kScatter>(r, row_index, index_div, lane);
+    const int ndst = kScatter ? index_div : 1;
+    float bmax[kU / 2];
+    float amax = 0.f;
+#pragma unroll
+    for (int u = 0; u < kU / 2; ++u) {
+      float v[8], w[8];
+      bf16x8_to_float(raw[2 * u], v);
+      bf16x8_to_float(raw[2 * u + 1], w);
+      float m = 0.f;
+#pragma unroll
+      for (int e = 0; e < 8; ++e) m = fmaxf(m, fmaxf(fabsf(v[e]), fabsf(w[e])));
+      bmax[u] = m;
+      amax = fmaxf(amax, m);
+    }
+#pragma unroll
+    for (int d = 16; d > 0; d >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, d));
+    const float o = __fdiv_rn(amax, 2688.0f);
+    for (int j = 0; j < ndst; ++j) {
+      const int d = __shfl_sync(0xffffffffu, my_dst, j);
+      if (d >= 0 && lane == 0) outer[d] = o;
+    }
+#pragma unroll
+    for (int u = 0; u < kU / 2; ++u) {
+      if (u * 32 >= nb) break;  // (uniform)
+      const int b = u * 32 + lane;
+      uint2 packed = make_uint2(0u, 0u);
+      uint8_t sbyte = 0;
+      if (o != 0.f) {
+        float v[16];
+        {
+          float lo8[8], hi8[8];
+          bf16x8_to_float(raw[2 * u], lo8);
+          bf16x8_to_float(raw[2 * u + 1], hi8);
+#pragma unroll
+          for (int e = 0; e < 8; ++e) {
+            v[e] = lo8[e];
+            v[8 + e] = hi8[e];
+          }
+        }
+        sbyte = e4m3_rn_satfinite(__fdiv_rn(__fdiv_rn(bmax[u], o), 6.0f));
+        const float dd = __fmul_rn(e4m3_to_float(sbyte), o);
+        if (dd != 0.f) {
+          uint32_t lo = 0, hi = 0;
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            lo |= e2m1x2_rn_satfinite(__fdiv_rn(v[2 * e], dd), __fdiv_rn(v[2 * e + 1], dd)) << (8 * e);
+            hi |= e2m1x2_rn_satfinite(__fdiv_rn(v[8 + 2 * e], dd), __fdiv_rn(v[8 + 2 * e + 1], dd)) << (8 * e);
+          }
+          packed = make_uint2(lo, hi);
+        }
+      }
+      for (int j = 0; j < ndst; ++j) {
+        const int d = __shfl_sync(0xffffffffu, my_dst, j);
+        if (d < 0 || b >= nb) continue;
+        reinterpret_cast<uint2*>(codes + static_cast<size_t>(d) * (K / 2))[b] = packed;
+        sf[static_cast<size_t>(d) * nb + b] = sbyte;
+      }
+    }
+  }
+}
+
+// 16-byte words per lane for a row of K values (0: the row kernels do not take
+// it).  Measured on GB300 (NVFP4, 8192-token prefill): rows of 512 values
+// 30.5 -> 27 us with the row kernel; rows of 2048 (8 words a lane, ~90
+// registers, 16 warps per SM) 23 -> 29 us, the divisions then wanting more
+// warps than the registers leave, so longer rows keep the other kernels.
+static int rows_words_per_lane(int K, int index_div, bool scatter) {
+  if (scatter && index_div > 32) return 0;
+  const int w = (K / 8 + 31) / 32;
+  if (w <= 2) return 2;
+  if (w <= 4) return 4;
+  return 0;
+}
+
+template <bool kScatter>
+static cudaError_t launch_quant_rows(int act, int kU, const void* x, int R, int K, const int32_t* row_index,
+                                     int index_div, void* codes, void* scales, float* row_outer, cudaStream_t st) {
+  const int sms = current_sm_count();
+  long long blocks = (static_cast<long long>(R) + 7) / 8;
+  if (blocks > static_cast<long long>(sms) * 16) blocks = static_cast<long long>(sms) * 16;
+  if (blocks < 1) blocks = 1;
+  const dim3 grid(static_cast<int>(blocks)), block(256);
+  const auto* xb = static_cast<const __nv_bfloat16*>(x);
+  if (act == MNW_ACT_INT8_G128) {
+    auto* c = static_cast<int8_t*>(codes);
+    auto* sc = static_cast<float*>(scales);
+    switch (kU) {
+      case 2: return launch_pdl(quant_int8_rows_kernel<kScatter, 2>, grid, block, 0, st, xb, R, K, row_index, index_div, c, sc);
+      default: return launch_pdl(quant_int8_rows_kernel<kScatter, 4>, grid, block, 0, st, xb, R, K, row_index, index_div, c, sc);
+    }
+  }
+  auto* c = static_cast<uint8_t*>(codes);
+  auto* sfp = static_cast<uint8_t*>(scales);
+  switch (kU) {
+    case 2: return launch_pdl(quant_nvfp4_rows_kernel<kScatter, 2>, grid, block, 0, st, xb, R, K, row_index, index_div, c, sfp, row_outer);
+    default: return launch_pdl(quant_nvfp4_rows_kernel<kScatter, 4>, grid, block, 0, st, xb, R, K, row_index, index_div, c, sfp, row_outer);
+  }
+}
+
 cudaError_t launch_quantize(int act, const void* x, int R, int K, const int32_t* row_index, int index_div,
                             void* codes, void* scales, float* row_outer, cudaStream_t st) {
+  if (const int kU = rows_words_per_lane(K, index_div, false))
+    return launch_quant_rows<false>(act, kU, x, R, K, row_index, index_div, codes, scales, row_outer, st);
   const int sms = current_sm_count();
   if (act == MNW_ACT_INT8_G128) {
     const long long warps = static_cast<long long>(R) * (K / 128);
@@ -194,6 +401,8 @@ cudaError_t launch_quantize(int act, const void* x, int R, int K, const int32_t*
 
 cudaError_t launch_quantize_scatter(int act, const void* x, int R, int K, const int32_t* row_index, int index_div,
                             void* codes, void* scales, float* row_outer, cudaStream_t st) {
+  if (const int kU = rows_words_per_lane(K, index_div, true))
+    return launch_quant_rows<true>(act, kU, x, R, K, row_index, index_div, codes, scales, row_outer, st);
   const int sms = current_sm_count();
   if (act == MNW_ACT_INT8_G128) {
     const long long warps = static_cast<long long>(R) * (K / 128);

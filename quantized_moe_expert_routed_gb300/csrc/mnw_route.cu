@@ -227,9 +227,18 @@ __global__ void __launch_bounds__(1024, 1) permute_scan_kernel(int C, int E, int
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   pdl_launch_dependents();
   pdl_wait();
-  for (int i = tid; i < C * E; i += 1024) {
-    const int c = i / E, e = i - c * E;
-    cnt[i] = assign_pos[c * kChunk + e];
+  // the counts come from L2: eight loads in flight per thread, then the stores
+  for (int i0 = tid; i0 < C * E; i0 += 8 * 1024) {
+    int v[8];
+#pragma unroll
+    for (int u = 0; u < 8; ++u) {
+      const int i = i0 + u * 1024;
+      const int c = i / E, e = i - c * E;
+      v[u] = i < C * E ? assign_pos[c * kChunk + e] : 0;
+    }
+#pragma unroll
+    for (int u = 0; u < 8; ++u)
+      if (i0 + u * 1024 < C * E) cnt[i0 + u * 1024] = v[u];
   }
   __syncthreads();
   for (int e = tid; e < E; e += 1024) {

@@ -95,7 +95,11 @@ def test_permute_unaligned_ids_bitexact(M, T, k, E, shift):
     assert np.array_equal(pos.cpu().numpy(), o_pos)
 
 
-@pytest.mark.parametrize("R,K,gather", [(1, 128, False), (37, 512, False), (300, 2048, True)])
+# K: rows of up to 1024 values (a row per warp in registers, one to four
+# 16-byte words per lane), odd group counts, and longer rows (one warp per
+# 128-group)
+@pytest.mark.parametrize("R,K,gather", [(1, 128, False), (37, 512, False), (300, 2048, True), (5, 384, False),
+                                        (9, 1024, False), (40, 1536, True), (3, 4096, False), (2, 4352, False)])
 def test_quantize_int8_bitexact(M, R, K, gather):
     x = S.activations(R, K, seed=R, outlier_p=0.01)
     x[min(3, R - 1), :128] = 0  # an all-zero group
@@ -118,7 +122,10 @@ def test_quantize_int8_bitexact(M, R, K, gather):
     assert np.array_equal(scales.cpu().numpy().view(np.uint32), osc.view(np.uint32))
 
 
-@pytest.mark.parametrize("R,K,gather", [(1, 256, False), (29, 512, False), (200, 2048, True)])
+# K: blocks that do not fill the last lane pass (272), rows of up to 1024
+# values (a row per warp in registers) and longer rows (the two-pass kernel)
+@pytest.mark.parametrize("R,K,gather", [(1, 256, False), (29, 512, False), (200, 2048, True), (4, 272, False),
+                                        (16, 1024, True), (3, 4096, False), (2, 4608, False)])
 def test_quantize_nvfp4_bitexact(M, R, K, gather):
     x = S.activations(R, K, seed=R + 1)
     x[0, 5] = -1e-6        # tiny negative: rounds to E2M1 zero, sign kept
