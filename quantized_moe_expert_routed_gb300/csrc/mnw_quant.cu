@@ -10,8 +10,10 @@
 // Rows of up to 1024 values: one warp per row, the whole row loaded first
 // with 16-byte loads (lane l holds 16-byte words l, l + 32, ...), so a warp
 // has its row's bytes in flight at once; the group or block maxima are warp
-// reductions over the lanes that hold the group.  Longer rows: one warp per
-// (row, 128-group) for INT8, and a two-pass warp per row for NVFP4.
+// reductions over the lanes that hold the group.  Longer INT8 rows: chunks of
+// up to 512 values, one warp each; longer NVFP4 rows: a two-pass warp per row
+// (four or eight warps per row meeting in shared memory for the row's maximum
+// measured no faster on the 2048-value rows of the prefill batch).
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
@@ -194,20 +196,25 @@ __device__ __forceinline__ void bf16x8_to_float(const uint4& q, float (&v)[8]) {
   }
 }
 
-// INT8 per 128: word i of the row (8 values) belongs to group i / 16, so the
-// lanes of a half-warp hold one group per word slot.  index_div <= 32 when kScatter.
+// INT8 per 128: a warp takes one chunk of nch per row (Kc = K / nch values, a
+// multiple of 128); word i of the chunk (8 values) belongs to the chunk's
+// group i / 16, so the lanes of a half-warp hold one group per word slot.
+// index_div <= 32 when kScatter.
 template <bool kScatter, int kU>
 __global__ void __launch_bounds__(256) quant_int8_rows_kernel(const __nv_bfloat16* __restrict__ x, int R, int K,
-                                                              const int32_t* __restrict__ row_index,
+                                                              int nch, const int32_t* __restrict__ row_index,
                                                               int index_div, int8_t* __restrict__ codes,
                                                               float* __restrict__ scales) {
   pdl_launch_dependents();
   pdl_wait();
   const int lane = threadIdx.x & 31;
-  const int K8 = K / 8, G = K / 128;
-  for (int r = blockIdx.x * 8 + (threadIdx.x >> 5); r < R; r += gridDim.x * 8) {
+  const int Kc = K / nch, K8 = Kc / 8, G = K / 128;
+  const int items = R * nch;  // (< 2^31: checked by the launcher)
+  for (int wi = blockIdx.x * 8 + (threadIdx.x >> 5); wi < items; wi += gridDim.x * 8) {
+    const int r = nch == 1 ? wi : wi / nch;
+    const int c0 = (wi - r * nch) * Kc;  // the chunk's first value
     const int src = kScatter ? r : source_row(r, row_index, index_div);
-    const uint4* xr = reinterpret_cast<const uint4*>(x) + static_cast<size_t>(src < 0 ? 0 : src) * K8;
+    const uint4* xr = reinterpret_cast<const uint4*>(x + static_cast<size_t>(src < 0 ? 0 : src) * K + c0);
     uint4 raw[kU];
 #pragma unroll
     for (int u = 0; u < kU; ++u) {
@@ -241,11 +248,11 @@ __global__ void __launch_bounds__(256) quant_int8_rows_kernel(const __nv_bfloat1
         }
         packed = make_uint2(lo, hi);
       }
-      const int g = i >> 4;
+      const int g = c0 / 128 + (i >> 4);
       for (int j = 0; j < ndst; ++j) {
         const int d = __shfl_sync(0xffffffffu, my_dst, j);
         if (d < 0 || i >= K8) continue;
-        reinterpret_cast<uint2*>(codes + static_cast<size_t>(d) * K)[i] = packed;
+        reinterpret_cast<uint2*>(codes + static_cast<size_t>(d) * K + c0)[i] = packed;
         if ((lane & 15) == 0) scales[static_cast<size_t>(d) * G + g] = scale;
       }
     }
@@ -350,11 +357,24 @@ static int rows_words_per_lane(int K, int index_div, bool scatter) {
   return 0;
 }
 
+// INT8 rows of more than 1024 values are cut into chunks of 512 (or 256, or
+// 128) values, one warp each: the groups are independent.
+static int int8_chunks(int K) {
+  if (K <= 1024) return 1;
+  if (K % 512 == 0) return K / 512;
+  if (K % 256 == 0) return K / 256;
+  return K / 128;
+}
+
+// The chunked INT8 kernel counts its (row, chunk) items in 32 bits.
+static bool int8_items_fit(int R, int K) { return static_cast<long long>(R) * int8_chunks(K) < (1LL << 31); }
+
 template <bool kScatter>
 static cudaError_t launch_quant_rows(int act, int kU, const void* x, int R, int K, const int32_t* row_index,
                                      int index_div, void* codes, void* scales, float* row_outer, cudaStream_t st) {
   const int sms = current_sm_count();
-  long long blocks = (static_cast<long long>(R) + 7) / 8;
+  const int nch = act == MNW_ACT_INT8_G128 ? int8_chunks(K) : 1;
+  long long blocks = (static_cast<long long>(R) * nch + 7) / 8;
   if (blocks > static_cast<long long>(sms) * 16) blocks = static_cast<long long>(sms) * 16;
   if (blocks < 1) blocks = 1;
   const dim3 grid(static_cast<int>(blocks)), block(256);
@@ -362,9 +382,9 @@ static cudaError_t launch_quant_rows(int act, int kU, const void* x, int R, int 
   if (act == MNW_ACT_INT8_G128) {
     auto* c = static_cast<int8_t*>(codes);
     auto* sc = static_cast<float*>(scales);
-    switch (kU) {
-      case 2: return launch_pdl(quant_int8_rows_kernel<kScatter, 2>, grid, block, 0, st, xb, R, K, row_index, index_div, c, sc);
-      default: return launch_pdl(quant_int8_rows_kernel<kScatter, 4>, grid, block, 0, st, xb, R, K, row_index, index_div, c, sc);
+    switch (K / nch <= 512 ? 2 : 4) {  // 16-byte words per lane for a chunk
+      case 2: return launch_pdl(quant_int8_rows_kernel<kScatter, 2>, grid, block, 0, st, xb, R, K, nch, row_index, index_div, c, sc);
+      default: return launch_pdl(quant_int8_rows_kernel<kScatter, 4>, grid, block, 0, st, xb, R, K, nch, row_index, index_div, c, sc);
     }
   }
   auto* c = static_cast<uint8_t*>(codes);
@@ -377,6 +397,8 @@ static cudaError_t launch_quant_rows(int act, int kU, const void* x, int R, int 
 
 cudaError_t launch_quantize(int act, const void* x, int R, int K, const int32_t* row_index, int index_div,
                             void* codes, void* scales, float* row_outer, cudaStream_t st) {
+  if (act == MNW_ACT_INT8_G128 && int8_items_fit(R, K))  // (the chunk decides the words per lane)
+    return launch_quant_rows<false>(act, 0, x, R, K, row_index, index_div, codes, scales, row_outer, st);
   if (const int kU = rows_words_per_lane(K, index_div, false))
     return launch_quant_rows<false>(act, kU, x, R, K, row_index, index_div, codes, scales, row_outer, st);
   const int sms = current_sm_count();
@@ -401,6 +423,8 @@ cudaError_t launch_quantize(int act, const void* x, int R, int K, const int32_t*
 
 cudaError_t launch_quantize_scatter(int act, const void* x, int R, int K, const int32_t* row_index, int index_div,
                             void* codes, void* scales, float* row_outer, cudaStream_t st) {
+  if (act == MNW_ACT_INT8_G128 && index_div <= 32 && int8_items_fit(R, K))
+    return launch_quant_rows<true>(act, 0, x, R, K, row_index, index_div, codes, scales, row_outer, st);
   if (const int kU = rows_words_per_lane(K, index_div, true))
     return launch_quant_rows<true>(act, kU, x, R, K, row_index, index_div, codes, scales, row_outer, st);
   const int sms = current_sm_count();

@@ -96,8 +96,8 @@ def test_permute_unaligned_ids_bitexact(M, T, k, E, shift):
 
 
 # K: rows of up to 1024 values (a row per warp in registers, one to four
-# 16-byte words per lane), odd group counts, and longer rows (one warp per
-# 128-group)
+# 16-byte words per lane), odd group counts, and longer rows cut into chunks
+# of 512 (2048, 4096) or 256 values (4352)
 @pytest.mark.parametrize("R,K,gather", [(1, 128, False), (37, 512, False), (300, 2048, True), (5, 384, False),
                                         (9, 1024, False), (40, 1536, True), (3, 4096, False), (2, 4352, False)])
 def test_quantize_int8_bitexact(M, R, K, gather):
@@ -125,7 +125,8 @@ def test_quantize_int8_bitexact(M, R, K, gather):
 # K: blocks that do not fill the last lane pass (272), rows of up to 1024
 # values (a row per warp in registers) and longer rows (the two-pass kernel)
 @pytest.mark.parametrize("R,K,gather", [(1, 256, False), (29, 512, False), (200, 2048, True), (4, 272, False),
-                                        (16, 1024, True), (3, 4096, False), (2, 4608, False)])
+                                        (16, 1024, True), (3, 4096, False), (2, 4608, False), (5, 1536, False),
+                                        (11, 1040, False), (9, 2048, False)])
 def test_quantize_nvfp4_bitexact(M, R, K, gather):
     x = S.activations(R, K, seed=R + 1)
     x[0, 5] = -1e-6        # tiny negative: rounds to E2M1 zero, sign kept
