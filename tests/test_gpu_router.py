@@ -75,10 +75,12 @@ def _check_route(M, x, wr, k, scratch=None):
 
 
 # (T, H, E, k): one 32-token decode block, the 256-token decode batch, a
-# ragged batch, tiny, and one above 4096 assignments (the permutation then
-# runs in its own launches)
+# ragged batch, tiny, one above 4096 assignments (the permutation then runs
+# in its own launches), 1024 experts, and batches of 1024 tokens or more
+# (32-token tiles), with up to 256 and with more than 256 experts
 @pytest.mark.parametrize("T,H,E,k", [(32, 2048, 256, 8), (256, 2048, 256, 8), (300, 512, 64, 4), (5, 256, 8, 2),
-                                     (700, 512, 256, 8), (64, 1024, 1024, 8), (17, 128, 40, 1)])
+                                     (700, 512, 256, 8), (64, 1024, 1024, 8), (17, 128, 40, 1),
+                                     (1100, 512, 256, 4), (1030, 256, 600, 2), (1024, 128, 16, 2)])
 def test_route_matches_oracle(M, T, H, E, k):
     x = S.activations(T, H, seed=T + E).to(DEV)
     wr = S.router_weights(E, H, seed=H + k).to(DEV)
