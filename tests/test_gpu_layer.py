@@ -50,6 +50,17 @@ def test_small_versions_full(M, name):
     _run(M, wl, scale_down=small)
 
 
+@pytest.mark.parametrize("wfmt,act", [(S.FMT_BF16, S.ACT_BF16), (S.FMT_INT8_G128, S.ACT_BF16),
+                                      (S.FMT_INT4_G128, S.ACT_BF16), (S.FMT_INT8_G128, S.ACT_INT8_G128),
+                                      (S.FMT_INT4_G128, S.ACT_INT8_G128), (S.FMT_NVFP4_G16, S.ACT_NVFP4_G16)])
+@pytest.mark.parametrize("T,E,k", [(1, 8, 8), (1, 1, 1), (3, 4, 1)])
+def test_degenerate_shapes(M, wfmt, act, T, E, k):
+    """One token routed to every expert, a single expert, and three tokens of
+    top-1 over four experts (some experts empty): every format and mode."""
+    wl = S.Workload("degenerate", T, 256, E, 256, k, wfmt, act, 0.02, "uniform", 70 + T + E + k)
+    _run(M, wl)
+
+
 @pytest.mark.parametrize("name,nrows", [("decode_w4a16", 16), ("w8a8_2048", 8), ("prefill_nvfp4", 8),
                                         ("large_w4a16", 3), ("large_bf16", 3)])
 def test_full_size_sampled(M, name, nrows):
