@@ -339,6 +339,11 @@ int mnw_moe_layer_init(const void* header_host, const void* blob_dev, size_t blo
       const uint32_t box[3] = {128, 128, 1};
       ok = encode_map(&L.tm_codes[m], CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, experts + L.codes_off[m], dims, strides, box,
                       CU_TENSOR_MAP_SWIZZLE_128B);
+      if (ok && L.wfmt == MNW_FMT_INT4_G128) {  // the warp-MMA kernel's one-group stages
+        const uint32_t box64[3] = {64, 128, 1};
+        ok = encode_map(&L.tm_codes64[m], CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, experts + L.codes_off[m], dims, strides,
+                        box64, CU_TENSOR_MAP_SWIZZLE_64B);
+      }
     }
     if (ok && L.wfmt == MNW_FMT_NVFP4_G16) {
       const uint64_t dims[3] = {K / 16, N, static_cast<uint64_t>(L.E)};

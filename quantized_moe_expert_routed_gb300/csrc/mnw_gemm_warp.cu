@@ -74,11 +74,13 @@ int run_gemm_warp(const mnw_moe_layer* L, int wfmt, int act, int kind, const voi
   a.N = N;
   a.BN = BN;
   a.n_blocks = gu ? N / kRowsPerBox : N / (2 * kRowsPerBox);
-  const int a_boxes = wfmt == MNW_FMT_INT4_G128 ? 1 : 2;
-  a.box_bytes = kBoxBytes;
-  a.off_b = 2 * a_boxes * kBoxBytes;
+  const bool int4 = wfmt == MNW_FMT_INT4_G128;
+  const int a_boxes = int4 ? 1 : 2;                // code boxes per 128-row block per stage
+  const int kg = groups_per_stage(int4 ? WF_INT4 : WF_INT8);
+  a.box_bytes = int4 ? kBox64Bytes : kBoxBytes;
+  a.off_b = 2 * a_boxes * a.box_bytes;
   const bool act16 = act != MNW_ACT_INT8_G128;  // BF16 or FP16 rows
-  const uint32_t b_bytes = (act16 ? 4u : 2u) * BN * 128u;
+  const uint32_t b_bytes = (act16 ? 2u : 1u) * kg * BN * 128u;
   a.stage_bytes = align_up(a.off_b + b_bytes, 1024);
   a.scale_box_bytes = kRowsPerBox * G * 2;
   const uint32_t fixed = 4 * a.scale_box_bytes + align_up(2u * (L->E + 1) * 4u, 16) + align_up(sizeof(Bars), 16);
@@ -111,8 +113,8 @@ int run_gemm_warp(const mnw_moe_layer* L, int wfmt, int act, int kind, const voi
   }
 
   CUtensorMap maps[3];
-  maps[0] = L->tm_codes[m0];
-  maps[1] = L->tm_codes[m1];
+  maps[0] = int4 ? L->tm_codes64[m0] : L->tm_codes[m0];
+  maps[1] = int4 ? L->tm_codes64[m1] : L->tm_codes[m1];
   const uint64_t dims[2] = {static_cast<uint64_t>(K), static_cast<uint64_t>(P)};
   bool ok;
   if (act16) {

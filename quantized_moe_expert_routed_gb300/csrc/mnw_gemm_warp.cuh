@@ -75,8 +75,12 @@ constexpr int kThreads = (1 + kMmaWarps) * 32;  // warp 0 = producer
 constexpr int threads_for(int dep) { return kThreads + (dep == 1 ? 32 : 0); }
 constexpr int kMaxStages = 12;
 constexpr int kRowsPerBox = 128;
-constexpr int kGroups = 2;          // 128-K groups per pipeline stage
-constexpr int kBoxBytes = 128 * 128;  // one TMA box: 128 rows x 128 bytes
+// 128-K groups per pipeline stage: one for INT4 (a 64-byte code box per
+// 128-row block, 64-byte swizzle: small stages, so a deeper ring fits), two
+// for INT8 (one 128-byte box per group).
+__host__ __device__ constexpr int groups_per_stage(int wf) { return wf == 2 ? 1 : 2; }
+constexpr int kBoxBytes = 128 * 128;    // INT8: one TMA box, 128 rows x 128 bytes
+constexpr int kBox64Bytes = 128 * 64;   // INT4: one TMA box, 128 rows x 64 bytes
 // CTAs per SM: two (16 MMA warps) for INT4 with 8- and 16-token tiles, whose
 // registers fit in 96 and whose stages fit in half the shared memory; one
 // otherwise (INT8 stages are twice as large, 32-token accumulators need more).
@@ -346,9 +350,13 @@ __global__ void __launch_bounds__(threads_for(kDep), ctas_per_sm(WF, NT))
     moe_gemm_warp_kernel(const __grid_constant__ CUtensorMap tmA0, const __grid_constant__ CUtensorMap tmA1,
                          const __grid_constant__ CUtensorMap tmB, const Args args) {
   constexpr bool k16 = AM != AM_INT8;  // 16-bit activation rows (BF16 or FP16)
-  // A stage holds kGroups 128-K groups: per weight row 128 contiguous code
-  // bytes (INT4) or two 128-byte pieces (INT8), 128-byte swizzled.
-  constexpr int kABoxes = WF == WF_INT4 ? 1 : 2;  // 16 KB boxes per 128-row block per stage
+  // A stage holds kG 128-K groups: per weight row 64 contiguous code bytes
+  // (INT4, one group, 64-byte swizzle) or two 128-byte pieces (INT8, two
+  // groups, 128-byte swizzle).
+  constexpr int kG = groups_per_stage(WF);
+  constexpr int kABoxes = WF == WF_INT4 ? 1 : 2;  // code boxes per 128-row block per stage
+  constexpr uint32_t kABox = WF == WF_INT4 ? kBox64Bytes : kBoxBytes;
+  constexpr int kABoxX = WF == WF_INT4 ? 64 : 128;  // code bytes per box row
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   Bars* bars = reinterpret_cast<Bars*>(smem + args.off_bars);
@@ -425,9 +433,9 @@ __global__ void __launch_bounds__(threads_for(kDep), ctas_per_sm(WF, NT))
       tma_prefetch_desc(&tmA0);
       tma_prefetch_desc(&tmA1);
       tma_prefetch_desc(&tmB);
-      const uint32_t b_bytes = (k16 ? 4u : 2u) * BN * 128u;
-      const uint32_t tx = 2u * kABoxes * kBoxBytes + b_bytes;
-      const int nstages = (G + kGroups - 1) / kGroups;
+      const uint32_t b_bytes = (k16 ? 2u : 1u) * kG * BN * 128u;
+      const uint32_t tx = 2u * kABoxes * kABox + b_bytes;
+      const int nstages = (G + kG - 1) / kG;
       uint32_t it = 0, uit = 0, sit = 0;
       int s = 0;
       uint32_t ph = 0;  // stage index and phase of `it`, kept without divisions
@@ -478,18 +486,18 @@ __global__ void __launch_bounds__(threads_for(kDep), ctas_per_sm(WF, NT))
           if (!bounded_wait(&bars->empty[s], ph ^ 1, abort, args.err)) { ok = false; break; }
           uint8_t* st = smem + s * args.stage_bytes;
           mbar_arrive_expect_tx(&bars->full[s], tx);
-          // weight codes: box (i, q) holds rows of block i, 128 bytes at byte (ss*kABoxes + q)*128
+          // weight codes: box (i, q) holds rows of block i, kABoxX bytes at byte (ss*kABoxes + q)*kABoxX
 #pragma unroll
           for (int q = 0; q < kABoxes; ++q) {
-            tma_load_3d(st + (0 * kABoxes + q) * kBoxBytes, &tmA0, &bars->full[s], (ss * kABoxes + q) * 128,
+            tma_load_3d(st + (0 * kABoxes + q) * kABox, &tmA0, &bars->full[s], (ss * kABoxes + q) * kABoxX,
                         nb + args.box_row_off[0], x.e);
-            tma_load_3d(st + (1 * kABoxes + q) * kBoxBytes, &tmA1, &bars->full[s], (ss * kABoxes + q) * 128,
+            tma_load_3d(st + (1 * kABoxes + q) * kABox, &tmA1, &bars->full[s], (ss * kABoxes + q) * kABoxX,
                         nb + args.box_row_off[1], x.e);
           }
-          // tokens: 64-element 16-bit boxes or 128-element INT8 boxes covering the stage's 256 K
+          // tokens: 64-element 16-bit boxes or 128-element INT8 boxes covering the stage's kG * 128 K
 #pragma unroll
-          for (int b = 0; b < (k16 ? 4 : 2); ++b)
-            tma_load_2d(st + args.off_b + b * BN * 128, &tmB, &bars->full[s], ss * 256 + b * (k16 ? 64 : 128),
+          for (int b = 0; b < (k16 ? 2 : 1) * kG; ++b)
+            tma_load_2d(st + args.off_b + b * BN * 128, &tmB, &bars->full[s], ss * (kG * 128) + b * (k16 ? 64 : 128),
                         x.row0);
           if (++s == S) { s = 0; ph ^= 1; }
         }
@@ -533,9 +541,10 @@ __global__ void __launch_bounds__(threads_for(kDep), ctas_per_sm(WF, NT))
                         : args.off_b + row * 128 + (((2 * t + (c & 1)) ^ (row & 7)) << 4);
   }
   // a_off[gi][i][hh][c]: code chunk c of row 16w+g+8hh of block i for group gi of a stage
-  uint32_t a_off[kGroups][2][2][2];
+  // (INT4: 64-byte rows, 16-byte chunk t xor (row / 2) % 4; INT8: 128-byte rows, chunk xor row % 8)
+  uint32_t a_off[kG][2][2][2];
 #pragma unroll
-  for (int gi = 0; gi < kGroups; ++gi)
+  for (int gi = 0; gi < kG; ++gi)
 #pragma unroll
     for (int i = 0; i < 2; ++i)
 #pragma unroll
@@ -544,8 +553,8 @@ __global__ void __launch_bounds__(threads_for(kDep), ctas_per_sm(WF, NT))
 #pragma unroll
         for (int c = 0; c < 2; ++c)
           a_off[gi][i][hh][c] =
-              WF == WF_INT4 ? i * kBoxBytes + r * 128 + (((4 * gi + t) ^ (r & 7)) << 4)
-                            : (2 * i + gi) * kBoxBytes + r * 128 + (((2 * t + c) ^ (r & 7)) << 4);
+              WF == WF_INT4 ? i * kABox + r * 64 + ((t ^ ((r >> 1) & 3)) << 4)
+                            : (2 * i + gi) * kABox + r * 128 + (((2 * t + c) ^ (r & 7)) << 4);
       }
   const uint32_t b_gstep = (k16 ? 2u : 1u) * BN * 128u;  // token boxes per group
   for (;; ++uit) {
@@ -566,15 +575,15 @@ __global__ void __launch_bounds__(threads_for(kDep), ctas_per_sm(WF, NT))
 #pragma unroll
         for (int q = 0; q < 4; ++q) tot[i][j][q] = 0.f;
 
-    const int nstages = (G + kGroups - 1) / kGroups;
+    const int nstages = (G + kG - 1) / kG;
     for (int ss = 0; ss < nstages; ++ss, ++it) {
       if (!bounded_wait(&bars->full[s], ph, abort, args.err)) return;
       const uint32_t st = smem_u32(smem + s * args.stage_bytes);
       const int s_now = s;
       if (++s == S) { s = 0; ph ^= 1; }
 #pragma unroll
-      for (int gi = 0; gi < kGroups; ++gi) {
-      const int grp = ss * kGroups + gi;
+      for (int gi = 0; gi < kG; ++gi) {
+      const int grp = ss * kG + gi;
       if (grp >= G) break;
       const uint32_t stb = st + gi * b_gstep;
       // active token tiles of this unit (uniform across the CTA)

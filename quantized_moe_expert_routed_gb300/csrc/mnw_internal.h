@@ -23,6 +23,7 @@ struct mnw_moe_layer {
   bool f16_gate_up_ok, f16_down_ok;
   // Weight tensor maps (built once): codes per matrix, NVFP4 block scales per matrix.
   CUtensorMap tm_codes[3];
+  CUtensorMap tm_codes64[3];  // INT4 codes in 64-byte boxes (one 128-K group), 64-byte swizzle
   CUtensorMap tm_sf[3];
 };
 
