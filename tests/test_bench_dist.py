@@ -142,6 +142,14 @@ def test_gpu_arm_json_line_contract():
         assert e2e["value"] == pytest.approx(2 * wl.T / 0.174e-3)
         assert e2e["h2d_bytes_per_step"] == 2 * (wl.T * wl.H * 2 + wl.T * wl.k * 8)
         assert e2e["d2h_bytes_per_step"] == 2 * wl.T * wl.H * 2
+        assert "variants" not in line and "graph" not in line  # only when measured
+    # the comparison paths and the graph replay pass through with their notes
+    r.update(variants={"routed_forward_ms": 0.15, "route_ms": 0.02, "host_routing_forward_ms": 0.74,
+                       "unfused_forward_ms": 0.17, "fused_forward_ms": 0.135}, graph_ms=0.134)
+    line = bench.build_line(args, wl, {"workload": name}, r, (4.4, 10.0, 12), (12345, "test"))
+    assert line["variants"]["route_ms"] == 0.02 and "note" in line["variants"]
+    assert line["graph"]["ms_per_step_median"] == 0.134
+    assert line["graph"]["value"] == pytest.approx(2 * wl.T / 0.134e-3)
     # the captured traffic is read from the committed ncu summary table, and
     # reported only while the GEMM sources hash to the value recorded with it
     table = os.path.join(ROOT, "profiles", "gate_up_dram_traffic.txt")
